@@ -1,0 +1,179 @@
+"""CPU oracle for the blockwise-scaled FP8 grouped GEMM -- TEST INFRASTRUCTURE ONLY.
+
+Only the test suite, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The product (the CUDA library and its Python
+binding) never does, and this package never imports the product.  It shares no code
+with the CUDA kernels.
+
+The arithmetic lives in ``bsfp8_oracle.cpp`` (plain C++, fp64); see its header for the
+definition it writes out and the page passages it follows:
+
+  * promote_accumulators (MAX kernels, linalg/grouped_matmul_sm100_blockwise_fp8):
+    per-K-block partials times (A scale x B scale), accumulated in fp32 tiles;
+    b_scales [num_experts, N // BN, K // BK].
+  * Triton Gluon example "Overlapping Accumulator Block-Scaled Matrix Multiplication",
+    make_problem / random_quantized_tensor: the block-scaled result is the matmul of the
+    dequantized operands (UE8M0 scales repeated over 32 K elements).
+
+Parity pins (tests/test_oracle_pins.py) tie it to the e4m3 closed form, torch's own
+float8 decode, brute force, exact power-of-two linearity, per-expert concatenation and
+the exact-arithmetic inputs.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import time
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "bsfp8_oracle.cpp")
+_LIB = os.path.join(_HERE, "libbsfp8_oracle.so")
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into oracle/libbsfp8_oracle.so (skipped when up to date)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(["g++", "-O2", "-ffp-contract=off", "-std=c++17", "-shared",
+                               "-fPIC", "-pthread", "-o", tmp, _SRC])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+_lib = None
+
+
+def _L():
+    global _lib
+    if _lib is None:
+        build()
+        lib = ctypes.CDLL(_LIB)
+        p, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+        lib.bsfp8_oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
+        lib.bsfp8_oracle_e4m3_decode.restype = ctypes.c_double
+        lib.bsfp8_oracle_ue8m0_decode.argtypes = [ctypes.c_uint8]
+        lib.bsfp8_oracle_ue8m0_decode.restype = ctypes.c_double
+        lib.bsfp8_oracle_bf16_rne.argtypes = [ctypes.c_double]
+        lib.bsfp8_oracle_bf16_rne.restype = ctypes.c_uint16
+        for name in ("bsfp8_oracle_blockwise", "bsfp8_oracle_mx"):
+            f = getattr(lib, name)
+            f.argtypes = [p, p, p, p, p, i64, i64, i64, i64, p, p, i32]
+            f.restype = i32
+        for name in ("bsfp8_oracle_blockwise_points", "bsfp8_oracle_mx_points"):
+            f = getattr(lib, name)
+            f.argtypes = [p, p, p, p, p, i64, i64, i64, i64, p, p, i64, p, p, i32]
+            f.restype = i32
+        lib.bsfp8_oracle_threads.argtypes = [i32]
+        lib.bsfp8_oracle_threads.restype = i32
+        _lib = lib
+    return _lib
+
+
+class OracleError(RuntimeError):
+    pass
+
+
+def _c(a: np.ndarray, dtype) -> np.ndarray:
+    a = np.ascontiguousarray(a, dtype=dtype)
+    return a
+
+
+def e4m3_decode(code: int) -> float:
+    return float(_L().bsfp8_oracle_e4m3_decode(code))
+
+
+def ue8m0_decode(code: int) -> float:
+    return float(_L().bsfp8_oracle_ue8m0_decode(code))
+
+
+def bf16_rne(x: float) -> int:
+    return int(_L().bsfp8_oracle_bf16_rne(float(x)))
+
+
+def threads(n: int = 0) -> int:
+    return int(_L().bsfp8_oracle_threads(n))
+
+
+def _args(mode, A, B, a_scales, b_scales, offsets):
+    A = _c(A, np.uint8)
+    B = _c(B, np.uint8)
+    if mode == "blockwise":
+        a_scales = _c(a_scales, np.float32)
+        b_scales = _c(b_scales, np.float32)
+    elif mode == "mx":
+        a_scales = _c(a_scales, np.uint8)
+        b_scales = _c(b_scales, np.uint8)
+    else:
+        raise ValueError(mode)
+    offsets = _c(offsets, np.int32)
+    return A, B, a_scales, b_scales, offsets
+
+
+def grouped_gemm(mode: str, A, B, a_scales, b_scales, offsets, N: int, K: int,
+                 nthreads: int = 0, want_t: bool = True):
+    """Full output.  Returns (C as bf16 bit patterns uint16 [M_total, N], T float64 or None)."""
+    A, B, a_scales, b_scales, offsets = _args(mode, A, B, a_scales, b_scales, offsets)
+    E = offsets.shape[0] - 1
+    M = int(offsets[-1])
+    C = np.empty((M, N), np.uint16)
+    T = np.empty((M, N), np.float64) if want_t else None
+    f = _L().bsfp8_oracle_blockwise if mode == "blockwise" else _L().bsfp8_oracle_mx
+    rc = f(A.ctypes.data, B.ctypes.data, a_scales.ctypes.data, b_scales.ctypes.data,
+           offsets.ctypes.data, M, N, K, E, C.ctypes.data,
+           T.ctypes.data if T is not None else None, nthreads)
+    if rc:
+        raise OracleError(f"oracle rejected the problem (code {rc})")
+    return C, T
+
+
+def grouped_gemm_points(mode: str, A, B, a_scales, b_scales, offsets, N: int, K: int,
+                        rows, cols, nthreads: int = 0):
+    """Sampled output elements (rows[i], cols[i]).  Returns (C bits uint16 [n], T float64 [n])."""
+    A, B, a_scales, b_scales, offsets = _args(mode, A, B, a_scales, b_scales, offsets)
+    rows = _c(rows, np.int64)
+    cols = _c(cols, np.int64)
+    assert rows.shape == cols.shape
+    E = offsets.shape[0] - 1
+    M = int(offsets[-1])
+    C = np.empty(rows.shape, np.uint16)
+    T = np.empty(rows.shape, np.float64)
+    f = _L().bsfp8_oracle_blockwise_points if mode == "blockwise" else _L().bsfp8_oracle_mx_points
+    rc = f(A.ctypes.data, B.ctypes.data, a_scales.ctypes.data, b_scales.ctypes.data,
+           offsets.ctypes.data, M, N, K, E, rows.ctypes.data, cols.ctypes.data, rows.size,
+           C.ctypes.data, T.ctypes.data, nthreads)
+    if rc:
+        raise OracleError(f"oracle rejected the problem (code {rc})")
+    return C, T
+
+
+def problem_reference(p, nthreads: int = 0, want_t: bool = True):
+    """Full oracle output for a gen.Problem-like object (mode, A, B, scales, offsets, N, K)."""
+    return grouped_gemm(p.mode, p.A, p.B, p.a_scales, p.b_scales, p.offsets, p.N, p.K,
+                        nthreads=nthreads, want_t=want_t)
+
+
+def problem_points(p, rows, cols, nthreads: int = 0):
+    return grouped_gemm_points(p.mode, p.A, p.B, p.a_scales, p.b_scales, p.offsets, p.N, p.K,
+                               rows, cols, nthreads=nthreads)
+
+
+def timed_rows(p, row_count: int, nthreads: int = 0):
+    """Time the oracle on the first row_count rows of every column (a bounded sample of the
+    workload).  Returns (seconds, flops_done, threads_used)."""
+    M = p.M_total
+    rows_sel = np.linspace(0, M - 1, num=min(row_count, M)).astype(np.int64)
+    rows = np.repeat(rows_sel, p.N)
+    cols = np.tile(np.arange(p.N, dtype=np.int64), rows_sel.size)
+    t0 = time.perf_counter()
+    problem_points(p, rows, cols, nthreads=nthreads)
+    dt = time.perf_counter() - t0
+    return dt, 2.0 * rows.size * p.K, threads(nthreads)
+
+
+def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns -> float64 values (exact)."""
+    bits = np.asarray(bits, np.uint16)
+    return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)

@@ -1,0 +1,112 @@
+"""Test-side helpers: torch float64 brute force, exact bf16 rounding and the tolerance.
+
+The brute force here is deliberately written differently from the oracle: operands are
+decoded by torch's own float8 types, dequantized (value x scale, scales expanded over
+their blocks) and multiplied with torch.matmul in float64 -- the reference construction
+of make_problem in the Triton Gluon example "Overlapping Accumulator Block-Scaled Matrix
+Multiplication".  The acceptance bound is the workload's stated one:
+|gpu - ref| <= 2 ulp_bf16(ref) + 1e-6 * sum|scaled terms|.
+"""
+from __future__ import annotations
+
+import struct
+from fractions import Fraction
+
+import numpy as np
+import torch
+
+
+def decode_e4m3_torch(codes: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(codes)).view(torch.float8_e4m3fn).to(torch.float64)
+
+
+def decode_ue8m0_torch(codes: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(codes)).view(torch.float8_e8m0fnu).to(torch.float64)
+
+
+def dequantize(p):
+    """(A_deq [M,K], B_deq [E,N,K]) in float64 for a gen.Problem."""
+    A = decode_e4m3_torch(p.A)
+    B = decode_e4m3_torch(p.B)
+    if p.mode == "blockwise":
+        sa = torch.from_numpy(p.a_scales).to(torch.float64)            # [K/128, M]
+        A = A * sa.t().repeat_interleave(128, dim=1)
+        sb = torch.from_numpy(p.b_scales).to(torch.float64)            # [E, N/128, K/128]
+        B = B * sb.repeat_interleave(128, dim=1).repeat_interleave(128, dim=2)
+    else:
+        A = A * decode_ue8m0_torch(p.a_scales).repeat_interleave(32, dim=1)   # [M, K/32]
+        B = B * decode_ue8m0_torch(p.b_scales).repeat_interleave(32, dim=2)   # [E, N, K/32]
+    return A, B
+
+
+def brute_force(p):
+    """(C float64 [M,N], T float64 [M,N]) by dequantized matmul per expert."""
+    A, B = dequantize(p)
+    M, N = p.M_total, p.N
+    C = torch.zeros(M, N, dtype=torch.float64)
+    T = torch.zeros(M, N, dtype=torch.float64)
+    off = p.offsets
+    for e in range(p.E):
+        r0, r1 = int(off[e]), int(off[e + 1])
+        if r1 > r0:
+            C[r0:r1] = A[r0:r1] @ B[e].t()
+            T[r0:r1] = A[r0:r1].abs() @ B[e].abs().t()
+    return C.numpy(), T.numpy()
+
+
+def f32_bits(x: float) -> int:
+    return struct.unpack("<I", struct.pack("<f", x))[0]
+
+
+def bf16_exact_round(v) -> int:
+    """Round an exact rational (or float) to bf16 bits, RNE, with exact arithmetic."""
+    v = Fraction(v)
+    if v == 0:
+        return 0
+    sign = 0x8000 if v < 0 else 0
+    a = abs(v)
+    E = a.numerator.bit_length() - a.denominator.bit_length()
+    if Fraction(2) ** E > a:
+        E -= 1
+    if Fraction(2) ** (E + 1) <= a:
+        E += 1
+    E = max(E, -126)
+    q = Fraction(2) ** (E - 7)
+    r = a / q
+    fl = r.numerator // r.denominator
+    rem = r - fl
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and fl % 2 == 1):
+        fl += 1
+    val = fl * q
+    if val >= Fraction(2) ** 128:
+        return sign | 0x7F80
+    return sign | (f32_bits(float(val)) >> 16)
+
+
+def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    bits = np.asarray(bits, np.uint16)
+    return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def ulp_bf16(ref_vals: np.ndarray) -> np.ndarray:
+    """2^(max(floor(log2|x|), -126) - 7); 2^-133 at zero."""
+    a = np.abs(np.asarray(ref_vals, np.float64))
+    with np.errstate(divide="ignore"):
+        e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    e = np.where(a > 0, np.maximum(e, -126), -126)
+    return np.ldexp(1.0, (e - 7).astype(np.int64))
+
+
+def tolerance(ref_bits: np.ndarray, T: np.ndarray) -> np.ndarray:
+    return 2.0 * ulp_bf16(bf16_bits_to_f64(ref_bits)) + 1e-6 * np.asarray(T, np.float64)
+
+
+def parity_report(got_bits: np.ndarray, ref_bits: np.ndarray, T: np.ndarray):
+    """(n_bad, max_err/tol, n_exact) for bf16 outputs against the oracle."""
+    got = bf16_bits_to_f64(got_bits)
+    ref = bf16_bits_to_f64(ref_bits)
+    tol = tolerance(ref_bits, T)
+    err = np.abs(got - ref)
+    bad = ~(err <= tol)
+    ratio = float(np.max(err / tol)) if err.size else 0.0
+    return int(bad.sum()), ratio, int((np.asarray(got_bits) == np.asarray(ref_bits)).sum())
