@@ -1,0 +1,103 @@
+"""Python binding of the bsfp8 C ABI (include/bsfp8.h).
+
+Argument marshalling only: every step of the GEMM runs in the CUDA library
+``lib/libbsfp8.so``.  There is no fallback: if the library is missing or the device is
+not a GB300 (compute capability 10.3) the calls raise.
+
+    import block_scaled_fp8_persistent_gb300 as bsfp8
+    bsfp8.bsfp8_grouped_gemm(A, B, a_scales, b_scales, expert_offsets, C,
+                             M_total, N, K, num_experts, stream=None)
+
+Tensors are torch CUDA tensors (or raw device addresses as ints) in the layouts of
+include/bsfp8.h; ``stream`` is a torch.cuda.Stream, a raw cudaStream_t int, or None for
+torch's current stream.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "lib", "libbsfp8.so")
+
+BSFP8_OK = 0
+STATUS_NAMES = {
+    0: "BSFP8_OK", 1: "BSFP8_ERR_NULL", 2: "BSFP8_ERR_SHAPE", 3: "BSFP8_ERR_ALIGN",
+    4: "BSFP8_ERR_UNSUPPORTED_DEVICE", 5: "BSFP8_ERR_CUDA", 6: "BSFP8_ERR_DEVICE_OFFSETS",
+    7: "BSFP8_ERR_DEVICE_TIMEOUT",
+}
+
+# Every symbol include/bsfp8.h declares (the CPU test checks the library exports them).
+EXPORTED = ("bsfp8_grouped_gemm", "bsfp8_get_device_error", "bsfp8_status_string")
+
+
+class BsFp8Error(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)} ({status_string(status)})")
+
+
+_lib = None
+
+
+def load_library() -> ctypes.CDLL:
+    """Load lib/libbsfp8.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"{LIB_PATH} is missing: build it with "
+                              "`python -m block_scaled_fp8_persistent_gb300.build`")
+        lib = ctypes.CDLL(LIB_PATH)
+        p, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+        lib.bsfp8_grouped_gemm.argtypes = [p, p, p, p, p, p, i64, i32, i32, i32, p]
+        lib.bsfp8_grouped_gemm.restype = i32
+        lib.bsfp8_get_device_error.argtypes = [p, ctypes.POINTER(ctypes.c_int)]
+        lib.bsfp8_get_device_error.restype = i32
+        lib.bsfp8_status_string.argtypes = [i32]
+        lib.bsfp8_status_string.restype = ctypes.c_char_p
+        _lib = lib
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return load_library().bsfp8_status_string(int(status)).decode()
+
+
+def _addr(x) -> int | None:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if not x.is_cuda:
+        raise ValueError("tensors must be CUDA tensors (device memory)")
+    if not x.is_contiguous():
+        raise ValueError("tensors must be contiguous (row-major)")
+    return x.data_ptr() or None
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream or None
+    if isinstance(stream, int):
+        return stream or None
+    return stream.cuda_stream or None
+
+
+def bsfp8_grouped_gemm(A, B, a_scales, b_scales, expert_offsets, C, M_total: int, N: int,
+                       K: int, num_experts: int, stream=None) -> None:
+    """Blockwise FP8 grouped GEMM; see include/bsfp8.h for layouts.  Raises BsFp8Error."""
+    st = load_library().bsfp8_grouped_gemm(_addr(A), _addr(B), _addr(a_scales), _addr(b_scales),
+                                           _addr(expert_offsets), _addr(C), int(M_total), int(N),
+                                           int(K), int(num_experts), _stream(stream))
+    if st != BSFP8_OK:
+        raise BsFp8Error(st, "bsfp8_grouped_gemm")
+
+
+def bsfp8_get_device_error(stream=None) -> int:
+    """Read and clear the device error word (synchronises the stream)."""
+    code = ctypes.c_int(0)
+    st = load_library().bsfp8_get_device_error(_stream(stream), ctypes.byref(code))
+    if st != BSFP8_OK:
+        raise BsFp8Error(st, "bsfp8_get_device_error")
+    return code.value

@@ -1,0 +1,154 @@
+// C-ABI entry points: argument checks on the host, tensor-map encoding, kernel launch.
+// Declarations and the contract live in include/bsfp8.h.
+#include <mutex>
+
+#include "bsfp8.h"
+#include "common.cuh"
+
+namespace bsfp8 {
+
+// One device error word per device (static device memory: nothing is allocated).
+__device__ int g_error_word;
+
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return reinterpret_cast<EncodeTiledFn>(p);
+  }();
+  return fn;
+}
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  bool ready = false;
+  bool supported = false;
+  int num_sms = 0;
+  int* err_word = nullptr;
+};
+
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+// Device properties and the error word's address, once per device.
+bsfp8_status device_info(DeviceInfo** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return BSFP8_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_dev_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.ready) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return BSFP8_ERR_CUDA;
+    d.supported = (major == 10 && minor == 3);
+    d.num_sms = sms;
+    if (d.supported) {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return BSFP8_ERR_CUDA;
+      d.err_word = static_cast<int*>(p);
+    }
+    d.ready = true;
+  }
+  if (!d.supported) return BSFP8_ERR_UNSUPPORTED_DEVICE;
+  *out = &d;
+  return BSFP8_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// 2D uint8 tensor map over a row-major [rows, inner] byte matrix, box [box_rows, box_inner],
+// 128-byte swizzle (box_inner must be 128).
+bool encode_u8_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
+                  uint32_t box_inner, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {inner, rows};
+  const cuuint64_t strides[1] = {inner};
+  const cuuint32_t box[2] = {box_inner, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bsfp8_status check_common(const void* A, const void* B, const void* sa, const void* sb,
+                          const int32_t* off, void* C, int64_t M_total, int N, int K, int E) {
+  if (!off || !B || !sb) return BSFP8_ERR_NULL;
+  if (M_total > 0 && (!A || !sa || !C)) return BSFP8_ERR_NULL;
+  if (M_total < 0 || M_total > INT32_MAX || N < 128 || N % 128 != 0 || K < 128 ||
+      K % 128 != 0 || E < 1 || (int64_t)E * N > INT32_MAX)
+    return BSFP8_ERR_SHAPE;
+  if (!aligned(A, 16) || !aligned(B, 16) || !aligned(C, 16) || !aligned(sa, 4) ||
+      !aligned(sb, 4) || !aligned(off, 4))
+    return BSFP8_ERR_ALIGN;
+  return BSFP8_OK;
+}
+
+}  // namespace
+}  // namespace bsfp8
+
+using namespace bsfp8;
+
+extern "C" bsfp8_status bsfp8_grouped_gemm(const void* A, const void* B, const float* a_scales,
+                                           const float* b_scales, const int32_t* expert_offsets,
+                                           void* C, int64_t M_total, int N, int K,
+                                           int num_experts, cudaStream_t stream) {
+  bsfp8_status st = check_common(A, B, a_scales, b_scales, expert_offsets, C, M_total, N, K,
+                                 num_experts);
+  if (st != BSFP8_OK) return st;
+  DeviceInfo* dev = nullptr;
+  if ((st = device_info(&dev)) != BSFP8_OK) return st;
+  if (M_total == 0) return BSFP8_OK;
+  CUtensorMap tmA, tmB;
+  if (!encode_u8_2d(&tmA, A, (uint64_t)K, (uint64_t)M_total, 128, 128) ||
+      !encode_u8_2d(&tmB, B, (uint64_t)K, (uint64_t)num_experts * N, 128, 256))
+    return BSFP8_ERR_CUDA;
+  GemmArgs args{expert_offsets, a_scales, b_scales, C, M_total, N, K, num_experts, dev->err_word};
+  return launch_bsfp8_blockwise(tmA, tmB, args, dev->num_sms, stream) == cudaSuccess
+             ? BSFP8_OK
+             : BSFP8_ERR_CUDA;
+}
+
+extern "C" bsfp8_status bsfp8_get_device_error(cudaStream_t stream, int* code) {
+  if (!code) return BSFP8_ERR_NULL;
+  DeviceInfo* dev = nullptr;
+  bsfp8_status st = device_info(&dev);
+  if (st != BSFP8_OK) return st;
+  int v = 0;
+  if (cudaStreamSynchronize(stream) != cudaSuccess ||
+      cudaMemcpyAsync(&v, dev->err_word, sizeof(int), cudaMemcpyDeviceToHost, stream) !=
+          cudaSuccess ||
+      cudaMemsetAsync(dev->err_word, 0, sizeof(int), stream) != cudaSuccess ||
+      cudaStreamSynchronize(stream) != cudaSuccess)
+    return BSFP8_ERR_CUDA;
+  *code = v;
+  return BSFP8_OK;
+}
+
+extern "C" const char* bsfp8_status_string(bsfp8_status s) {
+  switch (s) {
+    case BSFP8_OK: return "ok";
+    case BSFP8_ERR_NULL: return "null pointer";
+    case BSFP8_ERR_SHAPE: return "invalid shape";
+    case BSFP8_ERR_ALIGN: return "misaligned pointer";
+    case BSFP8_ERR_UNSUPPORTED_DEVICE: return "device is not compute capability 10.3";
+    case BSFP8_ERR_CUDA: return "CUDA call failed";
+    case BSFP8_ERR_DEVICE_OFFSETS: return "device: invalid expert offsets";
+    case BSFP8_ERR_DEVICE_TIMEOUT: return "device: pipeline wait timed out";
+  }
+  return "unknown status";
+}

@@ -1,0 +1,32 @@
+// Types shared by the C-ABI layer (capi.cu) and the kernel translation units.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace bsfp8 {
+
+// Device-side error codes (written once per launch into the library's error word).
+enum DeviceError : int {
+  DEV_OK = 0,
+  DEV_BAD_OFFSETS = 6,  // offsets[0] != 0, offsets[E] != M_total or not non-decreasing
+  DEV_TIMEOUT = 7,      // a pipeline wait gave up (the kernel wound down cleanly)
+};
+
+// Plain pointers and sizes handed to every kernel (tensor maps travel separately as
+// __grid_constant__ parameters).
+struct GemmArgs {
+  const int32_t* offsets;  // [E+1] row offsets per expert
+  const void* a_scales;    // blockwise: f32 [K/128, M_total]   MX: u8 [M_total, K/32]
+  const void* b_scales;    // blockwise: f32 [E, N/128, K/128]  MX: u8 [E, N, K/32]
+  void* C;                 // bf16 [M_total, N]
+  int64_t M_total;
+  int N, K, E;
+  int* err;                // library-owned device error word
+};
+
+// Launchers (one per kernel family); return the launch error.
+cudaError_t launch_bsfp8_blockwise(const CUtensorMap& tmA, const CUtensorMap& tmB,
+                                   const GemmArgs& args, int num_sms, cudaStream_t stream);
+
+}  // namespace bsfp8

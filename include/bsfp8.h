@@ -1,0 +1,100 @@
+/*
+ * bsfp8 -- blockwise-scaled FP8 grouped GEMM for GB300 (sm_103a), C ABI.
+ *
+ * The operation (mixture-of-experts grouped GEMM with blockwise FP8 scaling):
+ *
+ *   for every expert e, every row m in [expert_offsets[e], expert_offsets[e+1]) and every
+ *   column n < N:
+ *     C[m, n] = bf16( sum_kb  sa(m, kb) * sb(e, n, kb) * sum_{k in block kb} A[m, k] * B[e, n, k] )
+ *
+ *   A, B are e4m3 ("fn") codes; the inner sums run over K blocks; accumulation is fp32 and
+ *   the result is rounded to bf16 (round to nearest even).
+ *
+ * Sources (the pages this library follows):
+ *   - promote_accumulators (MAX kernels, linalg/grouped_matmul_sm100_blockwise_fp8),
+ *     description and Args: each per-K-block MMA result is multiplied by the A scale of
+ *     its row and the B scale of its (expert, N block, K block) and accumulated in fp32
+ *     register tiles; b_scales has shape [num_experts, N // BN, K // BK]; problem_shape
+ *     is (M, N, K); expert_ids maps a group to its expert's rows of B.
+ *   - EpilogueWarpContext (MAX sm100_structured warp_context), per_k_stage: the blockwise
+ *     FP8 epilogue consumes one TMEM stage and one A-scale stage per K iteration.
+ *   - Triton Gluon example "Overlapping Accumulator Block-Scaled Matrix Multiplication",
+ *     async_mma_scaled_impl / random_quantized_tensor: the block-scaled MMA on e4m3
+ *     operands with UE8M0 (uint8) scales, one per VEC_SIZE = 32 elements of K.
+ *
+ * Conventions shared by every entry point:
+ *   - Every pointer is a DEVICE pointer (memory of the current CUDA device), row-major,
+ *     last index contiguous.  The caller owns every buffer and the stream; the library
+ *     keeps only a 4-byte device error word per device and allocates nothing per call.
+ *   - Calls are asynchronous and ordered on `stream`; nothing is synchronised.
+ *   - Host-detectable problems return a status immediately and launch nothing.
+ *   - Problems only the device can see (expert offsets that are not a valid partition of
+ *     [0, M_total), or a pipeline wait that exceeded its time limit) make the kernel write
+ *     a code into the device error word and finish without touching C further; read it
+ *     with bsfp8_get_device_error().
+ *   - Requirements: N % 128 == 0, K % 128 == 0, num_experts >= 1, 0 <= M_total < 2^31,
+ *     num_experts * N < 2^31; A, B, C 16-byte aligned; scales and offsets 4-byte aligned.
+ *     M_total == 0 is a valid no-op (nothing is read or written).
+ *   - The device must be compute capability 10.3 (GB300).
+ */
+#ifndef BSFP8_H_
+#define BSFP8_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#ifndef __CUDA_RUNTIME_API_H__
+/* Same type as the CUDA runtime's cudaStream_t. */
+typedef struct CUstream_st* cudaStream_t;
+#endif
+
+typedef enum {
+  BSFP8_OK = 0,
+  BSFP8_ERR_NULL = 1,               /* a required pointer is NULL */
+  BSFP8_ERR_SHAPE = 2,              /* sizes violate the requirements above */
+  BSFP8_ERR_ALIGN = 3,              /* a pointer is not aligned as required */
+  BSFP8_ERR_UNSUPPORTED_DEVICE = 4, /* current device is not compute capability 10.3 */
+  BSFP8_ERR_CUDA = 5,               /* a CUDA runtime/driver call failed (launch, ...) */
+  BSFP8_ERR_DEVICE_OFFSETS = 6,     /* device error word: invalid expert offsets */
+  BSFP8_ERR_DEVICE_TIMEOUT = 7      /* device error word: a pipeline wait gave up */
+} bsfp8_status;
+
+/*
+ * Blockwise FP8 grouped GEMM (1x128 A scales, 128x128 B scales).
+ *
+ *   A              e4m3 [M_total, K]        token rows, grouped by expert (expert e owns
+ *                                           rows expert_offsets[e] .. expert_offsets[e+1]-1)
+ *   B              e4m3 [num_experts, N, K] expert weights, K-major (row n of expert e is
+ *                                           B + (e*N + n)*K)
+ *   a_scales       fp32 [K/128, M_total]    sa(m, kb) = a_scales[kb*M_total + m]
+ *   b_scales       fp32 [num_experts, N/128, K/128]
+ *                                           sb(e, n, kb) = b_scales[(e*(N/128) + n/128)*(K/128) + kb]
+ *   expert_offsets int32 [num_experts+1]    expert_offsets[0] = 0, non-decreasing,
+ *                                           expert_offsets[num_experts] = M_total
+ *   C              bf16 [M_total, N]        output, fully written (every row belongs to
+ *                                           exactly one expert); experts with no rows
+ *                                           write nothing
+ */
+bsfp8_status bsfp8_grouped_gemm(const void* A, const void* B, const float* a_scales,
+                                const float* b_scales, const int32_t* expert_offsets, void* C,
+                                int64_t M_total, int N, int K, int num_experts,
+                                cudaStream_t stream);
+
+/*
+ * Read the device error word of the current device (after synchronising `stream`) into
+ * *code (0, BSFP8_ERR_DEVICE_OFFSETS or BSFP8_ERR_DEVICE_TIMEOUT) and reset it to 0.
+ * Returns BSFP8_ERR_NULL for a NULL code, BSFP8_ERR_CUDA if a CUDA call fails.
+ */
+bsfp8_status bsfp8_get_device_error(cudaStream_t stream, int* code);
+
+/* Static, human-readable name of a status code. */
+const char* bsfp8_status_string(bsfp8_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BSFP8_H_ */

@@ -1,0 +1,75 @@
+"""The C-ABI library on the host: it loads, exports every declared symbol, and rejects bad
+arguments with the documented status codes before touching any GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import block_scaled_fp8_persistent_gb300 as bsfp8
+from block_scaled_fp8_persistent_gb300 import build as libbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    libbuild.build()
+    return bsfp8.load_library()
+
+
+def _declared_functions():
+    names = []
+    for h in os.listdir(os.path.join(ROOT, "include")):
+        text = open(os.path.join(ROOT, "include", h)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names += re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*(bsfp8_[a-z0-9_]+)\s*\(",
+                            text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    declared = _declared_functions()
+    assert "bsfp8_grouped_gemm" in declared
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert set(declared) == set(bsfp8.EXPORTED)
+
+
+def test_status_strings(lib):
+    for code in range(8):
+        assert len(bsfp8.status_string(code)) > 0
+    assert bsfp8.status_string(99) == "unknown status"
+
+
+FAKE = 1 << 20  # a 16-byte aligned non-null address; never dereferenced on these paths
+
+
+def _call(lib, **kw):
+    a = dict(A=FAKE, B=FAKE, sa=FAKE, sb=FAKE, off=FAKE, C=FAKE, M=256, N=256, K=512, E=1)
+    a.update(kw)
+    return lib.bsfp8_grouped_gemm(a["A"], a["B"], a["sa"], a["sb"], a["off"], a["C"], a["M"],
+                                  a["N"], a["K"], a["E"], None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(B=None), 1), (dict(sb=None), 1), (dict(off=None), 1), (dict(A=None), 1),
+    (dict(C=None), 1), (dict(sa=None), 1),
+    (dict(N=192), 2), (dict(N=0), 2), (dict(K=100), 2), (dict(K=0), 2), (dict(E=0), 2),
+    (dict(M=-1), 2), (dict(M=1 << 31), 2), (dict(E=1 << 20, N=4096), 2),
+    (dict(A=FAKE + 8), 3), (dict(B=FAKE + 4), 3), (dict(C=FAKE + 2), 3), (dict(sa=FAKE + 2), 3),
+    (dict(off=FAKE + 1), 3),
+])
+def test_host_validation(lib, kw, status):
+    assert _call(lib, **kw) == status
+
+
+def test_empty_problem_needs_no_row_buffers(lib):
+    # M_total == 0: A, a_scales and C may be NULL; shape errors still reported first
+    assert _call(lib, M=0, A=None, sa=None, C=None, N=100) == 2
+
+
+def test_binding_raises_on_bad_shape():
+    with pytest.raises(bsfp8.BsFp8Error) as ei:
+        bsfp8.bsfp8_grouped_gemm(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 256, 200, 512, 1, stream=0)
+    assert ei.value.status == 2

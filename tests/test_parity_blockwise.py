@@ -1,0 +1,121 @@
+"""GPU parity of the blockwise FP8 grouped GEMM against the CPU oracle.
+
+Acceptance per element: |gpu - oracle| <= 2 ulp_bf16(oracle) + 1e-6 * sum|scaled terms|.
+Exact-arithmetic inputs (e2m1-grid values, scales in {0.5, 1, 2}) have a unique bf16
+result, which the GPU must hit bit for bit.
+"""
+import numpy as np
+import pytest
+import torch
+
+import gen
+import oracle
+from helpers import parity_report
+
+pytestmark = pytest.mark.gpu
+
+
+def _check_full(p, **kw):
+    from gpu_util import DeviceProblem
+    import block_scaled_fp8_persistent_gb300 as bsfp8
+    d = DeviceProblem(p, c_rows_extra=3)
+    d.run()
+    got = d.c_bits()
+    assert bsfp8.bsfp8_get_device_error() == 0
+    ref, T = oracle.problem_reference(p)
+    bad, ratio, exact = parity_report(got, ref, T)
+    assert bad == 0, f"{bad} elements outside tolerance (max err/tol {ratio:.3g})"
+    # nothing written past M_total
+    assert np.all(d.guard_bits() == d.sentinel)
+    return got, ref
+
+
+SMALL_CASES = [
+    ("config0", [256], 256, 512),
+    ("ragged_partial_ntile", [130, 0, 77, 1], 384, 640),
+    ("single_row", [1], 128, 128),
+    ("many_small_experts", [5, 0, 0, 33, 128, 127, 129, 2, 0, 64], 256, 256),
+    ("tail_rows_not_mult4", [3, 250, 7], 512, 384),
+]
+
+
+@pytest.mark.parametrize("name,counts,N,K", SMALL_CASES, ids=[c[0] for c in SMALL_CASES])
+def test_small_cases(name, counts, N, K):
+    p = gen.blockwise_problem(counts, N, K, seed=100 + len(name))
+    _check_full(p)
+
+
+@pytest.mark.parametrize("counts,N,K", [([200, 0, 57], 256, 1024), ([256], 384, 7168)])
+def test_exact_inputs_bitwise(counts, N, K):
+    p = gen.blockwise_problem(counts, N, K, seed=7, exact=True)
+    got, ref = _check_full(p)
+    assert np.array_equal(got, ref)
+
+
+def test_outlier_rows():
+    p = gen.blockwise_problem([300, 212], 256, 512, seed=31, outlier_rows=6)
+    _check_full(p)
+
+
+def test_all_experts_empty_but_one():
+    p = gen.blockwise_problem([0, 0, 0, 77, 0], 256, 256, seed=32)
+    _check_full(p)
+
+
+def test_repeated_calls_identical():
+    from gpu_util import DeviceProblem
+    p = gen.blockwise_problem([100, 29], 256, 512, seed=33)
+    d = DeviceProblem(p)
+    d.run()
+    a = d.c_bits()
+    for _ in range(3):
+        d.run()
+    assert np.array_equal(a, d.c_bits())
+
+
+def test_invalid_offsets_reported_on_device():
+    from gpu_util import DeviceProblem
+    import block_scaled_fp8_persistent_gb300 as bsfp8
+    p = gen.blockwise_problem([64, 64], 256, 256, seed=34)
+    d = DeviceProblem(p)
+    d.off.copy_(torch.tensor([0, 100, 90], dtype=torch.int32))  # not monotone, last != M
+    d.run()
+    assert bsfp8.bsfp8_get_device_error() == 6
+    assert np.all(d.c_bits() == d.sentinel)          # C untouched
+    assert bsfp8.bsfp8_get_device_error() == 0       # read clears
+
+
+def test_m_total_zero_is_noop():
+    import block_scaled_fp8_persistent_gb300 as bsfp8
+    B = torch.zeros((2, 128, 128), dtype=torch.uint8, device="cuda")
+    sb = torch.ones((2, 1, 1), dtype=torch.float32, device="cuda")
+    off = torch.zeros(3, dtype=torch.int32, device="cuda")
+    bsfp8.bsfp8_grouped_gemm(None, B, None, sb, off, None, 0, 128, 128, 2)
+    assert bsfp8.bsfp8_get_device_error() == 0
+
+
+def _sampled_parity(p, n_points=6000, seed=0):
+    """Full-size workload: every output of a few whole rows at expert boundaries plus
+    random sampled elements, each recomputed by the oracle one by one."""
+    from gpu_util import DeviceProblem
+    import block_scaled_fp8_persistent_gb300 as bsfp8
+    d = DeviceProblem(p)
+    d.run()
+    got = d.c_bits()
+    assert bsfp8.bsfp8_get_device_error() == 0
+    rng = np.random.default_rng(seed)
+    off = p.offsets.astype(np.int64)
+    edge_rows = sorted({int(r) for e in range(p.E) if off[e + 1] > off[e]
+                        for r in (off[e], off[e + 1] - 1)})[:16]
+    rows = np.concatenate([np.repeat(edge_rows, p.N), rng.integers(0, p.M_total, n_points)])
+    cols = np.concatenate([np.tile(np.arange(p.N), len(edge_rows)), rng.integers(0, p.N, n_points)])
+    ref, T = oracle.problem_points(p, rows, cols)
+    bad, ratio, exact = parity_report(got[rows, cols], ref, T)
+    assert bad == 0, f"{bad} sampled elements outside tolerance (max err/tol {ratio:.3g})"
+    return got
+
+
+@pytest.mark.parametrize("cfg", [1, 2, 3])
+def test_full_size_config_sampled(cfg):
+    p = gen.config_problem(cfg)
+    _sampled_parity(p, seed=cfg)
