@@ -1,30 +1,36 @@
-// Blockwise-scaled FP8 grouped GEMM for sm_103a (one CTA per SM, persistent).
+// Blockwise-scaled FP8 grouped GEMM for sm_103a (persistent, warp specialized).
 //
 //   C[m, n] = sum_kb a_scales[kb, m] * b_scales[e, n/128, kb] * sum_{k in kb} A[m,k] B[e,n,k]
 //
 // with e the expert owning row m, 1x128 A scales and 128x128 B scales over K blocks of
 // 128, fp32 accumulation and bf16 output.
 //
-// Structure (prior art: promote_accumulators in MAX kernels grouped_matmul_sm100_blockwise_fp8
-// -- per-K-block TMEM partials promoted with a_scale x b_scale into fp32 register tiles;
-// EpilogueWarpContext in MAX sm100_structured -- epilogue warps consuming a TMEM stage ring
-// per K stage; the warp-specialized partitions of the Triton Gluon example "Overlapping
-// Accumulator Block-Scaled Matrix Multiplication"):
+// Prior art followed (and where this differs):
+//  * promote_accumulators (MAX kernels, grouped_matmul_sm100_blockwise_fp8): every K block
+//    produces a TMEM partial that the epilogue warps multiply by a_scale x b_scale and add
+//    into fp32 register tiles; the B scale is read from global memory.
+//  * EpilogueWarpContext.per_k_stage (MAX sm100_structured): the epilogue consumes one
+//    TMEM stage per K iteration and signals the MMA warp when it is free.
+//  * Triton Gluon example "Overlapping Accumulator Block-Scaled Matrix Multiplication":
+//    load / MMA / epilogue partitions, persistent static tile stride, 2-CTA tiles.
 //
-//   warp 0       TMA producer: per K block, A tile [128 x 128] and B tile [256 x 128]
-//                (e4m3, 128-byte swizzle) into a 4-stage shared-memory ring.
-//   warp 1       TMEM owner + MMA issuer: per K block, 4 x tcgen05.mma kind::f8f6f4
-//                (M=128, N=256, K=32) into a fresh TMEM partial (2-stage ring, 2 x 256
-//                columns = all 512); commits release the SMEM stage and publish the partial.
-//   warps 4-11   epilogue: warp w reads TMEM lanes 32*(w%4).. (its rows) and columns
-//                128*((w-4)/4).. (its column half); per K block it loads the fp32 partial,
-//                releases the TMEM stage and promotes acc = fma(sa*sb, partial, acc) in
-//                registers (128 per thread); after the last K block it rounds to bf16 and
-//                stores the rows that belong to the tile's expert.
+// Roles (one CTA = 12 warps):
+//   warp 0       TMA producer: per K block, this CTA's A rows [128 x 128] and its share of
+//                B rows [BN/CG x 128] (e4m3, 128-byte swizzle) into a STAGES-deep ring.
+//   warp 1       TMEM owner; in the MMA CTA (rank 0 of the pair) the single issuing thread:
+//                per K block 4 x tcgen05.mma kind::f8f6f4 (K = 32 each) into a fresh TMEM
+//                partial (ACC_STAGES-deep ring of BN columns).
+//   warps 4-11   epilogue: warp w reads TMEM lanes 32*(w%4).. (rows) and columns
+//                (BN/2)*((w-4)/4).. ; per K block it loads its partial, hands the TMEM stage
+//                back, and promotes acc = fma(sa*sb, partial, acc) in registers.  After the
+//                last K block it rounds to bf16 and stores the rows of the tile's expert.
 //
-// The A and B scales are read by the epilogue from global memory one K block ahead (the
-// page reads b_scale from global memory and stages the A-scale strip in SMEM; here both
-// come through the read-only cache, which keeps the SMEM ring free for operands).
+// CG = 2 runs a CTA pair (cluster of 2) on a 256 x BN tile: each CTA loads its own 128 A
+// rows and half of the B rows (no multicast), the pair MMA (M = 256) reads both halves,
+// the TMA completions of both CTAs are counted on the leader's barrier, and the leader's
+// commits arrive on both CTAs' barriers.  Each CTA promotes and stores its own 128 rows.
+//
+// A and B scales reach the epilogue through the read-only cache, one K block ahead.
 #include <cuda_bf16.h>
 #include "common.cuh"
 #include "ptx.cuh"
@@ -33,29 +39,44 @@
 namespace bsfp8 {
 namespace bw {
 
-constexpr int BM = 128;
-constexpr int BN = 256;
 constexpr int BK = 128;
-constexpr int STAGES = 4;
-constexpr int ACC_STAGES = 2;
 constexpr int NUM_THREADS = 384;
 constexpr int EPI_WARP0 = 4;
 constexpr int NUM_EPI_WARPS = 8;
-constexpr int COLS_PER_WARP = BN / 2;  // two epilogue warps share each 32-lane quarter
 constexpr uint32_t TMEM_COLS = 512;
-static_assert(ACC_STAGES * BN <= (int)TMEM_COLS, "TMEM ring too large");
 
-constexpr uint32_t A_STAGE = BM * BK;  // 16 KB
-constexpr uint32_t B_STAGE = BN * BK;  // 32 KB
-constexpr uint32_t SMEM_A = 0;
-constexpr uint32_t SMEM_B = SMEM_A + STAGES * A_STAGE;
-constexpr uint32_t SMEM_CTL = SMEM_B + STAGES * B_STAGE;
+template <int CG_, int BN_, int STAGES_, int ACC_STAGES_>
+struct Cfg {
+  static constexpr int CG = CG_;                  // CTAs per tile (1 or 2)
+  static constexpr int BN = BN_;                  // tile columns
+  static constexpr int BM = 128 * CG;             // tile rows (128 per CTA)
+  static constexpr int STAGES = STAGES_;          // SMEM ring depth
+  static constexpr int ACC_STAGES = ACC_STAGES_;  // TMEM partial ring depth
+  static constexpr int B_ROWS = BN / CG;          // B rows loaded by each CTA
+  static constexpr int COLS = BN / 2;             // columns per epilogue warp
+  static constexpr int CHUNKS = COLS / 16;        // 16-column chunks per warp
+  // all of a warp's columns fit in registers next to its accumulators: load them all,
+  // release the TMEM stage, then promote
+  static constexpr bool LOAD_ALL = COLS <= 96;
+  static constexpr uint32_t A_STAGE = 128 * BK;
+  static constexpr uint32_t B_STAGE = B_ROWS * BK;
+  static constexpr uint32_t STAGE_TX = (A_STAGE + B_STAGE) * CG;  // bytes per stage, pair
+  static constexpr uint32_t SMEM_A = 0;
+  static constexpr uint32_t SMEM_B = SMEM_A + STAGES * A_STAGE;
+  static constexpr uint32_t SMEM_CTL = SMEM_B + STAGES * B_STAGE;
+  static constexpr uint32_t IDESC = idesc_f8f6f4_e4m3(BM, BN);
+  static_assert(ACC_STAGES * BN <= (int)TMEM_COLS, "TMEM ring too large");
+  static_assert(COLS % 16 == 0 && BN % 16 == 0 && B_ROWS % 8 == 0, "tile shape");
+  static_assert(LOAD_ALL || COLS % 64 == 0, "two-phase epilogue works in 64-column halves");
+  static_assert(B_STAGE % 1024 == 0, "128-byte-swizzle atoms need 1024-byte stages");
+};
 
+template <class C>
 struct Ctl {
-  uint64_t full[STAGES];
-  uint64_t empty[STAGES];
-  uint64_t tfull[ACC_STAGES];
-  uint64_t tempty[ACC_STAGES];
+  uint64_t full[C::STAGES];
+  uint64_t empty[C::STAGES];
+  uint64_t tfull[C::ACC_STAGES];
+  uint64_t tempty[C::ACC_STAGES];
   uint64_t mma_done;
   uint32_t tmem_base;
   int abort;
@@ -63,47 +84,58 @@ struct Ctl {
   int pad;
   long long total_tiles;
 };
-constexpr uint32_t SMEM_BYTES = SMEM_CTL + sizeof(Ctl) + 1024;  // + alignment slack
-static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
-constexpr uint32_t IDESC = idesc_f8f6f4_e4m3(BM, BN);
+template <class C>
+constexpr uint32_t smem_bytes() {
+  return C::SMEM_CTL + sizeof(Ctl<C>) + 1024;  // + alignment slack
+}
 
 __device__ __forceinline__ void record_error(int* err, int code, volatile int* abort) {
   atomicCAS(err, 0, code);
   *abort = 1;
 }
 
+// Promote 16 columns: acc[j] = fma(s, partial[j], acc[j]).
+__device__ __forceinline__ void promote16(float* acc, const uint32_t* p, float s) {
+#pragma unroll
+  for (int j = 0; j < 16; ++j) acc[j] = fmaf(s, __uint_as_float(p[j]), acc[j]);
+}
+
+template <class C>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 bsfp8_blockwise_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB, const GemmArgs args) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  Ctl* ctl = reinterpret_cast<Ctl*>(smem + SMEM_CTL);
+  Ctl<C>* ctl = reinterpret_cast<Ctl<C>*>(smem + C::SMEM_CTL);
   volatile int* abort = &ctl->abort;
   const uint32_t warp = threadIdx.x >> 5;
   const uint32_t lane = threadIdx.x & 31;
   const int KB = args.K / BK;
+  const uint32_t rank = (C::CG == 2) ? cluster_ctarank() : 0;  // 0 = MMA CTA of the pair
+  const int64_t tile0 = blockIdx.x / C::CG;                    // this pair's first tile
+  const int64_t tile_stride = gridDim.x / C::CG;
 
-  // ---- work discovery: validate the offsets, count tiles -------------------------------
+  // ---- work discovery: validate the offsets, count tiles (same answer in every CTA) ----
   if (warp == 0) {
     int ok;
     int64_t row_tiles;
-    validate_offsets<BM>(args.offsets, args.E, args.M_total, ok, row_tiles);
+    validate_offsets<C::BM>(args.offsets, args.E, args.M_total, ok, row_tiles);
     if (lane == 0) {
       ctl->valid = ok;
-      ctl->total_tiles = row_tiles * ((args.N + BN - 1) / BN);
+      ctl->total_tiles = row_tiles * ((args.N + C::BN - 1) / C::BN);
       ctl->abort = 0;
       if (!ok && blockIdx.x == 0) atomicCAS(args.err, 0, DEV_BAD_OFFSETS);
     }
   }
   __syncthreads();
   const int64_t total_tiles = ctl->total_tiles;
-  if (!ctl->valid || (int64_t)blockIdx.x >= total_tiles) return;
+  if (!ctl->valid || tile0 >= total_tiles) return;  // both CTAs of a pair agree
 
   // ---- setup: barriers, TMEM ---------------------------------------------------------
-  const uint32_t sA = smem_u32(smem + SMEM_A);
-  const uint32_t sB = smem_u32(smem + SMEM_B);
+  const uint32_t sA = smem_u32(smem + C::SMEM_A);
+  const uint32_t sB = smem_u32(smem + C::SMEM_B);
   auto full_bar = [&](int s) { return smem_u32(&ctl->full[s]); };
   auto empty_bar = [&](int s) { return smem_u32(&ctl->empty[s]); };
   auto tfull_bar = [&](int s) { return smem_u32(&ctl->tfull[s]); };
@@ -112,136 +144,160 @@ bsfp8_blockwise_kernel(const __grid_constant__ CUtensorMap tmA,
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), 1);
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(full_bar(s), 1);   // the leader's producer arrives (+ both CTAs' bytes)
+      mbar_init(empty_bar(s), 1);  // one MMA commit
     }
-    for (int s = 0; s < ACC_STAGES; ++s) {
-      mbar_init(tfull_bar(s), 1);
-      mbar_init(tempty_bar(s), NUM_EPI_WARPS);
+    for (int s = 0; s < C::ACC_STAGES; ++s) {
+      mbar_init(tfull_bar(s), 1);                       // one MMA commit
+      mbar_init(tempty_bar(s), NUM_EPI_WARPS * C::CG);  // every epilogue warp of the pair
     }
     mbar_init(smem_u32(&ctl->mma_done), 1);
     fence_mbarrier_init();
   }
   if (warp == 1) {
-    tmem_alloc<1>(smem_u32(&ctl->tmem_base), TMEM_COLS);
-    tmem_relinquish<1>();
+    tmem_alloc<C::CG>(smem_u32(&ctl->tmem_base), TMEM_COLS);
+    tmem_relinquish<C::CG>();
   }
   tc_fence_before();
   __syncthreads();
+  if constexpr (C::CG == 2) cluster_sync();  // peer barriers initialised before any use
   tc_fence_after();
   const uint32_t tmem_base = ctl->tmem_base;
 
   if (warp < EPI_WARP0) {
-    // warpgroup 0: producer, MMA issuer and two idle warps give registers away
+    // warpgroup 0 (producer, MMA issuer, two idle warps) gives registers away
     asm volatile("setmaxnreg.dec.sync.aligned.u32 40;");
-    if (warp == 0) {
-    // =============================== TMA producer ===============================
-    if (lane == 0) {
-      GroupedScheduler<BM, BN> sched(args.offsets, args.E, args.N);
+    if (warp == 0 && lane == 0) {
+      // =============================== TMA producer ===============================
+      GroupedScheduler<C::BM, C::BN> sched(args.offsets, args.E, args.N);
+      // B (expert weights) is re-read by every row tile of its expert, possibly in a later
+      // wave of tiles: keep it in L2 ahead of the streaming A rows and C output.
+      const uint64_t pol_b = l2_policy_evict_last();
       uint32_t stage = 0, phase = 0;
       int64_t issued = 0;
       bool ok = true;
       TileCoord tc;
-      for (int64_t t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
+      for (int64_t t = tile0; ok && t < total_tiles; t += tile_stride) {
         if (!sched.locate(t, tc)) break;
-        const int32_t a_row = (int32_t)tc.m0;
-        const int32_t b_row = tc.e * args.N + tc.n0;
+        const int32_t a_row = (int32_t)(tc.m0 + 128 * rank);
+        const int32_t b_row = tc.e * args.N + tc.n0 + C::B_ROWS * rank;
         for (int kb = 0; kb < KB; ++kb) {
-          if (!mbar_wait(empty_bar(stage), phase ^ 1, abort)) {
+          if (!mbar_wait_cg<C::CG>(empty_bar(stage), phase ^ 1, abort)) {
             record_error(args.err, DEV_TIMEOUT, abort);
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(full_bar(stage), A_STAGE + B_STAGE);
-          tma_load_2d(sA + stage * A_STAGE, &tmA, kb * BK, a_row, full_bar(stage));
-          tma_load_2d(sB + stage * B_STAGE, &tmB, kb * BK, b_row, full_bar(stage));
+          if constexpr (C::CG == 1) {
+            mbar_arrive_expect_tx(full_bar(stage), C::STAGE_TX);
+            tma_load_2d(sA + stage * C::A_STAGE, &tmA, kb * BK, a_row, full_bar(stage));
+            tma_load_2d_hint(sB + stage * C::B_STAGE, &tmB, kb * BK, b_row, full_bar(stage), pol_b);
+          } else {
+            // both CTAs' bytes are counted on the leader's barrier
+            const uint32_t bar = mapa_shared(full_bar(stage), 0);
+            if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), C::STAGE_TX);
+            tma_load_2d_pair(sA + stage * C::A_STAGE, &tmA, kb * BK, a_row, bar);
+            tma_load_2d_pair_hint(sB + stage * C::B_STAGE, &tmB, kb * BK, b_row, bar, pol_b);
+          }
           ++issued;
-          if (++stage == STAGES) { stage = 0; phase ^= 1; }
+          if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
         }
       }
-      // Let the last loads land before the CTA can exit (they are complete already on
-      // the normal path; after an abort they finish within microseconds).
-      const int64_t pending = issued < STAGES ? issued : STAGES;
+      // Let this CTA's last loads land before it can exit.  In the leader they complete
+      // its full barrier; in the peer, the MMA consuming them frees its empty barrier.
+      const int64_t pending = issued < C::STAGES ? issued : C::STAGES;
       for (int64_t i = 0; i < pending; ++i) {
-        stage = (stage + STAGES - 1) % STAGES;
-        if (stage == STAGES - 1) phase ^= 1;
-        mbar_wait_timed(full_bar(stage), phase);
+        stage = (stage + C::STAGES - 1) % C::STAGES;
+        if (stage == C::STAGES - 1) phase ^= 1;
+        if (rank == 0) mbar_wait_timed(full_bar(stage), phase);
+        else mbar_wait_timed(empty_bar(stage), phase);
       }
-    }
-    __syncwarp();
-    } else if (warp == 1) {
-    // ================================ MMA issuer ================================
-    if (lane == 0) {
-      GroupedScheduler<BM, BN> sched(args.offsets, args.E, args.N);
+    } else if (warp == 1 && lane == 0 && rank == 0) {
+      // ================================ MMA issuer ================================
+      GroupedScheduler<C::BM, C::BN> sched(args.offsets, args.E, args.N);
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
       TileCoord tc;
-      for (int64_t t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
+      for (int64_t t = tile0; ok && t < total_tiles; t += tile_stride) {
         if (!sched.locate(t, tc)) break;
         for (int kb = 0; kb < KB; ++kb) {
-          if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1, abort) ||
-              !mbar_wait(full_bar(stage), phase, abort)) {
+          if (!mbar_wait_cg<C::CG>(tempty_bar(acc), acc_phase ^ 1, abort) ||
+              !mbar_wait_cg<C::CG>(full_bar(stage), phase, abort)) {
             record_error(args.err, DEV_TIMEOUT, abort);
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t d_tmem = tmem_base + acc * BN;
-          const uint64_t adesc = kmajor_sw128_desc(sA + stage * A_STAGE);
-          const uint64_t bdesc = kmajor_sw128_desc(sB + stage * B_STAGE);
+          const uint32_t d_tmem = tmem_base + acc * C::BN;
+          const uint64_t adesc = kmajor_sw128_desc(sA + stage * C::A_STAGE);
+          const uint64_t bdesc = kmajor_sw128_desc(sB + stage * C::B_STAGE);
 #pragma unroll
           for (int k = 0; k < BK / 32; ++k)  // K = 32 e4m3 per instruction, 32 bytes
-            umma_f8f6f4<1>(d_tmem, adesc + (uint64_t)(k * 2), bdesc + (uint64_t)(k * 2), IDESC,
-                           k > 0 ? 1u : 0u);
-          umma_commit(empty_bar(stage));  // operands consumed -> stage free
-          umma_commit(tfull_bar(acc));    // partial ready for the epilogue
-          if (++stage == STAGES) { stage = 0; phase ^= 1; }
-          if (++acc == ACC_STAGES) { acc = 0; acc_phase ^= 1; }
+            umma_f8f6f4<C::CG>(d_tmem, adesc + (uint64_t)(k * 2), bdesc + (uint64_t)(k * 2),
+                               C::IDESC, k > 0 ? 1u : 0u);
+          if constexpr (C::CG == 1) {
+            umma_commit(empty_bar(stage));  // operands consumed -> stage free
+            umma_commit(tfull_bar(acc));    // partial ready for the epilogue
+          } else {
+            umma_commit_pair(empty_bar(stage), 0x3);
+            umma_commit_pair(tfull_bar(acc), 0x3);
+          }
+          if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
+          if (++acc == C::ACC_STAGES) { acc = 0; acc_phase ^= 1; }
         }
       }
       // Every MMA this thread issued has finished before TMEM is released.
-      umma_commit(smem_u32(&ctl->mma_done));
+      if constexpr (C::CG == 1) umma_commit(smem_u32(&ctl->mma_done));
+      else umma_commit_pair(smem_u32(&ctl->mma_done), 0x1);
       mbar_wait_timed(smem_u32(&ctl->mma_done), 0);
     }
     __syncwarp();
-    }
   } else {
     // ================================= epilogue =================================
     asm volatile("setmaxnreg.inc.sync.aligned.u32 232;");
     const uint32_t ew = warp - EPI_WARP0;
-    const uint32_t quarter = warp & 3;         // TMEM lanes 32*quarter .. +31
-    const uint32_t half = ew >> 2;             // columns half*128 .. +127
+    const uint32_t quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
+    const uint32_t half = ew >> 2;      // columns half*COLS .. +COLS-1
     const int nblk = args.N / 128;
     const float* a_scales = static_cast<const float*>(args.a_scales);
     const float* b_scales = static_cast<const float*>(args.b_scales);
-    __nv_bfloat16* C = static_cast<__nv_bfloat16*>(args.C);
-    GroupedScheduler<BM, BN> sched(args.offsets, args.E, args.N);
+    __nv_bfloat16* Cmat = static_cast<__nv_bfloat16*>(args.C);
+    // the MMA CTA's barrier that collects "TMEM stage drained" from both CTAs
+    auto tempty_mma = [&](int s) {
+      return (C::CG == 2) ? mapa_shared(tempty_bar(s), 0) : tempty_bar(s);
+    };
+    GroupedScheduler<C::BM, C::BN> sched(args.offsets, args.E, args.N);
     uint32_t acc_stage = 0, acc_phase = 0;
     bool ok = true;
     TileCoord tc;
-    for (int64_t t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
+    for (int64_t t = tile0; ok && t < total_tiles; t += tile_stride) {
       if (!sched.locate(t, tc)) break;
-      const int64_t row = tc.m0 + quarter * 32 + lane;
+      const int64_t row = tc.m0 + 128 * rank + quarter * 32 + lane;
       const bool row_in = row < args.M_total;
-      // N % 256 == 128: the second half of the last column tile is past N
-      const bool cols_in = tc.n0 + (int)half * COLS_PER_WARP < args.N;
+      const int col0 = tc.n0 + (int)half * C::COLS;  // first column of this warp
+      // this warp's columns touch scale blocks col0/128 and (col0+COLS-1)/128 (<= 2)
+      const int blk_lo = col0 / 128;
+      const int blk_hi = (col0 + C::COLS - 1) / 128;
+      const bool lo_in = blk_lo < nblk, hi_in = blk_hi < nblk;
       const float* sa_ptr = a_scales + (row_in ? row : 0);
-      const float* sb_ptr =
-          cols_in ? b_scales + ((int64_t)tc.e * nblk + (tc.n0 + half * COLS_PER_WARP) / 128) * KB
-                  : b_scales;
-      float acc[COLS_PER_WARP];
+      const float* sb_lo = b_scales + ((int64_t)tc.e * nblk + (lo_in ? blk_lo : 0)) * KB;
+      const float* sb_hi = b_scales + ((int64_t)tc.e * nblk + (hi_in ? blk_hi : 0)) * KB;
+      float acc[C::COLS];
 #pragma unroll
-      for (int j = 0; j < COLS_PER_WARP; ++j) acc[j] = 0.0f;
-      float sa_next = row_in ? ldg_f32(sa_ptr) : 0.0f;
-      float sb_next = ldg_f32(sb_ptr);
+      for (int j = 0; j < C::COLS; ++j) acc[j] = 0.0f;
+      float sa_n = row_in ? ldg_f32(sa_ptr) : 0.0f;
+      float sbl_n = lo_in ? ldg_f32(sb_lo) : 0.0f;
+      float sbh_n = hi_in ? ldg_f32(sb_hi) : 0.0f;
       for (int kb = 0; kb < KB; ++kb) {
-        const float s = sa_next * sb_next;
+        const float s_lo = sa_n * sbl_n;
+        const float s_hi = sa_n * sbh_n;
         if (kb + 1 < KB) {
-          sa_next = row_in ? ldg_f32(sa_ptr + (int64_t)(kb + 1) * args.M_total) : 0.0f;
-          sb_next = cols_in ? ldg_f32(sb_ptr + kb + 1) : 0.0f;
+          sa_n = row_in ? ldg_f32(sa_ptr + (int64_t)(kb + 1) * args.M_total) : 0.0f;
+          sbl_n = lo_in ? ldg_f32(sb_lo + kb + 1) : 0.0f;
+          sbh_n = hi_in ? ldg_f32(sb_hi + kb + 1) : 0.0f;
         }
-        const bool got = __all_sync(0xffffffffu, mbar_wait(tfull_bar(acc_stage), acc_phase, abort));
+        const bool got = __all_sync(
+            0xffffffffu, mbar_wait_cg<C::CG>(tfull_bar(acc_stage), acc_phase, abort));
         if (!got) {
           if (lane == 0) record_error(args.err, DEV_TIMEOUT, abort);
           ok = false;
@@ -249,38 +305,56 @@ bsfp8_blockwise_kernel(const __grid_constant__ CUtensorMap tmA,
         }
         tc_fence_after();
         const uint32_t taddr =
-            tmem_base + ((quarter * 32) << 16) + acc_stage * BN + half * COLS_PER_WARP;
-        uint32_t p0[32], p1[32];
-        tmem_ld_32x32b_x32(taddr + 0, p0);
-        tmem_ld_32x32b_x32(taddr + 32, p1);
-        tmem_ld_wait();
+            tmem_base + ((quarter * 32) << 16) + acc_stage * C::BN + half * C::COLS;
+        // 16-column chunks never straddle a 128-column scale block
+        auto chunk_scale = [&](int c) { return ((col0 + 16 * c) / 128 == blk_lo) ? s_lo : s_hi; };
+        if constexpr (C::LOAD_ALL) {
+          uint32_t p[C::CHUNKS][16];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          acc[j] = fmaf(s, __uint_as_float(p0[j]), acc[j]);
-          acc[32 + j] = fmaf(s, __uint_as_float(p1[j]), acc[32 + j]);
-        }
-        tmem_ld_32x32b_x32(taddr + 64, p0);
-        tmem_ld_32x32b_x32(taddr + 96, p1);
-        tmem_ld_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(tempty_bar(acc_stage));
+          for (int c = 0; c < C::CHUNKS; ++c) tmem_ld_32x32b_x16(taddr + 16 * c, p[c]);
+          tmem_ld_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive_cluster_or_local<C::CG>(tempty_mma(acc_stage));
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          acc[64 + j] = fmaf(s, __uint_as_float(p0[j]), acc[64 + j]);
-          acc[96 + j] = fmaf(s, __uint_as_float(p1[j]), acc[96 + j]);
+          for (int c = 0; c < C::CHUNKS; ++c) promote16(acc + 16 * c, p[c], chunk_scale(c));
+        } else {
+          // 64-column halves: load, promote, ..., load the last half, release, promote
+          uint32_t p0[32], p1[32];
+#pragma unroll
+          for (int h = 0; h < C::COLS / 64; ++h) {
+            tmem_ld_32x32b_x32(taddr + 64 * h, p0);
+            tmem_ld_32x32b_x32(taddr + 64 * h + 32, p1);
+            tmem_ld_wait();
+            if (h == C::COLS / 64 - 1) {
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive_cluster_or_local<C::CG>(tempty_mma(acc_stage));
+            }
+            promote16(acc + 64 * h + 0, p0, chunk_scale(4 * h + 0));
+            promote16(acc + 64 * h + 16, p0 + 16, chunk_scale(4 * h + 1));
+            promote16(acc + 64 * h + 32, p1, chunk_scale(4 * h + 2));
+            promote16(acc + 64 * h + 48, p1 + 16, chunk_scale(4 * h + 3));
+          }
         }
-        if (++acc_stage == ACC_STAGES) { acc_stage = 0; acc_phase ^= 1; }
+        if (++acc_stage == C::ACC_STAGES) { acc_stage = 0; acc_phase ^= 1; }
       }
       if (!ok) break;
-      if (row < tc.m_end && cols_in) {
-        __nv_bfloat16* dst = C + row * (int64_t)args.N + tc.n0 + half * COLS_PER_WARP;
+      if (row < tc.m_end) {
+        // C is written once and not read again here: first out of L2
+        const uint64_t pol_c = l2_policy_evict_first();
+        __nv_bfloat16* dst = Cmat + row * (int64_t)args.N + col0;
 #pragma unroll
-        for (int j = 0; j < COLS_PER_WARP / 8; ++j)
-          st_global_v4(dst + 8 * j, pack_bf16x2(acc[8 * j + 0], acc[8 * j + 1]),
-                       pack_bf16x2(acc[8 * j + 2], acc[8 * j + 3]),
-                       pack_bf16x2(acc[8 * j + 4], acc[8 * j + 5]),
-                       pack_bf16x2(acc[8 * j + 6], acc[8 * j + 7]));
+        for (int c = 0; c < C::CHUNKS; ++c) {
+          if (col0 + 16 * c < args.N) {  // the last column tile may pass N
+            const float* a = acc + 16 * c;
+            st_global_v4_hint(dst + 16 * c, pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]),
+                              pack_bf16x2(a[4], a[5]), pack_bf16x2(a[6], a[7]), pol_c);
+            st_global_v4_hint(dst + 16 * c + 8, pack_bf16x2(a[8], a[9]),
+                              pack_bf16x2(a[10], a[11]), pack_bf16x2(a[12], a[13]),
+                              pack_bf16x2(a[14], a[15]), pol_c);
+          }
+        }
       }
     }
   }
@@ -288,32 +362,80 @@ bsfp8_blockwise_kernel(const __grid_constant__ CUtensorMap tmA,
   // ---- teardown ------------------------------------------------------------------------
   tc_fence_before();
   __syncthreads();
+  // the pair's MMAs and remote arrivals are finished before either CTA frees TMEM or exits
+  if constexpr (C::CG == 2) cluster_sync();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc<1>(tmem_base, TMEM_COLS);
+    tmem_dealloc<C::CG>(tmem_base, TMEM_COLS);
   }
 }
 
-}  // namespace bw
-
-cudaError_t launch_bsfp8_blockwise(const CUtensorMap& tmA, const CUtensorMap& tmB,
-                                   const GemmArgs& args, int num_sms, cudaStream_t stream) {
+template <class C>
+cudaError_t launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& args,
+                   int num_sms, cudaStream_t stream) {
   static bool attr_set[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(bw::bsfp8_blockwise_kernel,
+    cudaError_t e = cudaFuncSetAttribute(bsfp8_blockwise_kernel<C>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)bw::SMEM_BYTES);
+                                         (int)smem_bytes<C>());
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
   // Upper bound of the tile count known on the host (offsets live on the device).
-  const int64_t max_row_tiles = (args.M_total + bw::BM - 1) / bw::BM + args.E;
-  const int64_t max_tiles = max_row_tiles * ((args.N + bw::BN - 1) / bw::BN);
-  const int grid = (int)(max_tiles < num_sms ? max_tiles : num_sms);
-  bw::bsfp8_blockwise_kernel<<<grid, bw::NUM_THREADS, bw::SMEM_BYTES, stream>>>(tmA, tmB, args);
-  return cudaGetLastError();
+  const int64_t max_row_tiles = (args.M_total + C::BM - 1) / C::BM + args.E;
+  const int64_t max_tiles = max_row_tiles * ((args.N + C::BN - 1) / C::BN);
+  const int64_t pairs = num_sms / C::CG;
+  const int grid = (int)((max_tiles < pairs ? max_tiles : pairs) * C::CG);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(NUM_THREADS);
+  cfg.dynamicSmemBytes = smem_bytes<C>();
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = C::CG;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, bsfp8_blockwise_kernel<C>, tmA, tmB, args);
+}
+
+// 1-CTA 128 x 256 (2 TMEM stages), CTA pair 256 x 256 (2 stages), CTA pair 256 x 160
+// (3 stages), CTA pair 256 x 128 (4 stages), 1-CTA 128 x 128 (4 stages).  With 160 or 128
+// columns each epilogue warp loads all of its columns at once and frees the stage early.
+using Cta1x256 = Cfg<1, 256, 4, 2>;
+using Pair256 = Cfg<2, 256, 6, 2>;
+using Pair160 = Cfg<2, 160, 8, 3>;
+using Pair128 = Cfg<2, 128, 8, 4>;
+using Cta1x128 = Cfg<1, 128, 6, 4>;
+
+}  // namespace bw
+
+int blockwise_b_rows(BlockwiseTile tile) {
+  switch (tile) {
+    case TILE_CTA1_256: return bw::Cta1x256::B_ROWS;
+    case TILE_PAIR_256: return bw::Pair256::B_ROWS;
+    case TILE_PAIR_160: return bw::Pair160::B_ROWS;
+    case TILE_PAIR_128: return bw::Pair128::B_ROWS;
+    case TILE_CTA1_128: return bw::Cta1x128::B_ROWS;
+  }
+  return 0;
+}
+
+cudaError_t launch_bsfp8_blockwise(BlockwiseTile tile, const CUtensorMap& tmA,
+                                   const CUtensorMap& tmB, const GemmArgs& args, int num_sms,
+                                   cudaStream_t stream) {
+  switch (tile) {
+    case TILE_CTA1_256: return bw::launch<bw::Cta1x256>(tmA, tmB, args, num_sms, stream);
+    case TILE_PAIR_256: return bw::launch<bw::Pair256>(tmA, tmB, args, num_sms, stream);
+    case TILE_PAIR_160: return bw::launch<bw::Pair160>(tmA, tmB, args, num_sms, stream);
+    case TILE_PAIR_128: return bw::launch<bw::Pair128>(tmA, tmB, args, num_sms, stream);
+    case TILE_CTA1_128: return bw::launch<bw::Cta1x128>(tmA, tmB, args, num_sms, stream);
+  }
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace bsfp8

@@ -1,5 +1,7 @@
 // C-ABI entry points: argument checks on the host, tensor-map encoding, kernel launch.
 // Declarations and the contract live in include/bsfp8.h.
+#include <cstdlib>
+#include <cstring>
 #include <mutex>
 
 #include "bsfp8.h"
@@ -98,6 +100,25 @@ bsfp8_status check_common(const void* A, const void* B, const void* sa, const vo
   return BSFP8_OK;
 }
 
+// Tile configuration for a launch.  The 1-CTA 128 x 256 tile is the default: measured on
+// GB300 it is the fastest on every workload tried (the CTA-pair 256 x 256 tile moves fewer
+// operand bytes but is bound by the same per-K-block TMEM hand-off, and the 160/128-column
+// tiles lose more to the fixed cost of each K = 32 MMA than they gain from a deeper TMEM
+// ring).  The environment variable BSFP8_BLOCKWISE_TILE (cta1_256 | pair_256 | pair_160 |
+// pair_128 | cta1_128) selects another one.
+BlockwiseTile choose_blockwise_tile(int64_t M_total, int E) {
+  if (const char* v = std::getenv("BSFP8_BLOCKWISE_TILE")) {
+    if (!std::strcmp(v, "cta1_256")) return TILE_CTA1_256;
+    if (!std::strcmp(v, "pair_256")) return TILE_PAIR_256;
+    if (!std::strcmp(v, "pair_160")) return TILE_PAIR_160;
+    if (!std::strcmp(v, "pair_128")) return TILE_PAIR_128;
+    if (!std::strcmp(v, "cta1_128")) return TILE_CTA1_128;
+  }
+  (void)M_total;
+  (void)E;
+  return TILE_CTA1_256;
+}
+
 }  // namespace
 }  // namespace bsfp8
 
@@ -113,12 +134,14 @@ extern "C" bsfp8_status bsfp8_grouped_gemm(const void* A, const void* B, const f
   DeviceInfo* dev = nullptr;
   if ((st = device_info(&dev)) != BSFP8_OK) return st;
   if (M_total == 0) return BSFP8_OK;
+  const BlockwiseTile tile = choose_blockwise_tile(M_total, num_experts);
   CUtensorMap tmA, tmB;
   if (!encode_u8_2d(&tmA, A, (uint64_t)K, (uint64_t)M_total, 128, 128) ||
-      !encode_u8_2d(&tmB, B, (uint64_t)K, (uint64_t)num_experts * N, 128, 256))
+      !encode_u8_2d(&tmB, B, (uint64_t)K, (uint64_t)num_experts * N, 128,
+                    (uint32_t)blockwise_b_rows(tile)))
     return BSFP8_ERR_CUDA;
   GemmArgs args{expert_offsets, a_scales, b_scales, C, M_total, N, K, num_experts, dev->err_word};
-  return launch_bsfp8_blockwise(tmA, tmB, args, dev->num_sms, stream) == cudaSuccess
+  return launch_bsfp8_blockwise(tile, tmA, tmB, args, dev->num_sms, stream) == cudaSuccess
              ? BSFP8_OK
              : BSFP8_ERR_CUDA;
 }

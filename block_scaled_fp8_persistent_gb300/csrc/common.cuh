@@ -25,8 +25,21 @@ struct GemmArgs {
   int* err;                // library-owned device error word
 };
 
+// Tile configurations of the blockwise kernel.
+enum BlockwiseTile : int {
+  TILE_CTA1_256 = 0,  // one CTA, 128 x 256 tile
+  TILE_PAIR_256 = 1,  // CTA pair, 256 x 256 tile
+  TILE_PAIR_160 = 2,  // CTA pair, 256 x 160 tile, 3-deep TMEM ring
+  TILE_PAIR_128 = 3,  // CTA pair, 256 x 128 tile, 4-deep TMEM ring
+  TILE_CTA1_128 = 4,  // one CTA, 128 x 128 tile, 4-deep TMEM ring
+};
+
+// Rows of B each CTA loads per stage (the B tensor map's box height) for a tile config.
+int blockwise_b_rows(BlockwiseTile tile);
+
 // Launchers (one per kernel family); return the launch error.
-cudaError_t launch_bsfp8_blockwise(const CUtensorMap& tmA, const CUtensorMap& tmB,
-                                   const GemmArgs& args, int num_sms, cudaStream_t stream);
+cudaError_t launch_bsfp8_blockwise(BlockwiseTile tile, const CUtensorMap& tmA,
+                                   const CUtensorMap& tmB, const GemmArgs& args, int num_sms,
+                                   cudaStream_t stream);
 
 }  // namespace bsfp8

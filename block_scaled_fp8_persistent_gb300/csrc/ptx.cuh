@@ -48,10 +48,12 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
-// Arrive on a barrier of another CTA of the cluster (address from mapa).
+// Arrive on a barrier of another CTA of the cluster (address from mapa).  Default
+// (CTA-scope release) semantics: what this arrival publishes is that this thread's TMEM
+// reads are finished (tcgen05.wait::ld + tcgen05.fence::before_thread_sync), not data in
+// generic memory, so no cluster-scope fence is needed on this hot path.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
-               : "memory");
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
 }
 
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
@@ -123,6 +125,15 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
   }
 }
 
+// Waits of the CTA-pair kernels.  The arrivals they observe come from TMA completions,
+// tcgen05.commit of the pair's MMAs, or the peer's epilogue signalling finished TMEM
+// reads; the tensor-memory ordering is carried by tcgen05 fences and the async proxy, so
+// the default CTA-scope acquire is used as for a single CTA.
+template <int CG>
+__device__ __forceinline__ bool mbar_wait_cg(uint32_t bar, uint32_t parity, volatile int* abort) {
+  return mbar_wait(bar, parity, abort);
+}
+
 // ---------------------------------------------------------------------------
 // cluster helpers
 // ---------------------------------------------------------------------------
@@ -141,6 +152,14 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t cta) {
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
                    : "memory");
+}
+
+// Arrive on a barrier given as a shared::cluster address (CG == 2, may be the peer CTA's)
+// or as this CTA's shared address (CG == 1).
+template <int CG>
+__device__ __forceinline__ void mbar_arrive_cluster_or_local(uint32_t bar) {
+  if constexpr (CG == 2) mbar_arrive_cluster(bar);
+  else mbar_arrive(bar);
 }
 
 // ---------------------------------------------------------------------------
@@ -179,6 +198,15 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void* tmap,
       "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d_pair_hint(uint32_t dst, const void* tmap, int32_t x,
+                                                      int32_t y, uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar), "l"(policy)
       : "memory");
 }
 
@@ -389,6 +417,14 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 __device__ __forceinline__ void st_global_v4(void* p, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
   asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(a), "r"(b), "r"(c), "r"(d)
+               : "memory");
+}
+
+// 16-byte store with an L2 eviction-priority policy (createpolicy).
+__device__ __forceinline__ void st_global_v4_hint(void* p, uint32_t a, uint32_t b, uint32_t c,
+                                                  uint32_t d, uint64_t policy) {
+  asm volatile("st.global.L2::cache_hint.v4.b32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "r"(a),
+               "r"(b), "r"(c), "r"(d), "l"(policy)
                : "memory");
 }
 

@@ -42,15 +42,18 @@ inline uint64_t mix64(uint64_t z) {
   z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
   return z ^ (z >> 31);
 }
+inline uint64_t stream_key(uint64_t seed, uint64_t stream) {
+  return mix64(seed * 0x9E3779B97F4A7C15ull + stream * 0xD1B54A32D192ED03ull + 1);
+}
+inline uint64_t hash_k(uint64_t key, uint64_t ctr) { return mix64(key ^ mix64(ctr + 0x632BE59BD9B4E019ull)); }
 inline uint64_t hash3(uint64_t seed, uint64_t stream, uint64_t ctr) {
-  const uint64_t key = mix64(seed * 0x9E3779B97F4A7C15ull + stream * 0xD1B54A32D192ED03ull + 1);
-  return mix64(key ^ mix64(ctr + 0x632BE59BD9B4E019ull));
+  return hash_k(stream_key(seed, stream), ctr);
 }
 // Uniform in [0, 1) with 53 random bits.
 inline double unit(uint64_t h) { return (double)(h >> 11) * (1.0 / 9007199254740992.0); }
 
 // Natural logarithm for x > 0 (finite), from frexp and the atanh series
-// ln(m) = 2*(t + t^3/3 + ... + t^19/19), t = (m-1)/(m+1), m in [sqrt(1/2), sqrt(2)].
+// ln(m) = 2*t*(1 + t^2/3 + ... + t^18/19), t = (m-1)/(m+1), m in [sqrt(1/2), sqrt(2)].
 double my_log(double x) {
   int e;
   double m = std::frexp(x, &e);  // x = m * 2^e, m in [0.5, 1)
@@ -62,12 +65,13 @@ double my_log(double x) {
   }
   const double t = (m - 1.0) / (m + 1.0);
   const double t2 = t * t;
-  double term = t, sum = 0.0;
-  for (int k = 1; k <= 19; k += 2) {
-    sum += term / (double)k;
-    term *= t2;
-  }
-  return 2.0 * sum + (double)e * 0.6931471805599453;
+  // Horner form of 1 + t2/3 + t2^2/5 + ... + t2^9/19 (coefficients rounded to double)
+  static const double inv_odd[10] = {1.0,        1.0 / 3.0,  1.0 / 5.0,  1.0 / 7.0,
+                                     1.0 / 9.0,  1.0 / 11.0, 1.0 / 13.0, 1.0 / 15.0,
+                                     1.0 / 17.0, 1.0 / 19.0};
+  double poly = inv_odd[9];
+  for (int i = 8; i >= 0; --i) poly = poly * t2 + inv_odd[i];
+  return 2.0 * t * poly + (double)e * 0.6931471805599453;
 }
 
 // exp(x) for |x| < 700: x = n*ln2 + r, |r| <= ln2/2, Taylor series of exp(r) to 24 terms.
@@ -84,10 +88,10 @@ double my_exp(double x) {
 
 // Pair j of standard normals for (seed, stream): Marsaglia's polar method, trying up to
 // 64 counter values; the chance of 64 rejections is ~1e-43.
-inline void normal_pair(uint64_t seed, uint64_t stream, uint64_t j, double* z0, double* z1) {
+inline void normal_pair(uint64_t key, uint64_t j, double* z0, double* z1) {
   for (uint64_t t = 0; t < 64; ++t) {
-    const uint64_t h1 = hash3(seed, stream, (j << 7) | (2 * t));
-    const uint64_t h2 = hash3(seed, stream, (j << 7) | (2 * t + 1));
+    const uint64_t h1 = hash_k(key, (j << 7) | (2 * t));
+    const uint64_t h2 = hash_k(key, (j << 7) | (2 * t + 1));
     const double x = 2.0 * unit(h1) - 1.0;
     const double y = 2.0 * unit(h2) - 1.0;
     const double s = x * x + y * y;
@@ -104,9 +108,10 @@ inline void normal_pair(uint64_t seed, uint64_t stream, uint64_t j, double* z0, 
 
 // count fp32 normals for element indices [start, start+count); start and count even.
 void normals(uint64_t seed, uint64_t stream, uint64_t start, uint64_t count, float* out) {
+  const uint64_t key = stream_key(seed, stream);
   for (uint64_t i = 0; i < count; i += 2) {
     double z0, z1;
-    normal_pair(seed, stream, (start + i) >> 1, &z0, &z1);
+    normal_pair(key, (start + i) >> 1, &z0, &z1);
     out[i] = (float)z0;
     out[i + 1] = (float)z1;
   }
@@ -132,7 +137,7 @@ uint8_t e4m3_encode(float xf) {
     E = e2 - 1;  // a in [2^E, 2^(E+1))
     q = std::ldexp(1.0, E - 3);
   }
-  double r = std::nearbyint(a / q);  // a / q is exact
+  double r = std::rint(a / q);  // a / q is exact; default rounding = nearest even
   if (a < 0.015625) {
     // subnormal: value r * 2^-9, r in [0, 8]; r == 8 is 2^-6, the smallest normal.
     if (r >= 8.0) return sign | 0x08;

@@ -14,6 +14,15 @@ from helpers import parity_report
 
 pytestmark = pytest.mark.gpu
 
+TILES = ["cta1_256", "pair_256", "pair_160", "pair_128", "cta1_128"]
+
+
+@pytest.fixture(params=TILES)
+def tile(request, monkeypatch):
+    """Run the test under each tile configuration of the blockwise kernel."""
+    monkeypatch.setenv("BSFP8_BLOCKWISE_TILE", request.param)
+    return request.param
+
 
 def _check_full(p, **kw):
     from gpu_util import DeviceProblem
@@ -40,29 +49,30 @@ SMALL_CASES = [
 
 
 @pytest.mark.parametrize("name,counts,N,K", SMALL_CASES, ids=[c[0] for c in SMALL_CASES])
-def test_small_cases(name, counts, N, K):
+def test_small_cases(name, counts, N, K, tile):
     p = gen.blockwise_problem(counts, N, K, seed=100 + len(name))
     _check_full(p)
 
 
-@pytest.mark.parametrize("counts,N,K", [([200, 0, 57], 256, 1024), ([256], 384, 7168)])
-def test_exact_inputs_bitwise(counts, N, K):
+@pytest.mark.parametrize("counts,N,K", [([200, 0, 57], 256, 1024), ([256], 384, 7168),
+                                         ([600, 3, 333], 640, 640)])
+def test_exact_inputs_bitwise(counts, N, K, tile):
     p = gen.blockwise_problem(counts, N, K, seed=7, exact=True)
     got, ref = _check_full(p)
     assert np.array_equal(got, ref)
 
 
-def test_outlier_rows():
+def test_outlier_rows(tile):
     p = gen.blockwise_problem([300, 212], 256, 512, seed=31, outlier_rows=6)
     _check_full(p)
 
 
-def test_all_experts_empty_but_one():
+def test_all_experts_empty_but_one(tile):
     p = gen.blockwise_problem([0, 0, 0, 77, 0], 256, 256, seed=32)
     _check_full(p)
 
 
-def test_repeated_calls_identical():
+def test_repeated_calls_identical(tile):
     from gpu_util import DeviceProblem
     p = gen.blockwise_problem([100, 29], 256, 512, seed=33)
     d = DeviceProblem(p)
@@ -73,7 +83,7 @@ def test_repeated_calls_identical():
     assert np.array_equal(a, d.c_bits())
 
 
-def test_invalid_offsets_reported_on_device():
+def test_invalid_offsets_reported_on_device(tile):
     from gpu_util import DeviceProblem
     import block_scaled_fp8_persistent_gb300 as bsfp8
     p = gen.blockwise_problem([64, 64], 256, 256, seed=34)
@@ -116,6 +126,6 @@ def _sampled_parity(p, n_points=6000, seed=0):
 
 
 @pytest.mark.parametrize("cfg", [1, 2, 3])
-def test_full_size_config_sampled(cfg):
+def test_full_size_config_sampled(cfg, tile):
     p = gen.config_problem(cfg)
     _sampled_parity(p, seed=cfg)
