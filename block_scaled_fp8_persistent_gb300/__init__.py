@@ -7,6 +7,7 @@ not a GB300 (compute capability 10.3) the calls raise.
     import block_scaled_fp8_persistent_gb300 as bsfp8
     bsfp8.bsfp8_grouped_gemm(A, B, a_scales, b_scales, expert_offsets, C,
                              M_total, N, K, num_experts, stream=None)
+    bsfp8.bsmxfp8_grouped_gemm(...)   # MXFP8: UE8M0 scales per 32 K
 
 Tensors are torch CUDA tensors (or raw device addresses as ints) in the layouts of
 include/bsfp8.h; ``stream`` is a torch.cuda.Stream, a raw cudaStream_t int, or None for
@@ -28,7 +29,8 @@ STATUS_NAMES = {
 }
 
 # Every symbol include/bsfp8.h declares (the CPU test checks the library exports them).
-EXPORTED = ("bsfp8_grouped_gemm", "bsfp8_get_device_error", "bsfp8_status_string")
+EXPORTED = ("bsfp8_grouped_gemm", "bsmxfp8_grouped_gemm", "bsfp8_get_device_error",
+            "bsfp8_status_string")
 
 
 class BsFp8Error(RuntimeError):
@@ -51,6 +53,8 @@ def load_library() -> ctypes.CDLL:
         p, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
         lib.bsfp8_grouped_gemm.argtypes = [p, p, p, p, p, p, i64, i32, i32, i32, p]
         lib.bsfp8_grouped_gemm.restype = i32
+        lib.bsmxfp8_grouped_gemm.argtypes = [p, p, p, p, p, p, i64, i32, i32, i32, p]
+        lib.bsmxfp8_grouped_gemm.restype = i32
         lib.bsfp8_get_device_error.argtypes = [p, ctypes.POINTER(ctypes.c_int)]
         lib.bsfp8_get_device_error.restype = i32
         lib.bsfp8_status_string.argtypes = [i32]
@@ -92,6 +96,16 @@ def bsfp8_grouped_gemm(A, B, a_scales, b_scales, expert_offsets, C, M_total: int
                                            int(K), int(num_experts), _stream(stream))
     if st != BSFP8_OK:
         raise BsFp8Error(st, "bsfp8_grouped_gemm")
+
+
+def bsmxfp8_grouped_gemm(A, B, a_scales, b_scales, expert_offsets, C, M_total: int, N: int,
+                         K: int, num_experts: int, stream=None) -> None:
+    """MXFP8 grouped GEMM (UE8M0 scales per 32 K); see include/bsfp8.h.  Raises BsFp8Error."""
+    st = load_library().bsmxfp8_grouped_gemm(_addr(A), _addr(B), _addr(a_scales), _addr(b_scales),
+                                             _addr(expert_offsets), _addr(C), int(M_total), int(N),
+                                             int(K), int(num_experts), _stream(stream))
+    if st != BSFP8_OK:
+        raise BsFp8Error(st, "bsmxfp8_grouped_gemm")
 
 
 def bsfp8_get_device_error(stream=None) -> int:

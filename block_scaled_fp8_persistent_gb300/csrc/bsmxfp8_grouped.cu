@@ -1,0 +1,370 @@
+// MXFP8 grouped GEMM for sm_103a: e4m3 operands with UE8M0 scales per 32 K elements,
+// applied by the block-scaled tensor-core MMA.
+//
+//   C[m, n] = sum_k A[m,k] * B[e,n,k] * 2^(a_scales[m, k/32] - 127) * 2^(b_scales[e, n, k/32] - 127)
+//
+// Prior art: the Triton Gluon example "Overlapping Accumulator Block-Scaled Matrix
+// Multiplication" -- scale tiles copied SMEM -> TMEM with tcgen05_copy in the 4 x 32 x 4
+// "packed block" arrangement of swizzle_scales_packed_block / unswizzle_scales_shared_memory,
+// then tcgen05_mma_scaled on "e4m3" operands, VEC_SIZE = 32 for uint8 scales; persistent
+// static tile stride; load / MMA / epilogue partitions.  Differences: the scales arrive in
+// their logical row-major layout and are packed on chip; tiles are grouped by expert; and
+// the tile is "swap-AB": the MMA's M operand is 128 rows of the expert's weights B and its
+// N operand is the expert's token rows of A (tn = 32 / 64 / 128), which suits the small
+// per-expert token counts of decode (the swapAB mode of the TileScheduler in the MAX
+// grouped_matmul_sm100_blockwise_fp8 kernels).
+//
+// Roles (8 warps):
+//   warp 0      TMA producer: per K stage (128 K) the weight tile [128 x 128] and the token
+//               tile [tn x 128] (128-byte swizzle) into a STAGES-deep ring.
+//   warp 1      TMEM owner + MMA thread: per stage tcgen05.cp of both scale blocks into
+//               TMEM, then 4 x tcgen05.mma kind::mxf8f6f4.block_scale (K = 32 each, the
+//               scale-factor id picks the byte of the 4-byte scale word), accumulating over
+//               all of K in a 2-deep TMEM accumulator ring.
+//   warp 2      scale loader: per stage each weight / token row's 4 UE8M0 codes (one 4-byte
+//               word, row-major source) are cp.async'ed into the packed 512-byte block
+//               (row r at byte (r%32)*16 + (r/32)*4); a few stages in flight.
+//   warps 4-7   epilogue: warp w holds weight rows 32*(w%4).. of the tile, reads the tn
+//               token columns of the accumulator, rounds to bf16 and stores C[m, n] for the
+//               tile's token rows that belong to the expert.
+#include <cuda_bf16.h>
+#include "common.cuh"
+#include "ptx.cuh"
+#include "sched.cuh"
+
+namespace bsfp8 {
+namespace mx {
+
+constexpr int BK = 128;              // K per stage
+constexpr int WROWS = 128;           // weight rows per tile (MMA M)
+constexpr int NUM_THREADS = 256;
+constexpr int EPI_WARP0 = 4;
+constexpr int SF_BLOCK = 512;        // packed scale block: 128 rows x 4 codes
+constexpr int SCALE_LOOKAHEAD = 4;   // scale stages in flight per loader warp
+
+template <int TN_>
+struct Cfg {
+  static constexpr int TN = TN_;                               // token rows per tile
+  static constexpr uint32_t W_STAGE = WROWS * BK;              // 16 KB
+  static constexpr uint32_t T_STAGE = TN * BK;                 // tn x 128 B
+  static constexpr int STAGES = (TN <= 32) ? 10 : (TN <= 64) ? 8 : 6;
+  static constexpr uint32_t SMEM_W = 0;
+  static constexpr uint32_t SMEM_T = SMEM_W + STAGES * W_STAGE;
+  static constexpr uint32_t SMEM_SFW = SMEM_T + STAGES * T_STAGE;
+  static constexpr uint32_t SMEM_SFT = SMEM_SFW + STAGES * SF_BLOCK;
+  static constexpr uint32_t SMEM_CTL = SMEM_SFT + STAGES * SF_BLOCK;
+  static constexpr uint32_t STAGE_TX = W_STAGE + T_STAGE;
+  // TMEM: 2 accumulators of TN columns, then 2 slots each of weight / token scales (4 cols)
+  static constexpr uint32_t ACC_COLS = 2 * TN;
+  static constexpr uint32_t SFW_COL = ACC_COLS;
+  static constexpr uint32_t SFT_COL = ACC_COLS + 8;
+  static constexpr uint32_t TMEM_COLS = (ACC_COLS + 16 <= 64) ? 64 : (ACC_COLS + 16 <= 128) ? 128
+                                        : (ACC_COLS + 16 <= 256) ? 256 : 512;
+  static_assert(SCALE_LOOKAHEAD < STAGES, "scale look-ahead must leave a free stage");
+  static_assert(T_STAGE % 1024 == 0 || TN % 8 == 0, "token tile");
+};
+
+template <class C>
+struct Ctl {
+  uint64_t full[C::STAGES];
+  uint64_t empty[C::STAGES];
+  uint64_t tfull[2];
+  uint64_t tempty[2];
+  uint64_t mma_done;
+  uint32_t tmem_base;
+  int abort;
+  int valid;
+  int pad;
+  long long total_tiles;
+};
+
+template <class C>
+constexpr uint32_t smem_bytes() {
+  return C::SMEM_CTL + sizeof(Ctl<C>) + 1024;
+}
+
+__device__ __forceinline__ void record_error(int* err, int code, volatile int* abort) {
+  atomicCAS(err, 0, code);
+  *abort = 1;
+}
+
+// Descriptor of a packed 512-byte scale block for tcgen05.cp (32 rows x 16 bytes, no
+// swizzle: 8-row core matrices of 128 bytes, 128 bytes apart).
+__device__ __forceinline__ uint64_t sf_block_desc(uint32_t saddr) {
+  return make_smem_desc(saddr, 0, 128, LAYOUT_NONE);
+}
+
+template <class C>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+bsmxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+               const GemmArgs args) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  Ctl<C>* ctl = reinterpret_cast<Ctl<C>*>(smem + C::SMEM_CTL);
+  volatile int* abort = &ctl->abort;
+  const uint32_t warp = threadIdx.x >> 5;
+  const uint32_t lane = threadIdx.x & 31;
+  const int KB = args.K / BK;
+  const int scale_row = args.K / 32;  // bytes per row of a row-major UE8M0 scale matrix
+
+  // Tiles: per expert ceil(M_e / TN) token tiles x N/128 weight tiles (weights fastest).
+  if (warp == 0) {
+    int ok;
+    int64_t row_tiles;
+    validate_offsets<C::TN>(args.offsets, args.E, args.M_total, ok, row_tiles);
+    if (lane == 0) {
+      ctl->valid = ok;
+      ctl->total_tiles = row_tiles * (args.N / WROWS);
+      ctl->abort = 0;
+      if (!ok && blockIdx.x == 0) atomicCAS(args.err, 0, DEV_BAD_OFFSETS);
+    }
+  }
+  __syncthreads();
+  const int64_t total_tiles = ctl->total_tiles;
+  if (!ctl->valid || (int64_t)blockIdx.x >= total_tiles) return;
+
+  const uint32_t sW = smem_u32(smem + C::SMEM_W);
+  const uint32_t sT = smem_u32(smem + C::SMEM_T);
+  const uint32_t sSFW = smem_u32(smem + C::SMEM_SFW);
+  const uint32_t sSFT = smem_u32(smem + C::SMEM_SFT);
+  auto full_bar = [&](int s) { return smem_u32(&ctl->full[s]); };
+  auto empty_bar = [&](int s) { return smem_u32(&ctl->empty[s]); };
+  auto tfull_bar = [&](int s) { return smem_u32(&ctl->tfull[s]); };
+  auto tempty_bar = [&](int s) { return smem_u32(&ctl->tempty[s]); };
+
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(full_bar(s), 2);   // producer (with bytes) + scale loader
+      mbar_init(empty_bar(s), 1);  // one MMA commit
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(tfull_bar(s), 1);
+      mbar_init(tempty_bar(s), 4);  // the 4 epilogue warps
+    }
+    mbar_init(smem_u32(&ctl->mma_done), 1);
+    fence_mbarrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc<1>(smem_u32(&ctl->tmem_base), C::TMEM_COLS);
+    tmem_relinquish<1>();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = ctl->tmem_base;
+
+  if (warp == 0) {
+    // =============================== TMA producer ===============================
+    if (lane == 0) {
+      GroupedScheduler<C::TN, WROWS> sched(args.offsets, args.E, args.N);
+      const uint64_t pol_w = l2_policy_evict_first();  // weights stream once per token tile
+      uint32_t stage = 0, phase = 0;
+      int64_t issued = 0;
+      bool ok = true;
+      TileCoord tc;
+      for (int64_t t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
+        if (!sched.locate(t, tc)) break;
+        const int32_t w_row = tc.e * args.N + tc.n0;
+        const int32_t t_row = (int32_t)tc.m0;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(empty_bar(stage), phase ^ 1, abort)) {
+            record_error(args.err, DEV_TIMEOUT, abort);
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(full_bar(stage), C::STAGE_TX);
+          tma_load_2d_hint(sW + stage * C::W_STAGE, &tmB, kb * BK, w_row, full_bar(stage), pol_w);
+          tma_load_2d(sT + stage * C::T_STAGE, &tmA, kb * BK, t_row, full_bar(stage));
+          ++issued;
+          if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
+        }
+      }
+      // The last loads have landed before the CTA can exit: once the MMA consumed a stage
+      // it had landed; wait (bounded) for the stages the MMA did not get to.
+      const int64_t pending = issued < C::STAGES ? issued : C::STAGES;
+      for (int64_t i = 0; i < pending; ++i) {
+        stage = (stage + C::STAGES - 1) % C::STAGES;
+        if (stage == C::STAGES - 1) phase ^= 1;
+        mbar_wait_timed(empty_bar(stage), phase);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ================================ MMA thread ================================
+    if (lane == 0) {
+      GroupedScheduler<C::TN, WROWS> sched(args.offsets, args.E, args.N);
+      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0, slot = 0;
+      bool ok = true;
+      TileCoord tc;
+      for (int64_t t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
+        if (!sched.locate(t, tc)) break;
+        if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1, abort)) {
+          record_error(args.err, DEV_TIMEOUT, abort);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * C::TN;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!mbar_wait(full_bar(stage), phase, abort)) {
+            record_error(args.err, DEV_TIMEOUT, abort);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sfw_t = tmem_base + C::SFW_COL + 4 * slot;
+          const uint32_t sft_t = tmem_base + C::SFT_COL + 4 * slot;
+          tmem_cp_32x128b_warpx4<1>(sfw_t, sf_block_desc(sSFW + stage * SF_BLOCK));
+          tmem_cp_32x128b_warpx4<1>(sft_t, sf_block_desc(sSFT + stage * SF_BLOCK));
+          const uint64_t wdesc = kmajor_sw128_desc(sW + stage * C::W_STAGE);
+          const uint64_t tdesc = kmajor_sw128_desc(sT + stage * C::T_STAGE);
+#pragma unroll
+          for (int k = 0; k < BK / 32; ++k)
+            umma_mxf8f6f4<1>(d_tmem, wdesc + (uint64_t)(k * 2), tdesc + (uint64_t)(k * 2),
+                             idesc_mxf8f6f4_e4m3(WROWS, C::TN, k, k), sfw_t, sft_t,
+                             (kb > 0 || k > 0) ? 1u : 0u);
+          umma_commit(empty_bar(stage));
+          slot ^= 1;
+          if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
+        }
+        if (!ok) break;
+        umma_commit(tfull_bar(acc));
+        if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+      }
+      umma_commit(smem_u32(&ctl->mma_done));
+      mbar_wait_timed(smem_u32(&ctl->mma_done), 0);
+    }
+    __syncwarp();
+  } else if (warp == 2) {
+    // =============================== scale loader ===============================
+    // Each lane moves 4-byte words: weight rows lane + 32*j (j < 4), token rows likewise.
+    // A stage is announced on its full barrier once its copies have landed, SCALE_LOOKAHEAD
+    // stages behind the newest issued one.
+    const uint8_t* a_sc = static_cast<const uint8_t*>(args.a_scales);
+    const uint8_t* b_sc = static_cast<const uint8_t*>(args.b_scales);
+    GroupedScheduler<C::TN, WROWS> sched(args.offsets, args.E, args.N);
+    uint32_t stage = 0, phase = 0;
+    uint32_t ring[SCALE_LOOKAHEAD + 1] = {};
+    int inflight = 0, head = 0;
+    bool ok = true;
+    TileCoord tc;
+    auto announce_oldest = [&]() {
+      fence_proxy_async_smem();  // cp.async (generic proxy) writes -> tcgen05.cp (async proxy)
+      __syncwarp();
+      if (lane == 0) mbar_arrive(full_bar(ring[head]));
+      head = (head + 1) % (SCALE_LOOKAHEAD + 1);
+      --inflight;
+    };
+    for (int64_t t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
+      if (!sched.locate(t, tc)) break;
+      const uint8_t* w_rows = b_sc + ((int64_t)tc.e * args.N + tc.n0) * scale_row;
+      for (int kb = 0; kb < KB; ++kb) {
+        const bool got = __all_sync(0xffffffffu, mbar_wait(empty_bar(stage), phase ^ 1, abort));
+        if (!got) {
+          if (lane == 0) record_error(args.err, DEV_TIMEOUT, abort);
+          ok = false;
+          break;
+        }
+        const uint32_t dw = sSFW + stage * SF_BLOCK + lane * 16;
+        const uint32_t dt = sSFT + stage * SF_BLOCK + lane * 16;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int r = j * 32 + (int)lane;
+          cp_async_4(dw + 4 * j, w_rows + (int64_t)r * scale_row + 4 * kb, 4);
+          const int64_t m = tc.m0 + r;
+          const bool live = (r < C::TN) && (m < args.M_total);
+          cp_async_4(dt + 4 * j, live ? a_sc + m * scale_row + 4 * kb : a_sc, live ? 4u : 0u);
+        }
+        cp_async_commit();
+        ring[(head + inflight) % (SCALE_LOOKAHEAD + 1)] = stage;
+        ++inflight;
+        if (inflight > SCALE_LOOKAHEAD) {
+          cp_async_wait_group<SCALE_LOOKAHEAD>();
+          announce_oldest();
+        }
+        if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
+      }
+    }
+    cp_async_wait_group<0>();
+    while (inflight > 0) announce_oldest();
+  } else if (warp >= EPI_WARP0) {
+    // ================================= epilogue =================================
+    const uint32_t quarter = warp & 3;
+    __nv_bfloat16* Cmat = static_cast<__nv_bfloat16*>(args.C);
+    GroupedScheduler<C::TN, WROWS> sched(args.offsets, args.E, args.N);
+    uint32_t acc = 0, acc_phase = 0;
+    TileCoord tc;
+    for (int64_t t = blockIdx.x; t < total_tiles; t += gridDim.x) {
+      if (!sched.locate(t, tc)) break;
+      const bool got = __all_sync(0xffffffffu, mbar_wait(tfull_bar(acc), acc_phase, abort));
+      if (!got) {
+        if (lane == 0) record_error(args.err, DEV_TIMEOUT, abort);
+        break;
+      }
+      tc_fence_after();
+      const int n = tc.n0 + (int)(quarter * 32 + lane);
+      const uint32_t taddr = tmem_base + ((quarter * 32) << 16) + acc * C::TN;
+      uint32_t v[C::TN];
+#pragma unroll
+      for (int c = 0; c < C::TN / 32; ++c)
+        tmem_ld_32x32b_x32(taddr + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(v + 32 * c));
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty_bar(acc));
+      if (++acc == 2) { acc = 0; acc_phase ^= 1; }
+      // token j of the tile is row tc.m0 + j; 32 lanes write 64 contiguous bytes per row
+      const int64_t rows = tc.m_end - tc.m0;
+#pragma unroll
+      for (int j = 0; j < C::TN; ++j) {
+        if (j < rows) {
+          const __nv_bfloat16 h = __float2bfloat16_rn(__uint_as_float(v[j]));
+          Cmat[(tc.m0 + j) * (int64_t)args.N + n] = h;
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc<1>(tmem_base, C::TMEM_COLS);
+  }
+}
+
+template <class C>
+cudaError_t launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& args,
+                   int num_sms, cudaStream_t stream) {
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(bsmxfp8_kernel<C>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem_bytes<C>());
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  const int64_t max_row_tiles = (args.M_total + C::TN - 1) / C::TN + args.E;
+  const int64_t max_tiles = max_row_tiles * (args.N / WROWS);
+  const int grid = (int)(max_tiles < num_sms ? max_tiles : num_sms);
+  bsmxfp8_kernel<C><<<grid, NUM_THREADS, smem_bytes<C>(), stream>>>(tmA, tmB, args);
+  return cudaGetLastError();
+}
+
+}  // namespace mx
+
+cudaError_t launch_bsmxfp8(int tn, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                           const GemmArgs& args, int num_sms, cudaStream_t stream) {
+  switch (tn) {
+    case 32: return mx::launch<mx::Cfg<32>>(tmA, tmB, args, num_sms, stream);
+    case 64: return mx::launch<mx::Cfg<64>>(tmA, tmB, args, num_sms, stream);
+    case 128: return mx::launch<mx::Cfg<128>>(tmA, tmB, args, num_sms, stream);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace bsfp8

@@ -119,6 +119,17 @@ BlockwiseTile choose_blockwise_tile(int64_t M_total, int E) {
   return TILE_CTA1_256;
 }
 
+// Token rows per MXFP8 tile: the smallest of 32 / 64 / 128 that holds the average expert
+// (decode batches give a few tokens per expert).  BSFP8_MX_TN overrides it.
+int choose_mx_token_tile(int64_t M_total, int E) {
+  if (const char* v = std::getenv("BSFP8_MX_TN")) {
+    const int t = std::atoi(v);
+    if (t == 32 || t == 64 || t == 128) return t;
+  }
+  const int64_t avg = (M_total + E - 1) / E;
+  return avg <= 32 ? 32 : avg <= 64 ? 64 : 128;
+}
+
 }  // namespace
 }  // namespace bsfp8
 
@@ -144,6 +155,26 @@ extern "C" bsfp8_status bsfp8_grouped_gemm(const void* A, const void* B, const f
   return launch_bsfp8_blockwise(tile, tmA, tmB, args, dev->num_sms, stream) == cudaSuccess
              ? BSFP8_OK
              : BSFP8_ERR_CUDA;
+}
+
+extern "C" bsfp8_status bsmxfp8_grouped_gemm(const void* A, const void* B, const uint8_t* a_scales,
+                                             const uint8_t* b_scales, const int32_t* expert_offsets,
+                                             void* C, int64_t M_total, int N, int K,
+                                             int num_experts, cudaStream_t stream) {
+  bsfp8_status st = check_common(A, B, a_scales, b_scales, expert_offsets, C, M_total, N, K,
+                                 num_experts);
+  if (st != BSFP8_OK) return st;
+  DeviceInfo* dev = nullptr;
+  if ((st = device_info(&dev)) != BSFP8_OK) return st;
+  if (M_total == 0) return BSFP8_OK;
+  const int tn = choose_mx_token_tile(M_total, num_experts);
+  CUtensorMap tmA, tmB;
+  if (!encode_u8_2d(&tmA, A, (uint64_t)K, (uint64_t)M_total, 128, (uint32_t)tn) ||
+      !encode_u8_2d(&tmB, B, (uint64_t)K, (uint64_t)num_experts * N, 128, 128))
+    return BSFP8_ERR_CUDA;
+  GemmArgs args{expert_offsets, a_scales, b_scales, C, M_total, N, K, num_experts, dev->err_word};
+  return launch_bsmxfp8(tn, tmA, tmB, args, dev->num_sms, stream) == cudaSuccess ? BSFP8_OK
+                                                                                 : BSFP8_ERR_CUDA;
 }
 
 extern "C" bsfp8_status bsfp8_get_device_error(cudaStream_t stream, int* code) {

@@ -42,4 +42,9 @@ cudaError_t launch_bsfp8_blockwise(BlockwiseTile tile, const CUtensorMap& tmA,
                                    const CUtensorMap& tmB, const GemmArgs& args, int num_sms,
                                    cudaStream_t stream);
 
+// MXFP8 (UE8M0 scales per 32 K) grouped GEMM, swap-AB tiles of 128 weight rows x tn token
+// rows; tn is 32, 64 or 128.
+cudaError_t launch_bsmxfp8(int tn, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                           const GemmArgs& args, int num_sms, cudaStream_t stream);
+
 }  // namespace bsfp8

@@ -19,8 +19,9 @@
  *   - EpilogueWarpContext (MAX sm100_structured warp_context), per_k_stage: the blockwise
  *     FP8 epilogue consumes one TMEM stage and one A-scale stage per K iteration.
  *   - Triton Gluon example "Overlapping Accumulator Block-Scaled Matrix Multiplication",
- *     async_mma_scaled_impl / random_quantized_tensor: the block-scaled MMA on e4m3
- *     operands with UE8M0 (uint8) scales, one per VEC_SIZE = 32 elements of K.
+ *     async_mma_scaled_impl / random_quantized_tensor / swizzle_scales_packed_block: the
+ *     block-scaled MMA on e4m3 operands with UE8M0 (uint8) scales, one per VEC_SIZE = 32
+ *     elements of K, the scales arranged in 128-row packed blocks for the tensor core.
  *
  * Conventions shared by every entry point:
  *   - Every pointer is a DEVICE pointer (memory of the current CUDA device), row-major,
@@ -33,7 +34,8 @@
  *     a code into the device error word and finish without touching C further; read it
  *     with bsfp8_get_device_error().
  *   - Requirements: N % 128 == 0, K % 128 == 0, num_experts >= 1, 0 <= M_total < 2^31,
- *     num_experts * N < 2^31; A, B, C 16-byte aligned; scales and offsets 4-byte aligned.
+ *     num_experts * N < 2^31; A, B, C 16-byte aligned; scales and offsets 4-byte aligned
+ *     (also the UE8M0 scale arrays, which are read 4 codes at a time).
  *     M_total == 0 is a valid no-op (nothing is read or written).
  *   - The device must be compute capability 10.3 (GB300).
  */
@@ -82,6 +84,29 @@ bsfp8_status bsfp8_grouped_gemm(const void* A, const void* B, const float* a_sca
                                 const float* b_scales, const int32_t* expert_offsets, void* C,
                                 int64_t M_total, int N, int K, int num_experts,
                                 cudaStream_t stream);
+
+/*
+ * MXFP8 grouped GEMM: e4m3 operands, UE8M0 scales (2^(code-127)) per 32 elements of K,
+ * applied by the block-scaled tensor-core MMA:
+ *
+ *   C[m, n] = bf16( sum_k A[m,k] * B[e,n,k] * 2^(a_scales[m, k/32] - 127) * 2^(b_scales[e, n, k/32] - 127) )
+ *
+ *   A              e4m3 [M_total, K]             token rows, grouped by expert
+ *   B              e4m3 [num_experts, N, K]      expert weights, K-major
+ *   a_scales       UE8M0 [M_total, K/32]         row-major (row m's codes are contiguous)
+ *   b_scales       UE8M0 [num_experts, N, K/32]  row-major
+ *   expert_offsets int32 [num_experts+1]         as for bsfp8_grouped_gemm
+ *   C              bf16 [M_total, N]             output
+ *
+ * Same requirements, ownership and error behaviour as bsfp8_grouped_gemm.  Tiles pair 128
+ * rows of an expert's weights with up to 32 / 64 / 128 of its token rows ("swap-AB"); the
+ * token-tile height follows M_total / num_experts (environment variable BSFP8_MX_TN =
+ * 32 | 64 | 128 overrides it).
+ */
+bsfp8_status bsmxfp8_grouped_gemm(const void* A, const void* B, const uint8_t* a_scales,
+                                  const uint8_t* b_scales, const int32_t* expert_offsets,
+                                  void* C, int64_t M_total, int N, int K, int num_experts,
+                                  cudaStream_t stream);
 
 /*
  * Read the device error word of the current device (after synchronising `stream`) into

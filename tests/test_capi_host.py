@@ -23,7 +23,7 @@ def _declared_functions():
     for h in os.listdir(os.path.join(ROOT, "include")):
         text = open(os.path.join(ROOT, "include", h)).read()
         text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-        names += re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*(bsfp8_[a-z0-9_]+)\s*\(",
+        names += re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*(bs[a-z0-9_]+)\s*\(",
                             text, flags=re.M)
     return sorted(set(names))
 

@@ -1,0 +1,91 @@
+"""GPU parity of the MXFP8 grouped GEMM (UE8M0 scales per 32 K, hardware block scaling)
+against the CPU oracle.  Same acceptance bound as the blockwise mode; exact-arithmetic
+inputs (e2m1-grid values, scale codes 126..128) must match bit for bit."""
+import numpy as np
+import pytest
+import torch
+
+import gen
+import oracle
+from helpers import parity_report
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(params=[32, 64, 128])
+def tn(request, monkeypatch):
+    """Token rows per tile (swap-AB tile height)."""
+    monkeypatch.setenv("BSFP8_MX_TN", str(request.param))
+    return request.param
+
+
+def _check_full(p):
+    from gpu_util import DeviceProblem
+    import block_scaled_fp8_persistent_gb300 as bsfp8
+    d = DeviceProblem(p, c_rows_extra=2)
+    d.run()
+    got = d.c_bits()
+    assert bsfp8.bsfp8_get_device_error() == 0
+    ref, T = oracle.problem_reference(p)
+    bad, ratio, exact = parity_report(got, ref, T)
+    assert bad == 0, f"{bad} elements outside tolerance (max err/tol {ratio:.3g})"
+    assert np.all(d.guard_bits() == d.sentinel)
+    return got, ref
+
+
+CASES = [
+    ("decode_like", [3, 17, 0, 32, 1, 9], 256, 512),
+    ("ragged_k", [40, 0, 7], 384, 640),
+    ("one_expert_many_rows", [300], 128, 256),
+    ("mixed", [0, 129, 64, 65, 2, 0, 31], 256, 384),
+]
+
+
+@pytest.mark.parametrize("name,counts,N,K", CASES, ids=[c[0] for c in CASES])
+def test_small_cases(name, counts, N, K, tn):
+    _check_full(gen.mx_problem(counts, N, K, seed=200 + len(name)))
+
+
+@pytest.mark.parametrize("counts,N,K", [([5, 30, 0, 12], 256, 1024), ([200, 3], 384, 768)])
+def test_exact_inputs_bitwise(counts, N, K, tn):
+    got, ref = _check_full(gen.mx_problem(counts, N, K, seed=9, exact=True))
+    assert np.array_equal(got, ref)
+
+
+def test_scale_extremes(tn):
+    """Scale codes far from 127 on both sides (the exponent path, not only the values)."""
+    p = gen.mx_problem([20, 11], 128, 256, seed=10)
+    rng = np.random.default_rng(5)
+    p.a_scales[:] = rng.integers(100, 150, p.a_scales.shape).astype(np.uint8)
+    p.b_scales[:] = rng.integers(110, 140, p.b_scales.shape).astype(np.uint8)
+    _check_full(p)
+
+
+def test_invalid_offsets_reported_on_device():
+    from gpu_util import DeviceProblem
+    import block_scaled_fp8_persistent_gb300 as bsfp8
+    p = gen.mx_problem([10, 10], 128, 128, seed=11)
+    d = DeviceProblem(p)
+    d.off.copy_(torch.tensor([0, 15, 12], dtype=torch.int32))
+    d.run()
+    assert bsfp8.bsfp8_get_device_error() == 6
+    assert np.all(d.c_bits() == d.sentinel)
+
+
+def test_decode_config_sampled():
+    """The full decode-shaped workload (128 experts x U{1..32} tokens, N=4096, K=7168)."""
+    from gpu_util import DeviceProblem
+    import block_scaled_fp8_persistent_gb300 as bsfp8
+    p = gen.config_problem(4)
+    d = DeviceProblem(p)
+    d.run()
+    got = d.c_bits()
+    assert bsfp8.bsfp8_get_device_error() == 0
+    rng = np.random.default_rng(4)
+    off = p.offsets.astype(np.int64)
+    rows_full = sorted({int(off[e]) for e in range(0, p.E, 9) if off[e + 1] > off[e]})
+    rows = np.concatenate([np.repeat(rows_full, p.N), rng.integers(0, p.M_total, 8000)])
+    cols = np.concatenate([np.tile(np.arange(p.N), len(rows_full)), rng.integers(0, p.N, 8000)])
+    ref, T = oracle.problem_points(p, rows, cols)
+    bad, ratio, _ = parity_report(got[rows, cols], ref, T)
+    assert bad == 0, f"{bad} sampled elements outside tolerance (max err/tol {ratio:.3g})"
