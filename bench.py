@@ -231,6 +231,52 @@ def run_reference(args):
     return 0
 
 
+def time_secondary(cfg, args, flush, stream, peaks, peak_src):
+    """Time the MXFP8 decode workload (config 4) with the same protocol: warm-up, then
+    args.steps launches, each bracketed by CUDA events, L2 flushed between them."""
+    import numpy as np
+    import torch
+    import gen
+    import block_scaled_fp8_persistent_gb300 as bsfp8
+    dev = flush.device
+    p = gen.config_problem(cfg)
+    d = {k: torch.from_numpy(np.ascontiguousarray(getattr(p, k))).to(dev)
+         for k in ("A", "B", "a_scales", "b_scales", "offsets")}
+    C = torch.empty((p.M_total, p.N), dtype=torch.bfloat16, device=dev)
+
+    def step():
+        bsfp8.bsmxfp8_grouped_gemm(d["A"], d["B"], d["a_scales"], d["b_scales"], d["offsets"], C,
+                                   p.M_total, p.N, p.K, p.E, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    ms = statistics.mean(s.elapsed_time(e) for s, e in zip(starts, ends))
+    err = bsfp8.bsfp8_get_device_error(stream)
+    gbs = p.bytes() / (ms * 1e-3) / 1e9
+    traffic, prof_file = traffic_from_profiles(f"config{cfg}")
+    out = {"workload": f"config {cfg}: {gen.CONFIG_NAMES[cfg]}", "M_total": p.M_total,
+           "ms_per_step": ms, "value": p.flops() / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+           "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                        "frac": gbs / peaks["hbm_gbs"], "traffic": traffic,
+                        "algorithmic_bytes": p.bytes(),
+                        "peak_source": f"{peak_src} copy bandwidth"},
+           "device_error": err, "gpu_launches": args.steps}
+    if prof_file:
+        out["roofline"]["traffic_source"] = f"profiles/{prof_file}"
+    del d, C
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -250,7 +296,15 @@ def run_ours(args):
 
     cfg = args.config
     t0 = time.time()
-    p = gen.config_problem(cfg)
+    if args.n_override:
+        # profiling-sized copy of a workload: same routing, K and kernel, fewer columns
+        if not args.profile:
+            raise SystemExit("--n-override is for --profile runs only")
+        counts = gen.config_counts(cfg)
+        make = gen.mx_problem if cfg == 4 else gen.blockwise_problem
+        p = make(counts, args.n_override, gen.CONFIG_SHAPES[cfg][1], seed=cfg)
+    else:
+        p = gen.config_problem(cfg)
     log(f"[bench] rank {rank}: generated config {cfg} in {time.time() - t0:.1f}s "
         f"(M_total={p.M_total}, E={p.E})")
     dev = torch.device("cuda", local)
@@ -354,6 +408,11 @@ def run_ours(args):
     if prof_file:
         roof["traffic_source"] = f"profiles/{prof_file}"
 
+    # ---- the second mode of the path: the MXFP8 decode workload, timed the same way ----
+    secondary = None
+    if not args.no_secondary and cfg != 4:
+        secondary = time_secondary(4, args, flush, stream, peaks, peak_src)
+
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         rows = oracle_rows_for(p, args.cpu_seconds)
@@ -377,6 +436,8 @@ def run_ours(args):
         "device_error": dev_err,
         "kernel_sources_sha256_12": kernel_hash(),
     }
+    if secondary is not None:
+        line["secondary"] = secondary
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
@@ -392,6 +453,10 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-secondary", action="store_true",
+                    help="skip the MXFP8 decode workload that is timed after the main one")
+    ap.add_argument("--n-override", type=int, default=0,
+                    help="with --profile: run the workload with this many columns N")
     ap.add_argument("--profile", action="store_true",
                     help="only warm-up + timed steps (for ncu): no soak, e2e, clocks or CPU baseline")
     args = ap.parse_args(argv)
