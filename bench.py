@@ -207,7 +207,7 @@ def run_reference(args):
         return 0
     import gen
     p = gen.config_problem(args.config)
-    budget = 150.0  # seconds for the whole reference run
+    budget = args.ref_budget  # seconds of oracle work for the whole reference run
     rows = oracle_rows_for(p, budget / max(1, args.steps + args.warmup))
     for _ in range(args.warmup):
         oracle_sample(p, rows)
@@ -453,6 +453,8 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-budget", type=float, default=150.0,
+                    help="--impl reference: seconds of oracle work across all steps")
     ap.add_argument("--no-secondary", action="store_true",
                     help="skip the MXFP8 decode workload that is timed after the main one")
     ap.add_argument("--n-override", type=int, default=0,
