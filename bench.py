@@ -301,7 +301,7 @@ def run_ours(args):
         if not args.profile:
             raise SystemExit("--n-override is for --profile runs only")
         counts = gen.config_counts(cfg)
-        make = gen.mx_problem if cfg == 4 else gen.blockwise_problem
+        make = gen.mx_problem if cfg in (4, 5) else gen.blockwise_problem
         p = make(counts, args.n_override, gen.CONFIG_SHAPES[cfg][1], seed=cfg)
     else:
         p = gen.config_problem(cfg)
@@ -390,8 +390,10 @@ def run_ours(args):
     peaks, peak_src = load_peaks()
     value = total_flops / (max_ms * 1e-3) / 1e12
     achieved = flops / (local_ms * 1e-3) / 1e12
-    if p.mode == "blockwise":
-        peak = peaks["bf16_tflops"] * FP8_PER_BF16
+    fp8_peak = peaks["bf16_tflops"] * FP8_PER_BF16
+    tensor_bound = p.flops() / (fp8_peak * 1e12) >= p.bytes() / (peaks["hbm_gbs"] * 1e9)
+    if tensor_bound:
+        peak = fp8_peak
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak,
                 "peak_source": f"{peak_src} bf16 burst {peaks['bf16_tflops']} TFLOP/s x {FP8_PER_BF16} "
@@ -449,7 +451,7 @@ def main(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", type=int, default=1, choices=[0, 1, 2, 3, 4])
+    ap.add_argument("--config", type=int, default=1, choices=[0, 1, 2, 3, 4, 5])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -29,8 +29,8 @@ STATUS_NAMES = {
 }
 
 # Every symbol include/bsfp8.h declares (the CPU test checks the library exports them).
-EXPORTED = ("bsfp8_grouped_gemm", "bsmxfp8_grouped_gemm", "bsfp8_get_device_error",
-            "bsfp8_status_string")
+EXPORTED = ("bsfp8_grouped_gemm", "bsmxfp8_grouped_gemm", "bsmxfp8_tmem_plan",
+            "bsfp8_get_device_error", "bsfp8_status_string")
 
 
 class BsFp8Error(RuntimeError):
@@ -55,6 +55,8 @@ def load_library() -> ctypes.CDLL:
         lib.bsfp8_grouped_gemm.restype = i32
         lib.bsmxfp8_grouped_gemm.argtypes = [p, p, p, p, p, p, i64, i32, i32, i32, p]
         lib.bsmxfp8_grouped_gemm.restype = i32
+        lib.bsmxfp8_tmem_plan.argtypes = [i32, i32, i32, i32, ctypes.POINTER(ctypes.c_int32)]
+        lib.bsmxfp8_tmem_plan.restype = i32
         lib.bsfp8_get_device_error.argtypes = [p, ctypes.POINTER(ctypes.c_int)]
         lib.bsfp8_get_device_error.restype = i32
         lib.bsfp8_status_string.argtypes = [i32]
@@ -106,6 +108,19 @@ def bsmxfp8_grouped_gemm(A, B, a_scales, b_scales, expert_offsets, C, M_total: i
                                              int(K), int(num_experts), _stream(stream))
     if st != BSFP8_OK:
         raise BsFp8Error(st, "bsmxfp8_grouped_gemm")
+
+
+def bsmxfp8_tmem_plan(block_k: int, epilogue_n: int, vec: int, overlap: bool) -> dict:
+    """TMEM plan of double-buffered block-scaled accumulators (host only).  block_k=0 gives
+    the plan the CTA-pair MXFP8 kernel is compiled with."""
+    out = (ctypes.c_int32 * 9)()
+    st = load_library().bsmxfp8_tmem_plan(int(block_k), int(epilogue_n), int(vec), int(bool(overlap)),
+                                          out)
+    if st != BSFP8_OK:
+        raise BsFp8Error(st, "bsmxfp8_tmem_plan")
+    keys = ("left_offset", "left_cols", "right_offset", "right_cols", "a_scale_offset",
+            "a_scale_cols", "b_scale_offset", "b_scale_cols", "early_release_subtile")
+    return dict(zip(keys, list(out)))
 
 
 def bsfp8_get_device_error(stream=None) -> int:

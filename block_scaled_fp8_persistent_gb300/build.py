@@ -19,7 +19,7 @@ OBJDIR = os.path.join(PKG, "_build")
 LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "libbsfp8.so")
 
-SOURCES = ["capi.cu", "bsfp8_grouped.cu", "bsmxfp8_grouped.cu"]
+SOURCES = ["capi.cu", "bsfp8_grouped.cu", "bsmxfp8_grouped.cu", "bsmxfp8_pair.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I" + CSRC, "-I" + INCLUDE]
 

@@ -119,6 +119,17 @@ BlockwiseTile choose_blockwise_tile(int64_t M_total, int E) {
   return TILE_CTA1_256;
 }
 
+// MXFP8 kernel choice: experts averaging at least 256 token rows use the CTA-pair 256 x 256
+// tiles with overlapping accumulators; smaller ones the swap-AB tiles.  BSFP8_MX_KERNEL
+// (pair | swap) overrides it.
+bool use_mx_pair(int64_t M_total, int E) {
+  if (const char* v = std::getenv("BSFP8_MX_KERNEL")) {
+    if (!std::strcmp(v, "pair")) return true;
+    if (!std::strcmp(v, "swap")) return false;
+  }
+  return M_total >= (int64_t)256 * E;
+}
+
 // Token rows per MXFP8 tile: the smallest of 32 / 64 / 128 that holds the average expert
 // (decode batches give a few tokens per expert).  BSFP8_MX_TN overrides it.
 int choose_mx_token_tile(int64_t M_total, int E) {
@@ -167,6 +178,17 @@ extern "C" bsfp8_status bsmxfp8_grouped_gemm(const void* A, const void* B, const
   DeviceInfo* dev = nullptr;
   if ((st = device_info(&dev)) != BSFP8_OK) return st;
   if (M_total == 0) return BSFP8_OK;
+  if (use_mx_pair(M_total, num_experts)) {
+    CUtensorMap tmA, tmB;
+    if (!encode_u8_2d(&tmA, A, (uint64_t)K, (uint64_t)M_total, 128, 128) ||
+        !encode_u8_2d(&tmB, B, (uint64_t)K, (uint64_t)num_experts * N, 128, 128))
+      return BSFP8_ERR_CUDA;
+    GemmArgs args{expert_offsets, a_scales, b_scales, C, M_total, N, K, num_experts,
+                  dev->err_word};
+    return launch_bsmxfp8_pair(tmA, tmB, args, dev->num_sms, stream) == cudaSuccess
+               ? BSFP8_OK
+               : BSFP8_ERR_CUDA;
+  }
   const int tn = choose_mx_token_tile(M_total, num_experts);
   CUtensorMap tmA, tmB;
   if (!encode_u8_2d(&tmA, A, (uint64_t)K, (uint64_t)M_total, 128, (uint32_t)tn) ||
@@ -175,6 +197,24 @@ extern "C" bsfp8_status bsmxfp8_grouped_gemm(const void* A, const void* B, const
   GemmArgs args{expert_offsets, a_scales, b_scales, C, M_total, N, K, num_experts, dev->err_word};
   return launch_bsmxfp8(tn, tmA, tmB, args, dev->num_sms, stream) == cudaSuccess ? BSFP8_OK
                                                                                  : BSFP8_ERR_CUDA;
+}
+
+extern "C" bsfp8_status bsmxfp8_tmem_plan(int block_k, int epilogue_n, int vec, int overlap,
+                                          int32_t* out) {
+  if (!out) return BSFP8_ERR_NULL;
+  TmemPlan p;
+  if (block_k == 0) {
+    p = mx_pair_tmem_plan();  // the plan the CTA-pair MXFP8 kernel is compiled with
+  } else {
+    if (block_k < 0 || epilogue_n <= 0 || (vec != 16 && vec != 32) || block_k % vec != 0)
+      return BSFP8_ERR_SHAPE;
+    p = tmem_overlap_plan(block_k, epilogue_n, vec, overlap != 0);
+  }
+  const int32_t v[9] = {p.left_offset,    p.left_cols,    p.right_offset,
+                        p.right_cols,     p.a_scale_offset, p.a_scale_cols,
+                        p.b_scale_offset, p.b_scale_cols, p.early_release_subtile};
+  for (int i = 0; i < 9; ++i) out[i] = v[i];
+  return BSFP8_OK;
 }
 
 extern "C" bsfp8_status bsfp8_get_device_error(cudaStream_t stream, int* code) {

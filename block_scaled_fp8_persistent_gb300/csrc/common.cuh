@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <cstdint>
 
+#include "tmem_plan.cuh"
+
 namespace bsfp8 {
 
 // Device-side error codes (written once per launch into the library's error word).
@@ -46,5 +48,11 @@ cudaError_t launch_bsfp8_blockwise(BlockwiseTile tile, const CUtensorMap& tmA,
 // rows; tn is 32, 64 or 128.
 cudaError_t launch_bsmxfp8(int tn, const CUtensorMap& tmA, const CUtensorMap& tmB,
                            const GemmArgs& args, int num_sms, cudaStream_t stream);
+
+// MXFP8 grouped GEMM with CTA-pair 256 x 256 tiles and overlapping TMEM accumulators.
+cudaError_t launch_bsmxfp8_pair(const CUtensorMap& tmA, const CUtensorMap& tmB,
+                                const GemmArgs& args, int num_sms, cudaStream_t stream);
+// The TMEM plan that kernel is compiled with.
+TmemPlan mx_pair_tmem_plan();
 
 }  // namespace bsfp8

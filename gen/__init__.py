@@ -254,6 +254,7 @@ CONFIG_NAMES = {
     2: "grouped MoE blockwise FP8 skewed, E=64 M_total=16384 (Zipf 1.2, 1% x50 outlier rows) N=2048 K=7168",
     3: "dense blockwise FP8, M=N=K=8192 (256x256 CTA-pair tiles)",
     4: "decode MXFP8 grouped, E=128 x U{1..32} rows, N=4096 K=7168, swap-AB",
+    5: "extra workload (not one of the five above): dense MXFP8, M=N=K=8192",
 }
 
 
@@ -268,17 +269,20 @@ def config_counts(idx: int) -> np.ndarray:
         return np.array([8192], np.int32)
     if idx == 4:
         return route_counts(4, 128, 1, 32)
+    if idx == 5:
+        return np.array([8192], np.int32)
     raise ValueError(idx)
 
 
-CONFIG_SHAPES = {0: (256, 512), 1: (4096, 7168), 2: (2048, 7168), 3: (8192, 8192), 4: (4096, 7168)}
+CONFIG_SHAPES = {0: (256, 512), 1: (4096, 7168), 2: (2048, 7168), 3: (8192, 8192), 4: (4096, 7168),
+                 5: (8192, 8192)}
 
 
 def config_problem(idx: int, nthreads: int = 0) -> Problem:
     counts = config_counts(idx)
     N, K = CONFIG_SHAPES[idx]
-    if idx == 4:
-        return mx_problem(counts, N, K, seed=4, nthreads=nthreads, name=CONFIG_NAMES[4])
+    if idx in (4, 5):
+        return mx_problem(counts, N, K, seed=idx, nthreads=nthreads, name=CONFIG_NAMES[idx])
     outliers = int(round(0.01 * int(counts.sum()))) if idx == 2 else 0
     return blockwise_problem(counts, N, K, seed=idx, outlier_rows=outliers, nthreads=nthreads,
                              name=CONFIG_NAMES[idx])

@@ -98,15 +98,32 @@ bsfp8_status bsfp8_grouped_gemm(const void* A, const void* B, const float* a_sca
  *   expert_offsets int32 [num_experts+1]         as for bsfp8_grouped_gemm
  *   C              bf16 [M_total, N]             output
  *
- * Same requirements, ownership and error behaviour as bsfp8_grouped_gemm.  Tiles pair 128
- * rows of an expert's weights with up to 32 / 64 / 128 of its token rows ("swap-AB"); the
- * token-tile height follows M_total / num_experts (environment variable BSFP8_MX_TN =
- * 32 | 64 | 128 overrides it).
+ * Same requirements, ownership and error behaviour as bsfp8_grouped_gemm.  When experts
+ * average fewer than 256 token rows, tiles pair 128 rows of an expert's weights with up to
+ * 32 / 64 / 128 of its token rows ("swap-AB"; the height follows M_total / num_experts,
+ * environment variable BSFP8_MX_TN = 32 | 64 | 128 overrides it); otherwise CTA-pair
+ * 256 x 256 tiles with overlapping double-buffered TMEM accumulators are used (environment
+ * variable BSFP8_MX_KERNEL = swap | pair overrides the choice).
  */
 bsfp8_status bsmxfp8_grouped_gemm(const void* A, const void* B, const uint8_t* a_scales,
                                   const uint8_t* b_scales, const int32_t* expert_offsets,
                                   void* C, int64_t M_total, int N, int K, int num_experts,
                                   cudaStream_t stream);
+
+/*
+ * TMEM storage plan of double-buffered block-scaled accumulators (host only, no GPU use).
+ * For a 256-column tile with 512 TMEM columns, block_k elements of K per MMA stage,
+ * epilogue subtiles of epilogue_n columns and one scale per vec (16 or 32) elements of K,
+ * writes into out[9]: left accumulator offset and columns, right accumulator offset and
+ * columns, A-scale offset and columns, B-scale offset and columns, and the epilogue
+ * subtile that holds the overlapped columns.  With overlap != 0 the second accumulator
+ * overlaps the first by the scale columns (the Overlapping Accumulator Layout section and
+ * tmem_overlap_storage_plan of the Triton Gluon example "Overlapping Accumulator
+ * Block-Scaled Matrix Multiplication"); with overlap == 0 a single accumulator is
+ * followed by the scales.  block_k == 0 returns the plan the CTA-pair MXFP8 kernel of
+ * bsmxfp8_grouped_gemm is compiled with.  BSFP8_ERR_NULL / BSFP8_ERR_SHAPE on bad input.
+ */
+bsfp8_status bsmxfp8_tmem_plan(int block_k, int epilogue_n, int vec, int overlap, int32_t* out);
 
 /*
  * Read the device error word of the current device (after synchronising `stream`) into

@@ -12,10 +12,15 @@ from helpers import parity_report
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(params=[32, 64, 128])
+@pytest.fixture(params=["swap32", "swap64", "swap128", "pair"])
 def tn(request, monkeypatch):
-    """Token rows per tile (swap-AB tile height)."""
-    monkeypatch.setenv("BSFP8_MX_TN", str(request.param))
+    """The MXFP8 kernel form: swap-AB with 32/64/128 token rows per tile, or CTA-pair
+    256 x 256 tiles with overlapping accumulators."""
+    if request.param == "pair":
+        monkeypatch.setenv("BSFP8_MX_KERNEL", "pair")
+    else:
+        monkeypatch.setenv("BSFP8_MX_KERNEL", "swap")
+        monkeypatch.setenv("BSFP8_MX_TN", request.param[4:])
     return request.param
 
 
@@ -35,6 +40,7 @@ def _check_full(p):
 
 CASES = [
     ("decode_like", [3, 17, 0, 32, 1, 9], 256, 512),
+    ("many_tiles", [700, 0, 513], 640, 512),
     ("ragged_k", [40, 0, 7], 384, 640),
     ("one_expert_many_rows", [300], 128, 256),
     ("mixed", [0, 129, 64, 65, 2, 0, 31], 256, 384),
@@ -86,6 +92,24 @@ def test_decode_config_sampled():
     rows_full = sorted({int(off[e]) for e in range(0, p.E, 9) if off[e + 1] > off[e]})
     rows = np.concatenate([np.repeat(rows_full, p.N), rng.integers(0, p.M_total, 8000)])
     cols = np.concatenate([np.tile(np.arange(p.N), len(rows_full)), rng.integers(0, p.N, 8000)])
+    ref, T = oracle.problem_points(p, rows, cols)
+    bad, ratio, _ = parity_report(got[rows, cols], ref, T)
+    assert bad == 0, f"{bad} sampled elements outside tolerance (max err/tol {ratio:.3g})"
+
+
+def test_dense_large_mx_sampled(monkeypatch):
+    """Dense 8192^3 MXFP8 (one expert), the CTA-pair kernel with overlapping accumulators."""
+    from gpu_util import DeviceProblem
+    import block_scaled_fp8_persistent_gb300 as bsfp8
+    monkeypatch.setenv("BSFP8_MX_KERNEL", "pair")
+    p = gen.config_problem(5)
+    d = DeviceProblem(p)
+    d.run()
+    got = d.c_bits()
+    assert bsfp8.bsfp8_get_device_error() == 0
+    rng = np.random.default_rng(5)
+    rows = np.concatenate([np.repeat([0, 255, 256, 8191], p.N), rng.integers(0, p.M_total, 6000)])
+    cols = np.concatenate([np.tile(np.arange(p.N), 4), rng.integers(0, p.N, 6000)])
     ref, T = oracle.problem_points(p, rows, cols)
     bad, ratio, _ = parity_report(got[rows, cols], ref, T)
     assert bad == 0, f"{bad} sampled elements outside tolerance (max err/tol {ratio:.3g})"
