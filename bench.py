@@ -35,7 +35,8 @@ sys.path.insert(0, ROOT)
 METRIC = "grouped blockwise-FP8 GEMM TFLOP/s and % of GB300 FP8 tensor peak (1 GPU)"
 FP8_PER_BF16 = 2.0  # nominal dense fp8 / bf16 tensor throughput ratio (4.5 / 2.25 PFLOP/s)
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-KERNEL_SOURCES = ("ptx.cuh", "sched.cuh", "common.cuh", "bsfp8_grouped.cu", "bsmxfp8_grouped.cu")
+KERNEL_SOURCES = ("ptx.cuh", "sched.cuh", "common.cuh", "tmem_plan.cuh", "bsfp8_grouped.cu",
+                  "bsmxfp8_grouped.cu", "bsmxfp8_pair.cu")
 
 
 def log(*a):

@@ -30,7 +30,7 @@ STATUS_NAMES = {
 
 # Every symbol include/bsfp8.h declares (the CPU test checks the library exports them).
 EXPORTED = ("bsfp8_grouped_gemm", "bsmxfp8_grouped_gemm", "bsmxfp8_tmem_plan",
-            "bsfp8_get_device_error", "bsfp8_status_string")
+            "bsfp8_blockwise_plan", "bsfp8_get_device_error", "bsfp8_status_string")
 
 
 class BsFp8Error(RuntimeError):
@@ -57,6 +57,9 @@ def load_library() -> ctypes.CDLL:
         lib.bsmxfp8_grouped_gemm.restype = i32
         lib.bsmxfp8_tmem_plan.argtypes = [i32, i32, i32, i32, ctypes.POINTER(ctypes.c_int32)]
         lib.bsmxfp8_tmem_plan.restype = i32
+        lib.bsfp8_blockwise_plan.argtypes = [ctypes.c_int64, i32, i32, i32,
+                                             ctypes.POINTER(ctypes.c_int32)]
+        lib.bsfp8_blockwise_plan.restype = i32
         lib.bsfp8_get_device_error.argtypes = [p, ctypes.POINTER(ctypes.c_int)]
         lib.bsfp8_get_device_error.restype = i32
         lib.bsfp8_status_string.argtypes = [i32]
@@ -121,6 +124,16 @@ def bsmxfp8_tmem_plan(block_k: int, epilogue_n: int, vec: int, overlap: bool) ->
     keys = ("left_offset", "left_cols", "right_offset", "right_cols", "a_scale_offset",
             "a_scale_cols", "b_scale_offset", "b_scale_cols", "early_release_subtile")
     return dict(zip(keys, list(out)))
+
+
+def bsfp8_blockwise_plan(M_total: int, N: int, num_experts: int, num_sms: int) -> dict:
+    """Tile plan of the blockwise GEMM for this problem size on num_sms SMs (host only)."""
+    out = (ctypes.c_int32 * 3)()
+    st = load_library().bsfp8_blockwise_plan(int(M_total), int(N), int(num_experts),
+                                             int(num_sms), out)
+    if st != BSFP8_OK:
+        raise BsFp8Error(st, "bsfp8_blockwise_plan")
+    return {"tile_rows": out[0], "tile_cols": out[1], "ctas_per_tile": out[2]}
 
 
 def bsfp8_get_device_error(stream=None) -> int:

@@ -14,7 +14,7 @@
 //  * Triton Gluon example "Overlapping Accumulator Block-Scaled Matrix Multiplication":
 //    load / MMA / epilogue partitions, persistent static tile stride, 2-CTA tiles.
 //
-// Roles (one CTA = 12 warps):
+// Roles with 128 A rows per CTA (12 warps):
 //   warp 0       TMA producer: per K block, this CTA's A rows [128 x 128] and its share of
 //                B rows [BN/CG x 128] (e4m3, 128-byte swizzle) into a STAGES-deep ring.
 //   warp 1       TMEM owner; in the MMA CTA (rank 0 of the pair) the single issuing thread:
@@ -25,12 +25,27 @@
 //                back, and promotes acc = fma(sa*sb, partial, acc) in registers.  After the
 //                last K block it rounds to bf16 and stores the rows of the tile's expert.
 //
+// With 96 A rows per CTA (8 warps) the M = 128 MMA computes TMEM lanes 96..127 from
+// shared-memory rows that are never loaded, and nobody reads them.  A warp can only read
+// the TMEM lanes of its own SM sub-partition (lanes 32*(w%4)..), so the sub-partition of
+// lanes 96..127 is free: warp 3 is the producer and warp 7 the TMEM owner / MMA issuer,
+// and warps 0-2 and 4-6 are the epilogue (columns (BN/2)*(w/4)..).  The role warps' barrier
+// polling and TMA / MMA issue then share no SMSP with a warp that drains a TMEM stage.
+// Measured on the 128-row layout, epilogue warps on the role warps' SMSPs see each
+// TMEM-full barrier 500-1000 cycles after the others, which with two TMEM stages stalls
+// the tensor core every K block; a quarter of the MMA work is the price of removing that.
+//
 // CG = 2 runs a CTA pair (cluster of 2) on a 256 x BN tile: each CTA loads its own 128 A
 // rows and half of the B rows (no multicast), the pair MMA (M = 256) reads both halves,
 // the TMA completions of both CTAs are counted on the leader's barrier, and the leader's
 // commits arrive on both CTAs' barriers.  Each CTA promotes and stores its own 128 rows.
 //
-// A and B scales reach the epilogue through the read-only cache, one K block ahead.
+// A and B scales reach the epilogue through the read-only cache one K block ahead, and the
+// A scales' lines are prefetched into L1 SCALE_LOOKAHEAD K blocks ahead.  a_scales is
+// [K/128, M_total], so every K block touches a new line per 32 rows; without the L1
+// prefetch the one-ahead load often missed to DRAM and stalled both warps of that TMEM
+// lane quarter at the sa * sb multiply for 300-1300 cycles, holding up the release of the
+// TMEM stage (B scales of consecutive K blocks share a line and hit L1).
 #include <cuda_bf16.h>
 #include "common.cuh"
 #include "ptx.cuh"
@@ -40,16 +55,19 @@ namespace bsfp8 {
 namespace bw {
 
 constexpr int BK = 128;
-constexpr int NUM_THREADS = 384;
-constexpr int EPI_WARP0 = 4;
-constexpr int NUM_EPI_WARPS = 8;
 constexpr uint32_t TMEM_COLS = 512;
 
-template <int CG_, int BN_, int STAGES_, int ACC_STAGES_>
+template <int CG_, int BN_, int STAGES_, int ACC_STAGES_, int ROWS_ = 128>
 struct Cfg {
   static constexpr int CG = CG_;                  // CTAs per tile (1 or 2)
   static constexpr int BN = BN_;                  // tile columns
-  static constexpr int BM = 128 * CG;             // tile rows (128 per CTA)
+  static constexpr int ROWS = ROWS_;              // A rows per CTA (128, or 96: see above)
+  static constexpr int BM = ROWS * CG;            // tile rows
+  static constexpr bool SPARE_QUARTER = ROWS == 96;  // TMEM lanes 96..127 unused
+  static constexpr int THREADS = SPARE_QUARTER ? 256 : 384;
+  static constexpr int PRODUCER_WARP = SPARE_QUARTER ? 3 : 0;
+  static constexpr int MMA_WARP = SPARE_QUARTER ? 7 : 1;  // also allocates TMEM
+  static constexpr int NUM_EPI_WARPS = SPARE_QUARTER ? 6 : 8;
   static constexpr int STAGES = STAGES_;          // SMEM ring depth
   static constexpr int ACC_STAGES = ACC_STAGES_;  // TMEM partial ring depth
   static constexpr int B_ROWS = BN / CG;          // B rows loaded by each CTA
@@ -58,13 +76,21 @@ struct Cfg {
   // all of a warp's columns fit in registers next to its accumulators: load them all,
   // release the TMEM stage, then promote
   static constexpr bool LOAD_ALL = COLS <= 96;
-  static constexpr uint32_t A_STAGE = 128 * BK;
+  static constexpr uint32_t A_STAGE = 128 * BK;  // the MMA reads 128 rows per CTA
   static constexpr uint32_t B_STAGE = B_ROWS * BK;
-  static constexpr uint32_t STAGE_TX = (A_STAGE + B_STAGE) * CG;  // bytes per stage, pair
+  static constexpr uint32_t STAGE_TX = (ROWS * BK + B_STAGE) * CG;  // bytes loaded, pair
+  static constexpr int SCALE_LOOKAHEAD = 6;  // K blocks of A-scale L1 prefetch
   static constexpr uint32_t SMEM_A = 0;
   static constexpr uint32_t SMEM_B = SMEM_A + STAGES * A_STAGE;
   static constexpr uint32_t SMEM_CTL = SMEM_B + STAGES * B_STAGE;
-  static constexpr uint32_t IDESC = idesc_f8f6f4_e4m3(BM, BN);
+  static constexpr uint32_t IDESC = idesc_f8f6f4_e4m3(128 * CG, BN);
+  static_assert(ROWS == 128 || ROWS == 96, "A rows per CTA");
+  __device__ static bool is_epilogue(uint32_t warp) {
+    return SPARE_QUARTER ? (warp & 3) != 3 : warp >= 4;
+  }
+  __device__ static uint32_t column_half(uint32_t warp) {
+    return SPARE_QUARTER ? warp >> 2 : (warp - 4) >> 2;
+  }
   static_assert(ACC_STAGES * BN <= (int)TMEM_COLS, "TMEM ring too large");
   static_assert(COLS % 16 == 0 && BN % 16 == 0 && B_ROWS % 8 == 0, "tile shape");
   static_assert(LOAD_ALL || COLS % 64 == 0, "two-phase epilogue works in 64-column halves");
@@ -102,7 +128,7 @@ __device__ __forceinline__ void promote16(float* acc, const uint32_t* p, float s
 }
 
 template <class C>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__global__ void __launch_bounds__(C::THREADS, 1)
 bsfp8_blockwise_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB, const GemmArgs args) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -150,12 +176,12 @@ bsfp8_blockwise_kernel(const __grid_constant__ CUtensorMap tmA,
     }
     for (int s = 0; s < C::ACC_STAGES; ++s) {
       mbar_init(tfull_bar(s), 1);                       // one MMA commit
-      mbar_init(tempty_bar(s), NUM_EPI_WARPS * C::CG);  // every epilogue warp of the pair
+      mbar_init(tempty_bar(s), C::NUM_EPI_WARPS * C::CG);  // every epilogue warp of the pair
     }
     mbar_init(smem_u32(&ctl->mma_done), 1);
     fence_mbarrier_init();
   }
-  if (warp == 1) {
+  if (warp == C::MMA_WARP) {
     tmem_alloc<C::CG>(smem_u32(&ctl->tmem_base), TMEM_COLS);
     tmem_relinquish<C::CG>();
   }
@@ -165,10 +191,10 @@ bsfp8_blockwise_kernel(const __grid_constant__ CUtensorMap tmA,
   tc_fence_after();
   const uint32_t tmem_base = ctl->tmem_base;
 
-  if (warp < EPI_WARP0) {
-    // warpgroup 0 (producer, MMA issuer, two idle warps) gives registers away
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 40;");
-    if (warp == 0 && lane == 0) {
+  if (!C::is_epilogue(warp)) {
+    // 128 rows: warpgroup 0 (producer, MMA issuer, two idle warps) gives registers away
+    if constexpr (!C::SPARE_QUARTER) asm volatile("setmaxnreg.dec.sync.aligned.u32 40;");
+    if (warp == C::PRODUCER_WARP && lane == 0) {
       // =============================== TMA producer ===============================
       GroupedScheduler<C::BM, C::BN> sched(args.offsets, args.E, args.N);
       // B (expert weights) is re-read by every row tile of its expert, possibly in a later
@@ -180,7 +206,7 @@ bsfp8_blockwise_kernel(const __grid_constant__ CUtensorMap tmA,
       TileCoord tc;
       for (int64_t t = tile0; ok && t < total_tiles; t += tile_stride) {
         if (!sched.locate(t, tc)) break;
-        const int32_t a_row = (int32_t)(tc.m0 + 128 * rank);
+        const int32_t a_row = (int32_t)(tc.m0 + C::ROWS * rank);
         const int32_t b_row = tc.e * args.N + tc.n0 + C::B_ROWS * rank;
         for (int kb = 0; kb < KB; ++kb) {
           if (!mbar_wait_cg<C::CG>(empty_bar(stage), phase ^ 1, abort)) {
@@ -212,7 +238,7 @@ bsfp8_blockwise_kernel(const __grid_constant__ CUtensorMap tmA,
         if (rank == 0) mbar_wait_timed(full_bar(stage), phase);
         else mbar_wait_timed(empty_bar(stage), phase);
       }
-    } else if (warp == 1 && lane == 0 && rank == 0) {
+    } else if (warp == C::MMA_WARP && lane == 0 && rank == 0) {
       // ================================ MMA issuer ================================
       GroupedScheduler<C::BM, C::BN> sched(args.offsets, args.E, args.N);
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
@@ -221,8 +247,9 @@ bsfp8_blockwise_kernel(const __grid_constant__ CUtensorMap tmA,
       for (int64_t t = tile0; ok && t < total_tiles; t += tile_stride) {
         if (!sched.locate(t, tc)) break;
         for (int kb = 0; kb < KB; ++kb) {
-          if (!mbar_wait_cg<C::CG>(tempty_bar(acc), acc_phase ^ 1, abort) ||
-              !mbar_wait_cg<C::CG>(full_bar(stage), phase, abort)) {
+          // operands first: they are usually in place well before the TMEM stage is free
+          if (!mbar_wait_cg<C::CG>(full_bar(stage), phase, abort) ||
+              !mbar_wait_cg<C::CG>(tempty_bar(acc), acc_phase ^ 1, abort)) {
             record_error(args.err, DEV_TIMEOUT, abort);
             ok = false;
             break;
@@ -254,10 +281,9 @@ bsfp8_blockwise_kernel(const __grid_constant__ CUtensorMap tmA,
     __syncwarp();
   } else {
     // ================================= epilogue =================================
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 232;");
-    const uint32_t ew = warp - EPI_WARP0;
-    const uint32_t quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
-    const uint32_t half = ew >> 2;      // columns half*COLS .. +COLS-1
+    if constexpr (!C::SPARE_QUARTER) asm volatile("setmaxnreg.inc.sync.aligned.u32 232;");
+    const uint32_t quarter = warp & 3;              // TMEM lanes 32*quarter .. +31
+    const uint32_t half = C::column_half(warp);     // columns half*COLS .. +COLS-1
     const int nblk = args.N / 128;
     const float* a_scales = static_cast<const float*>(args.a_scales);
     const float* b_scales = static_cast<const float*>(args.b_scales);
@@ -267,12 +293,14 @@ bsfp8_blockwise_kernel(const __grid_constant__ CUtensorMap tmA,
       return (C::CG == 2) ? mapa_shared(tempty_bar(s), 0) : tempty_bar(s);
     };
     GroupedScheduler<C::BM, C::BN> sched(args.offsets, args.E, args.N);
+    // C rows go out as one 32-byte sector per lane when C allows it
+    const bool c_vec32 = (reinterpret_cast<uintptr_t>(args.C) & 31) == 0;
     uint32_t acc_stage = 0, acc_phase = 0;
     bool ok = true;
     TileCoord tc;
     for (int64_t t = tile0; ok && t < total_tiles; t += tile_stride) {
       if (!sched.locate(t, tc)) break;
-      const int64_t row = tc.m0 + 128 * rank + quarter * 32 + lane;
+      const int64_t row = tc.m0 + C::ROWS * rank + quarter * 32 + lane;
       const bool row_in = row < args.M_total;
       const int col0 = tc.n0 + (int)half * C::COLS;  // first column of this warp
       // this warp's columns touch scale blocks col0/128 and (col0+COLS-1)/128 (<= 2)
@@ -285,12 +313,18 @@ bsfp8_blockwise_kernel(const __grid_constant__ CUtensorMap tmA,
       float acc[C::COLS];
 #pragma unroll
       for (int j = 0; j < C::COLS; ++j) acc[j] = 0.0f;
+      if (row_in) {
+        for (int k = 1; k < C::SCALE_LOOKAHEAD && k < KB; ++k)
+          prefetch_l1(sa_ptr + (int64_t)k * args.M_total);
+      }
       float sa_n = row_in ? ldg_f32(sa_ptr) : 0.0f;
       float sbl_n = lo_in ? ldg_f32(sb_lo) : 0.0f;
       float sbh_n = hi_in ? ldg_f32(sb_hi) : 0.0f;
       for (int kb = 0; kb < KB; ++kb) {
         const float s_lo = sa_n * sbl_n;
         const float s_hi = sa_n * sbh_n;
+        if (row_in && kb + C::SCALE_LOOKAHEAD < KB)
+          prefetch_l1(sa_ptr + (int64_t)(kb + C::SCALE_LOOKAHEAD) * args.M_total);
         if (kb + 1 < KB) {
           sa_n = row_in ? ldg_f32(sa_ptr + (int64_t)(kb + 1) * args.M_total) : 0.0f;
           sbl_n = lo_in ? ldg_f32(sb_lo + kb + 1) : 0.0f;
@@ -348,11 +382,16 @@ bsfp8_blockwise_kernel(const __grid_constant__ CUtensorMap tmA,
         for (int c = 0; c < C::CHUNKS; ++c) {
           if (col0 + 16 * c < args.N) {  // the last column tile may pass N
             const float* a = acc + 16 * c;
-            st_global_v4_hint(dst + 16 * c, pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]),
-                              pack_bf16x2(a[4], a[5]), pack_bf16x2(a[6], a[7]), pol_c);
-            st_global_v4_hint(dst + 16 * c + 8, pack_bf16x2(a[8], a[9]),
-                              pack_bf16x2(a[10], a[11]), pack_bf16x2(a[12], a[13]),
-                              pack_bf16x2(a[14], a[15]), pol_c);
+            uint32_t v[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v[j] = pack_bf16x2(a[2 * j], a[2 * j + 1]);
+            // N % 128 == 0 and col0 % 16 == 0: dst + 16c is 32-byte aligned when C is
+            if (c_vec32) {
+              st_global_v8_hint(dst + 16 * c, v, pol_c);
+            } else {
+              st_global_v4_hint(dst + 16 * c, v[0], v[1], v[2], v[3], pol_c);
+              st_global_v4_hint(dst + 16 * c + 8, v[4], v[5], v[6], v[7], pol_c);
+            }
           }
         }
       }
@@ -364,7 +403,7 @@ bsfp8_blockwise_kernel(const __grid_constant__ CUtensorMap tmA,
   __syncthreads();
   // the pair's MMAs and remote arrivals are finished before either CTA frees TMEM or exits
   if constexpr (C::CG == 2) cluster_sync();
-  if (warp == 1) {
+  if (warp == C::MMA_WARP) {
     tc_fence_after();
     tmem_dealloc<C::CG>(tmem_base, TMEM_COLS);
   }
@@ -390,7 +429,7 @@ cudaError_t launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArg
   const int grid = (int)((max_tiles < pairs ? max_tiles : pairs) * C::CG);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(NUM_THREADS);
+  cfg.blockDim = dim3(C::THREADS);
   cfg.dynamicSmemBytes = smem_bytes<C>();
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
@@ -406,11 +445,14 @@ cudaError_t launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArg
 // 1-CTA 128 x 256 (2 TMEM stages), CTA pair 256 x 256 (2 stages), CTA pair 256 x 160
 // (3 stages), CTA pair 256 x 128 (4 stages), 1-CTA 128 x 128 (4 stages).  With 160 or 128
 // columns each epilogue warp loads all of its columns at once and frees the stage early.
+// 1-CTA 96 x 256 and CTA pair 192 x 256: 96 A rows per CTA, role warps on their own SMSP.
 using Cta1x256 = Cfg<1, 256, 4, 2>;
 using Pair256 = Cfg<2, 256, 6, 2>;
 using Pair160 = Cfg<2, 160, 8, 3>;
 using Pair128 = Cfg<2, 128, 8, 4>;
 using Cta1x128 = Cfg<1, 128, 6, 4>;
+using Cta1x96x256 = Cfg<1, 256, 4, 2, 96>;
+using Pair192x256 = Cfg<2, 256, 6, 2, 96>;
 
 }  // namespace bw
 
@@ -421,8 +463,18 @@ int blockwise_b_rows(BlockwiseTile tile) {
     case TILE_PAIR_160: return bw::Pair160::B_ROWS;
     case TILE_PAIR_128: return bw::Pair128::B_ROWS;
     case TILE_CTA1_128: return bw::Cta1x128::B_ROWS;
+    case TILE_CTA1_96: return bw::Cta1x96x256::B_ROWS;
+    case TILE_PAIR_192: return bw::Pair192x256::B_ROWS;
   }
   return 0;
+}
+
+int blockwise_a_rows(BlockwiseTile tile) {
+  switch (tile) {
+    case TILE_CTA1_96: return bw::Cta1x96x256::ROWS;
+    case TILE_PAIR_192: return bw::Pair192x256::ROWS;
+    default: return 128;
+  }
 }
 
 cudaError_t launch_bsfp8_blockwise(BlockwiseTile tile, const CUtensorMap& tmA,
@@ -434,6 +486,8 @@ cudaError_t launch_bsfp8_blockwise(BlockwiseTile tile, const CUtensorMap& tmA,
     case TILE_PAIR_160: return bw::launch<bw::Pair160>(tmA, tmB, args, num_sms, stream);
     case TILE_PAIR_128: return bw::launch<bw::Pair128>(tmA, tmB, args, num_sms, stream);
     case TILE_CTA1_128: return bw::launch<bw::Cta1x128>(tmA, tmB, args, num_sms, stream);
+    case TILE_CTA1_96: return bw::launch<bw::Cta1x96x256>(tmA, tmB, args, num_sms, stream);
+    case TILE_PAIR_192: return bw::launch<bw::Pair192x256>(tmA, tmB, args, num_sms, stream);
   }
   return cudaErrorInvalidValue;
 }

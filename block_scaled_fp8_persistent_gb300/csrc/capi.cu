@@ -1,6 +1,7 @@
 // C-ABI entry points: argument checks on the host, tensor-map encoding, kernel launch.
 // Declarations and the contract live in include/bsfp8.h.
 #include <cstdlib>
+#include <cmath>
 #include <cstring>
 #include <mutex>
 
@@ -100,23 +101,40 @@ bsfp8_status check_common(const void* A, const void* B, const void* sa, const vo
   return BSFP8_OK;
 }
 
-// Tile configuration for a launch.  The 1-CTA 128 x 256 tile is the default: measured on
-// GB300 it is the fastest on every workload tried (the CTA-pair 256 x 256 tile moves fewer
-// operand bytes but is bound by the same per-K-block TMEM hand-off, and the 160/128-column
-// tiles lose more to the fixed cost of each K = 32 MMA than they gain from a deeper TMEM
-// ring).  The environment variable BSFP8_BLOCKWISE_TILE (cta1_256 | pair_256 | pair_160 |
-// pair_128 | cta1_128) selects another one.
-BlockwiseTile choose_blockwise_tile(int64_t M_total, int E) {
+// Estimated makespan of a blockwise tile configuration, in tiles: persistent CTAs (or CTA
+// pairs) take tiles with a static stride, so the busiest one runs ceil(tiles / units) of
+// them.  The expert offsets live on the device, so row tiles are estimated from M_total with
+// half a ragged tile per expert.
+double blockwise_makespan(int64_t M_total, int N, int E, int tile_rows, int units) {
+  const double row_tiles =
+      std::ceil((double)M_total / tile_rows) + (E > 1 ? 0.5 * (double)E : 0.0);
+  const double tiles = row_tiles * (double)((N + 255) / 256);
+  return std::ceil(tiles / (double)(units > 0 ? units : 1));
+}
+
+// Tile configuration for a launch.  The default is the 96 x 256 tile with the role warps on
+// the spare TMEM sub-partition, on one CTA or on a CTA pair (192 x 256), whichever has the
+// smaller estimated makespan; a pair tile runs about 3 % faster than two single-CTA tiles
+// (half the B bytes per SM) but there are half as many of them to spread over the SMs.
+// Measured on GB300 the 128-row tiles are slower: their epilogue warps share SMSPs with the
+// producer and MMA warps and lag them by up to ~1000 cycles per K block.  The environment
+// variable BSFP8_BLOCKWISE_TILE (cta1_96 | pair_192 | cta1_256 | pair_256 | pair_160 |
+// pair_128 | cta1_128) selects a configuration.
+constexpr double kPairTileTime = 0.97;  // pair 192 x 256 tile time / 1-CTA 96 x 256 tile time
+
+BlockwiseTile choose_blockwise_tile(int64_t M_total, int N, int E, int num_sms) {
   if (const char* v = std::getenv("BSFP8_BLOCKWISE_TILE")) {
     if (!std::strcmp(v, "cta1_256")) return TILE_CTA1_256;
     if (!std::strcmp(v, "pair_256")) return TILE_PAIR_256;
     if (!std::strcmp(v, "pair_160")) return TILE_PAIR_160;
     if (!std::strcmp(v, "pair_128")) return TILE_PAIR_128;
     if (!std::strcmp(v, "cta1_128")) return TILE_CTA1_128;
+    if (!std::strcmp(v, "cta1_96")) return TILE_CTA1_96;
+    if (!std::strcmp(v, "pair_192")) return TILE_PAIR_192;
   }
-  (void)M_total;
-  (void)E;
-  return TILE_CTA1_256;
+  const double single = blockwise_makespan(M_total, N, E, 96, num_sms);
+  const double pair = blockwise_makespan(M_total, N, E, 192, num_sms / 2) * kPairTileTime;
+  return pair < single ? TILE_PAIR_192 : TILE_CTA1_96;
 }
 
 // MXFP8 kernel choice: experts averaging at least 256 token rows use the CTA-pair 256 x 256
@@ -156,9 +174,10 @@ extern "C" bsfp8_status bsfp8_grouped_gemm(const void* A, const void* B, const f
   DeviceInfo* dev = nullptr;
   if ((st = device_info(&dev)) != BSFP8_OK) return st;
   if (M_total == 0) return BSFP8_OK;
-  const BlockwiseTile tile = choose_blockwise_tile(M_total, num_experts);
+  const BlockwiseTile tile = choose_blockwise_tile(M_total, N, num_experts, dev->num_sms);
   CUtensorMap tmA, tmB;
-  if (!encode_u8_2d(&tmA, A, (uint64_t)K, (uint64_t)M_total, 128, 128) ||
+  if (!encode_u8_2d(&tmA, A, (uint64_t)K, (uint64_t)M_total, 128,
+                    (uint32_t)blockwise_a_rows(tile)) ||
       !encode_u8_2d(&tmB, B, (uint64_t)K, (uint64_t)num_experts * N, 128,
                     (uint32_t)blockwise_b_rows(tile)))
     return BSFP8_ERR_CUDA;
@@ -214,6 +233,20 @@ extern "C" bsfp8_status bsmxfp8_tmem_plan(int block_k, int epilogue_n, int vec, 
                         p.right_cols,     p.a_scale_offset, p.a_scale_cols,
                         p.b_scale_offset, p.b_scale_cols, p.early_release_subtile};
   for (int i = 0; i < 9; ++i) out[i] = v[i];
+  return BSFP8_OK;
+}
+
+extern "C" bsfp8_status bsfp8_blockwise_plan(int64_t M_total, int N, int num_experts,
+                                            int num_sms, int32_t* out) {
+  if (!out) return BSFP8_ERR_NULL;
+  if (M_total < 0 || N < 128 || N % 128 != 0 || num_experts < 1 || num_sms < 2)
+    return BSFP8_ERR_SHAPE;
+  const BlockwiseTile tile = choose_blockwise_tile(M_total, N, num_experts, num_sms);
+  const int ctas = (tile == TILE_PAIR_256 || tile == TILE_PAIR_160 || tile == TILE_PAIR_128 ||
+                    tile == TILE_PAIR_192) ? 2 : 1;
+  out[0] = blockwise_a_rows(tile) * ctas;
+  out[1] = blockwise_b_rows(tile) * ctas;
+  out[2] = ctas;
   return BSFP8_OK;
 }
 

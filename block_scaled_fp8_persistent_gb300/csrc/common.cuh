@@ -34,10 +34,14 @@ enum BlockwiseTile : int {
   TILE_PAIR_160 = 2,  // CTA pair, 256 x 160 tile, 3-deep TMEM ring
   TILE_PAIR_128 = 3,  // CTA pair, 256 x 128 tile, 4-deep TMEM ring
   TILE_CTA1_128 = 4,  // one CTA, 128 x 128 tile, 4-deep TMEM ring
+  TILE_CTA1_96 = 5,   // one CTA, 96 x 256 tile, role warps on the spare TMEM sub-partition
+  TILE_PAIR_192 = 6,  // CTA pair, 192 x 256 tile, the same per CTA
 };
 
 // Rows of B each CTA loads per stage (the B tensor map's box height) for a tile config.
 int blockwise_b_rows(BlockwiseTile tile);
+// Rows of A each CTA loads per stage (the A tensor map's box height).
+int blockwise_a_rows(BlockwiseTile tile);
 
 // Launchers (one per kernel family); return the launch error.
 cudaError_t launch_bsfp8_blockwise(BlockwiseTile tile, const CUtensorMap& tmA,

@@ -426,6 +426,11 @@ __device__ __forceinline__ void cp_async_wait_group() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// Bring the line holding p into this SM's L1 (no register, nothing waits for it).
+__device__ __forceinline__ void prefetch_l1(const void* p) {
+  asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
+}
+
 // ---------------------------------------------------------------------------
 // misc
 // ---------------------------------------------------------------------------
@@ -446,6 +451,15 @@ __device__ __forceinline__ void st_global_v4_hint(void* p, uint32_t a, uint32_t 
                                                   uint32_t d, uint64_t policy) {
   asm volatile("st.global.L2::cache_hint.v4.b32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "r"(a),
                "r"(b), "r"(c), "r"(d), "l"(policy)
+               : "memory");
+}
+
+// 32-byte store (p 32-byte aligned): one full L2 sector per lane.
+__device__ __forceinline__ void st_global_v8_hint(void* p, const uint32_t (&v)[8],
+                                                  uint64_t policy) {
+  asm volatile("st.global.L2::cache_hint.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8}, %9;" ::"l"(p),
+               "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]),
+               "r"(v[7]), "l"(policy)
                : "memory");
 }
 

@@ -35,7 +35,8 @@
  *     with bsfp8_get_device_error().
  *   - Requirements: N % 128 == 0, K % 128 == 0, num_experts >= 1, 0 <= M_total < 2^31,
  *     num_experts * N < 2^31; A, B, C 16-byte aligned; scales and offsets 4-byte aligned
- *     (also the UE8M0 scale arrays, which are read 4 codes at a time).
+ *     (also the UE8M0 scale arrays, which are read 4 codes at a time).  A 32-byte aligned C
+ *     is written with 32-byte stores (faster), a 16-byte aligned one with 16-byte stores.
  *     M_total == 0 is a valid no-op (nothing is read or written).
  *   - The device must be compute capability 10.3 (GB300).
  */
@@ -124,6 +125,19 @@ bsfp8_status bsmxfp8_grouped_gemm(const void* A, const void* B, const uint8_t* a
  * bsmxfp8_grouped_gemm is compiled with.  BSFP8_ERR_NULL / BSFP8_ERR_SHAPE on bad input.
  */
 bsfp8_status bsmxfp8_tmem_plan(int block_k, int epilogue_n, int vec, int overlap, int32_t* out);
+
+/*
+ * Tile plan bsfp8_grouped_gemm uses for a problem of this size on a device with num_sms SMs
+ * (host only, no GPU use; BSFP8_BLOCKWISE_TILE is honoured as in the GEMM): writes out[0] =
+ * tile rows, out[1] = tile columns, out[2] = CTAs per tile (1, or 2 for a CTA pair).  The
+ * persistent kernel gives each CTA (pair) every (SMs / CTAs per tile)-th tile; tiles are
+ * ceil(M_e / rows) x ceil(N / columns) per expert e.  The default picks 96 x 256 tiles on
+ * one CTA or 192 x 256 on a pair by estimated makespan (the tile rows leave the TMEM lanes
+ * of one SM sub-partition to the producer and MMA warps).  This is a performance choice
+ * only: every plan computes the same result.  BSFP8_ERR_NULL / BSFP8_ERR_SHAPE on bad input.
+ */
+bsfp8_status bsfp8_blockwise_plan(int64_t M_total, int N, int num_experts, int num_sms,
+                                  int32_t* out);
 
 /*
  * Read the device error word of the current device (after synchronising `stream`) into

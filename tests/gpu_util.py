@@ -9,7 +9,7 @@ import block_scaled_fp8_persistent_gb300 as bsfp8
 
 
 class DeviceProblem:
-    def __init__(self, p, c_rows_extra: int = 0, sentinel: int = 0x7FC1):
+    def __init__(self, p, c_rows_extra: int = 0, sentinel: int = 0x7FC1, c_offset: int = 0):
         dev = torch.device("cuda", 0)
         self.p = p
         self.A = torch.from_numpy(np.ascontiguousarray(p.A)).to(dev)
@@ -17,9 +17,12 @@ class DeviceProblem:
         self.sa = torch.from_numpy(np.ascontiguousarray(p.a_scales)).to(dev)
         self.sb = torch.from_numpy(np.ascontiguousarray(p.b_scales)).to(dev)
         self.off = torch.from_numpy(np.ascontiguousarray(p.offsets)).to(dev)
-        # C with optional guard rows after M_total, filled with a sentinel bit pattern
-        self.C_full = torch.full((p.M_total + c_rows_extra, p.N), sentinel, dtype=torch.int16,
-                                 device=dev).view(torch.bfloat16)
+        # C with optional guard rows after M_total, filled with a sentinel bit pattern, and
+        # optionally starting c_offset bf16 elements into its allocation (c_offset = 8 makes
+        # C 16-byte but not 32-byte aligned)
+        rows = p.M_total + c_rows_extra
+        flat = torch.full((c_offset + rows * p.N,), sentinel, dtype=torch.int16, device=dev)
+        self.C_full = flat[c_offset:].view(rows, p.N).view(torch.bfloat16)
         self.C = self.C_full[: p.M_total]
         self.sentinel = sentinel
 

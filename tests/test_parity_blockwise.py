@@ -14,7 +14,7 @@ from helpers import parity_report
 
 pytestmark = pytest.mark.gpu
 
-TILES = ["cta1_256", "pair_256", "pair_160", "pair_128", "cta1_128"]
+TILES = ["cta1_256", "pair_256", "pair_160", "pair_128", "cta1_128", "cta1_96", "pair_192"]
 
 
 @pytest.fixture(params=TILES)
@@ -27,7 +27,7 @@ def tile(request, monkeypatch):
 def _check_full(p, **kw):
     from gpu_util import DeviceProblem
     import block_scaled_fp8_persistent_gb300 as bsfp8
-    d = DeviceProblem(p, c_rows_extra=3)
+    d = DeviceProblem(p, c_rows_extra=3, **kw)
     d.run()
     got = d.c_bits()
     assert bsfp8.bsfp8_get_device_error() == 0
@@ -60,6 +60,12 @@ def test_exact_inputs_bitwise(counts, N, K, tile):
     p = gen.blockwise_problem(counts, N, K, seed=7, exact=True)
     got, ref = _check_full(p)
     assert np.array_equal(got, ref)
+
+
+def test_c_only_16_byte_aligned(tile):
+    # C 16-byte aligned (the documented minimum) but not 32-byte aligned
+    p = gen.blockwise_problem([150, 0, 61], 384, 512, seed=35)
+    _check_full(p, c_offset=8)
 
 
 def test_outlier_rows(tile):
