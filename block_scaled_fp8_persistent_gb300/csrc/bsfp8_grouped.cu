@@ -121,10 +121,37 @@ __device__ __forceinline__ void record_error(int* err, int code, volatile int* a
   *abort = 1;
 }
 
-// Promote 16 columns: acc[j] = fma(s, partial[j], acc[j]).
-__device__ __forceinline__ void promote16(float* acc, const uint32_t* p, float s) {
+// Promote 16 columns: acc[j] = fma(s, partial[j], acc[j]), two columns per packed fp32
+// FMA (each lane of it rounds exactly like fmaf).
+__device__ __forceinline__ void promote16(float2* acc, const uint32_t* p, float s) {
+  const float2 s2 = make_float2(s, s);
 #pragma unroll
-  for (int j = 0; j < 16; ++j) acc[j] = fmaf(s, __uint_as_float(p[j]), acc[j]);
+  for (int j = 0; j < 8; ++j)
+    acc[j] = __ffma2_rn(s2, make_float2(__uint_as_float(p[2 * j]), __uint_as_float(p[2 * j + 1])),
+                        acc[j]);
+}
+
+// Issue the MMAs of one K block: 4 x tcgen05.mma kind::f8f6f4 (K = 32 e4m3 each, 32 bytes
+// along the swizzled row) from operand stage `stage` into the TMEM partial `acc`, then
+// commit "operands consumed" to empty_bar and "partial ready" to tfull_bar.
+template <class C>
+__device__ __forceinline__ void issue_kblock(uint32_t tmem_base, uint32_t sA, uint32_t sB,
+                                             uint32_t stage, uint32_t acc, uint32_t empty_bar,
+                                             uint32_t tfull_bar) {
+  const uint32_t d_tmem = tmem_base + acc * C::BN;
+  const uint64_t adesc = kmajor_sw128_desc(sA + stage * C::A_STAGE);
+  const uint64_t bdesc = kmajor_sw128_desc(sB + stage * C::B_STAGE);
+#pragma unroll
+  for (int k = 0; k < BK / 32; ++k)
+    umma_f8f6f4<C::CG>(d_tmem, adesc + (uint64_t)(k * 2), bdesc + (uint64_t)(k * 2), C::IDESC,
+                       k > 0 ? 1u : 0u);
+  if constexpr (C::CG == 1) {
+    umma_commit(empty_bar);
+    umma_commit(tfull_bar);
+  } else {
+    umma_commit_pair(empty_bar, 0x3);
+    umma_commit_pair(tfull_bar, 0x3);
+  }
 }
 
 template <class C>
@@ -255,20 +282,7 @@ bsfp8_blockwise_kernel(const __grid_constant__ CUtensorMap tmA,
             break;
           }
           tc_fence_after();
-          const uint32_t d_tmem = tmem_base + acc * C::BN;
-          const uint64_t adesc = kmajor_sw128_desc(sA + stage * C::A_STAGE);
-          const uint64_t bdesc = kmajor_sw128_desc(sB + stage * C::B_STAGE);
-#pragma unroll
-          for (int k = 0; k < BK / 32; ++k)  // K = 32 e4m3 per instruction, 32 bytes
-            umma_f8f6f4<C::CG>(d_tmem, adesc + (uint64_t)(k * 2), bdesc + (uint64_t)(k * 2),
-                               C::IDESC, k > 0 ? 1u : 0u);
-          if constexpr (C::CG == 1) {
-            umma_commit(empty_bar(stage));  // operands consumed -> stage free
-            umma_commit(tfull_bar(acc));    // partial ready for the epilogue
-          } else {
-            umma_commit_pair(empty_bar(stage), 0x3);
-            umma_commit_pair(tfull_bar(acc), 0x3);
-          }
+          issue_kblock<C>(tmem_base, sA, sB, stage, acc, empty_bar(stage), tfull_bar(acc));
           if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
           if (++acc == C::ACC_STAGES) { acc = 0; acc_phase ^= 1; }
         }
@@ -296,6 +310,13 @@ bsfp8_blockwise_kernel(const __grid_constant__ CUtensorMap tmA,
     // C rows go out as one 32-byte sector per lane when C allows it
     const bool c_vec32 = (reinterpret_cast<uintptr_t>(args.C) & 31) == 0;
     uint32_t acc_stage = 0, acc_phase = 0;
+    // This warp has finished reading TMEM stage acc_stage: tell the MMA thread (in the MMA
+    // CTA of a pair).
+    auto release_stage = [&]() {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster_or_local<C::CG>(tempty_mma(acc_stage));
+    };
     bool ok = true;
     TileCoord tc;
     for (int64_t t = tile0; ok && t < total_tiles; t += tile_stride) {
@@ -310,9 +331,9 @@ bsfp8_blockwise_kernel(const __grid_constant__ CUtensorMap tmA,
       const float* sa_ptr = a_scales + (row_in ? row : 0);
       const float* sb_lo = b_scales + ((int64_t)tc.e * nblk + (lo_in ? blk_lo : 0)) * KB;
       const float* sb_hi = b_scales + ((int64_t)tc.e * nblk + (hi_in ? blk_hi : 0)) * KB;
-      float acc[C::COLS];
+      float2 acc[C::COLS / 2];  // columns 2j, 2j+1
 #pragma unroll
-      for (int j = 0; j < C::COLS; ++j) acc[j] = 0.0f;
+      for (int j = 0; j < C::COLS / 2; ++j) acc[j] = make_float2(0.0f, 0.0f);
       if (row_in) {
         for (int k = 1; k < C::SCALE_LOOKAHEAD && k < KB; ++k)
           prefetch_l1(sa_ptr + (int64_t)k * args.M_total);
@@ -347,11 +368,9 @@ bsfp8_blockwise_kernel(const __grid_constant__ CUtensorMap tmA,
 #pragma unroll
           for (int c = 0; c < C::CHUNKS; ++c) tmem_ld_32x32b_x16(taddr + 16 * c, p[c]);
           tmem_ld_wait();
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive_cluster_or_local<C::CG>(tempty_mma(acc_stage));
+          release_stage();
 #pragma unroll
-          for (int c = 0; c < C::CHUNKS; ++c) promote16(acc + 16 * c, p[c], chunk_scale(c));
+          for (int c = 0; c < C::CHUNKS; ++c) promote16(acc + 8 * c, p[c], chunk_scale(c));
         } else {
           // 64-column halves: load, promote, ..., load the last half, release, promote
           uint32_t p0[32], p1[32];
@@ -360,15 +379,11 @@ bsfp8_blockwise_kernel(const __grid_constant__ CUtensorMap tmA,
             tmem_ld_32x32b_x32(taddr + 64 * h, p0);
             tmem_ld_32x32b_x32(taddr + 64 * h + 32, p1);
             tmem_ld_wait();
-            if (h == C::COLS / 64 - 1) {
-              tc_fence_before();
-              __syncwarp();
-              if (lane == 0) mbar_arrive_cluster_or_local<C::CG>(tempty_mma(acc_stage));
-            }
-            promote16(acc + 64 * h + 0, p0, chunk_scale(4 * h + 0));
-            promote16(acc + 64 * h + 16, p0 + 16, chunk_scale(4 * h + 1));
-            promote16(acc + 64 * h + 32, p1, chunk_scale(4 * h + 2));
-            promote16(acc + 64 * h + 48, p1 + 16, chunk_scale(4 * h + 3));
+            if (h == C::COLS / 64 - 1) release_stage();
+            promote16(acc + 32 * h + 0, p0, chunk_scale(4 * h + 0));
+            promote16(acc + 32 * h + 8, p0 + 16, chunk_scale(4 * h + 1));
+            promote16(acc + 32 * h + 16, p1, chunk_scale(4 * h + 2));
+            promote16(acc + 32 * h + 24, p1 + 16, chunk_scale(4 * h + 3));
           }
         }
         if (++acc_stage == C::ACC_STAGES) { acc_stage = 0; acc_phase ^= 1; }
@@ -381,10 +396,10 @@ bsfp8_blockwise_kernel(const __grid_constant__ CUtensorMap tmA,
 #pragma unroll
         for (int c = 0; c < C::CHUNKS; ++c) {
           if (col0 + 16 * c < args.N) {  // the last column tile may pass N
-            const float* a = acc + 16 * c;
+            const float2* a = acc + 8 * c;
             uint32_t v[8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) v[j] = pack_bf16x2(a[2 * j], a[2 * j + 1]);
+            for (int j = 0; j < 8; ++j) v[j] = pack_bf16x2(a[j].x, a[j].y);
             // N % 128 == 0 and col0 % 16 == 0: dst + 16c is 32-byte aligned when C is
             if (c_vec32) {
               st_global_v8_hint(dst + 16 * c, v, pol_c);
