@@ -35,8 +35,16 @@ sys.path.insert(0, ROOT)
 METRIC = "grouped blockwise-FP8 GEMM TFLOP/s and % of GB300 FP8 tensor peak (1 GPU)"
 FP8_PER_BF16 = 2.0  # nominal dense fp8 / bf16 tensor throughput ratio (4.5 / 2.25 PFLOP/s)
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-KERNEL_SOURCES = ("ptx.cuh", "sched.cuh", "common.cuh", "tmem_plan.cuh", "bsfp8_grouped.cu",
-                  "bsmxfp8_grouped.cu", "bsmxfp8_pair.cu")
+# The sources each workload's kernel is built from: a committed ncu summary is used for
+# `traffic` only while these are byte-identical to the ones it was captured on.
+_COMMON_SOURCES = ("ptx.cuh", "sched.cuh", "common.cuh", "tmem_plan.cuh")
+KERNEL_SOURCES = {
+    "blockwise": _COMMON_SOURCES + ("bsfp8_grouped.cu",),
+    "mx_swap": _COMMON_SOURCES + ("bsmxfp8_grouped.cu",),
+    "mx_pair": _COMMON_SOURCES + ("bsmxfp8_pair.cu",),
+}
+WORKLOAD_KERNEL = {"config0": "blockwise", "config1": "blockwise", "config2": "blockwise",
+                   "config3": "blockwise", "config4": "mx_swap", "config5": "mx_pair"}
 
 
 def log(*a):
@@ -55,10 +63,11 @@ def load_peaks():
     return dict(FALLBACK), "fallback"
 
 
-def kernel_hash() -> str:
+def kernel_hash(workload_key: str = "config1") -> str:
+    """First 12 hex digits of the SHA-256 over the sources of this workload's kernel."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "block_scaled_fp8_persistent_gb300", "csrc")
-    for name in KERNEL_SOURCES:
+    for name in KERNEL_SOURCES[WORKLOAD_KERNEL[workload_key]]:
         p = os.path.join(csrc, name)
         if os.path.exists(p):
             with open(p, "rb") as f:
@@ -72,7 +81,7 @@ def traffic_from_profiles(workload_key: str):
     pdir = os.path.join(ROOT, "profiles")
     if not os.path.isdir(pdir):
         return None, None
-    want = kernel_hash()
+    want = kernel_hash(workload_key)
     for name in sorted(os.listdir(pdir)):
         if not name.endswith(".txt"):
             continue
@@ -448,7 +457,7 @@ def run_ours(args):
         "step_ms": {"min": min(step_ms), "median": statistics.median(step_ms), "max": max(step_ms)},
         "wall_s_timed_region": wall1 - wall0,
         "device_error": dev_err,
-        "kernel_sources_sha256_12": kernel_hash(),
+        "kernel_sources_sha256_12": kernel_hash(f"config{cfg}"),
     }
     if secondary is not None:
         line["secondary"] = secondary
