@@ -295,6 +295,38 @@ def time_secondary(cfg, args, flush, stream, peaks, peak_src):
     return out
 
 
+def time_expert_ids(p, d, C, args, flush, stream):
+    """The same workload routed through the expert indirection (group g multiplies expert
+    perm[g] of the same B, perm a seeded permutation) with the same protocol."""
+    import numpy as np
+    import torch
+    import block_scaled_fp8_persistent_gb300 as bsfp8
+    perm = np.random.default_rng(p.E).permutation(p.E).astype(np.int32)
+    ids = torch.from_numpy(perm).to(flush.device)
+    fn = bsfp8.bsfp8_grouped_gemm_ids if p.mode == "blockwise" else bsfp8.bsmxfp8_grouped_gemm_ids
+
+    def step():
+        fn(d["A"], d["B"], d["a_scales"], d["b_scales"], d["offsets"], ids, C, p.M_total, p.N,
+           p.K, p.E, p.E, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    ms = statistics.mean(s.elapsed_time(e) for s, e in zip(starts, ends))
+    return {"workload": "the main workload with group g on expert perm[g] (seeded permutation)",
+            "entry_point": fn.__name__, "expert_ids": perm.tolist(), "ms_per_step": ms,
+            "value": p.flops() / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+            "device_error": bsfp8.bsfp8_get_device_error(stream), "gpu_launches": args.steps}
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -429,6 +461,9 @@ def run_ours(args):
     if prof_file:
         roof["traffic_source"] = f"profiles/{prof_file}"
 
+    # ---- the same workload through the expert indirection (group -> expert ids) ----
+    routed = None if args.no_secondary else time_expert_ids(p, d, C, args, flush, stream)
+
     # ---- the second mode of the path: the MXFP8 decode workload, timed the same way ----
     secondary = extra = None
     if not args.no_secondary and cfg != 4:
@@ -459,6 +494,8 @@ def run_ours(args):
         "device_error": dev_err,
         "kernel_sources_sha256_12": kernel_hash(f"config{cfg}"),
     }
+    if routed is not None:
+        line["expert_ids_variant"] = routed
     if secondary is not None:
         line["secondary"] = secondary
     if extra is not None:

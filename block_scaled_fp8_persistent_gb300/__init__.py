@@ -25,12 +25,13 @@ BSFP8_OK = 0
 STATUS_NAMES = {
     0: "BSFP8_OK", 1: "BSFP8_ERR_NULL", 2: "BSFP8_ERR_SHAPE", 3: "BSFP8_ERR_ALIGN",
     4: "BSFP8_ERR_UNSUPPORTED_DEVICE", 5: "BSFP8_ERR_CUDA", 6: "BSFP8_ERR_DEVICE_OFFSETS",
-    7: "BSFP8_ERR_DEVICE_TIMEOUT",
+    7: "BSFP8_ERR_DEVICE_TIMEOUT", 8: "BSFP8_ERR_DEVICE_EXPERT_IDS",
 }
 
 # Every symbol include/bsfp8.h declares (the CPU test checks the library exports them).
-EXPORTED = ("bsfp8_grouped_gemm", "bsmxfp8_grouped_gemm", "bsmxfp8_tmem_plan",
-            "bsfp8_blockwise_plan", "bsfp8_get_device_error", "bsfp8_status_string")
+EXPORTED = ("bsfp8_grouped_gemm", "bsmxfp8_grouped_gemm", "bsfp8_grouped_gemm_ids",
+            "bsmxfp8_grouped_gemm_ids", "bsmxfp8_tmem_plan", "bsfp8_blockwise_plan",
+            "bsfp8_get_device_error", "bsfp8_status_string")
 
 
 class BsFp8Error(RuntimeError):
@@ -55,6 +56,10 @@ def load_library() -> ctypes.CDLL:
         lib.bsfp8_grouped_gemm.restype = i32
         lib.bsmxfp8_grouped_gemm.argtypes = [p, p, p, p, p, p, i64, i32, i32, i32, p]
         lib.bsmxfp8_grouped_gemm.restype = i32
+        lib.bsfp8_grouped_gemm_ids.argtypes = [p, p, p, p, p, p, p, i64, i32, i32, i32, i32, p]
+        lib.bsfp8_grouped_gemm_ids.restype = i32
+        lib.bsmxfp8_grouped_gemm_ids.argtypes = [p, p, p, p, p, p, p, i64, i32, i32, i32, i32, p]
+        lib.bsmxfp8_grouped_gemm_ids.restype = i32
         lib.bsmxfp8_tmem_plan.argtypes = [i32, i32, i32, i32, ctypes.POINTER(ctypes.c_int32)]
         lib.bsmxfp8_tmem_plan.restype = i32
         lib.bsfp8_blockwise_plan.argtypes = [ctypes.c_int64, i32, i32, i32,
@@ -111,6 +116,31 @@ def bsmxfp8_grouped_gemm(A, B, a_scales, b_scales, expert_offsets, C, M_total: i
                                              int(K), int(num_experts), _stream(stream))
     if st != BSFP8_OK:
         raise BsFp8Error(st, "bsmxfp8_grouped_gemm")
+
+
+def bsfp8_grouped_gemm_ids(A, B, a_scales, b_scales, group_offsets, expert_ids, C, M_total: int,
+                           N: int, K: int, num_groups: int, num_experts: int, stream=None) -> None:
+    """Blockwise FP8 grouped GEMM where group g uses expert expert_ids[g]'s weights; see
+    include/bsfp8.h.  Raises BsFp8Error."""
+    st = load_library().bsfp8_grouped_gemm_ids(
+        _addr(A), _addr(B), _addr(a_scales), _addr(b_scales), _addr(group_offsets),
+        _addr(expert_ids), _addr(C), int(M_total), int(N), int(K), int(num_groups),
+        int(num_experts), _stream(stream))
+    if st != BSFP8_OK:
+        raise BsFp8Error(st, "bsfp8_grouped_gemm_ids")
+
+
+def bsmxfp8_grouped_gemm_ids(A, B, a_scales, b_scales, group_offsets, expert_ids, C,
+                             M_total: int, N: int, K: int, num_groups: int, num_experts: int,
+                             stream=None) -> None:
+    """MXFP8 grouped GEMM where group g uses expert expert_ids[g]'s weights; see
+    include/bsfp8.h.  Raises BsFp8Error."""
+    st = load_library().bsmxfp8_grouped_gemm_ids(
+        _addr(A), _addr(B), _addr(a_scales), _addr(b_scales), _addr(group_offsets),
+        _addr(expert_ids), _addr(C), int(M_total), int(N), int(K), int(num_groups),
+        int(num_experts), _stream(stream))
+    if st != BSFP8_OK:
+        raise BsFp8Error(st, "bsmxfp8_grouped_gemm_ids")
 
 
 def bsmxfp8_tmem_plan(block_k: int, epilogue_n: int, vec: int, overlap: bool) -> dict:

@@ -172,14 +172,15 @@ bsfp8_blockwise_kernel(const __grid_constant__ CUtensorMap tmA,
 
   // ---- work discovery: validate the offsets, count tiles (same answer in every CTA) ----
   if (warp == 0) {
-    int ok;
+    int status;
     int64_t row_tiles;
-    validate_offsets<C::BM>(args.offsets, args.E, args.M_total, ok, row_tiles);
+    validate_offsets<C::BM>(args.offsets, args.expert_ids, args.E, args.num_experts, args.M_total,
+                            DEV_BAD_OFFSETS, DEV_BAD_EXPERT_IDS, status, row_tiles);
     if (lane == 0) {
-      ctl->valid = ok;
+      ctl->valid = status == 0;
       ctl->total_tiles = row_tiles * ((args.N + C::BN - 1) / C::BN);
       ctl->abort = 0;
-      if (!ok && blockIdx.x == 0) atomicCAS(args.err, 0, DEV_BAD_OFFSETS);
+      if (status && blockIdx.x == 0) atomicCAS(args.err, 0, status);
     }
   }
   __syncthreads();
@@ -223,7 +224,7 @@ bsfp8_blockwise_kernel(const __grid_constant__ CUtensorMap tmA,
     if constexpr (!C::SPARE_QUARTER) asm volatile("setmaxnreg.dec.sync.aligned.u32 40;");
     if (warp == C::PRODUCER_WARP && lane == 0) {
       // =============================== TMA producer ===============================
-      GroupedScheduler<C::BM, C::BN> sched(args.offsets, args.E, args.N);
+      GroupedScheduler<C::BM, C::BN> sched;
       // B (expert weights) is re-read by every row tile of its expert, possibly in a later
       // wave of tiles: keep it in L2 ahead of the streaming A rows and C output.
       const uint64_t pol_b = l2_policy_evict_last();
@@ -232,9 +233,9 @@ bsfp8_blockwise_kernel(const __grid_constant__ CUtensorMap tmA,
       bool ok = true;
       TileCoord tc;
       for (int64_t t = tile0; ok && t < total_tiles; t += tile_stride) {
-        if (!sched.locate(t, tc)) break;
+        if (!sched.locate(args, t, tc)) break;
         const int32_t a_row = (int32_t)(tc.m0 + C::ROWS * rank);
-        const int32_t b_row = tc.e * args.N + tc.n0 + C::B_ROWS * rank;
+        const int32_t b_row = tc.be * args.N + tc.n0 + C::B_ROWS * rank;
         for (int kb = 0; kb < KB; ++kb) {
           if (!mbar_wait_cg<C::CG>(empty_bar(stage), phase ^ 1, abort)) {
             record_error(args.err, DEV_TIMEOUT, abort);
@@ -267,12 +268,12 @@ bsfp8_blockwise_kernel(const __grid_constant__ CUtensorMap tmA,
       }
     } else if (warp == C::MMA_WARP && lane == 0 && rank == 0) {
       // ================================ MMA issuer ================================
-      GroupedScheduler<C::BM, C::BN> sched(args.offsets, args.E, args.N);
+      GroupedScheduler<C::BM, C::BN> sched;
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
       TileCoord tc;
       for (int64_t t = tile0; ok && t < total_tiles; t += tile_stride) {
-        if (!sched.locate(t, tc)) break;
+        if (!sched.locate(args, t, tc)) break;
         for (int kb = 0; kb < KB; ++kb) {
           // operands first: they are usually in place well before the TMEM stage is free
           if (!mbar_wait_cg<C::CG>(full_bar(stage), phase, abort) ||
@@ -306,7 +307,7 @@ bsfp8_blockwise_kernel(const __grid_constant__ CUtensorMap tmA,
     auto tempty_mma = [&](int s) {
       return (C::CG == 2) ? mapa_shared(tempty_bar(s), 0) : tempty_bar(s);
     };
-    GroupedScheduler<C::BM, C::BN> sched(args.offsets, args.E, args.N);
+    GroupedScheduler<C::BM, C::BN> sched;
     // C rows go out as one 32-byte sector per lane when C allows it
     const bool c_vec32 = (reinterpret_cast<uintptr_t>(args.C) & 31) == 0;
     uint32_t acc_stage = 0, acc_phase = 0;
@@ -320,7 +321,7 @@ bsfp8_blockwise_kernel(const __grid_constant__ CUtensorMap tmA,
     bool ok = true;
     TileCoord tc;
     for (int64_t t = tile0; ok && t < total_tiles; t += tile_stride) {
-      if (!sched.locate(t, tc)) break;
+      if (!sched.locate(args, t, tc)) break;
       const int64_t row = tc.m0 + C::ROWS * rank + quarter * 32 + lane;
       const bool row_in = row < args.M_total;
       const int col0 = tc.n0 + (int)half * C::COLS;  // first column of this warp
@@ -329,8 +330,10 @@ bsfp8_blockwise_kernel(const __grid_constant__ CUtensorMap tmA,
       const int blk_hi = (col0 + C::COLS - 1) / 128;
       const bool lo_in = blk_lo < nblk, hi_in = blk_hi < nblk;
       const float* sa_ptr = a_scales + (row_in ? row : 0);
-      const float* sb_lo = b_scales + ((int64_t)tc.e * nblk + (lo_in ? blk_lo : 0)) * KB;
-      const float* sb_hi = b_scales + ((int64_t)tc.e * nblk + (hi_in ? blk_hi : 0)) * KB;
+      // the group's expert, re-read per tile (kept out of the scheduler's live registers)
+      const int64_t be = args.expert_ids ? ldg_s32(args.expert_ids + tc.e) : tc.e;
+      const float* sb_lo = b_scales + (be * nblk + (lo_in ? blk_lo : 0)) * KB;
+      const float* sb_hi = b_scales + (be * nblk + (hi_in ? blk_hi : 0)) * KB;
       float2 acc[C::COLS / 2];  // columns 2j, 2j+1
 #pragma unroll
       for (int j = 0; j < C::COLS / 2; ++j) acc[j] = make_float2(0.0f, 0.0f);

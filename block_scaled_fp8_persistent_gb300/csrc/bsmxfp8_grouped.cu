@@ -110,14 +110,15 @@ bsmxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 
   // Tiles: per expert ceil(M_e / TN) token tiles x N/128 weight tiles (weights fastest).
   if (warp == 0) {
-    int ok;
+    int status;
     int64_t row_tiles;
-    validate_offsets<C::TN>(args.offsets, args.E, args.M_total, ok, row_tiles);
+    validate_offsets<C::TN>(args.offsets, args.expert_ids, args.E, args.num_experts, args.M_total,
+                            DEV_BAD_OFFSETS, DEV_BAD_EXPERT_IDS, status, row_tiles);
     if (lane == 0) {
-      ctl->valid = ok;
+      ctl->valid = status == 0;
       ctl->total_tiles = row_tiles * (args.N / WROWS);
       ctl->abort = 0;
-      if (!ok && blockIdx.x == 0) atomicCAS(args.err, 0, DEV_BAD_OFFSETS);
+      if (status && blockIdx.x == 0) atomicCAS(args.err, 0, status);
     }
   }
   __syncthreads();
@@ -159,15 +160,15 @@ bsmxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   if (warp == 0) {
     // =============================== TMA producer ===============================
     if (lane == 0) {
-      GroupedScheduler<C::TN, WROWS> sched(args.offsets, args.E, args.N);
+      GroupedScheduler<C::TN, WROWS> sched;
       const uint64_t pol_w = l2_policy_evict_first();  // weights stream once per token tile
       uint32_t stage = 0, phase = 0;
       int64_t issued = 0;
       bool ok = true;
       TileCoord tc;
       for (int64_t t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
-        if (!sched.locate(t, tc)) break;
-        const int32_t w_row = tc.e * args.N + tc.n0;
+        if (!sched.locate(args, t, tc)) break;
+        const int32_t w_row = tc.be * args.N + tc.n0;
         const int32_t t_row = (int32_t)tc.m0;
         for (int kb = 0; kb < KB; ++kb) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1, abort)) {
@@ -195,12 +196,12 @@ bsmxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   } else if (warp == 1) {
     // ================================ MMA thread ================================
     if (lane == 0) {
-      GroupedScheduler<C::TN, WROWS> sched(args.offsets, args.E, args.N);
+      GroupedScheduler<C::TN, WROWS> sched;
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0, slot = 0;
       bool ok = true;
       TileCoord tc;
       for (int64_t t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
-        if (!sched.locate(t, tc)) break;
+        if (!sched.locate(args, t, tc)) break;
         if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1, abort)) {
           record_error(args.err, DEV_TIMEOUT, abort);
           break;
@@ -244,7 +245,7 @@ bsmxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     // stages behind the newest issued one.
     const uint8_t* a_sc = static_cast<const uint8_t*>(args.a_scales);
     const uint8_t* b_sc = static_cast<const uint8_t*>(args.b_scales);
-    GroupedScheduler<C::TN, WROWS> sched(args.offsets, args.E, args.N);
+    GroupedScheduler<C::TN, WROWS> sched;
     uint32_t stage = 0, phase = 0;
     uint32_t ring[SCALE_LOOKAHEAD + 1] = {};
     int inflight = 0, head = 0;
@@ -258,8 +259,8 @@ bsmxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       --inflight;
     };
     for (int64_t t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
-      if (!sched.locate(t, tc)) break;
-      const uint8_t* w_rows = b_sc + ((int64_t)tc.e * args.N + tc.n0) * scale_row;
+      if (!sched.locate(args, t, tc)) break;
+      const uint8_t* w_rows = b_sc + ((int64_t)tc.be * args.N + tc.n0) * scale_row;
       for (int kb = 0; kb < KB; ++kb) {
         const bool got = __all_sync(0xffffffffu, mbar_wait(empty_bar(stage), phase ^ 1, abort));
         if (!got) {
@@ -293,11 +294,11 @@ bsmxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     // ================================= epilogue =================================
     const uint32_t quarter = warp & 3;
     __nv_bfloat16* Cmat = static_cast<__nv_bfloat16*>(args.C);
-    GroupedScheduler<C::TN, WROWS> sched(args.offsets, args.E, args.N);
+    GroupedScheduler<C::TN, WROWS> sched;
     uint32_t acc = 0, acc_phase = 0;
     TileCoord tc;
     for (int64_t t = blockIdx.x; t < total_tiles; t += gridDim.x) {
-      if (!sched.locate(t, tc)) break;
+      if (!sched.locate(args, t, tc)) break;
       const bool got = __all_sync(0xffffffffu, mbar_wait(tfull_bar(acc), acc_phase, abort));
       if (!got) {
         if (lane == 0) record_error(args.err, DEV_TIMEOUT, abort);

@@ -107,14 +107,15 @@ bsmxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
   const int64_t tile_stride = gridDim.x / 2;
 
   if (warp == 0) {
-    int ok;
+    int status;
     int64_t row_tiles;
-    validate_offsets<BM>(args.offsets, args.E, args.M_total, ok, row_tiles);
+    validate_offsets<BM>(args.offsets, args.expert_ids, args.E, args.num_experts, args.M_total,
+                            DEV_BAD_OFFSETS, DEV_BAD_EXPERT_IDS, status, row_tiles);
     if (lane == 0) {
-      ctl->valid = ok;
+      ctl->valid = status == 0;
       ctl->total_tiles = row_tiles * ((args.N + BN - 1) / BN);
       ctl->abort = 0;
-      if (!ok && blockIdx.x == 0) atomicCAS(args.err, 0, DEV_BAD_OFFSETS);
+      if (status && blockIdx.x == 0) atomicCAS(args.err, 0, status);
     }
   }
   __syncthreads();
@@ -159,16 +160,16 @@ bsmxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
   if (warp == 0) {
     // =============================== TMA producer ===============================
     if (lane == 0) {
-      GroupedScheduler<BM, BN> sched(args.offsets, args.E, args.N);
+      GroupedScheduler<BM, BN> sched;
       const uint64_t pol_b = l2_policy_evict_last();
       uint32_t stage = 0, phase = 0;
       int64_t issued = 0;
       bool ok = true;
       TileCoord tc;
       for (int64_t t = tile0; ok && t < total_tiles; t += tile_stride) {
-        if (!sched.locate(t, tc)) break;
+        if (!sched.locate(args, t, tc)) break;
         const int32_t a_row = (int32_t)(tc.m0 + 128 * rank);
-        const int32_t b_row = tc.e * args.N + tc.n0 + 128 * rank;
+        const int32_t b_row = tc.be * args.N + tc.n0 + 128 * rank;
         for (int kb = 0; kb < KB; ++kb) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1, abort)) {
             record_error(args.err, DEV_TIMEOUT, abort);
@@ -194,13 +195,13 @@ bsmxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
   } else if (warp == 1) {
     // ================================ MMA thread ================================
     if (lane == 0 && rank == 0) {
-      GroupedScheduler<BM, BN> sched(args.offsets, args.E, args.N);
+      GroupedScheduler<BM, BN> sched;
       uint32_t stage = 0, phase = 0;
       bool ok = true;
       int64_t i = 0;  // tiles issued by this pair
       TileCoord tc;
       for (int64_t t = tile0; ok && t < total_tiles; t += tile_stride, ++i) {
-        if (!sched.locate(t, tc)) break;
+        if (!sched.locate(args, t, tc)) break;
         const uint32_t buf = (uint32_t)(i & 1);
         // the accumulator this tile reuses was drained (tile i-2), and the columns it shares
         // with the other accumulator were drained by tile i-1's epilogue
@@ -247,7 +248,7 @@ bsmxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     // scales from each CTA's own TMEM).  Announced on the MMA CTA's full barrier.
     const uint8_t* a_sc = static_cast<const uint8_t*>(args.a_scales);
     const uint8_t* b_sc = static_cast<const uint8_t*>(args.b_scales);
-    GroupedScheduler<BM, BN> sched(args.offsets, args.E, args.N);
+    GroupedScheduler<BM, BN> sched;
     uint32_t stage = 0, phase = 0;
     // Grouped path: when a row's codes for 4 consecutive stages form one aligned 16-byte
     // chunk (K % 512 == 0, 16-byte aligned scale arrays), fetch a 4-stage group per row with
@@ -260,10 +261,10 @@ bsmxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
       const int G = KB / GROUP;  // groups per tile
       const uint32_t sSTG = smem_u32(smem + SMEM_STG);
       const uint8_t* stg = smem + SMEM_STG;
-      GroupedScheduler<BM, BN> pre(args.offsets, args.E, args.N);
+      GroupedScheduler<BM, BN> pre;
       TileCoord tp;
       int64_t tp_t = tile0;
-      bool pre_ok = pre.locate(tp_t, tp);
+      bool pre_ok = pre.locate(args, tp_t, tp);
       int qp = 0;
       auto issue_group = [&](int slot) {
         if (pre_ok) {
@@ -280,13 +281,13 @@ bsmxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             const int r = 32 * i + (int)lane;
             const int n = tp.n0 + r;
             const bool live = n < args.N;
-            const uint8_t* src = b_sc + ((int64_t)tp.e * args.N + n) * scale_row + 16 * qp;
+            const uint8_t* src = b_sc + ((int64_t)tp.be * args.N + n) * scale_row + 16 * qp;
             cp_async_16(dst + STG_A + r * 16, live ? src : b_sc, live ? 16u : 0u);
           }
           if (++qp == G) {
             qp = 0;
             tp_t += tile_stride;
-            pre_ok = tp_t < total_tiles && pre.locate(tp_t, tp);
+            pre_ok = tp_t < total_tiles && pre.locate(args, tp_t, tp);
           }
         }
         cp_async_commit();  // an empty group keeps the group count in step
@@ -297,7 +298,7 @@ bsmxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
       bool ok = true;
       TileCoord tc;
       for (int64_t t = tile0; ok && t < total_tiles; t += tile_stride) {
-        if (!sched.locate(t, tc)) break;
+        if (!sched.locate(args, t, tc)) break;
         for (int q = 0; ok && q < G; ++q, ++g) {
           cp_async_wait_group<1>();  // group g has landed (g + 1 may be in flight)
           __syncwarp();
@@ -348,7 +349,7 @@ bsmxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
       --inflight;
     };
     for (int64_t t = tile0; ok && t < total_tiles; t += tile_stride) {
-      if (!sched.locate(t, tc)) break;
+      if (!sched.locate(args, t, tc)) break;
       for (int kb = 0; kb < KB; ++kb) {
         const bool got = __all_sync(0xffffffffu, mbar_wait(empty_bar(stage), phase ^ 1, abort));
         if (!got) {
@@ -368,7 +369,7 @@ bsmxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
           for (int h = 0; h < 2; ++h) {
             const int n = tc.n0 + 128 * h + r;
             const bool b_live = n < args.N;
-            const uint8_t* src = b_sc + ((int64_t)tc.e * args.N + n) * scale_row + 4 * kb;
+            const uint8_t* src = b_sc + ((int64_t)tc.be * args.N + n) * scale_row + 4 * kb;
             cp_async_4(db + h * SF_BLOCK + 4 * j, b_live ? src : b_sc, b_live ? 4u : 0u);
           }
         }
@@ -391,12 +392,12 @@ bsmxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     const uint32_t quarter = warp & 3;
     const uint32_t half = ew >> 2;  // accumulator columns half*128 .. +127
     __nv_bfloat16* Cmat = static_cast<__nv_bfloat16*>(args.C);
-    GroupedScheduler<BM, BN> sched(args.offsets, args.E, args.N);
+    GroupedScheduler<BM, BN> sched;
     const uint64_t pol_c = l2_policy_evict_first();
     int64_t i = 0;
     TileCoord tc;
     for (int64_t t = tile0; t < total_tiles; t += tile_stride, ++i) {
-      if (!sched.locate(t, tc)) break;
+      if (!sched.locate(args, t, tc)) break;
       const uint32_t buf = (uint32_t)(i & 1);
       const bool got =
           __all_sync(0xffffffffu, mbar_wait(accf_bar(buf), (uint32_t)((i >> 1) & 1), abort));

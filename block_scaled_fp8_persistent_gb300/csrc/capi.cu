@@ -89,14 +89,15 @@ bool encode_u8_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t r
 }
 
 bsfp8_status check_common(const void* A, const void* B, const void* sa, const void* sb,
-                          const int32_t* off, void* C, int64_t M_total, int N, int K, int E) {
+                          const int32_t* off, const int32_t* ids, void* C, int64_t M_total,
+                          int N, int K, int G, int E) {
   if (!off || !B || !sb) return BSFP8_ERR_NULL;
   if (M_total > 0 && (!A || !sa || !C)) return BSFP8_ERR_NULL;
   if (M_total < 0 || M_total > INT32_MAX || N < 128 || N % 128 != 0 || K < 128 ||
-      K % 128 != 0 || E < 1 || (int64_t)E * N > INT32_MAX)
+      K % 128 != 0 || G < 1 || E < 1 || (int64_t)E * N > INT32_MAX)
     return BSFP8_ERR_SHAPE;
   if (!aligned(A, 16) || !aligned(B, 16) || !aligned(C, 16) || !aligned(sa, 4) ||
-      !aligned(sb, 4) || !aligned(off, 4))
+      !aligned(sb, 4) || !aligned(off, 4) || !aligned(ids, 4))
     return BSFP8_ERR_ALIGN;
   return BSFP8_OK;
 }
@@ -164,58 +165,98 @@ int choose_mx_token_tile(int64_t M_total, int E) {
 
 using namespace bsfp8;
 
-extern "C" bsfp8_status bsfp8_grouped_gemm(const void* A, const void* B, const float* a_scales,
-                                           const float* b_scales, const int32_t* expert_offsets,
-                                           void* C, int64_t M_total, int N, int K,
-                                           int num_experts, cudaStream_t stream) {
-  bsfp8_status st = check_common(A, B, a_scales, b_scales, expert_offsets, C, M_total, N, K,
-                                 num_experts);
+namespace bsfp8 {
+namespace {
+
+// Grouped GEMMs over G row groups; group g multiplies the weights of expert ids[g] (of E
+// experts in B), or of expert g when ids is null.
+bsfp8_status blockwise_gemm(const void* A, const void* B, const float* a_scales,
+                            const float* b_scales, const int32_t* offsets, const int32_t* ids,
+                            void* C, int64_t M_total, int N, int K, int G, int E,
+                            cudaStream_t stream) {
+  bsfp8_status st = check_common(A, B, a_scales, b_scales, offsets, ids, C, M_total, N, K, G, E);
   if (st != BSFP8_OK) return st;
   DeviceInfo* dev = nullptr;
   if ((st = device_info(&dev)) != BSFP8_OK) return st;
   if (M_total == 0) return BSFP8_OK;
-  const BlockwiseTile tile = choose_blockwise_tile(M_total, N, num_experts, dev->num_sms);
+  const BlockwiseTile tile = choose_blockwise_tile(M_total, N, G, dev->num_sms);
   CUtensorMap tmA, tmB;
   if (!encode_u8_2d(&tmA, A, (uint64_t)K, (uint64_t)M_total, 128,
                     (uint32_t)blockwise_a_rows(tile)) ||
-      !encode_u8_2d(&tmB, B, (uint64_t)K, (uint64_t)num_experts * N, 128,
+      !encode_u8_2d(&tmB, B, (uint64_t)K, (uint64_t)E * N, 128,
                     (uint32_t)blockwise_b_rows(tile)))
     return BSFP8_ERR_CUDA;
-  GemmArgs args{expert_offsets, a_scales, b_scales, C, M_total, N, K, num_experts, dev->err_word};
+  GemmArgs args{offsets, a_scales, b_scales, C, M_total, N, K, G, dev->err_word, ids, E};
   return launch_bsfp8_blockwise(tile, tmA, tmB, args, dev->num_sms, stream) == cudaSuccess
              ? BSFP8_OK
              : BSFP8_ERR_CUDA;
+}
+
+bsfp8_status mx_gemm(const void* A, const void* B, const uint8_t* a_scales,
+                     const uint8_t* b_scales, const int32_t* offsets, const int32_t* ids,
+                     void* C, int64_t M_total, int N, int K, int G, int E, cudaStream_t stream) {
+  bsfp8_status st = check_common(A, B, a_scales, b_scales, offsets, ids, C, M_total, N, K, G, E);
+  if (st != BSFP8_OK) return st;
+  DeviceInfo* dev = nullptr;
+  if ((st = device_info(&dev)) != BSFP8_OK) return st;
+  if (M_total == 0) return BSFP8_OK;
+  GemmArgs args{offsets, a_scales, b_scales, C, M_total, N, K, G, dev->err_word, ids, E};
+  if (use_mx_pair(M_total, G)) {
+    CUtensorMap tmA, tmB;
+    if (!encode_u8_2d(&tmA, A, (uint64_t)K, (uint64_t)M_total, 128, 128) ||
+        !encode_u8_2d(&tmB, B, (uint64_t)K, (uint64_t)E * N, 128, 128))
+      return BSFP8_ERR_CUDA;
+    return launch_bsmxfp8_pair(tmA, tmB, args, dev->num_sms, stream) == cudaSuccess
+               ? BSFP8_OK
+               : BSFP8_ERR_CUDA;
+  }
+  const int tn = choose_mx_token_tile(M_total, G);
+  CUtensorMap tmA, tmB;
+  if (!encode_u8_2d(&tmA, A, (uint64_t)K, (uint64_t)M_total, 128, (uint32_t)tn) ||
+      !encode_u8_2d(&tmB, B, (uint64_t)K, (uint64_t)E * N, 128, 128))
+    return BSFP8_ERR_CUDA;
+  return launch_bsmxfp8(tn, tmA, tmB, args, dev->num_sms, stream) == cudaSuccess ? BSFP8_OK
+                                                                                 : BSFP8_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace bsfp8
+
+extern "C" bsfp8_status bsfp8_grouped_gemm(const void* A, const void* B, const float* a_scales,
+                                           const float* b_scales, const int32_t* expert_offsets,
+                                           void* C, int64_t M_total, int N, int K,
+                                           int num_experts, cudaStream_t stream) {
+  return blockwise_gemm(A, B, a_scales, b_scales, expert_offsets, nullptr, C, M_total, N, K,
+                        num_experts, num_experts, stream);
+}
+
+extern "C" bsfp8_status bsfp8_grouped_gemm_ids(const void* A, const void* B, const float* a_scales,
+                                               const float* b_scales, const int32_t* group_offsets,
+                                               const int32_t* expert_ids, void* C, int64_t M_total,
+                                               int N, int K, int num_groups, int num_experts,
+                                               cudaStream_t stream) {
+  if (!expert_ids) return BSFP8_ERR_NULL;
+  return blockwise_gemm(A, B, a_scales, b_scales, group_offsets, expert_ids, C, M_total, N, K,
+                        num_groups, num_experts, stream);
 }
 
 extern "C" bsfp8_status bsmxfp8_grouped_gemm(const void* A, const void* B, const uint8_t* a_scales,
                                              const uint8_t* b_scales, const int32_t* expert_offsets,
                                              void* C, int64_t M_total, int N, int K,
                                              int num_experts, cudaStream_t stream) {
-  bsfp8_status st = check_common(A, B, a_scales, b_scales, expert_offsets, C, M_total, N, K,
-                                 num_experts);
-  if (st != BSFP8_OK) return st;
-  DeviceInfo* dev = nullptr;
-  if ((st = device_info(&dev)) != BSFP8_OK) return st;
-  if (M_total == 0) return BSFP8_OK;
-  if (use_mx_pair(M_total, num_experts)) {
-    CUtensorMap tmA, tmB;
-    if (!encode_u8_2d(&tmA, A, (uint64_t)K, (uint64_t)M_total, 128, 128) ||
-        !encode_u8_2d(&tmB, B, (uint64_t)K, (uint64_t)num_experts * N, 128, 128))
-      return BSFP8_ERR_CUDA;
-    GemmArgs args{expert_offsets, a_scales, b_scales, C, M_total, N, K, num_experts,
-                  dev->err_word};
-    return launch_bsmxfp8_pair(tmA, tmB, args, dev->num_sms, stream) == cudaSuccess
-               ? BSFP8_OK
-               : BSFP8_ERR_CUDA;
-  }
-  const int tn = choose_mx_token_tile(M_total, num_experts);
-  CUtensorMap tmA, tmB;
-  if (!encode_u8_2d(&tmA, A, (uint64_t)K, (uint64_t)M_total, 128, (uint32_t)tn) ||
-      !encode_u8_2d(&tmB, B, (uint64_t)K, (uint64_t)num_experts * N, 128, 128))
-    return BSFP8_ERR_CUDA;
-  GemmArgs args{expert_offsets, a_scales, b_scales, C, M_total, N, K, num_experts, dev->err_word};
-  return launch_bsmxfp8(tn, tmA, tmB, args, dev->num_sms, stream) == cudaSuccess ? BSFP8_OK
-                                                                                 : BSFP8_ERR_CUDA;
+  return mx_gemm(A, B, a_scales, b_scales, expert_offsets, nullptr, C, M_total, N, K,
+                 num_experts, num_experts, stream);
+}
+
+extern "C" bsfp8_status bsmxfp8_grouped_gemm_ids(const void* A, const void* B,
+                                                 const uint8_t* a_scales, const uint8_t* b_scales,
+                                                 const int32_t* group_offsets,
+                                                 const int32_t* expert_ids, void* C,
+                                                 int64_t M_total, int N, int K, int num_groups,
+                                                 int num_experts, cudaStream_t stream) {
+  if (!expert_ids) return BSFP8_ERR_NULL;
+  return mx_gemm(A, B, a_scales, b_scales, group_offsets, expert_ids, C, M_total, N, K,
+                 num_groups, num_experts, stream);
 }
 
 extern "C" bsfp8_status bsmxfp8_tmem_plan(int block_k, int epilogue_n, int vec, int overlap,
@@ -276,6 +317,7 @@ extern "C" const char* bsfp8_status_string(bsfp8_status s) {
     case BSFP8_ERR_CUDA: return "CUDA call failed";
     case BSFP8_ERR_DEVICE_OFFSETS: return "device: invalid expert offsets";
     case BSFP8_ERR_DEVICE_TIMEOUT: return "device: pipeline wait timed out";
+    case BSFP8_ERR_DEVICE_EXPERT_IDS: return "device: expert id out of range";
   }
   return "unknown status";
 }

@@ -13,6 +13,7 @@ enum DeviceError : int {
   DEV_OK = 0,
   DEV_BAD_OFFSETS = 6,  // offsets[0] != 0, offsets[E] != M_total or not non-decreasing
   DEV_TIMEOUT = 7,      // a pipeline wait gave up (the kernel wound down cleanly)
+  DEV_BAD_EXPERT_IDS = 8,  // an expert id outside [0, num_experts)
 };
 
 // Plain pointers and sizes handed to every kernel (tensor maps travel separately as
@@ -23,8 +24,11 @@ struct GemmArgs {
   const void* b_scales;    // blockwise: f32 [E, N/128, K/128]  MX: u8 [E, N, K/32]
   void* C;                 // bf16 [M_total, N]
   int64_t M_total;
-  int N, K, E;
+  int N, K;
+  int E;                   // groups (row segments of A): offsets has E+1 entries
   int* err;                // library-owned device error word
+  const int32_t* expert_ids;  // [E] group -> expert (rows of B and B scales); nullptr: identity
+  int num_experts;         // experts in B (bound of expert_ids)
 };
 
 // Tile configurations of the blockwise kernel.

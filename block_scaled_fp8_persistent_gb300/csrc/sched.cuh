@@ -7,9 +7,10 @@
 // Partitions section), and maps a tile id to (expert, first row, first column) by walking
 // the expert row offsets forward -- the ids a CTA visits only grow, so each role keeps a
 // cursor and the walk costs O(E + tiles) per CTA without any table in memory.  Experts
-// with no rows own no tiles.  The expert -> B rows mapping is the identity (group e uses
-// expert e's weights), the reading of expert_ids in promote_accumulators (MAX kernels,
-// grouped_matmul_sm100_blockwise_fp8, Args).
+// with no rows own no tiles.  Row segments are groups; group g multiplies the weights (B
+// rows and B scales) of expert expert_ids[g], the mapping from group index to expert rows of
+// B in promote_accumulators (MAX kernels, grouped_matmul_sm100_blockwise_fp8, Args); without
+// an expert_ids array group g uses expert g.
 #pragma once
 #include <cstdint>
 #include "ptx.cuh"
@@ -17,7 +18,8 @@
 namespace bsfp8 {
 
 struct TileCoord {
-  int e;           // expert
+  int e;           // group (row segment)
+  int be;          // expert whose weights the group multiplies (rows of B and B scales)
   int64_t m0;      // first row of the tile (global row index)
   int n0;          // first column of the tile
   int64_t m_end;   // one past the expert's last row (rows >= m_end are not this tile's)
@@ -25,29 +27,31 @@ struct TileCoord {
 
 template <int BM, int BN>
 struct GroupedScheduler {
-  const int32_t* off;
-  int E;
-  int n_tiles;      // ceil(N / BN); the last column tile may be partial
-  int e;            // current expert (-1 before the first locate)
-  int64_t base;     // id of the first tile of expert e
-  int64_t e_tiles;  // tiles of expert e
-  int64_t r0, r1;   // rows of expert e
+  // Only the cursor lives here; offsets, expert ids, group count and N are read from the
+  // kernel's parameter block (constant memory) at each call, so they cost no registers.
+  int e = -1;           // current group (-1 before the first locate)
+  int be = 0;           // its expert
+  int64_t base = 0;     // id of the first tile of group e
+  int64_t e_tiles = 0;  // tiles of group e
+  int64_t r0 = 0, r1 = 0;  // rows of group e
 
-  __device__ GroupedScheduler(const int32_t* offsets, int num_experts, int N)
-      : off(offsets), E(num_experts), n_tiles((N + BN - 1) / BN), e(-1), base(0), e_tiles(0), r0(0), r1(0) {}
-
-  // t must not decrease between calls.  Returns false past the last tile.
-  __device__ bool locate(int64_t t, TileCoord& c) {
+  // t must not decrease between calls.  Returns false past the last tile.  Args has
+  // offsets [E+1], expert_ids [E] (or nullptr), E (groups) and N.
+  template <class Args>
+  __device__ bool locate(const Args& a, int64_t t, TileCoord& c) {
+    const int n_tiles = (a.N + BN - 1) / BN;  // the last column tile may be partial
     while (t >= base + e_tiles) {
       base += e_tiles;
       ++e;
-      if (e >= E) return false;
-      r0 = ldg_s32(off + e);
-      r1 = ldg_s32(off + e + 1);
+      if (e >= a.E) return false;
+      r0 = ldg_s32(a.offsets + e);
+      r1 = ldg_s32(a.offsets + e + 1);
       e_tiles = ((r1 - r0 + BM - 1) / BM) * (int64_t)n_tiles;
+      be = a.expert_ids ? ldg_s32(a.expert_ids + e) : e;
     }
     const int64_t local = t - base;
     c.e = e;
+    c.be = be;
     c.m0 = r0 + (local / n_tiles) * BM;
     c.n0 = (int)(local % n_tiles) * BN;
     c.m_end = r1;
@@ -55,22 +59,31 @@ struct GroupedScheduler {
   }
 };
 
-// Validate the offsets and count the row tiles (sum over experts of ceil(M_e / BM)).
-// Executed by one full warp; every lane gets the results.
+// Validate the group offsets (and the expert ids, when given) and count the row tiles (sum
+// over groups of ceil(M_g / BM)).  Executed by one full warp; every lane gets the results:
+// status 0, or the device error code (bad_offsets_code / bad_ids_code) to report.
 template <int BM>
-__device__ __forceinline__ void validate_offsets(const int32_t* off, int E, int64_t M_total,
-                                                 int& ok, int64_t& row_tiles) {
+__device__ __forceinline__ void validate_offsets(const int32_t* off, const int32_t* ids, int E,
+                                                 int num_experts, int64_t M_total,
+                                                 int bad_offsets_code, int bad_ids_code,
+                                                 int& status, int64_t& row_tiles) {
   const uint32_t lane = lane_id();
-  int good = 1;
+  int good = 1, good_ids = 1;
   long long tiles = 0;
   for (int e = (int)lane; e < E; e += 32) {
     const int a = ldg_s32(off + e), b = ldg_s32(off + e + 1);
     if (b < a) good = 0;
     else tiles += (b - a + BM - 1) / BM;
+    if (ids) {
+      const int x = ldg_s32(ids + e);
+      if (x < 0 || x >= num_experts) good_ids = 0;
+    }
   }
   if (lane == 0 && (ldg_s32(off) != 0 || (int64_t)ldg_s32(off + E) != M_total)) good = 0;
   for (int s = 16; s > 0; s >>= 1) tiles += __shfl_xor_sync(0xffffffffu, tiles, s);
-  ok = __all_sync(0xffffffffu, good);
+  status = !__all_sync(0xffffffffu, good)       ? bad_offsets_code
+           : !__all_sync(0xffffffffu, good_ids) ? bad_ids_code
+                                                : 0;
   row_tiles = tiles;
 }
 

@@ -155,6 +155,8 @@ class Problem:
                b_scales f32 [E, N/128, K/128]
     mx:        A, B as above, a_scales u8 [M_total, K/32], b_scales u8 [E, N, K/32]
     offsets:   i32 [E+1], offsets[0] = 0, offsets[E] = M_total
+    expert_ids: None (group e uses expert e; B has E experts), or i32 [E]: group e uses
+               expert expert_ids[e] of the B.shape[0] experts in B
     """
     mode: str
     A: np.ndarray
@@ -166,6 +168,11 @@ class Problem:
     K: int
     name: str = ""
     meta: dict = field(default_factory=dict)
+    expert_ids: np.ndarray | None = None
+
+    @property
+    def num_experts(self) -> int:
+        return int(self.B.shape[0])
 
     @property
     def E(self) -> int:
@@ -185,9 +192,12 @@ class Problem:
 
     def bytes(self) -> int:
         """Algorithmic bytes: A + B of experts with rows + scales + C, each once."""
-        active = int((self.counts > 0).sum())
+        if self.expert_ids is None:
+            active = int((self.counts > 0).sum())
+        else:
+            active = int(np.unique(self.expert_ids[self.counts > 0]).size)
         b = self.A.nbytes + active * self.N * self.K + self.a_scales.nbytes
-        per_expert_sb = self.b_scales.nbytes // self.E
+        per_expert_sb = self.b_scales.nbytes // self.num_experts
         b += active * per_expert_sb + self.M_total * self.N * 2
         return int(b)
 
@@ -246,6 +256,21 @@ def mx_problem(counts, N: int, K: int, seed: int, exact: bool = False, nthreads:
         L.bsfp8_gen_mx_rows(seed, STREAM_B, 0, E * N, K, None, _ptr(B), _ptr(sb), nthreads)
     return Problem("mx", A, B, sa, sb, off, N, K, name=name,
                    meta={"seed": seed, "exact": exact})
+
+
+def routed_problem(counts, expert_ids, num_experts: int, N: int, K: int, seed: int,
+                   mode: str = "blockwise", exact: bool = False, nthreads: int = 0,
+                   name: str = "") -> Problem:
+    """Rows in len(counts) groups, group g multiplying expert expert_ids[g] of num_experts:
+    the rows (A and its scales) come from a problem with these group counts, the experts (B
+    and its scales) from one with num_experts empty groups and another seed."""
+    make = blockwise_problem if mode == "blockwise" else mx_problem
+    ids = np.asarray(expert_ids, np.int32)
+    assert ids.shape == (len(counts),)
+    rows = make(counts, N, K, seed=seed, exact=exact, nthreads=nthreads)
+    experts = make([0] * num_experts, N, K, seed=seed + 7919, exact=exact, nthreads=nthreads)
+    return Problem(mode, rows.A, experts.B, rows.a_scales, experts.b_scales, rows.offsets, N, K,
+                   name=name, meta={"seed": seed, "exact": exact}, expert_ids=ids)
 
 
 CONFIG_NAMES = {

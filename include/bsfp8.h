@@ -62,7 +62,8 @@ typedef enum {
   BSFP8_ERR_UNSUPPORTED_DEVICE = 4, /* current device is not compute capability 10.3 */
   BSFP8_ERR_CUDA = 5,               /* a CUDA runtime/driver call failed (launch, ...) */
   BSFP8_ERR_DEVICE_OFFSETS = 6,     /* device error word: invalid expert offsets */
-  BSFP8_ERR_DEVICE_TIMEOUT = 7      /* device error word: a pipeline wait gave up */
+  BSFP8_ERR_DEVICE_TIMEOUT = 7,     /* device error word: a pipeline wait gave up */
+  BSFP8_ERR_DEVICE_EXPERT_IDS = 8   /* device error word: an expert id outside [0, num_experts) */
 } bsfp8_status;
 
 /*
@@ -112,6 +113,42 @@ bsfp8_status bsmxfp8_grouped_gemm(const void* A, const void* B, const uint8_t* a
                                   cudaStream_t stream);
 
 /*
+ * The same two GEMMs with an expert indirection: the rows of A form num_groups groups
+ * (group g owns rows group_offsets[g] .. group_offsets[g+1]-1) and group g multiplies the
+ * weights of expert expert_ids[g] -- its rows of B and of b_scales -- instead of expert g.
+ * This is the expert_ids argument of promote_accumulators (MAX kernels,
+ * grouped_matmul_sm100_blockwise_fp8, Args: "mapping from group index to expert row offset
+ * in B"): only the experts that received tokens need a group, and several groups may use the
+ * same expert.
+ *
+ *   group_offsets  int32 [num_groups+1]  as expert_offsets above, per group
+ *   expert_ids     int32 [num_groups]    device array, each in [0, num_experts)
+ *   B, b_scales    as above, with num_experts experts
+ *   A, a_scales, C as above (M_total rows)
+ *
+ *   C[m, n] = bf16( sum_kb sa(m, kb) * sb(x, n, kb) * sum_{k in kb} A[m,k] * B[x,n,k] ),
+ *             x = expert_ids[g] for the group g that owns row m (blockwise; the MXFP8 entry
+ *             point applies its UE8M0 scales the same way)
+ *
+ * expert_ids may not be NULL (BSFP8_ERR_NULL); num_groups >= 1 and num_experts >= 1
+ * (BSFP8_ERR_SHAPE); expert_ids 4-byte aligned.  An id outside [0, num_experts) is found on the
+ * device: the kernel writes nothing, records BSFP8_ERR_DEVICE_EXPERT_IDS in the device error
+ * word and finishes.  Everything else (requirements, ownership, asynchrony) is as for the
+ * entry points without ids, which are these with expert_ids[g] = g and num_groups =
+ * num_experts.
+ */
+bsfp8_status bsfp8_grouped_gemm_ids(const void* A, const void* B, const float* a_scales,
+                                    const float* b_scales, const int32_t* group_offsets,
+                                    const int32_t* expert_ids, void* C, int64_t M_total, int N,
+                                    int K, int num_groups, int num_experts, cudaStream_t stream);
+
+bsfp8_status bsmxfp8_grouped_gemm_ids(const void* A, const void* B, const uint8_t* a_scales,
+                                      const uint8_t* b_scales, const int32_t* group_offsets,
+                                      const int32_t* expert_ids, void* C, int64_t M_total, int N,
+                                      int K, int num_groups, int num_experts,
+                                      cudaStream_t stream);
+
+/*
  * TMEM storage plan of double-buffered block-scaled accumulators (host only, no GPU use).
  * For a 256-column tile with 512 TMEM columns, block_k elements of K per MMA stage,
  * epilogue subtiles of epilogue_n columns and one scale per vec (16 or 32) elements of K,
@@ -141,7 +178,8 @@ bsfp8_status bsfp8_blockwise_plan(int64_t M_total, int N, int num_experts, int n
 
 /*
  * Read the device error word of the current device (after synchronising `stream`) into
- * *code (0, BSFP8_ERR_DEVICE_OFFSETS or BSFP8_ERR_DEVICE_TIMEOUT) and reset it to 0.
+ * *code (0, BSFP8_ERR_DEVICE_OFFSETS, BSFP8_ERR_DEVICE_TIMEOUT or BSFP8_ERR_DEVICE_EXPERT_IDS)
+ * and reset it to 0.
  * Returns BSFP8_ERR_NULL for a NULL code, BSFP8_ERR_CUDA if a CUDA call fails.
  */
 bsfp8_status bsfp8_get_device_error(cudaStream_t stream, int* code);

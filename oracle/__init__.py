@@ -66,6 +66,8 @@ def _L():
             f = getattr(lib, name)
             f.argtypes = [p, p, p, p, p, i64, i64, i64, i64, p, p, i64, p, p, i32]
             f.restype = i32
+        lib.bsfp8_oracle_ids.argtypes = [i32, p, p, p, p, p, p, i64, i64, i64, i64, i64, p, p, i32]
+        lib.bsfp8_oracle_ids.restype = i32
         lib.bsfp8_oracle_threads.argtypes = [i32]
         lib.bsfp8_oracle_threads.restype = i32
         _lib = lib
@@ -129,6 +131,26 @@ def grouped_gemm(mode: str, A, B, a_scales, b_scales, offsets, N: int, K: int,
     return C, T
 
 
+def grouped_gemm_ids(mode: str, A, B, a_scales, b_scales, offsets, expert_ids, N: int, K: int,
+                     nthreads: int = 0, want_t: bool = True):
+    """Full output with an expert indirection: group g (rows offsets[g]..offsets[g+1]-1)
+    uses expert expert_ids[g] of B [num_experts, N, K].  Returns (C bits, T or None)."""
+    A, B, a_scales, b_scales, offsets = _args(mode, A, B, a_scales, b_scales, offsets)
+    ids = _c(expert_ids, np.int32)
+    G = offsets.shape[0] - 1
+    assert ids.shape == (G,)
+    M = int(offsets[-1])
+    C = np.empty((M, N), np.uint16)
+    T = np.empty((M, N), np.float64) if want_t else None
+    rc = _L().bsfp8_oracle_ids(0 if mode == "blockwise" else 1, A.ctypes.data, B.ctypes.data,
+                               a_scales.ctypes.data, b_scales.ctypes.data, offsets.ctypes.data,
+                               ids.ctypes.data, M, N, K, G, B.shape[0], C.ctypes.data,
+                               T.ctypes.data if T is not None else None, nthreads)
+    if rc:
+        raise OracleError(f"oracle rejected the problem (code {rc})")
+    return C, T
+
+
 def grouped_gemm_points(mode: str, A, B, a_scales, b_scales, offsets, N: int, K: int,
                         rows, cols, nthreads: int = 0):
     """Sampled output elements (rows[i], cols[i]).  Returns (C bits uint16 [n], T float64 [n])."""
@@ -150,7 +172,11 @@ def grouped_gemm_points(mode: str, A, B, a_scales, b_scales, offsets, N: int, K:
 
 
 def problem_reference(p, nthreads: int = 0, want_t: bool = True):
-    """Full oracle output for a gen.Problem-like object (mode, A, B, scales, offsets, N, K)."""
+    """Full oracle output for a gen.Problem-like object (mode, A, B, scales, offsets, N, K,
+    and expert_ids when it has them)."""
+    if getattr(p, "expert_ids", None) is not None:
+        return grouped_gemm_ids(p.mode, p.A, p.B, p.a_scales, p.b_scales, p.offsets,
+                                p.expert_ids, p.N, p.K, nthreads=nthreads, want_t=want_t)
     return grouped_gemm(p.mode, p.A, p.B, p.a_scales, p.b_scales, p.offsets, p.N, p.K,
                         nthreads=nthreads, want_t=want_t)
 

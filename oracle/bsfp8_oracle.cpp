@@ -7,7 +7,8 @@
 //
 // What it computes (the plain definition, written out):
 //
-//   For every expert e, every row m in [off[e], off[e+1]) and every column n < N,
+//   For every group g, every row m in [off[g], off[g+1]) and every column n < N, with
+//   e = expert_ids[g] (e = g when no expert_ids are given),
 //     C[m,n] = bf16_RNE( sum_kb  sa(m,kb) * sb(e,n,kb) * sum_{k in block kb} dec(A[m,k]) * dec(B[e,n,k]) )
 //     T[m,n] = sum_kb |sa*sb| * sum_{k in block kb} |dec(A[m,k]) * dec(B[e,n,k])|
 //
@@ -124,7 +125,9 @@ struct Problem {
   const int32_t* offsets;    // [E+1]
   int64_t M_total;
   int64_t N, K;
-  int64_t E;
+  int64_t E;                 // groups (row segments)
+  const int32_t* expert_ids; // [E] group -> expert of B, or nullptr (group g uses expert g)
+  int64_t num_experts;       // experts in B and b_scales
 };
 
 int check(const Problem& p) {
@@ -135,11 +138,18 @@ int check(const Problem& p) {
   if (p.offsets[0] != 0 || p.offsets[p.E] != p.M_total) return 6;
   for (int64_t e = 0; e < p.E; ++e)
     if (p.offsets[e + 1] < p.offsets[e]) return 6;
+  if (p.num_experts <= 0) return 2;
+  if (p.expert_ids) {
+    for (int64_t g = 0; g < p.E; ++g)
+      if (p.expert_ids[g] < 0 || p.expert_ids[g] >= p.num_experts) return 8;
+  } else if (p.num_experts != p.E) {
+    return 2;
+  }
   return 0;
 }
 
-// Expert that owns row m: the e with off[e] <= m < off[e+1] (empty experts own no row).
-int64_t expert_of_row(const Problem& p, int64_t m) {
+// Group that owns row m: the g with off[g] <= m < off[g+1] (empty groups own no row).
+int64_t group_of_row(const Problem& p, int64_t m) {
   int64_t lo = 0, hi = p.E - 1;
   while (lo < hi) {  // smallest e with off[e+1] > m
     const int64_t mid = (lo + hi) / 2;
@@ -151,7 +161,9 @@ int64_t expert_of_row(const Problem& p, int64_t m) {
 // One output element, straight from the definition above.
 void element(const Problem& p, int64_t m, int64_t n, uint16_t* c_out, double* t_out) {
   const Lut& L = lut();
-  const int64_t e = expert_of_row(p, m);
+  // expert_ids: "mapping from group index to expert row offset in B" (promote_accumulators)
+  const int64_t g = group_of_row(p, m);
+  const int64_t e = p.expert_ids ? (int64_t)p.expert_ids[g] : g;
   const int64_t blk = (p.mode == BLOCKWISE) ? 128 : 32;
   const int64_t nkb = p.K / blk;
   const uint8_t* arow = p.A + m * p.K;
@@ -234,7 +246,8 @@ int run_points(const Problem& p, const int64_t* rows, const int64_t* cols, int64
 
 extern "C" {
 
-// Return codes: 0 ok, 2 bad shape, 6 bad expert offsets (same meaning as the library's).
+// Return codes: 0 ok, 2 bad shape, 6 bad expert offsets, 8 expert id out of range (same
+// meaning as the library's).
 
 double bsfp8_oracle_e4m3_decode(uint8_t code) { return lut().e4m3[code]; }
 double bsfp8_oracle_ue8m0_decode(uint8_t code) { return lut().ue8m0[code]; }
@@ -244,14 +257,14 @@ int bsfp8_oracle_blockwise(const uint8_t* A, const uint8_t* B, const float* a_sc
                            const float* b_scales, const int32_t* offsets, int64_t M_total,
                            int64_t N, int64_t K, int64_t E, uint16_t* C, double* T,
                            int nthreads) {
-  Problem p{BLOCKWISE, A, B, a_scales, b_scales, offsets, M_total, N, K, E};
+  Problem p{BLOCKWISE, A, B, a_scales, b_scales, offsets, M_total, N, K, E, nullptr, E};
   return run_full(p, C, T, nthreads);
 }
 
 int bsfp8_oracle_mx(const uint8_t* A, const uint8_t* B, const uint8_t* a_scales,
                     const uint8_t* b_scales, const int32_t* offsets, int64_t M_total,
                     int64_t N, int64_t K, int64_t E, uint16_t* C, double* T, int nthreads) {
-  Problem p{MX, A, B, a_scales, b_scales, offsets, M_total, N, K, E};
+  Problem p{MX, A, B, a_scales, b_scales, offsets, M_total, N, K, E, nullptr, E};
   return run_full(p, C, T, nthreads);
 }
 
@@ -260,7 +273,7 @@ int bsfp8_oracle_blockwise_points(const uint8_t* A, const uint8_t* B, const floa
                                   int64_t M_total, int64_t N, int64_t K, int64_t E,
                                   const int64_t* rows, const int64_t* cols, int64_t npts,
                                   uint16_t* C, double* T, int nthreads) {
-  Problem p{BLOCKWISE, A, B, a_scales, b_scales, offsets, M_total, N, K, E};
+  Problem p{BLOCKWISE, A, B, a_scales, b_scales, offsets, M_total, N, K, E, nullptr, E};
   return run_points(p, rows, cols, npts, C, T, nthreads);
 }
 
@@ -269,8 +282,21 @@ int bsfp8_oracle_mx_points(const uint8_t* A, const uint8_t* B, const uint8_t* a_
                            int64_t N, int64_t K, int64_t E, const int64_t* rows,
                            const int64_t* cols, int64_t npts, uint16_t* C, double* T,
                            int nthreads) {
-  Problem p{MX, A, B, a_scales, b_scales, offsets, M_total, N, K, E};
+  Problem p{MX, A, B, a_scales, b_scales, offsets, M_total, N, K, E, nullptr, E};
   return run_points(p, rows, cols, npts, C, T, nthreads);
+}
+
+// Grouped GEMM with an expert indirection: G groups of rows (offsets [G+1]), group g using
+// expert expert_ids[g] of num_experts (B [num_experts, N, K] and its scales).  mode 0 is
+// blockwise (fp32 scales), 1 is MX (UE8M0 scales).
+int bsfp8_oracle_ids(int mode, const uint8_t* A, const uint8_t* B, const void* a_scales,
+                     const void* b_scales, const int32_t* offsets, const int32_t* expert_ids,
+                     int64_t M_total, int64_t N, int64_t K, int64_t G, int64_t num_experts,
+                     uint16_t* C, double* T, int nthreads) {
+  if (!expert_ids || (mode != 0 && mode != 1)) return 2;
+  Problem p{mode == 0 ? BLOCKWISE : MX, A, B, a_scales, b_scales, offsets, M_total, N, K, G,
+            expert_ids, num_experts};
+  return run_full(p, C, T, nthreads);
 }
 
 int bsfp8_oracle_threads(int nthreads) { return resolve_threads(nthreads); }

@@ -17,6 +17,8 @@ class DeviceProblem:
         self.sa = torch.from_numpy(np.ascontiguousarray(p.a_scales)).to(dev)
         self.sb = torch.from_numpy(np.ascontiguousarray(p.b_scales)).to(dev)
         self.off = torch.from_numpy(np.ascontiguousarray(p.offsets)).to(dev)
+        ids = getattr(p, "expert_ids", None)
+        self.ids = None if ids is None else torch.from_numpy(np.ascontiguousarray(ids)).to(dev)
         # C with optional guard rows after M_total, filled with a sentinel bit pattern, and
         # optionally starting c_offset bf16 elements into its allocation (c_offset = 8 makes
         # C 16-byte but not 32-byte aligned)
@@ -28,6 +30,12 @@ class DeviceProblem:
 
     def run(self, stream=None):
         p = self.p
+        if self.ids is not None:
+            fn = (bsfp8.bsfp8_grouped_gemm_ids if p.mode == "blockwise"
+                  else bsfp8.bsmxfp8_grouped_gemm_ids)
+            fn(self.A, self.B, self.sa, self.sb, self.off, self.ids, self.C, p.M_total, p.N, p.K,
+               p.E, p.num_experts, stream=stream)
+            return
         fn = bsfp8.bsfp8_grouped_gemm if p.mode == "blockwise" else bsfp8.bsmxfp8_grouped_gemm
         fn(self.A, self.B, self.sa, self.sb, self.off, self.C, p.M_total, p.N, p.K, p.E,
            stream=stream)

@@ -40,17 +40,20 @@ def dequantize(p):
 
 
 def brute_force(p):
-    """(C float64 [M,N], T float64 [M,N]) by dequantized matmul per expert."""
+    """(C float64 [M,N], T float64 [M,N]) by dequantized matmul per group (group e uses
+    expert expert_ids[e] when the problem has expert ids, else expert e)."""
     A, B = dequantize(p)
     M, N = p.M_total, p.N
     C = torch.zeros(M, N, dtype=torch.float64)
     T = torch.zeros(M, N, dtype=torch.float64)
     off = p.offsets
+    ids = getattr(p, "expert_ids", None)
     for e in range(p.E):
         r0, r1 = int(off[e]), int(off[e + 1])
+        x = int(ids[e]) if ids is not None else e
         if r1 > r0:
-            C[r0:r1] = A[r0:r1] @ B[e].t()
-            T[r0:r1] = A[r0:r1].abs() @ B[e].abs().t()
+            C[r0:r1] = A[r0:r1] @ B[x].t()
+            T[r0:r1] = A[r0:r1].abs() @ B[x].abs().t()
     return C.numpy(), T.numpy()
 
 

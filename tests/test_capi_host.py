@@ -37,8 +37,9 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_status_strings(lib):
-    for code in range(8):
+    for code in range(9):
         assert len(bsfp8.status_string(code)) > 0
+    assert bsfp8.status_string(8) == "device: expert id out of range"
     assert bsfp8.status_string(99) == "unknown status"
 
 
@@ -73,3 +74,29 @@ def test_binding_raises_on_bad_shape():
     with pytest.raises(bsfp8.BsFp8Error) as ei:
         bsfp8.bsfp8_grouped_gemm(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 256, 200, 512, 1, stream=0)
     assert ei.value.status == 2
+
+
+def _call_ids(lib, mx=False, **kw):
+    a = dict(A=FAKE, B=FAKE, sa=FAKE, sb=FAKE, off=FAKE, ids=FAKE, C=FAKE, M=256, N=256, K=512,
+             G=3, E=2)
+    a.update(kw)
+    f = lib.bsmxfp8_grouped_gemm_ids if mx else lib.bsfp8_grouped_gemm_ids
+    return f(a["A"], a["B"], a["sa"], a["sb"], a["off"], a["ids"], a["C"], a["M"], a["N"],
+             a["K"], a["G"], a["E"], None)
+
+
+@pytest.mark.parametrize("mx", [False, True])
+@pytest.mark.parametrize("kw,status", [
+    (dict(ids=None), 1), (dict(off=None), 1), (dict(B=None), 1),
+    (dict(G=0), 2), (dict(E=0), 2), (dict(E=1 << 20, N=4096), 2), (dict(N=192), 2),
+    (dict(ids=FAKE + 2), 3), (dict(off=FAKE + 1), 3),
+])
+def test_host_validation_expert_ids(lib, mx, kw, status):
+    assert _call_ids(lib, mx=mx, **kw) == status
+
+
+def test_binding_ids_raises_on_null_ids():
+    with pytest.raises(bsfp8.BsFp8Error) as ei:
+        bsfp8.bsfp8_grouped_gemm_ids(FAKE, FAKE, FAKE, FAKE, FAKE, 0, FAKE, 256, 256, 512, 2, 2,
+                                     stream=0)
+    assert ei.value.status == 1

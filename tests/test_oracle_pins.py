@@ -14,7 +14,10 @@ fails at least one of them:
   * doubling one row's A scales doubles that row of C exactly;
   * the grouped result equals per-expert GEMMs concatenated, empty experts own no rows;
   * MX with every scale code 127 equals blockwise with every scale 1.0;
-  * T equals |A_deq| @ |B_deq|^T.
+  * T equals |A_deq| @ |B_deq|^T;
+  * expert ids (group -> expert, the expert_ids argument of promote_accumulators): the
+    result equals the brute force run on the groups' gathered experts, identity ids give the
+    plain grouped result, ids outside [0, num_experts) are rejected.
 """
 import math
 
@@ -250,3 +253,43 @@ def test_empty_problem():
     p = gen.blockwise_problem([0, 0], 128, 128, seed=16)
     C, T = oracle.problem_reference(p)
     assert C.shape == (0, 128)
+
+
+# ---------------------------------------------------------------------------
+# expert ids: group g multiplies expert expert_ids[g]
+# ---------------------------------------------------------------------------
+def test_expert_ids_blockwise_exact_bitwise():
+    # 5 groups over 6 experts: expert 2 used twice, experts 4 and 5 never, one empty group
+    p = gen.routed_problem([37, 0, 20, 130, 5], [2, 0, 2, 1, 3], 6, 384, 640, seed=21,
+                           exact=True)
+    C, _ = _oracle_vs_bruteforce(p, exact_bits=True)
+    # ignoring the ids (group g -> expert g) gives a different result
+    q = gen.Problem(p.mode, p.A, p.B[:5], p.a_scales, p.b_scales[:5], p.offsets, p.N, p.K)
+    assert not np.array_equal(C, oracle.problem_reference(q)[0])
+
+
+def test_expert_ids_blockwise_random_inputs():
+    p = gen.routed_problem([64, 3, 0, 90], [3, 3, 0, 1], 4, 256, 512, seed=22)
+    _oracle_vs_bruteforce(p, exact_bits=False)
+
+
+def test_expert_ids_mx_exact_bitwise():
+    p = gen.routed_problem([9, 40, 0, 17], [1, 0, 1, 2], 3, 64, 256, seed=23, mode="mx",
+                           exact=True)
+    _oracle_vs_bruteforce(p, exact_bits=True)
+
+
+def test_expert_ids_identity_equals_plain_grouped():
+    p = gen.blockwise_problem([30, 0, 70], 256, 384, seed=24)
+    C0, T0 = oracle.problem_reference(p)
+    C1, T1 = oracle.grouped_gemm_ids(p.mode, p.A, p.B, p.a_scales, p.b_scales, p.offsets,
+                                     np.arange(3, dtype=np.int32), p.N, p.K)
+    assert np.array_equal(C0, C1) and np.array_equal(T0, T1)
+
+
+@pytest.mark.parametrize("bad", [-1, 4])
+def test_expert_ids_out_of_range_rejected(bad):
+    p = gen.routed_problem([8, 8], [0, 1], 4, 128, 128, seed=25)
+    with pytest.raises(oracle.OracleError, match="code 8"):
+        oracle.grouped_gemm_ids(p.mode, p.A, p.B, p.a_scales, p.b_scales, p.offsets,
+                                np.array([0, bad], np.int32), p.N, p.K)
