@@ -30,7 +30,8 @@ STATUS_NAMES = {
 
 # Every symbol include/bsfp8.h declares (the CPU test checks the library exports them).
 EXPORTED = ("bsfp8_grouped_gemm", "bsmxfp8_grouped_gemm", "bsfp8_grouped_gemm_ids",
-            "bsmxfp8_grouped_gemm_ids", "bsmxfp8_tmem_plan", "bsfp8_blockwise_plan",
+            "bsmxfp8_grouped_gemm_ids", "bsmxfp8_pack_b_scales", "bsmxfp8_grouped_gemm_prepacked",
+            "bsmxfp8_tmem_plan", "bsfp8_blockwise_plan",
             "bsfp8_get_device_error", "bsfp8_status_string")
 
 
@@ -60,6 +61,10 @@ def load_library() -> ctypes.CDLL:
         lib.bsfp8_grouped_gemm_ids.restype = i32
         lib.bsmxfp8_grouped_gemm_ids.argtypes = [p, p, p, p, p, p, p, i64, i32, i32, i32, i32, p]
         lib.bsmxfp8_grouped_gemm_ids.restype = i32
+        lib.bsmxfp8_pack_b_scales.argtypes = [p, p, i32, i32, i32, p]
+        lib.bsmxfp8_pack_b_scales.restype = i32
+        lib.bsmxfp8_grouped_gemm_prepacked.argtypes = [p, p, p, p, p, p, i64, i32, i32, i32, p]
+        lib.bsmxfp8_grouped_gemm_prepacked.restype = i32
         lib.bsmxfp8_tmem_plan.argtypes = [i32, i32, i32, i32, ctypes.POINTER(ctypes.c_int32)]
         lib.bsmxfp8_tmem_plan.restype = i32
         lib.bsfp8_blockwise_plan.argtypes = [ctypes.c_int64, i32, i32, i32,
@@ -141,6 +146,27 @@ def bsmxfp8_grouped_gemm_ids(A, B, a_scales, b_scales, group_offsets, expert_ids
         int(num_experts), _stream(stream))
     if st != BSFP8_OK:
         raise BsFp8Error(st, "bsmxfp8_grouped_gemm_ids")
+
+
+def bsmxfp8_pack_b_scales(b_scales, b_scales_packed, num_experts: int, N: int, K: int,
+                          stream=None) -> None:
+    """Rearrange UE8M0 weight scales [E, N, K/32] into the packed 512-byte block layout
+    (include/bsfp8.h).  Raises BsFp8Error."""
+    st = load_library().bsmxfp8_pack_b_scales(_addr(b_scales), _addr(b_scales_packed),
+                                              int(num_experts), int(N), int(K), _stream(stream))
+    if st != BSFP8_OK:
+        raise BsFp8Error(st, "bsmxfp8_pack_b_scales")
+
+
+def bsmxfp8_grouped_gemm_prepacked(A, B, a_scales, b_scales_packed, expert_offsets, C,
+                                   M_total: int, N: int, K: int, num_experts: int,
+                                   stream=None) -> None:
+    """MXFP8 grouped GEMM with pre-packed weight scales; see include/bsfp8.h."""
+    st = load_library().bsmxfp8_grouped_gemm_prepacked(
+        _addr(A), _addr(B), _addr(a_scales), _addr(b_scales_packed), _addr(expert_offsets),
+        _addr(C), int(M_total), int(N), int(K), int(num_experts), _stream(stream))
+    if st != BSFP8_OK:
+        raise BsFp8Error(st, "bsmxfp8_grouped_gemm_prepacked")
 
 
 def bsmxfp8_tmem_plan(block_k: int, epilogue_n: int, vec: int, overlap: bool) -> dict:

@@ -107,6 +107,7 @@ bsmxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   const uint32_t lane = threadIdx.x & 31;
   const int KB = args.K / BK;
   const int scale_row = args.K / 32;  // bytes per row of a row-major UE8M0 scale matrix
+  const bool packed_b = args.b_scales_packed != 0;
 
   // Tiles: per expert ceil(M_e / TN) token tiles x N/128 weight tiles (weights fastest).
   if (warp == 0) {
@@ -170,15 +171,21 @@ bsmxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         if (!sched.locate(args, t, tc)) break;
         const int32_t w_row = tc.be * args.N + tc.n0;
         const int32_t t_row = (int32_t)tc.m0;
+        // packed weight scales: this tile's 128 rows, K block 0 (blocks of a row are adjacent)
+        const uint8_t* w_sf = static_cast<const uint8_t*>(args.b_scales) +
+                              ((int64_t)w_row / WROWS) * KB * SF_BLOCK;
         for (int kb = 0; kb < KB; ++kb) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1, abort)) {
             record_error(args.err, DEV_TIMEOUT, abort);
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(full_bar(stage), C::STAGE_TX);
+          mbar_arrive_expect_tx(full_bar(stage), C::STAGE_TX + (packed_b ? SF_BLOCK : 0u));
           tma_load_2d_hint(sW + stage * C::W_STAGE, &tmB, kb * BK, w_row, full_bar(stage), pol_w);
           tma_load_2d(sT + stage * C::T_STAGE, &tmA, kb * BK, t_row, full_bar(stage));
+          if (packed_b)  // the stage's weight-scale block is stored ready-made
+            bulk_copy_g2s_hint(sSFW + stage * SF_BLOCK, w_sf + (int64_t)kb * SF_BLOCK, SF_BLOCK,
+                               full_bar(stage), pol_w);
           ++issued;
           if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
         }
@@ -273,7 +280,7 @@ bsmxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const int r = j * 32 + (int)lane;
-          cp_async_4(dw + 4 * j, w_rows + (int64_t)r * scale_row + 4 * kb, 4);
+          if (!packed_b) cp_async_4(dw + 4 * j, w_rows + (int64_t)r * scale_row + 4 * kb, 4);
           const int64_t m = tc.m0 + r;
           const bool live = (r < C::TN) && (m < args.M_total);
           cp_async_4(dt + 4 * j, live ? a_sc + m * scale_row + 4 * kb : a_sc, live ? 4u : 0u);
@@ -356,7 +363,31 @@ cudaError_t launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArg
   return cudaGetLastError();
 }
 
+// One 512-byte block per iteration: thread r moves row r's 4 codes of the K block (one
+// aligned 4-byte word of the row-major source) to byte (r % 32) * 16 + (r / 32) * 4.
+__global__ void __launch_bounds__(128)
+pack_b_scales_kernel(const uint8_t* src, uint8_t* dst, int64_t blocks, int KB, int scale_row) {
+  const int r = (int)threadIdx.x;
+  for (int64_t b = blockIdx.x; b < blocks; b += gridDim.x) {
+    const int64_t kb = b % KB;
+    const int64_t row = (b / KB) * WROWS + r;  // (e * N/128 + n block) * 128 + r = e * N + n
+    const uint32_t w = *reinterpret_cast<const uint32_t*>(src + row * scale_row + 4 * kb);
+    *reinterpret_cast<uint32_t*>(dst + b * SF_BLOCK + (r & 31) * 16 + (r >> 5) * 4) = w;
+  }
+}
+
 }  // namespace mx
+
+cudaError_t launch_pack_mx_b_scales(const uint8_t* src, uint8_t* dst, int E, int N, int K,
+                                    int num_sms, cudaStream_t stream) {
+  const int KB = K / mx::BK;
+  const int64_t blocks = (int64_t)E * (N / mx::WROWS) * KB;
+  if (blocks == 0) return cudaSuccess;
+  const int64_t cap = (int64_t)num_sms * 16;
+  const int grid = (int)(blocks < cap ? blocks : cap);
+  mx::pack_b_scales_kernel<<<grid, 128, 0, stream>>>(src, dst, blocks, KB, K / 32);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_bsmxfp8(int tn, const CUtensorMap& tmA, const CUtensorMap& tmB,
                            const GemmArgs& args, int num_sms, cudaStream_t stream) {

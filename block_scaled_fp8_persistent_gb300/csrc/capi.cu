@@ -186,22 +186,27 @@ bsfp8_status blockwise_gemm(const void* A, const void* B, const float* a_scales,
       !encode_u8_2d(&tmB, B, (uint64_t)K, (uint64_t)E * N, 128,
                     (uint32_t)blockwise_b_rows(tile)))
     return BSFP8_ERR_CUDA;
-  GemmArgs args{offsets, a_scales, b_scales, C, M_total, N, K, G, dev->err_word, ids, E};
+  GemmArgs args{offsets, a_scales, b_scales, C, M_total, N, K, G, dev->err_word, ids, E, 0};
   return launch_bsfp8_blockwise(tile, tmA, tmB, args, dev->num_sms, stream) == cudaSuccess
              ? BSFP8_OK
              : BSFP8_ERR_CUDA;
 }
 
+// packed_b: b_scales are in the 512-byte block layout of bsmxfp8_pack_b_scales (swap-AB
+// tiles only: their weight tile is one 128-row block).
 bsfp8_status mx_gemm(const void* A, const void* B, const uint8_t* a_scales,
                      const uint8_t* b_scales, const int32_t* offsets, const int32_t* ids,
-                     void* C, int64_t M_total, int N, int K, int G, int E, cudaStream_t stream) {
+                     void* C, int64_t M_total, int N, int K, int G, int E, cudaStream_t stream,
+                     bool packed_b = false) {
   bsfp8_status st = check_common(A, B, a_scales, b_scales, offsets, ids, C, M_total, N, K, G, E);
   if (st != BSFP8_OK) return st;
+  if (packed_b && !aligned(b_scales, 16)) return BSFP8_ERR_ALIGN;
   DeviceInfo* dev = nullptr;
   if ((st = device_info(&dev)) != BSFP8_OK) return st;
   if (M_total == 0) return BSFP8_OK;
-  GemmArgs args{offsets, a_scales, b_scales, C, M_total, N, K, G, dev->err_word, ids, E};
-  if (use_mx_pair(M_total, G)) {
+  GemmArgs args{offsets, a_scales, b_scales, C, M_total, N, K, G, dev->err_word, ids, E,
+                packed_b ? 1 : 0};
+  if (!packed_b && use_mx_pair(M_total, G)) {
     CUtensorMap tmA, tmB;
     if (!encode_u8_2d(&tmA, A, (uint64_t)K, (uint64_t)M_total, 128, 128) ||
         !encode_u8_2d(&tmB, B, (uint64_t)K, (uint64_t)E * N, 128, 128))
@@ -257,6 +262,32 @@ extern "C" bsfp8_status bsmxfp8_grouped_gemm_ids(const void* A, const void* B,
   if (!expert_ids) return BSFP8_ERR_NULL;
   return mx_gemm(A, B, a_scales, b_scales, group_offsets, expert_ids, C, M_total, N, K,
                  num_groups, num_experts, stream);
+}
+
+extern "C" bsfp8_status bsmxfp8_pack_b_scales(const uint8_t* b_scales, uint8_t* b_scales_packed,
+                                              int num_experts, int N, int K, cudaStream_t stream) {
+  if (!b_scales || !b_scales_packed) return BSFP8_ERR_NULL;
+  if (num_experts < 1 || N < 128 || N % 128 != 0 || K < 128 || K % 128 != 0 ||
+      (int64_t)num_experts * N > INT32_MAX)
+    return BSFP8_ERR_SHAPE;
+  if (!aligned(b_scales, 4) || !aligned(b_scales_packed, 16)) return BSFP8_ERR_ALIGN;
+  DeviceInfo* dev = nullptr;
+  bsfp8_status st = device_info(&dev);
+  if (st != BSFP8_OK) return st;
+  return launch_pack_mx_b_scales(b_scales, b_scales_packed, num_experts, N, K, dev->num_sms,
+                                 stream) == cudaSuccess
+             ? BSFP8_OK
+             : BSFP8_ERR_CUDA;
+}
+
+extern "C" bsfp8_status bsmxfp8_grouped_gemm_prepacked(const void* A, const void* B,
+                                                       const uint8_t* a_scales,
+                                                       const uint8_t* b_scales_packed,
+                                                       const int32_t* expert_offsets, void* C,
+                                                       int64_t M_total, int N, int K,
+                                                       int num_experts, cudaStream_t stream) {
+  return mx_gemm(A, B, a_scales, b_scales_packed, expert_offsets, nullptr, C, M_total, N, K,
+                 num_experts, num_experts, stream, true);
 }
 
 extern "C" bsfp8_status bsmxfp8_tmem_plan(int block_k, int epilogue_n, int vec, int overlap,

@@ -29,6 +29,7 @@ struct GemmArgs {
   int* err;                // library-owned device error word
   const int32_t* expert_ids;  // [E] group -> expert (rows of B and B scales); nullptr: identity
   int num_experts;         // experts in B (bound of expert_ids)
+  int b_scales_packed;     // MX swap-AB kernel: b_scales in the 512-byte block layout
 };
 
 // Tile configurations of the blockwise kernel.
@@ -62,5 +63,10 @@ cudaError_t launch_bsmxfp8_pair(const CUtensorMap& tmA, const CUtensorMap& tmB,
                                 const GemmArgs& args, int num_sms, cudaStream_t stream);
 // The TMEM plan that kernel is compiled with.
 TmemPlan mx_pair_tmem_plan();
+
+// Rearrange UE8M0 B scales [E, N, K/32] into [E, N/128, K/128] blocks of 512 bytes: row r of
+// a 128-row block keeps its 4 codes of the 128-K block at byte (r % 32) * 16 + (r / 32) * 4.
+cudaError_t launch_pack_mx_b_scales(const uint8_t* src, uint8_t* dst, int E, int N, int K,
+                                    int num_sms, cudaStream_t stream);
 
 }  // namespace bsfp8

@@ -149,6 +149,37 @@ bsfp8_status bsmxfp8_grouped_gemm_ids(const void* A, const void* B, const uint8_
                                       cudaStream_t stream);
 
 /*
+ * Pre-packed MXFP8 weight scales.  Expert weights are static, so their UE8M0 scales can be
+ * rearranged once into the tensor core's scale-factor layout, which the GEMM then copies
+ * straight into shared memory instead of gathering and transposing 4 codes per row per
+ * K block.  The layout is the 128-row "packed block" of swizzle_scales_packed_block in the
+ * Triton Gluon example "Overlapping Accumulator Block-Scaled Matrix Multiplication" (rows
+ * padded to 128 and scale columns to 4, viewed as (rows/128, 4, 32, cols/4, 4) and permuted
+ * (0, 3, 2, 1, 4)); here N % 128 == 0 and K % 128 == 0, so nothing is padded:
+ *
+ *   b_scales_packed  UE8M0 [num_experts, N/128, K/128, 512]
+ *     byte (r % 32) * 16 + (r / 32) * 4 + j of block (e, nb, kb) =
+ *     b_scales[e, nb*128 + r, 4*kb + j]          (r < 128, j < 4)
+ *
+ * bsmxfp8_pack_b_scales writes it (num_experts * N * K/32 bytes, the size of the source)
+ * on `stream`; b_scales 4-byte aligned, b_scales_packed 16-byte aligned.  Errors:
+ * BSFP8_ERR_NULL, BSFP8_ERR_SHAPE (num_experts >= 1, N and K multiples of 128,
+ * num_experts * N < 2^31), BSFP8_ERR_ALIGN, BSFP8_ERR_UNSUPPORTED_DEVICE, BSFP8_ERR_CUDA.
+ *
+ * bsmxfp8_grouped_gemm_prepacked is bsmxfp8_grouped_gemm with b_scales_packed (16-byte
+ * aligned) in place of b_scales; it always runs the swap-AB tiles (128 weight rows = one
+ * packed block per K block).  Same result, requirements and errors otherwise.
+ */
+bsfp8_status bsmxfp8_pack_b_scales(const uint8_t* b_scales, uint8_t* b_scales_packed,
+                                   int num_experts, int N, int K, cudaStream_t stream);
+
+bsfp8_status bsmxfp8_grouped_gemm_prepacked(const void* A, const void* B, const uint8_t* a_scales,
+                                            const uint8_t* b_scales_packed,
+                                            const int32_t* expert_offsets, void* C,
+                                            int64_t M_total, int N, int K, int num_experts,
+                                            cudaStream_t stream);
+
+/*
  * TMEM storage plan of double-buffered block-scaled accumulators (host only, no GPU use).
  * For a 256-column tile with 512 TMEM columns, block_k elements of K per MMA stage,
  * epilogue subtiles of epilogue_n columns and one scale per vec (16 or 32) elements of K,

@@ -199,6 +199,22 @@ def timed_rows(p, row_count: int, nthreads: int = 0):
     return dt, 2.0 * rows.size * p.K, threads(nthreads)
 
 
+def pack_mx_scales(S) -> np.ndarray:
+    """UE8M0 scales [rows, cols] in the tensor core's 128-row packed block layout, as
+    swizzle_scales_packed_block of the Triton Gluon example "Overlapping Accumulator
+    Block-Scaled Matrix Multiplication" builds it: zero-pad rows to a multiple of 128 and
+    columns to a multiple of 4, view as (rows/128, 4, 32, cols/4, 4), swap axes 1 and 3
+    (permute (0, 3, 2, 1, 4)), flatten.  For weight scales [E, N, K/32] pass them reshaped
+    to [E*N, K/32]: the result is [E][N/128][K/128] blocks of 512 bytes."""
+    S = np.asarray(S, np.uint8)
+    R, SK = S.shape
+    Rp, SKp = -(-R // 128) * 128, -(-SK // 4) * 4
+    P = np.zeros((Rp, SKp), np.uint8)
+    P[:R, :SK] = S
+    return np.ascontiguousarray(
+        P.reshape(Rp // 128, 4, 32, SKp // 4, 4).transpose(0, 3, 2, 1, 4)).reshape(-1)
+
+
 def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
     """bf16 bit patterns -> float64 values (exact)."""
     bits = np.asarray(bits, np.uint16)

@@ -100,3 +100,21 @@ def test_binding_ids_raises_on_null_ids():
         bsfp8.bsfp8_grouped_gemm_ids(FAKE, FAKE, FAKE, FAKE, FAKE, 0, FAKE, 256, 256, 512, 2, 2,
                                      stream=0)
     assert ei.value.status == 1
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(src=None), 1), (dict(dst=None), 1), (dict(E=0), 2), (dict(N=192), 2), (dict(K=100), 2),
+    (dict(E=1 << 20, N=4096), 2), (dict(src=FAKE + 2), 3), (dict(dst=FAKE + 4), 3),
+])
+def test_host_validation_pack_b_scales(lib, kw, status):
+    a = dict(src=FAKE, dst=FAKE, E=2, N=256, K=512)
+    a.update(kw)
+    assert lib.bsmxfp8_pack_b_scales(a["src"], a["dst"], a["E"], a["N"], a["K"], None) == status
+
+
+def test_host_validation_prepacked_gemm(lib):
+    f = lib.bsmxfp8_grouped_gemm_prepacked
+    # packed scales must be 16-byte aligned (they are copied as 512-byte blocks)
+    assert f(FAKE, FAKE, FAKE, FAKE + 4, FAKE, FAKE, 256, 256, 512, 1, None) == 3
+    assert f(FAKE, FAKE, FAKE, None, FAKE, FAKE, 256, 256, 512, 1, None) == 1
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 256, 200, 512, 1, None) == 2

@@ -17,7 +17,10 @@ fails at least one of them:
   * T equals |A_deq| @ |B_deq|^T;
   * expert ids (group -> expert, the expert_ids argument of promote_accumulators): the
     result equals the brute force run on the groups' gathered experts, identity ids give the
-    plain grouped result, ids outside [0, num_experts) are rejected.
+    plain grouped result, ids outside [0, num_experts) are rejected;
+  * the packed scale layout: every byte at the position the closed form of the page's
+    reshape/permute gives (written out as loops), including padded shapes, and the inverse
+    view restores the input.
 """
 import math
 
@@ -293,3 +296,31 @@ def test_expert_ids_out_of_range_rejected(bad):
     with pytest.raises(oracle.OracleError, match="code 8"):
         oracle.grouped_gemm_ids(p.mode, p.A, p.B, p.a_scales, p.b_scales, p.offsets,
                                 np.array([0, bad], np.int32), p.N, p.K)
+
+
+# ---------------------------------------------------------------------------
+# packed scale-factor layout (swizzle_scales_packed_block of the Gluon example)
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("R,SK", [(128, 4), (256, 12), (300, 7), (5, 1)])
+def test_pack_mx_scales_element_formula(R, SK):
+    rng = np.random.default_rng(R * 100 + SK)
+    S = rng.integers(0, 256, size=(R, SK), dtype=np.uint8)
+    P = oracle.pack_mx_scales(S)
+    rep_mn, rep_k = -(-R // 128), -(-SK // 4)
+    assert P.size == rep_mn * 128 * rep_k * 4
+    for mb in range(rep_mn):
+        for kq in range(rep_k):
+            base = (mb * rep_k + kq) * 512
+            for r in range(128):
+                for j in range(4):
+                    row, col = mb * 128 + r, kq * 4 + j
+                    want = S[row, col] if (row < R and col < SK) else 0
+                    assert P[base + (r % 32) * 16 + (r // 32) * 4 + j] == want
+
+
+def test_pack_mx_scales_inverse_view():
+    rng = np.random.default_rng(3)
+    S = rng.integers(0, 256, size=(384, 8), dtype=np.uint8)
+    P = oracle.pack_mx_scales(S)
+    back = P.reshape(3, 2, 32, 4, 4).transpose(0, 3, 2, 1, 4).reshape(384, 8)
+    assert np.array_equal(back, S)
