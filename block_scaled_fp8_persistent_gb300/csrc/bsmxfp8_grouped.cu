@@ -21,9 +21,11 @@
 //               TMEM, then 4 x tcgen05.mma kind::mxf8f6f4.block_scale (K = 32 each, the
 //               scale-factor id picks the byte of the 4-byte scale word), accumulating over
 //               all of K in a 2-deep TMEM accumulator ring.
-//   warp 2      scale loader: per stage each weight / token row's 4 UE8M0 codes (one 4-byte
-//               word, row-major source) are cp.async'ed into the packed 512-byte block
-//               (row r at byte (r%32)*16 + (r/32)*4); a few stages in flight.
+//   warps 2, 3  scale loaders (token rows, weight rows): per stage each row's 4 UE8M0 codes
+//               (one 4-byte word, row-major source) are cp.async'ed into the packed
+//               512-byte block (row r at byte (r%32)*16 + (r/32)*4); a few stages in
+//               flight.  With pre-packed weight scales the producer copies the weight block
+//               and warp 3 idles.
 //   warps 4-7   epilogue: warp w holds weight rows 32*(w%4).. of the tile, reads the tn
 //               token columns of the accumulator, rounds to bf16 and stores C[m, n] for the
 //               tile's token rows that belong to the expert.
@@ -41,6 +43,9 @@ constexpr int NUM_THREADS = 256;
 constexpr int EPI_WARP0 = 4;
 constexpr int SF_BLOCK = 512;        // packed scale block: 128 rows x 4 codes
 constexpr int SCALE_LOOKAHEAD = 4;   // scale stages in flight per loader warp
+constexpr int GROUP = 4;             // stages whose 4 codes per row form one 16-byte chunk
+constexpr int STG_SLOTS = 3;         // staged 16-byte groups: one in use, two in flight
+constexpr uint32_t STG_SLOT = WROWS * 16;
 
 template <int TN_>
 struct Cfg {
@@ -52,7 +57,9 @@ struct Cfg {
   static constexpr uint32_t SMEM_T = SMEM_W + STAGES * W_STAGE;
   static constexpr uint32_t SMEM_SFW = SMEM_T + STAGES * T_STAGE;
   static constexpr uint32_t SMEM_SFT = SMEM_SFW + STAGES * SF_BLOCK;
-  static constexpr uint32_t SMEM_CTL = SMEM_SFT + STAGES * SF_BLOCK;
+  // weight-scale staging of the grouped loader: STG_SLOTS x (128 rows x 16 bytes)
+  static constexpr uint32_t SMEM_STG = SMEM_SFT + STAGES * SF_BLOCK;
+  static constexpr uint32_t SMEM_CTL = SMEM_STG + STG_SLOTS * STG_SLOT;
   static constexpr uint32_t STAGE_TX = W_STAGE + T_STAGE;
   // TMEM: 2 accumulators of TN columns, then 2 slots each of weight / token scales (4 cols)
   static constexpr uint32_t ACC_COLS = 2 * TN;
@@ -139,7 +146,8 @@ bsmxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
     for (int s = 0; s < C::STAGES; ++s) {
-      mbar_init(full_bar(s), 2);   // producer (with bytes) + scale loader
+      // producer (with bytes) + token-scale loader (+ weight-scale loader)
+      mbar_init(full_bar(s), packed_b ? 2 : 3);
       mbar_init(empty_bar(s), 1);  // one MMA commit
     }
     for (int s = 0; s < 2; ++s) {
@@ -245,13 +253,22 @@ bsmxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       mbar_wait_timed(smem_u32(&ctl->mma_done), 0);
     }
     __syncwarp();
-  } else if (warp == 2) {
-    // =============================== scale loader ===============================
-    // Each lane moves 4-byte words: weight rows lane + 32*j (j < 4), token rows likewise.
-    // A stage is announced on its full barrier once its copies have landed, SCALE_LOOKAHEAD
-    // stages behind the newest issued one.
+  } else if (warp == 2 || (warp == 3 && !packed_b)) {
+    // =============================== scale loaders ===============================
+    // Warp 2 gathers the token rows' scales, warp 3 the weight rows' (unless they arrive
+    // pre-packed with the producer's copies).  Each lane moves 4-byte words (one row's 4
+    // codes of the stage) into the packed block, row r at byte (r % 32) * 16 + (r / 32) * 4,
+    // and a stage is announced on its full barrier once its copies have landed,
+    // SCALE_LOOKAHEAD stages behind the newest issued one.  Token rows >= TN of every
+    // block stay zero (written once here).
+    const bool weights = warp == 3;
     const uint8_t* a_sc = static_cast<const uint8_t*>(args.a_scales);
     const uint8_t* b_sc = static_cast<const uint8_t*>(args.b_scales);
+    if (!weights && C::TN < WROWS) {
+      for (int s = 0; s < C::STAGES; ++s)
+        for (int rg = C::TN / 32; rg < 4; ++rg)
+          *reinterpret_cast<uint32_t*>(smem + C::SMEM_SFT + s * SF_BLOCK + lane * 16 + rg * 4) = 0u;
+    }
     GroupedScheduler<C::TN, WROWS> sched;
     uint32_t stage = 0, phase = 0;
     uint32_t ring[SCALE_LOOKAHEAD + 1] = {};
@@ -259,13 +276,80 @@ bsmxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     bool ok = true;
     TileCoord tc;
     auto announce_oldest = [&]() {
-      fence_proxy_async_smem();  // cp.async (generic proxy) writes -> tcgen05.cp (async proxy)
+      fence_proxy_async_smem();  // generic-proxy writes -> tcgen05.cp (async proxy)
       __syncwarp();
       if (lane == 0) mbar_arrive(full_bar(ring[head]));
       head = (head + 1) % (SCALE_LOOKAHEAD + 1);
       --inflight;
     };
-    for (int64_t t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
+    // Weight rows, grouped: when a row's codes for GROUP consecutive stages form one
+    // aligned 16-byte chunk (K % 512 == 0, 16-byte aligned b_scales), fetch each row's chunk
+    // with one 16-byte copy two groups ahead and transpose each stage's words into its
+    // packed block in shared memory.
+    const bool grouped = weights && (args.K % (GROUP * BK) == 0) &&
+                         (reinterpret_cast<uintptr_t>(b_sc) % 16 == 0);
+    if (grouped) {
+      const int G = KB / GROUP;
+      const uint32_t sSTG = smem_u32(smem + C::SMEM_STG);
+      const uint8_t* stg = smem + C::SMEM_STG;
+      GroupedScheduler<C::TN, WROWS> pre;
+      TileCoord tp;
+      int64_t tp_t = blockIdx.x;
+      bool pre_ok = pre.locate(args, tp_t, tp);
+      int qp = 0;
+      auto issue_group = [&](int slot) {
+        if (pre_ok) {
+          const uint8_t* rows = b_sc + ((int64_t)tp.be * args.N + tp.n0) * scale_row + 16 * qp;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int r = 32 * j + (int)lane;
+            cp_async_16(sSTG + slot * STG_SLOT + r * 16, rows + (int64_t)r * scale_row, 16u);
+          }
+          if (++qp == G) {
+            qp = 0;
+            tp_t += gridDim.x;
+            pre_ok = tp_t < total_tiles && pre.locate(args, tp_t, tp);
+          }
+        }
+        cp_async_commit();  // an empty group keeps the group count in step
+      };
+      issue_group(0);
+      issue_group(1);
+      int64_t g = 0;
+      for (int64_t t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
+        if (!sched.locate(args, t, tc)) break;
+        for (int q = 0; ok && q < G; ++q, ++g) {
+          cp_async_wait_group<1>();  // group g has landed (g + 1 may be in flight)
+          __syncwarp();
+          const uint8_t* src = stg + (g % STG_SLOTS) * STG_SLOT;
+          for (int j = 0; j < GROUP; ++j) {
+            const bool got =
+                __all_sync(0xffffffffu, mbar_wait(empty_bar(stage), phase ^ 1, abort));
+            if (!got) {
+              if (lane == 0) record_error(args.err, DEV_TIMEOUT, abort);
+              ok = false;
+              break;
+            }
+            // packed block: row 32*rg + lane at byte lane*16 + rg*4
+            uint4 w;
+            w.x = *reinterpret_cast<const uint32_t*>(src + (0 * 32 + lane) * 16 + 4 * j);
+            w.y = *reinterpret_cast<const uint32_t*>(src + (1 * 32 + lane) * 16 + 4 * j);
+            w.z = *reinterpret_cast<const uint32_t*>(src + (2 * 32 + lane) * 16 + 4 * j);
+            w.w = *reinterpret_cast<const uint32_t*>(src + (3 * 32 + lane) * 16 + 4 * j);
+            *reinterpret_cast<uint4*>(smem + C::SMEM_SFW + stage * SF_BLOCK + lane * 16) = w;
+            fence_proxy_async_smem();  // generic-proxy writes -> tcgen05.cp (async proxy)
+            __syncwarp();
+            if (lane == 0) mbar_arrive(full_bar(stage));
+            if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
+          }
+          if (!ok) break;
+          __syncwarp();
+          issue_group((int)((g + 2) % STG_SLOTS));  // the slot group g - 1 used is free
+        }
+      }
+      cp_async_wait_group<0>();
+    }
+    for (int64_t t = blockIdx.x; !grouped && ok && t < total_tiles; t += gridDim.x) {
       if (!sched.locate(args, t, tc)) break;
       const uint8_t* w_rows = b_sc + ((int64_t)tc.be * args.N + tc.n0) * scale_row;
       for (int kb = 0; kb < KB; ++kb) {
@@ -275,15 +359,21 @@ bsmxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           ok = false;
           break;
         }
-        const uint32_t dw = sSFW + stage * SF_BLOCK + lane * 16;
-        const uint32_t dt = sSFT + stage * SF_BLOCK + lane * 16;
+        if (weights) {
+          const uint32_t dw = sSFW + stage * SF_BLOCK + lane * 16;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int r = j * 32 + (int)lane;
-          if (!packed_b) cp_async_4(dw + 4 * j, w_rows + (int64_t)r * scale_row + 4 * kb, 4);
-          const int64_t m = tc.m0 + r;
-          const bool live = (r < C::TN) && (m < args.M_total);
-          cp_async_4(dt + 4 * j, live ? a_sc + m * scale_row + 4 * kb : a_sc, live ? 4u : 0u);
+          for (int j = 0; j < 4; ++j) {
+            const int r = j * 32 + (int)lane;
+            cp_async_4(dw + 4 * j, w_rows + (int64_t)r * scale_row + 4 * kb, 4);
+          }
+        } else {
+          const uint32_t dt = sSFT + stage * SF_BLOCK + lane * 16;
+#pragma unroll
+          for (int j = 0; j < C::TN / 32; ++j) {
+            const int64_t m = tc.m0 + j * 32 + (int)lane;
+            const bool live = m < args.M_total;
+            cp_async_4(dt + 4 * j, live ? a_sc + m * scale_row + 4 * kb : a_sc, live ? 4u : 0u);
+          }
         }
         cp_async_commit();
         ring[(head + inflight) % (SCALE_LOOKAHEAD + 1)] = stage;
