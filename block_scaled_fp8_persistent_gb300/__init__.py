@@ -32,7 +32,7 @@ STATUS_NAMES = {
 EXPORTED = ("bsfp8_grouped_gemm", "bsmxfp8_grouped_gemm", "bsfp8_grouped_gemm_ids",
             "bsmxfp8_grouped_gemm_ids", "bsmxfp8_pack_b_scales", "bsmxfp8_grouped_gemm_prepacked",
             "bsmxfp8_tmem_plan", "bsfp8_blockwise_plan",
-            "bsfp8_get_device_error", "bsfp8_status_string")
+            "bsfp8_get_device_error", "bsfp8_check_wait_timeout", "bsfp8_status_string")
 
 
 class BsFp8Error(RuntimeError):
@@ -72,6 +72,8 @@ def load_library() -> ctypes.CDLL:
         lib.bsfp8_blockwise_plan.restype = i32
         lib.bsfp8_get_device_error.argtypes = [p, ctypes.POINTER(ctypes.c_int)]
         lib.bsfp8_get_device_error.restype = i32
+        lib.bsfp8_check_wait_timeout.argtypes = [ctypes.c_int64, p]
+        lib.bsfp8_check_wait_timeout.restype = i32
         lib.bsfp8_status_string.argtypes = [i32]
         lib.bsfp8_status_string.restype = ctypes.c_char_p
         _lib = lib
@@ -190,6 +192,14 @@ def bsfp8_blockwise_plan(M_total: int, N: int, num_experts: int, num_sms: int) -
     if st != BSFP8_OK:
         raise BsFp8Error(st, "bsfp8_blockwise_plan")
     return {"tile_rows": out[0], "tile_cols": out[1], "ctas_per_tile": out[2]}
+
+
+def bsfp8_check_wait_timeout(limit_ns: int, stream=None) -> None:
+    """Launch the failure-detection check: a bounded wait that nothing completes gives up
+    after limit_ns and records BSFP8_ERR_DEVICE_TIMEOUT in the device error word."""
+    st = load_library().bsfp8_check_wait_timeout(int(limit_ns), _stream(stream))
+    if st != BSFP8_OK:
+        raise BsFp8Error(st, "bsfp8_check_wait_timeout")
 
 
 def bsfp8_get_device_error(stream=None) -> int:

@@ -7,11 +7,26 @@
 
 #include "bsfp8.h"
 #include "common.cuh"
+#include "ptx.cuh"
 
 namespace bsfp8 {
 
 // One device error word per device (static device memory: nothing is allocated).
 __device__ int g_error_word;
+
+// Failure-detection check: one thread waits, with the GEMM kernels' bounded wait, for a
+// phase of an mbarrier that nothing arrives on; when the wait gives up after limit_ns it
+// records DEV_TIMEOUT in the device error word, as a GEMM kernel whose pipeline stalled
+// would, and the kernel returns.
+__global__ void wait_timeout_check_kernel(int* err, uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x != 0) return;
+  abort_flag = 0;
+  mbar_init(smem_u32(&bar), 1);
+  fence_mbarrier_init();
+  if (!mbar_wait(smem_u32(&bar), 0, &abort_flag, limit_ns)) atomicCAS(err, 0, DEV_TIMEOUT);
+}
 
 namespace {
 
@@ -288,6 +303,15 @@ extern "C" bsfp8_status bsmxfp8_grouped_gemm_prepacked(const void* A, const void
                                                        int num_experts, cudaStream_t stream) {
   return mx_gemm(A, B, a_scales, b_scales_packed, expert_offsets, nullptr, C, M_total, N, K,
                  num_experts, num_experts, stream, true);
+}
+
+extern "C" bsfp8_status bsfp8_check_wait_timeout(int64_t limit_ns, cudaStream_t stream) {
+  if (limit_ns <= 0 || limit_ns > 1000000000LL) return BSFP8_ERR_SHAPE;
+  DeviceInfo* dev = nullptr;
+  bsfp8_status st = device_info(&dev);
+  if (st != BSFP8_OK) return st;
+  wait_timeout_check_kernel<<<1, 32, 0, stream>>>(dev->err_word, (uint64_t)limit_ns);
+  return cudaGetLastError() == cudaSuccess ? BSFP8_OK : BSFP8_ERR_CUDA;
 }
 
 extern "C" bsfp8_status bsmxfp8_tmem_plan(int block_k, int epilogue_n, int vec, int overlap,

@@ -88,7 +88,8 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
 
 // Bounded wait for the phase with the given parity to complete.  Returns false when the
 // time limit passed or *abort became non-zero (another role gave up).
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
+                                          uint64_t limit_ns = BSFP8_WAIT_LIMIT_NS) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   uint32_t spins = 0;
@@ -96,7 +97,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     if (mbar_try_wait(bar, parity)) return true;
     if ((++spins & 63u) == 0) {
       if (*abort) return false;
-      if (globaltimer_ns() - t0 > BSFP8_WAIT_LIMIT_NS) return false;
+      if (globaltimer_ns() - t0 > limit_ns) return false;
     }
   }
 }

@@ -215,6 +215,17 @@ bsfp8_status bsfp8_blockwise_plan(int64_t M_total, int N, int num_experts, int n
  */
 bsfp8_status bsfp8_get_device_error(cudaStream_t stream, int* code);
 
+/*
+ * Failure-detection check (no GEMM): launches one thread on `stream` that waits, with the
+ * same bounded mbarrier wait every pipeline stage of the GEMM kernels uses, for a barrier
+ * phase that nothing completes.  After limit_ns nanoseconds of %globaltimer (0 < limit_ns
+ * <= 1e9; the GEMM kernels use 1 s) the wait gives up, BSFP8_ERR_DEVICE_TIMEOUT is recorded
+ * in the device error word -- read it with bsfp8_get_device_error() -- and the kernel
+ * returns, leaving the context usable.  Nothing else is read or written.
+ * BSFP8_ERR_SHAPE for a limit out of range, BSFP8_ERR_UNSUPPORTED_DEVICE, BSFP8_ERR_CUDA.
+ */
+bsfp8_status bsfp8_check_wait_timeout(int64_t limit_ns, cudaStream_t stream);
+
 /* Static, human-readable name of a status code. */
 const char* bsfp8_status_string(bsfp8_status status);
 

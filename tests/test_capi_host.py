@@ -118,3 +118,8 @@ def test_host_validation_prepacked_gemm(lib):
     assert f(FAKE, FAKE, FAKE, FAKE + 4, FAKE, FAKE, 256, 256, 512, 1, None) == 3
     assert f(FAKE, FAKE, FAKE, None, FAKE, FAKE, 256, 256, 512, 1, None) == 1
     assert f(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 256, 200, 512, 1, None) == 2
+
+
+@pytest.mark.parametrize("limit", [0, -5, 2_000_000_000])
+def test_host_validation_wait_timeout_check(lib, limit):
+    assert lib.bsfp8_check_wait_timeout(limit, None) == 2
