@@ -46,6 +46,7 @@
 // prefetch the one-ahead load often missed to DRAM and stalled both warps of that TMEM
 // lane quarter at the sa * sb multiply for 300-1300 cycles, holding up the release of the
 // TMEM stage (B scales of consecutive K blocks share a line and hit L1).
+#include <atomic>
 #include <cuda_bf16.h>
 #include "common.cuh"
 #include "ptx.cuh"
@@ -430,15 +431,15 @@ bsfp8_blockwise_kernel(const __grid_constant__ CUtensorMap tmA,
 template <class C>
 cudaError_t launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& args,
                    int num_sms, cudaStream_t stream) {
-  static bool attr_set[64] = {};
+  static std::atomic<bool> attr_set[64];  // per device; several host threads may launch
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 64 && !attr_set[dev]) {
+  if (dev >= 64 || !attr_set[dev].load(std::memory_order_acquire)) {
     cudaError_t e = cudaFuncSetAttribute(bsfp8_blockwise_kernel<C>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem_bytes<C>());
     if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
+    if (dev < 64) attr_set[dev].store(true, std::memory_order_release);
   }
   // Upper bound of the tile count known on the host (offsets live on the device).
   const int64_t max_row_tiles = (args.M_total + C::BM - 1) / C::BM + args.E;

@@ -29,6 +29,7 @@
 //   warps 4-7   epilogue: warp w holds weight rows 32*(w%4).. of the tile, reads the tn
 //               token columns of the accumulator, rounds to bf16 and stores C[m, n] for the
 //               tile's token rows that belong to the expert.
+#include <atomic>
 #include <cuda_bf16.h>
 #include "common.cuh"
 #include "ptx.cuh"
@@ -436,15 +437,15 @@ bsmxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 template <class C>
 cudaError_t launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& args,
                    int num_sms, cudaStream_t stream) {
-  static bool attr_set[64] = {};
+  static std::atomic<bool> attr_set[64];  // per device; several host threads may launch
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 64 && !attr_set[dev]) {
+  if (dev >= 64 || !attr_set[dev].load(std::memory_order_acquire)) {
     cudaError_t e = cudaFuncSetAttribute(bsmxfp8_kernel<C>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem_bytes<C>());
     if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
+    if (dev < 64) attr_set[dev].store(true, std::memory_order_release);
   }
   const int64_t max_row_tiles = (args.M_total + C::TN - 1) / C::TN + args.E;
   const int64_t max_tiles = max_row_tiles * (args.N / WROWS);

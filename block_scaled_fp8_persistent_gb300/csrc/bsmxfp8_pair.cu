@@ -25,6 +25,7 @@
 // blocks, 4 x tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale per 128-K stage, commits
 // multicast to both CTAs); warp 2 scale loader; warps 4-11 epilogue (TMEM lane quarter
 // w%4, column half (w-4)/4, 32-column subtiles).
+#include <atomic>
 #include <cuda_bf16.h>
 #include "common.cuh"
 #include "ptx.cuh"
@@ -452,15 +453,15 @@ bsmxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
 
 cudaError_t launch_bsmxfp8_pair(const CUtensorMap& tmA, const CUtensorMap& tmB,
                                 const GemmArgs& args, int num_sms, cudaStream_t stream) {
-  static bool attr_set[64] = {};
+  static std::atomic<bool> attr_set[64];  // per device; several host threads may launch
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 64 && !attr_set[dev]) {
+  if (dev >= 64 || !attr_set[dev].load(std::memory_order_acquire)) {
     cudaError_t e = cudaFuncSetAttribute(mxp::bsmxfp8_pair_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)mxp::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
+    if (dev < 64) attr_set[dev].store(true, std::memory_order_release);
   }
   const int64_t max_row_tiles = (args.M_total + mxp::BM - 1) / mxp::BM + args.E;
   const int64_t max_tiles = max_row_tiles * ((args.N + mxp::BN - 1) / mxp::BN);
