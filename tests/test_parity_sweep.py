@@ -1,0 +1,58 @@
+"""Seeded randomized sweep against the oracle: expert sizes around every tile height the
+kernels use (96, 128, 192, 256 rows; 32 / 64 / 128 token rows in MX swap-AB tiles), random
+N and K, every tile form; both modes."""
+import numpy as np
+import pytest
+
+import gen
+import oracle
+from helpers import parity_report
+
+pytestmark = pytest.mark.gpu
+
+SIZES = [0, 1, 7, 31, 32, 33, 63, 64, 65, 95, 96, 97, 127, 128, 129, 191, 192, 193, 255, 256, 257]
+BLOCKWISE_TILES = ["cta1_96", "pair_192", "cta1_256", "pair_256", "pair_160", "pair_128",
+                   "cta1_128"]
+MX_FORMS = [("swap", "32"), ("swap", "64"), ("swap", "128"), ("pair", None)]
+
+
+def _case(rng):
+    E = int(rng.integers(1, 6))
+    counts = [int(c) for c in rng.choice(SIZES, size=E)]
+    if sum(counts) == 0:
+        counts[0] = 1
+    N = int(rng.choice([128, 256, 384, 640]))
+    K = int(rng.choice([128, 256, 384, 640, 1024]))
+    return counts, N, K
+
+
+def _check(p):
+    from gpu_util import DeviceProblem
+    import block_scaled_fp8_persistent_gb300 as bsfp8
+    d = DeviceProblem(p, c_rows_extra=2)
+    d.run()
+    got = d.c_bits()
+    assert bsfp8.bsfp8_get_device_error() == 0
+    ref, T = oracle.problem_reference(p)
+    bad, ratio, _ = parity_report(got, ref, T)
+    assert bad == 0, f"{bad} elements outside tolerance (max err/tol {ratio:.3g})"
+    assert np.all(d.guard_bits() == d.sentinel)
+
+
+@pytest.mark.parametrize("seed", range(2 * len(BLOCKWISE_TILES)))
+def test_blockwise_sweep(seed, monkeypatch):
+    rng = np.random.default_rng(1000 + seed)
+    counts, N, K = _case(rng)
+    monkeypatch.setenv("BSFP8_BLOCKWISE_TILE", BLOCKWISE_TILES[seed % len(BLOCKWISE_TILES)])
+    _check(gen.blockwise_problem(counts, N, K, seed=1000 + seed, exact=bool(seed % 2)))
+
+
+@pytest.mark.parametrize("seed", range(2 * len(MX_FORMS)))
+def test_mx_sweep(seed, monkeypatch):
+    rng = np.random.default_rng(2000 + seed)
+    counts, N, K = _case(rng)
+    kernel, tn = MX_FORMS[seed % len(MX_FORMS)]
+    monkeypatch.setenv("BSFP8_MX_KERNEL", kernel)
+    if tn:
+        monkeypatch.setenv("BSFP8_MX_TN", tn)
+    _check(gen.mx_problem(counts, N, K, seed=2000 + seed, exact=bool(seed % 2)))
