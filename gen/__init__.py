@@ -70,6 +70,9 @@ def _L():
         lib.bsfp8_gen_exact_codes.argtypes = [u64, u64, i64, p, i32]
         lib.bsfp8_gen_exact_scales_f32.argtypes = [u64, u64, i64, p]
         lib.bsfp8_gen_exact_scales_ue8m0.argtypes = [u64, u64, i64, p]
+        lib.bsfp8_gen_fp4_bytes.argtypes = [u64, u64, i64, p, i32]
+        lib.bsfp8_gen_pow2_scales.argtypes = [u64, u64, i64, i32, p]
+        lib.bsfp8_gen_e4m3_scale_codes.argtypes = [u64, u64, i64, i32, i32, p]
         lib.bsfp8_gen_route_uniform.argtypes = [u64, i64, i64, p]
         lib.bsfp8_gen_route_zipf.argtypes = [u64, i64, i64, ctypes.c_double, i64, p]
         lib.bsfp8_gen_route_counts.argtypes = [u64, i64, i64, i64, p]
@@ -154,6 +157,9 @@ class Problem:
     blockwise: A u8 [M_total, K], B u8 [E, N, K], a_scales f32 [K/128, M_total],
                b_scales f32 [E, N/128, K/128]
     mx:        A, B as above, a_scales u8 [M_total, K/32], b_scales u8 [E, N, K/32]
+               with operand formats a_fmt / b_fmt other than "mxfp8": an "mxfp4" or
+               "nvfp4" operand holds e2m1 codes two per byte along K ([rows, K/2]); nvfp4
+               scales are e4m3 codes per 16 K ([rows, K/16])
     offsets:   i32 [E+1], offsets[0] = 0, offsets[E] = M_total
     expert_ids: None (group e uses expert e; B has E experts), or i32 [E]: group e uses
                expert expert_ids[e] of the B.shape[0] experts in B
@@ -169,6 +175,8 @@ class Problem:
     name: str = ""
     meta: dict = field(default_factory=dict)
     expert_ids: np.ndarray | None = None
+    a_fmt: str = "mxfp8"
+    b_fmt: str = "mxfp8"
 
     @property
     def num_experts(self) -> int:
@@ -196,7 +204,7 @@ class Problem:
             active = int((self.counts > 0).sum())
         else:
             active = int(np.unique(self.expert_ids[self.counts > 0]).size)
-        b = self.A.nbytes + active * self.N * self.K + self.a_scales.nbytes
+        b = self.A.nbytes + active * (self.B.nbytes // self.num_experts) + self.a_scales.nbytes
         per_expert_sb = self.b_scales.nbytes // self.num_experts
         b += active * per_expert_sb + self.M_total * self.N * 2
         return int(b)
@@ -256,6 +264,64 @@ def mx_problem(counts, N: int, K: int, seed: int, exact: bool = False, nthreads:
         L.bsfp8_gen_mx_rows(seed, STREAM_B, 0, E * N, K, None, _ptr(B), _ptr(sb), nthreads)
     return Problem("mx", A, B, sa, sb, off, N, K, name=name,
                    meta={"seed": seed, "exact": exact})
+
+
+STREAM_A_FP4, STREAM_B_FP4, STREAM_SA_FMT, STREAM_SB_FMT = 10, 11, 12, 13
+FP4_FORMATS = ("mxfp8", "mxfp4", "nvfp4")
+
+
+def _fmt_operand(fmt: str, rows: int, K: int, seed: int, s_elem: int, s_scale: int,
+                 scales: str, exact_stream: int, nthreads: int):
+    """One operand [rows, K] in format fmt, drawn as random_quantized_tensor draws it:
+    fp4-grid values (random e2m1 codes; for mxfp8 the same grid stored as e4m3) and
+    power-of-two scales in [1/128, 2] (scales="pow2"), or for nvfp4 general positive e4m3
+    scale codes 0x20..0x47 (0.125 .. 3.75, scales="e4m3")."""
+    L = _L()
+    vec = 16 if fmt == "nvfp4" else 32
+    if fmt == "mxfp8":
+        Q = np.empty((rows, K), np.uint8)
+        L.bsfp8_gen_exact_codes(seed, exact_stream, Q.size, _ptr(Q), nthreads)
+    else:
+        Q = np.empty((rows, K // 2), np.uint8)
+        L.bsfp8_gen_fp4_bytes(seed, s_elem, Q.size, _ptr(Q), nthreads)
+    S = np.empty((rows, K // vec), np.uint8)
+    if fmt == "nvfp4" and scales == "e4m3":
+        L.bsfp8_gen_e4m3_scale_codes(seed, s_scale, S.size, 0x20, 0x47, _ptr(S))
+    else:
+        L.bsfp8_gen_pow2_scales(seed, s_scale, S.size, 1 if fmt == "nvfp4" else 0, _ptr(S))
+    return Q, S
+
+
+def fmt_problem(counts, N: int, K: int, seed: int, a_fmt: str, b_fmt: str,
+                a_recipe: str = "grid", scales: str = "pow2", expert_ids=None,
+                num_experts: int | None = None, nthreads: int = 0, name: str = "") -> Problem:
+    """Block-scaled MX problem with a format per operand (the format pairs of the Gluon
+    example: mxfp8 x mxfp8, mxfp8 x mxfp4, mxfp4 x mxfp4, nvfp4 x nvfp4).  Operands follow
+    random_quantized_tensor (see _fmt_operand); a_recipe="quantized" instead draws an mxfp8 A
+    as the decode workload does (N(0,1) rows, 2^ceil(log2(amax/448)) UE8M0 scales per 32).
+    With expert_ids, group g uses expert expert_ids[g] of num_experts."""
+    assert a_fmt in FP4_FORMATS and b_fmt in FP4_FORMATS
+    counts = np.asarray(counts, np.int32)
+    off = counts_to_offsets(counts)
+    M = int(off[-1])
+    E = len(counts) if expert_ids is None else int(num_experts)
+    assert N % 128 == 0 and K % 128 == 0
+    if a_fmt == "mxfp8" and a_recipe == "quantized":
+        A = np.empty((M, K), np.uint8)
+        sa = np.empty((M, K // 32), np.uint8)
+        if M:
+            _L().bsfp8_gen_mx_rows(seed, STREAM_A, 0, M, K, None, _ptr(A), _ptr(sa), nthreads)
+    else:
+        A, sa = _fmt_operand(a_fmt, M, K, seed, STREAM_A_FP4, STREAM_SA_FMT, scales,
+                             STREAM_A_EXACT, nthreads)
+    B, sb = _fmt_operand(b_fmt, E * N, K, seed, STREAM_B_FP4, STREAM_SB_FMT, scales,
+                         STREAM_B_EXACT, nthreads)
+    B = B.reshape(E, N, -1)
+    sb = sb.reshape(E, N, -1)
+    ids = None if expert_ids is None else np.asarray(expert_ids, np.int32)
+    return Problem("mx", A, B, sa, sb, off, N, K, name=name,
+                   meta={"seed": seed, "a_recipe": a_recipe, "scales": scales},
+                   expert_ids=ids, a_fmt=a_fmt, b_fmt=b_fmt)
 
 
 def routed_problem(counts, expert_ids, num_experts: int, N: int, K: int, seed: int,

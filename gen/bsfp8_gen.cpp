@@ -304,6 +304,35 @@ void bsfp8_gen_exact_scales_ue8m0(uint64_t seed, uint64_t stream, int64_t count,
   for (int64_t i = 0; i < count; ++i) s[i] = (uint8_t)(126 + hash3(seed, stream, (uint64_t)i) % 3);
 }
 
+// fp4 operand as random_quantized_tensor draws it: every e2m1 code (4 bits, sign
+// included) uniform, two per byte along K (element 2i in the low nibble of byte i).
+void bsfp8_gen_fp4_bytes(uint64_t seed, uint64_t stream, int64_t nbytes, uint8_t* out,
+                         int nthreads) {
+  const int64_t per = 4096;
+  parallel_for((nbytes + per - 1) / per, nthreads, [&](int64_t c) {
+    for (int64_t i = c * per; i < std::min(nbytes, (c + 1) * per); ++i)
+      out[i] = (uint8_t)(hash3(seed, stream, (uint64_t)i) & 0xFF);
+  });
+}
+
+// Power-of-two scales 2^j, j uniform in [-7, 1] (the [1/128, 2] range of
+// random_quantized_tensor), as UE8M0 codes (e4m3 == 0) or as e4m3 codes (e4m3 != 0; exact:
+// 2^-7 is the e4m3 subnormal 4/8 * 2^-6).
+void bsfp8_gen_pow2_scales(uint64_t seed, uint64_t stream, int64_t count, int e4m3,
+                           uint8_t* out) {
+  for (int64_t i = 0; i < count; ++i) {
+    const int j = -7 + (int)(hash3(seed, stream, (uint64_t)i) % 9);
+    out[i] = e4m3 ? e4m3_encode(std::ldexp(1.0f, j)) : (uint8_t)(127 + j);
+  }
+}
+
+// General positive e4m3 scale codes, uniform over the codes lo .. hi (finite, > 0).
+void bsfp8_gen_e4m3_scale_codes(uint64_t seed, uint64_t stream, int64_t count, int lo, int hi,
+                                uint8_t* out) {
+  for (int64_t i = 0; i < count; ++i)
+    out[i] = (uint8_t)(lo + (int)(hash3(seed, stream, (uint64_t)i) % (uint64_t)(hi - lo + 1)));
+}
+
 // Routing: counts[E] of rows per expert.
 // Uniform multinomial: each of M_total tokens picks expert floor(u * E).
 void bsfp8_gen_route_uniform(uint64_t seed, int64_t M_total, int64_t E, int32_t* counts) {

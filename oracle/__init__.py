@@ -68,6 +68,14 @@ def _L():
             f.restype = i32
         lib.bsfp8_oracle_ids.argtypes = [i32, p, p, p, p, p, p, i64, i64, i64, i64, i64, p, p, i32]
         lib.bsfp8_oracle_ids.restype = i32
+        lib.bsfp8_oracle_fmt.argtypes = [i32, i32, p, p, p, p, p, p, i64, i64, i64, i64, i64,
+                                         p, p, i32]
+        lib.bsfp8_oracle_fmt.restype = i32
+        lib.bsfp8_oracle_fmt_points.argtypes = [i32, i32, p, p, p, p, p, p, i64, i64, i64, i64,
+                                                i64, p, p, i64, p, p, i32]
+        lib.bsfp8_oracle_fmt_points.restype = i32
+        lib.bsfp8_oracle_e2m1_decode.argtypes = [ctypes.c_uint8]
+        lib.bsfp8_oracle_e2m1_decode.restype = ctypes.c_double
         lib.bsfp8_oracle_threads.argtypes = [i32]
         lib.bsfp8_oracle_threads.restype = i32
         _lib = lib
@@ -89,6 +97,10 @@ def e4m3_decode(code: int) -> float:
 
 def ue8m0_decode(code: int) -> float:
     return float(_L().bsfp8_oracle_ue8m0_decode(code))
+
+
+def e2m1_decode(nibble: int) -> float:
+    return float(_L().bsfp8_oracle_e2m1_decode(nibble))
 
 
 def bf16_rne(x: float) -> int:
@@ -171,9 +183,73 @@ def grouped_gemm_points(mode: str, A, B, a_scales, b_scales, offsets, N: int, K:
     return C, T
 
 
+FORMATS = {"mxfp8": 0, "mxfp4": 1, "nvfp4": 2}
+
+
+def _fmt_args(a_fmt, b_fmt, A, B, a_scales, b_scales, offsets, expert_ids):
+    A, B = _c(A, np.uint8), _c(B, np.uint8)
+    a_scales, b_scales = _c(a_scales, np.uint8), _c(b_scales, np.uint8)
+    offsets = _c(offsets, np.int32)
+    ids = None if expert_ids is None else _c(expert_ids, np.int32)
+    G = offsets.shape[0] - 1
+    assert ids is None or ids.shape == (G,)
+    return FORMATS[a_fmt], FORMATS[b_fmt], A, B, a_scales, b_scales, offsets, ids, G
+
+
+def grouped_gemm_fmt(a_fmt: str, b_fmt: str, A, B, a_scales, b_scales, offsets, N: int, K: int,
+                     expert_ids=None, nthreads: int = 0, want_t: bool = True):
+    """Block-scaled grouped GEMM with a format per operand ("mxfp8", "mxfp4", "nvfp4").
+    fp4 operands are packed two elements per byte along K (A [M_total, K/2], B [E, N, K/2]);
+    scales are [rows, K/32] UE8M0 (mx formats) or [rows, K/16] e4m3 codes (nvfp4).  Group g
+    uses expert expert_ids[g] of B, or expert g when expert_ids is None.
+    Returns (C bits uint16 [M_total, N], T float64 or None)."""
+    fa, fb, A, B, a_scales, b_scales, offsets, ids, G = _fmt_args(
+        a_fmt, b_fmt, A, B, a_scales, b_scales, offsets, expert_ids)
+    M = int(offsets[-1])
+    C = np.empty((M, N), np.uint16)
+    T = np.empty((M, N), np.float64) if want_t else None
+    rc = _L().bsfp8_oracle_fmt(fa, fb, A.ctypes.data, B.ctypes.data, a_scales.ctypes.data,
+                               b_scales.ctypes.data, offsets.ctypes.data,
+                               ids.ctypes.data if ids is not None else None, M, N, K, G,
+                               B.shape[0], C.ctypes.data,
+                               T.ctypes.data if T is not None else None, nthreads)
+    if rc:
+        raise OracleError(f"oracle rejected the problem (code {rc})")
+    return C, T
+
+
+def grouped_gemm_fmt_points(a_fmt: str, b_fmt: str, A, B, a_scales, b_scales, offsets, N: int,
+                            K: int, rows, cols, expert_ids=None, nthreads: int = 0):
+    """Sampled elements of grouped_gemm_fmt.  Returns (C bits [n], T float64 [n])."""
+    fa, fb, A, B, a_scales, b_scales, offsets, ids, G = _fmt_args(
+        a_fmt, b_fmt, A, B, a_scales, b_scales, offsets, expert_ids)
+    rows = _c(rows, np.int64)
+    cols = _c(cols, np.int64)
+    assert rows.shape == cols.shape
+    M = int(offsets[-1])
+    C = np.empty(rows.shape, np.uint16)
+    T = np.empty(rows.shape, np.float64)
+    rc = _L().bsfp8_oracle_fmt_points(fa, fb, A.ctypes.data, B.ctypes.data, a_scales.ctypes.data,
+                                      b_scales.ctypes.data, offsets.ctypes.data,
+                                      ids.ctypes.data if ids is not None else None, M, N, K, G,
+                                      B.shape[0], rows.ctypes.data, cols.ctypes.data, rows.size,
+                                      C.ctypes.data, T.ctypes.data, nthreads)
+    if rc:
+        raise OracleError(f"oracle rejected the problem (code {rc})")
+    return C, T
+
+
+def _formats(p):
+    return getattr(p, "a_fmt", "mxfp8"), getattr(p, "b_fmt", "mxfp8")
+
+
 def problem_reference(p, nthreads: int = 0, want_t: bool = True):
     """Full oracle output for a gen.Problem-like object (mode, A, B, scales, offsets, N, K,
-    and expert_ids when it has them)."""
+    and expert_ids / operand formats when it has them)."""
+    if p.mode == "mx" and _formats(p) != ("mxfp8", "mxfp8"):
+        return grouped_gemm_fmt(*_formats(p), p.A, p.B, p.a_scales, p.b_scales, p.offsets, p.N,
+                                p.K, expert_ids=getattr(p, "expert_ids", None),
+                                nthreads=nthreads, want_t=want_t)
     if getattr(p, "expert_ids", None) is not None:
         return grouped_gemm_ids(p.mode, p.A, p.B, p.a_scales, p.b_scales, p.offsets,
                                 p.expert_ids, p.N, p.K, nthreads=nthreads, want_t=want_t)
@@ -182,6 +258,12 @@ def problem_reference(p, nthreads: int = 0, want_t: bool = True):
 
 
 def problem_points(p, rows, cols, nthreads: int = 0):
+    if p.mode == "mx" and (_formats(p) != ("mxfp8", "mxfp8") or
+                           getattr(p, "expert_ids", None) is not None):
+        return grouped_gemm_fmt_points(*_formats(p), p.A, p.B, p.a_scales, p.b_scales,
+                                       p.offsets, p.N, p.K, rows, cols,
+                                       expert_ids=getattr(p, "expert_ids", None),
+                                       nthreads=nthreads)
     return grouped_gemm_points(p.mode, p.A, p.B, p.a_scales, p.b_scales, p.offsets, p.N, p.K,
                                rows, cols, nthreads=nthreads)
 

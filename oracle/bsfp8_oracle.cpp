@@ -18,6 +18,13 @@
 //   MX mode (K blocks of 32):
 //     sa(m,kb)   = 2^(a_scales[m, kb] - 127)   UE8M0, layout [M_total, K/32]
 //     sb(e,n,kb) = 2^(b_scales[e, n, kb] - 127) UE8M0, layout [E, N, K/32]
+//   Block-scaled formats per operand (bsfp8_oracle_fmt), as named in the Gluon example:
+//     mxfp8  elements e4m3, one byte each          scale UE8M0 per 32 K
+//     mxfp4  elements e2m1, two per byte along K   scale UE8M0 per 32 K
+//     nvfp4  elements e2m1, two per byte along K   scale e4m3 per 16 K
+//   so the term of k is dec(A[m,k]) * dec(B[e,n,k]) * sa(m, k/vec_a) * sb(e, n, k/vec_b);
+//   the K blocks of the sum are min(vec_a, vec_b) wide.  A packed row holds K/2 bytes;
+//   element k of a row is the low nibble of byte k/2 for even k, the high nibble for odd k.
 //
 // Sources:
 //  * promote_accumulators (MAX kernels, linalg/grouped_matmul_sm100_blockwise_fp8),
@@ -27,14 +34,17 @@
 //    a group to its expert's rows of B; problem_shape is (M, N, K).
 //  * Overlapping Accumulator Block-Scaled Matrix Multiplication (Triton Gluon example),
 //    random_quantized_tensor / make_problem: the reference result of a block-scaled MMA is
-//    the matmul of the dequantized operands, value * scale repeated over VEC_SIZE=32 K
-//    elements for uint8 (UE8M0) scales; async_mma_scaled_impl: operands are "e4m3".
+//    the matmul of the dequantized operands, value * scale repeated over VEC_SIZE K
+//    elements (32 for uint8 UE8M0 scales, 16 for nvfp4's float8_e4m3fn scales);
+//    async_mma_scaled_impl: operands are "e4m3", or "e2m1" when stored as uint8 (two fp4
+//    elements packed per byte along K); Fixed Configuration: the format pairs (mxfp8,
+//    mxfp8), (mxfp8, mxfp4), (mxfp4, mxfp4), (nvfp4, nvfp4).
 //
 // Precision (the plain reading; every step is exact except where stated):
-//  * dec() is the exact e4m3 ("fn") value in double.
+//  * dec() is the exact e4m3 ("fn") or e2m1 value in double.
 //  * Each product dec(a)*dec(b) is exact in double (4-bit significands), and every
 //    partial sum of one 128-wide block is exact too (the products span 2^-18 .. 2^18,
-//    so 128 of them need < 53 bits).
+//    so 128 of them need < 53 bits).  nvfp4's e4m3 scales multiply exactly as well.
 //  * sa*sb is exact in double (two fp32 significands).  The product with the block sum
 //    and the sum over blocks round in double (relative error ~1e-16).
 //  * The double result is rounded once, directly, to bf16 with round-to-nearest-even.
@@ -70,6 +80,17 @@ double e4m3_value(uint8_t code) {
   return sign ? -mag : mag;
 }
 
+// e2m1 (the 4-bit element of mxfp4 / nvfp4): sign (bit 3), 2 exponent bits (bias 1),
+// 1 mantissa bit; exponent 0 is subnormal (M/2) * 2^0; no NaN, no infinity.  The
+// magnitudes are 0, 0.5, 1, 1.5, 2, 3, 4, 6.
+double e2m1_value(uint8_t nibble) {
+  const int sign = (nibble >> 3) & 1;
+  const int E = (nibble >> 1) & 0x3;
+  const int M = nibble & 0x1;
+  const double mag = (E == 0) ? (double)M / 2.0 : std::ldexp(1.0 + (double)M / 2.0, E - 1);
+  return sign ? -mag : mag;
+}
+
 // UE8M0: 2^(code - 127); 0xFF is NaN.
 double ue8m0_value(uint8_t code) {
   if (code == 0xFF) return std::nan("");
@@ -79,11 +100,13 @@ double ue8m0_value(uint8_t code) {
 struct Lut {
   double e4m3[256];
   double ue8m0[256];
+  double e2m1[16];
   Lut() {
     for (int c = 0; c < 256; ++c) {
       e4m3[c] = e4m3_value((uint8_t)c);
       ue8m0[c] = ue8m0_value((uint8_t)c);
     }
+    for (int c = 0; c < 16; ++c) e2m1[c] = e2m1_value((uint8_t)c);
   }
 };
 const Lut& lut() {
@@ -116,6 +139,9 @@ uint16_t bf16_rne(double x) {
 
 enum Mode { BLOCKWISE = 0, MX = 1 };
 
+// Block-scaled operand formats (MX mode).
+enum Format { MXFP8 = 0, MXFP4 = 1, NVFP4 = 2 };
+
 struct Problem {
   Mode mode;
   const uint8_t* A;          // [M_total, K]
@@ -128,12 +154,30 @@ struct Problem {
   int64_t E;                 // groups (row segments)
   const int32_t* expert_ids; // [E] group -> expert of B, or nullptr (group g uses expert g)
   int64_t num_experts;       // experts in B and b_scales
+  Format a_fmt = MXFP8;      // MX mode only
+  Format b_fmt = MXFP8;
 };
+
+bool packed(Format f) { return f != MXFP8; }
+int64_t vec_of(Format f) { return f == NVFP4 ? 16 : 32; }
+int64_t row_bytes(Format f, int64_t K) { return packed(f) ? K / 2 : K; }
+
+// Element k of an operand row in format f.
+double elem(const Lut& L, Format f, const uint8_t* row, int64_t k) {
+  if (!packed(f)) return L.e4m3[row[k]];
+  const uint8_t byte = row[k / 2];
+  return L.e2m1[(k & 1) ? (byte >> 4) : (byte & 0xF)];
+}
+
+// Scale code c of a block in format f.
+double scale_of(const Lut& L, Format f, uint8_t c) { return f == NVFP4 ? L.e4m3[c] : L.ue8m0[c]; }
 
 int check(const Problem& p) {
   if (p.M_total < 0 || p.N <= 0 || p.K <= 0 || p.E <= 0) return 2;
   const int64_t blk = (p.mode == BLOCKWISE) ? 128 : 32;
   if (p.K % blk != 0) return 2;
+  if (p.mode == MX && (p.a_fmt < MXFP8 || p.a_fmt > NVFP4 || p.b_fmt < MXFP8 || p.b_fmt > NVFP4))
+    return 2;
   if (p.mode == BLOCKWISE && p.N % 128 != 0) return 2;
   if (p.offsets[0] != 0 || p.offsets[p.E] != p.M_total) return 6;
   for (int64_t e = 0; e < p.E; ++e)
@@ -158,12 +202,42 @@ int64_t group_of_row(const Problem& p, int64_t m) {
   return lo;
 }
 
+// One output element of an MX problem with per-operand formats: K blocks of
+// min(vec_a, vec_b) elements, each block's exact sum times its two scales.
+void element_fmt(const Problem& p, const Lut& L, int64_t m, int64_t n, int64_t e,
+                 uint16_t* c_out, double* t_out) {
+  const int64_t va = vec_of(p.a_fmt), vb = vec_of(p.b_fmt);
+  const int64_t blk = std::min(va, vb);
+  const uint8_t* arow = p.A + m * row_bytes(p.a_fmt, p.K);
+  const uint8_t* brow = p.B + (e * p.N + n) * row_bytes(p.b_fmt, p.K);
+  const uint8_t* asc = (const uint8_t*)p.a_scales + m * (p.K / va);
+  const uint8_t* bsc = (const uint8_t*)p.b_scales + (e * p.N + n) * (p.K / vb);
+  double acc = 0.0, tsum = 0.0;
+  for (int64_t k0 = 0; k0 < p.K; k0 += blk) {
+    double inner = 0.0, inner_abs = 0.0;
+    for (int64_t k = k0; k < k0 + blk; ++k) {
+      const double prod = elem(L, p.a_fmt, arow, k) * elem(L, p.b_fmt, brow, k);
+      inner += prod;
+      inner_abs += std::fabs(prod);
+    }
+    const double s = scale_of(L, p.a_fmt, asc[k0 / va]) * scale_of(L, p.b_fmt, bsc[k0 / vb]);
+    acc += s * inner;
+    tsum += std::fabs(s) * inner_abs;
+  }
+  *c_out = bf16_rne(acc);
+  if (t_out) *t_out = tsum;
+}
+
 // One output element, straight from the definition above.
 void element(const Problem& p, int64_t m, int64_t n, uint16_t* c_out, double* t_out) {
   const Lut& L = lut();
   // expert_ids: "mapping from group index to expert row offset in B" (promote_accumulators)
   const int64_t g = group_of_row(p, m);
   const int64_t e = p.expert_ids ? (int64_t)p.expert_ids[g] : g;
+  if (p.mode == MX && (p.a_fmt != MXFP8 || p.b_fmt != MXFP8)) {
+    element_fmt(p, L, m, n, e, c_out, t_out);
+    return;
+  }
   const int64_t blk = (p.mode == BLOCKWISE) ? 128 : 32;
   const int64_t nkb = p.K / blk;
   const uint8_t* arow = p.A + m * p.K;
@@ -298,6 +372,32 @@ int bsfp8_oracle_ids(int mode, const uint8_t* A, const uint8_t* B, const void* a
             expert_ids, num_experts};
   return run_full(p, C, T, nthreads);
 }
+
+// MX grouped GEMM with a format per operand (0 mxfp8, 1 mxfp4, 2 nvfp4): A [M_total,
+// K or K/2 bytes], a_scales [M_total, K/vec_a]; B [num_experts, N, K or K/2 bytes],
+// b_scales [num_experts, N, K/vec_b]; G groups of rows (offsets [G+1]); group g uses expert
+// expert_ids[g], or expert g when expert_ids is null (then num_experts must equal G).
+int bsfp8_oracle_fmt(int a_fmt, int b_fmt, const uint8_t* A, const uint8_t* B,
+                     const uint8_t* a_scales, const uint8_t* b_scales, const int32_t* offsets,
+                     const int32_t* expert_ids, int64_t M_total, int64_t N, int64_t K, int64_t G,
+                     int64_t num_experts, uint16_t* C, double* T, int nthreads) {
+  Problem p{MX, A, B, a_scales, b_scales, offsets, M_total, N, K, G, expert_ids, num_experts,
+            (Format)a_fmt, (Format)b_fmt};
+  return run_full(p, C, T, nthreads);
+}
+
+int bsfp8_oracle_fmt_points(int a_fmt, int b_fmt, const uint8_t* A, const uint8_t* B,
+                            const uint8_t* a_scales, const uint8_t* b_scales,
+                            const int32_t* offsets, const int32_t* expert_ids, int64_t M_total,
+                            int64_t N, int64_t K, int64_t G, int64_t num_experts,
+                            const int64_t* rows, const int64_t* cols, int64_t npts, uint16_t* C,
+                            double* T, int nthreads) {
+  Problem p{MX, A, B, a_scales, b_scales, offsets, M_total, N, K, G, expert_ids, num_experts,
+            (Format)a_fmt, (Format)b_fmt};
+  return run_points(p, rows, cols, npts, C, T, nthreads);
+}
+
+double bsfp8_oracle_e2m1_decode(uint8_t nibble) { return lut().e2m1[nibble & 0xF]; }
 
 int bsfp8_oracle_threads(int nthreads) { return resolve_threads(nthreads); }
 

@@ -24,8 +24,42 @@ def decode_ue8m0_torch(codes: np.ndarray) -> torch.Tensor:
     return torch.from_numpy(np.ascontiguousarray(codes)).view(torch.float8_e8m0fnu).to(torch.float64)
 
 
+# The FP4 (E2M1) values of the OCP Microscaling formats, codes 0..7; codes 8..15 are the
+# same values negated.  A literal table, not the oracle's bit-field formula.
+E2M1_TABLE = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0,
+                       -0.0, -0.5, -1.0, -1.5, -2.0, -3.0, -4.0, -6.0], np.float64)
+
+
+def unpack_fp4(Q: np.ndarray) -> np.ndarray:
+    """e2m1 codes [..., 2*bytes] from packed bytes [..., bytes]: element 2i is the low
+    nibble of byte i, element 2i+1 the high nibble."""
+    Q = np.asarray(Q, np.uint8)
+    out = np.empty(Q.shape[:-1] + (2 * Q.shape[-1],), np.uint8)
+    out[..., 0::2] = Q & 0xF
+    out[..., 1::2] = Q >> 4
+    return out
+
+
+def decode_operand(Q: np.ndarray, fmt: str) -> torch.Tensor:
+    if fmt == "mxfp8":
+        return decode_e4m3_torch(Q)
+    return torch.from_numpy(E2M1_TABLE[unpack_fp4(Q)])
+
+
+def decode_scales(S: np.ndarray, fmt: str) -> torch.Tensor:
+    """Scales expanded over their K blocks (32 for mxfp8 / mxfp4, 16 for nvfp4)."""
+    if fmt == "nvfp4":
+        return decode_e4m3_torch(S).repeat_interleave(16, dim=-1)
+    return decode_ue8m0_torch(S).repeat_interleave(32, dim=-1)
+
+
 def dequantize(p):
     """(A_deq [M,K], B_deq [E,N,K]) in float64 for a gen.Problem."""
+    a_fmt, b_fmt = getattr(p, "a_fmt", "mxfp8"), getattr(p, "b_fmt", "mxfp8")
+    if p.mode == "mx" and (a_fmt, b_fmt) != ("mxfp8", "mxfp8"):
+        A = decode_operand(p.A, a_fmt) * decode_scales(p.a_scales, a_fmt)
+        B = decode_operand(p.B, b_fmt) * decode_scales(p.b_scales, b_fmt)
+        return A, B
     A = decode_e4m3_torch(p.A)
     B = decode_e4m3_torch(p.B)
     if p.mode == "blockwise":

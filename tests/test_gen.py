@@ -131,3 +131,31 @@ def test_config0_problem_shapes():
     assert p.A.shape == (256, 512) and p.B.shape == (1, 256, 512)
     assert p.a_scales.shape == (4, 256) and p.b_scales.shape == (1, 2, 4)
     assert p.flops() == 2 * 256 * 256 * 512
+
+
+@pytest.mark.parametrize("a_fmt,b_fmt", [("mxfp8", "mxfp4"), ("mxfp4", "mxfp4"),
+                                         ("nvfp4", "nvfp4")])
+def test_fmt_problem_layouts_and_ranges(a_fmt, b_fmt):
+    p = gen.fmt_problem([3, 0, 9], 256, 384, seed=4, a_fmt=a_fmt, b_fmt=b_fmt)
+    q = gen.fmt_problem([3, 0, 9], 256, 384, seed=4, a_fmt=a_fmt, b_fmt=b_fmt)
+    assert np.array_equal(p.A, q.A) and np.array_equal(p.B, q.B)
+    a_cols = 384 if a_fmt == "mxfp8" else 192
+    assert p.A.shape == (12, a_cols) and p.B.shape == (3, 256, 192)
+    vec = 16 if b_fmt == "nvfp4" else 32
+    assert p.a_scales.shape == (12, 384 // vec) and p.b_scales.shape == (3, 256, 384 // vec)
+    if b_fmt == "nvfp4":
+        # powers of two 2^-7 .. 2 as e4m3 codes: 0x04 (subnormal 2^-7), then (j + 7) << 3
+        assert set(np.unique(p.b_scales)) <= {0x04} | {(j + 7) << 3 for j in range(-6, 2)}
+    else:
+        assert p.b_scales.min() >= 120 and p.b_scales.max() <= 128
+    # every nibble value occurs (uniform codes)
+    nib = np.concatenate([(p.B & 0xF).ravel(), (p.B >> 4).ravel()])
+    assert set(np.unique(nib)) == set(range(16))
+    assert p.bytes() == p.A.nbytes + p.a_scales.nbytes + 2 * (p.B.nbytes // 3) + \
+        2 * (p.b_scales.nbytes // 3) + 12 * 256 * 2
+
+
+def test_fmt_problem_general_nvfp4_scales():
+    p = gen.fmt_problem([5], 128, 256, seed=6, a_fmt="nvfp4", b_fmt="nvfp4", scales="e4m3")
+    assert p.a_scales.min() >= 0x20 and p.a_scales.max() <= 0x47
+    assert len(np.unique(p.a_scales)) > 20

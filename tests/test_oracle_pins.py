@@ -20,7 +20,12 @@ fails at least one of them:
     plain grouped result, ids outside [0, num_experts) are rejected;
   * the packed scale layout: every byte at the position the closed form of the page's
     reshape/permute gives (written out as loops), including padded shapes, and the inverse
-    view restores the input.
+    view restores the input;
+  * the fp4 formats (mxfp4, nvfp4; the format pairs of the Gluon example): all 16 e2m1
+    codes against the literal FP4 value table, a hand-worked two-element case fixing the
+    nibble order, dequantize-then-matmul bitwise for every format pair (general e4m3
+    nvfp4 scales included), an mxfp4 operand re-encoded as e4m3 giving the mxfp8 result
+    bit for bit, and the nvfp4 scale block being 16 wide (mxfp4: 32).
 """
 import math
 
@@ -30,8 +35,8 @@ import torch
 
 import gen
 import oracle
-from helpers import (bf16_bits_to_f64, bf16_exact_round, brute_force, decode_e4m3_torch,
-                     decode_ue8m0_torch, f32_bits, ulp_bf16)
+from helpers import (E2M1_TABLE, bf16_bits_to_f64, bf16_exact_round, brute_force,
+                     decode_e4m3_torch, decode_ue8m0_torch, f32_bits, ulp_bf16, unpack_fp4)
 
 
 # ---------------------------------------------------------------------------
@@ -324,3 +329,93 @@ def test_pack_mx_scales_inverse_view():
     P = oracle.pack_mx_scales(S)
     back = P.reshape(3, 2, 32, 4, 4).transpose(0, 3, 2, 1, 4).reshape(384, 8)
     assert np.array_equal(back, S)
+
+
+# ---------------------------------------------------------------------------
+# fp4 formats (mxfp4, nvfp4)
+# ---------------------------------------------------------------------------
+def test_e2m1_all_16_codes():
+    for c in range(16):
+        v = oracle.e2m1_decode(c)
+        assert v == E2M1_TABLE[c] and math.copysign(1.0, v) == math.copysign(1.0, E2M1_TABLE[c])
+
+
+def test_fp4_nibble_order_hand_case():
+    # A row 0: byte 0 = 0x21 -> element 0 = code 1 (0.5), element 1 = code 2 (1.0).
+    # B row 0: byte 0 = 0x02 -> (1.0, 0); row 1: byte 0 = 0x20 -> (0, 1.0).  Unit scales.
+    # So C[0,0] = 0.5 (bf16 0x3F00) and C[0,1] = 1.0 (0x3F80); every other element is 0.
+    K, N = 128, 128
+    A = np.zeros((1, K // 2), np.uint8)
+    A[0, 0] = 0x21
+    B = np.zeros((1, N, K // 2), np.uint8)
+    B[0, 0, 0] = 0x02
+    B[0, 1, 0] = 0x20
+    sa = np.full((1, K // 32), 127, np.uint8)
+    sb = np.full((1, N, K // 32), 127, np.uint8)
+    off = np.array([0, 1], np.int32)
+    C, _ = oracle.grouped_gemm_fmt("mxfp4", "mxfp4", A, B, sa, sb, off, N, K)
+    assert C[0, 0] == 0x3F00 and C[0, 1] == 0x3F80
+    assert not C[0, 2:].any()
+    # the same through an nvfp4 view: unit e4m3 scales (code 0x38) per 16
+    sa16 = np.full((1, K // 16), 0x38, np.uint8)
+    sb16 = np.full((1, N, K // 16), 0x38, np.uint8)
+    C2, _ = oracle.grouped_gemm_fmt("nvfp4", "nvfp4", A, B, sa16, sb16, off, N, K)
+    assert np.array_equal(C, C2)
+
+
+@pytest.mark.parametrize("a_fmt,b_fmt,scales", [("mxfp8", "mxfp4", "pow2"),
+                                                ("mxfp4", "mxfp4", "pow2"),
+                                                ("nvfp4", "nvfp4", "pow2"),
+                                                ("nvfp4", "nvfp4", "e4m3"),
+                                                ("mxfp8", "mxfp8", "pow2")])
+def test_fmt_exact_inputs_bitwise(a_fmt, b_fmt, scales):
+    # fp4-grid values with power-of-two or e4m3 scales: every product and sum is exact in
+    # float64, so the brute force rounds to the one correct bf16 value
+    p = gen.fmt_problem([5, 0, 21, 3], 256, 384, seed=31, a_fmt=a_fmt, b_fmt=b_fmt,
+                        scales=scales)
+    _oracle_vs_bruteforce(p, exact_bits=True)
+
+
+def test_fmt_expert_ids_exact_bitwise():
+    p = gen.fmt_problem([4, 9, 0, 2], 128, 256, seed=32, a_fmt="mxfp8", b_fmt="mxfp4",
+                        expert_ids=[2, 0, 1, 2], num_experts=3)
+    _oracle_vs_bruteforce(p, exact_bits=True)
+
+
+def test_mxfp4_equals_mxfp8_reencoded():
+    # every e2m1 value is an e4m3 value: re-encode the fp4 codes as e4m3 (the generator's
+    # encoder, pinned on its own) and the mxfp8 path must give the same bits
+    p = gen.fmt_problem([7, 30], 256, 512, seed=33, a_fmt="mxfp4", b_fmt="mxfp4")
+    enc = np.array([gen.e4m3_encode(float(v)) for v in E2M1_TABLE], np.uint8)
+    A8 = enc[unpack_fp4(p.A)]
+    B8 = enc[unpack_fp4(p.B)]
+    C4, T4 = oracle.problem_reference(p)
+    C8, T8 = oracle.grouped_gemm("mx", A8, B8, p.a_scales, p.b_scales, p.offsets, p.N, p.K)
+    assert np.array_equal(C4, C8)
+    assert np.array_equal(T4, T8)
+    C48, _ = oracle.grouped_gemm_fmt("mxfp8", "mxfp4", A8, p.B, p.a_scales, p.b_scales,
+                                     p.offsets, p.N, p.K)
+    assert np.array_equal(C4, C48)
+
+
+@pytest.mark.parametrize("fmt,vec", [("nvfp4", 16), ("mxfp4", 32)])
+def test_fp4_scale_block_width(fmt, vec):
+    # only elements k in [16, 32) are non-zero in B: scale block 1 of nvfp4 covers them, block
+    # 0 of mxfp4 does.  Doubling the scale of the block that covers them doubles C exactly;
+    # changing any other block of that row leaves C unchanged.
+    p = gen.fmt_problem([6], 128, 256, seed=34, a_fmt=fmt, b_fmt=fmt)
+    p.B[:] = 0
+    src = gen.fmt_problem([6], 128, 256, seed=35, a_fmt=fmt, b_fmt=fmt)
+    p.B[..., 8:16] = src.B[..., 8:16]          # bytes 8..15 hold elements 16..31
+    step = 8 if fmt == "nvfp4" else 1          # e4m3 code + 8 doubles a normal value
+    blk = 16 // vec                            # the block holding element 16
+    p.b_scales[:, :, blk] = 0x38 if fmt == "nvfp4" else 127   # 1.0 (normal)
+    C0, _ = oracle.problem_reference(p)
+    other = 3
+    p.b_scales[:, :, other] += step
+    C1, _ = oracle.problem_reference(p)
+    assert np.array_equal(C1, C0)
+    p.b_scales[:, :, blk] += step
+    C2, _ = oracle.problem_reference(p)
+    assert np.array_equal(bf16_bits_to_f64(C2), 2.0 * bf16_bits_to_f64(C0))
+    assert np.any(C0 != 0)
