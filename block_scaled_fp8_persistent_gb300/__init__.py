@@ -8,6 +8,7 @@ not a GB300 (compute capability 10.3) the calls raise.
     bsfp8.bsfp8_grouped_gemm(A, B, a_scales, b_scales, expert_offsets, C,
                              M_total, N, K, num_experts, stream=None)
     bsfp8.bsmxfp8_grouped_gemm(...)   # MXFP8: UE8M0 scales per 32 K
+    bsfp8.bsmx_grouped_gemm("mxfp8", "mxfp4", ...)   # a format per operand
 
 Tensors are torch CUDA tensors (or raw device addresses as ints) in the layouts of
 include/bsfp8.h; ``stream`` is a torch.cuda.Stream, a raw cudaStream_t int, or None for
@@ -25,14 +26,18 @@ BSFP8_OK = 0
 STATUS_NAMES = {
     0: "BSFP8_OK", 1: "BSFP8_ERR_NULL", 2: "BSFP8_ERR_SHAPE", 3: "BSFP8_ERR_ALIGN",
     4: "BSFP8_ERR_UNSUPPORTED_DEVICE", 5: "BSFP8_ERR_CUDA", 6: "BSFP8_ERR_DEVICE_OFFSETS",
-    7: "BSFP8_ERR_DEVICE_TIMEOUT", 8: "BSFP8_ERR_DEVICE_EXPERT_IDS",
+    7: "BSFP8_ERR_DEVICE_TIMEOUT", 8: "BSFP8_ERR_DEVICE_EXPERT_IDS", 9: "BSFP8_ERR_FORMAT",
 }
+
+# bsmx_format values of include/bsfp8.h
+FORMATS = {"mxfp8": 0, "mxfp4": 1, "nvfp4": 2}
 
 # Every symbol include/bsfp8.h declares (the CPU test checks the library exports them).
 EXPORTED = ("bsfp8_grouped_gemm", "bsmxfp8_grouped_gemm", "bsfp8_grouped_gemm_ids",
             "bsmxfp8_grouped_gemm_ids", "bsmxfp8_pack_b_scales", "bsmxfp8_grouped_gemm_prepacked",
             "bsmxfp8_tmem_plan", "bsfp8_blockwise_plan",
-            "bsfp8_get_device_error", "bsfp8_check_wait_timeout", "bsfp8_status_string")
+            "bsmx_grouped_gemm", "bsfp8_get_device_error", "bsfp8_check_wait_timeout",
+            "bsfp8_status_string")
 
 
 class BsFp8Error(RuntimeError):
@@ -61,6 +66,9 @@ def load_library() -> ctypes.CDLL:
         lib.bsfp8_grouped_gemm_ids.restype = i32
         lib.bsmxfp8_grouped_gemm_ids.argtypes = [p, p, p, p, p, p, p, i64, i32, i32, i32, i32, p]
         lib.bsmxfp8_grouped_gemm_ids.restype = i32
+        lib.bsmx_grouped_gemm.argtypes = [i32, i32, p, p, p, p, i32, p, p, p, i64, i32, i32,
+                                          i32, i32, p]
+        lib.bsmx_grouped_gemm.restype = i32
         lib.bsmxfp8_pack_b_scales.argtypes = [p, p, i32, i32, i32, p]
         lib.bsmxfp8_pack_b_scales.restype = i32
         lib.bsmxfp8_grouped_gemm_prepacked.argtypes = [p, p, p, p, p, p, i64, i32, i32, i32, p]
@@ -148,6 +156,20 @@ def bsmxfp8_grouped_gemm_ids(A, B, a_scales, b_scales, group_offsets, expert_ids
         int(num_experts), _stream(stream))
     if st != BSFP8_OK:
         raise BsFp8Error(st, "bsmxfp8_grouped_gemm_ids")
+
+
+def bsmx_grouped_gemm(a_format: str, b_format: str, A, B, a_scales, b_scales, group_offsets,
+                      C, M_total: int, N: int, K: int, num_groups: int, num_experts: int,
+                      expert_ids=None, b_scales_packed: bool = False, stream=None) -> None:
+    """Block-scaled grouped GEMM with a format per operand ("mxfp8", "mxfp4", "nvfp4");
+    see include/bsfp8.h.  expert_ids None: group g uses expert g.  Raises BsFp8Error."""
+    st = load_library().bsmx_grouped_gemm(
+        FORMATS[a_format], FORMATS[b_format], _addr(A), _addr(B), _addr(a_scales),
+        _addr(b_scales), 1 if b_scales_packed else 0, _addr(group_offsets), _addr(expert_ids),
+        _addr(C), int(M_total), int(N), int(K), int(num_groups), int(num_experts),
+        _stream(stream))
+    if st != BSFP8_OK:
+        raise BsFp8Error(st, "bsmx_grouped_gemm")
 
 
 def bsmxfp8_pack_b_scales(b_scales, b_scales_packed, num_experts: int, N: int, K: int,

@@ -14,9 +14,18 @@
 // per-expert token counts of decode (the swapAB mode of the TileScheduler in the MAX
 // grouped_matmul_sm100_blockwise_fp8 kernels).
 //
-// Roles (8 warps):
+// fp4 operands (the mxfp4 format of the same example: e2m1 elements packed two per byte
+// along K, UE8M0 scales per 32): every e2m1 value v is exactly an e4m3 value, and the e4m3
+// code (sign << 7) | (magnitude code << 2) is exactly v * 2^-6 (e2m1's subnormal 0.5 lands
+// on e4m3's subnormal 2^-7, zero on zero).  So the kernel loads the packed tiles with TMA,
+// a converter warpgroup re-encodes them into the 128-byte-swizzled e4m3 tile the MMA
+// reads, the MMA and its scales are those of mxfp8, and the epilogue multiplies by 2^6 per
+// fp4 operand (exact in fp32).  The result is the mxfp8 result of the same values.
+//
+// Roles (8 warps; 12 with fp4 operands):
 //   warp 0      TMA producer: per K stage (128 K) the weight tile [128 x 128] and the token
-//               tile [tn x 128] (128-byte swizzle) into a STAGES-deep ring.
+//               tile [tn x 128] (128-byte swizzle; fp4 operands packed [rows x 64 B],
+//               unswizzled) into a STAGES-deep ring.
 //   warp 1      TMEM owner + MMA thread: per stage tcgen05.cp of both scale blocks into
 //               TMEM, then 4 x tcgen05.mma kind::mxf8f6f4.block_scale (K = 32 each, the
 //               scale-factor id picks the byte of the 4-byte scale word), accumulating over
@@ -29,6 +38,12 @@
 //   warps 4-7   epilogue: warp w holds weight rows 32*(w%4).. of the tile, reads the tn
 //               token columns of the accumulator, rounds to bf16 and stores C[m, n] for the
 //               tile's token rows that belong to the expert.
+//   warps 8-15  (fp4 operands, tn <= 64) converters: each takes every NCONV-th stage and
+//               re-encodes its packed weight tile (and packed token tile) from the load
+//               ring into its own slot of e4m3 tiles, which the MMA reads; the load ring
+//               stays deep (up to 16 stages of 8 KB weight tiles) to keep HBM requests in
+//               flight.  Warps 9 and 13 idle: they would share the MMA thread's
+//               sub-partition, whose issue slots its tcgen05 instructions need.
 #include <atomic>
 #include <cuda_bf16.h>
 #include "common.cuh"
@@ -40,21 +55,67 @@ namespace mx {
 
 constexpr int BK = 128;              // K per stage
 constexpr int WROWS = 128;           // weight rows per tile (MMA M)
-constexpr int NUM_THREADS = 256;
 constexpr int EPI_WARP0 = 4;
+constexpr int CONV_WARP0 = 8;        // converter warps 8..15 but 9, 13 (fp4 operands)
+
+// Converter index of warp 8..15 (0..5), or -1 for warps 9 and 13 (sub-partition 1, the MMA
+// thread's: its tcgen05 instructions need that sub-partition's issue slots).
+__device__ __forceinline__ int converter_index(uint32_t warp) {
+  const int w = (int)warp - CONV_WARP0;
+  if (w < 0 || (w & 3) == 1) return -1;
+  return (w >> 2) * 3 + ((w & 3) == 0 ? 0 : (w & 3) - 1);
+}
+constexpr uint32_t SMEM_LIMIT = 232448;  // dynamic shared memory per block (227 KB)
+
+// Operand formats of a launch: A (tokens) x B (weights).
+enum Format : int {
+  FMT_MXFP8 = 0,        // e4m3 x e4m3
+  FMT_MXFP8_MXFP4 = 1,  // e4m3 x e2m1
+  FMT_MXFP4 = 2,        // e2m1 x e2m1
+};
 constexpr int SF_BLOCK = 512;        // packed scale block: 128 rows x 4 codes
 constexpr int SCALE_LOOKAHEAD = 4;   // scale stages in flight per loader warp
 constexpr int GROUP = 4;             // stages whose 4 codes per row form one 16-byte chunk
 constexpr int STG_SLOTS = 3;         // staged 16-byte groups: one in use, two in flight
 constexpr uint32_t STG_SLOT = WROWS * 16;
 
-template <int TN_>
+template <int TN_, int FMT_ = FMT_MXFP8>
 struct Cfg {
   static constexpr int TN = TN_;                               // token rows per tile
-  static constexpr uint32_t W_STAGE = WROWS * BK;              // 16 KB
-  static constexpr uint32_t T_STAGE = TN * BK;                 // tn x 128 B
-  static constexpr int STAGES = (TN <= 32) ? 10 : (TN <= 64) ? 8 : 6;
-  static constexpr uint32_t SMEM_W = 0;
+  static constexpr int FMT = FMT_;
+  static constexpr bool B_FP4 = FMT_ != FMT_MXFP8;
+  static constexpr bool A_FP4 = FMT_ == FMT_MXFP4;
+  static constexpr bool CONVERT = B_FP4;
+  static constexpr int THREADS = CONVERT ? 512 : 256;
+  static_assert(!CONVERT || TN <= 64, "fp4 tiles: 512 threads leave 128 registers each");
+  // Load ring (STAGES deep): per stage the weight tile, the token tile and the two scale
+  // blocks as they arrive -- e4m3 tiles with the 128-byte swizzle, packed e2m1 tiles
+  // [rows x 64 B] without swizzle.  Byte offsets of a K block along a row: W_KX, T_KX.
+  static constexpr uint32_t W_STAGE = B_FP4 ? WROWS * BK / 2 : WROWS * BK;  // 8 / 16 KB
+  static constexpr uint32_t T_STAGE = A_FP4 ? TN * BK / 2 : TN * BK;
+  static constexpr int W_KX = B_FP4 ? BK / 2 : BK;
+  static constexpr int T_KX = A_FP4 ? BK / 2 : BK;
+  // Converted ring (fp4 formats): the e4m3 tiles the MMA reads in place of the packed ones,
+  // one slot per converter warp; converter c re-encodes the stages i with i % NCONV == c
+  // into slot c.  The load ring keeps the HBM requests in flight.
+  static constexpr int NCONV = !CONVERT ? 0 : (A_FP4 && TN > 32) ? 4 : 6;
+  static constexpr int CSTAGES = NCONV;
+  static constexpr uint32_t CW_STAGE = CONVERT ? WROWS * BK : 0;  // 16 KB
+  static constexpr uint32_t CT_STAGE = A_FP4 ? TN * BK : 0;
+  static constexpr uint32_t CONV_BYTES = CSTAGES * (CW_STAGE + CT_STAGE);
+  static constexpr uint32_t PER_STAGE = W_STAGE + T_STAGE + 2 * SF_BLOCK;
+  // fp4: as many load stages as fit next to the converted ring, the staging slots, the
+  // barriers and the alignment pad
+  static constexpr int FIT =
+      (int)((SMEM_LIMIT - CONV_BYTES - STG_SLOTS * STG_SLOT - 2048) / PER_STAGE);
+  static constexpr int STAGES = !CONVERT ? ((TN <= 32) ? 10 : (TN <= 64) ? 8 : 6)
+                                         : (FIT < 16 ? FIT : 16);
+  static constexpr int LOOKAHEAD = SCALE_LOOKAHEAD < STAGES - 1 ? SCALE_LOOKAHEAD : STAGES - 1;
+  // the epilogue's factor: 2^6 per fp4 operand undoes the re-encoding's 2^-6
+  static constexpr float POST = A_FP4 ? 4096.0f : (B_FP4 ? 64.0f : 1.0f);
+  static constexpr uint32_t SMEM_CW = 0;
+  static constexpr uint32_t SMEM_CT = SMEM_CW + CSTAGES * CW_STAGE;
+  static constexpr uint32_t SMEM_W = SMEM_CT + CSTAGES * CT_STAGE;
   static constexpr uint32_t SMEM_T = SMEM_W + STAGES * W_STAGE;
   static constexpr uint32_t SMEM_SFW = SMEM_T + STAGES * T_STAGE;
   static constexpr uint32_t SMEM_SFT = SMEM_SFW + STAGES * SF_BLOCK;
@@ -68,14 +129,19 @@ struct Cfg {
   static constexpr uint32_t SFT_COL = ACC_COLS + 8;
   static constexpr uint32_t TMEM_COLS = (ACC_COLS + 16 <= 64) ? 64 : (ACC_COLS + 16 <= 128) ? 128
                                         : (ACC_COLS + 16 <= 256) ? 256 : 512;
-  static_assert(SCALE_LOOKAHEAD < STAGES, "scale look-ahead must leave a free stage");
-  static_assert(T_STAGE % 1024 == 0 || TN % 8 == 0, "token tile");
+  static_assert(LOOKAHEAD >= 1 && LOOKAHEAD < STAGES, "scale look-ahead must leave a free stage");
+  static_assert(STAGES > CSTAGES, "the load ring is deeper than the converted ring");
+  // 128-byte-swizzled tiles start on 1024-byte boundaries
+  static_assert(SMEM_W % 1024 == 0 && SMEM_T % 1024 == 0 && CT_STAGE % 1024 == 0, "swizzle");
+  static_assert(A_FP4 || T_STAGE % 1024 == 0, "token tiles keep the 1024-byte alignment");
+  static_assert(B_FP4 || W_STAGE % 1024 == 0, "weight tiles keep the 1024-byte alignment");
 };
 
 template <class C>
 struct Ctl {
   uint64_t full[C::STAGES];
   uint64_t empty[C::STAGES];
+  uint64_t cfull[C::CSTAGES > 0 ? C::CSTAGES : 1];  // converted tiles written (fp4 formats)
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t mma_done;
@@ -91,6 +157,68 @@ constexpr uint32_t smem_bytes() {
   return C::SMEM_CTL + sizeof(Ctl<C>) + 1024;
 }
 
+// Four e2m1 pairs (one 32-bit word of a packed row: element 2i in the low nibble of byte
+// i) to eight e4m3 codes, each exactly 2^-6 times the e2m1 value: the sign moves from bit
+// 3 of the nibble to bit 7 of the byte, the 3 magnitude bits to bits 2..4.
+__device__ __forceinline__ uint2 e2m1x8_to_e4m3x8(uint32_t w) {
+  const uint32_t lo = ((w << 4) & 0x80808080u) | ((w << 2) & 0x1C1C1C1Cu);  // even elements
+  const uint32_t hi = (w & 0x80808080u) | ((w >> 2) & 0x1C1C1C1Cu);         // odd elements
+  return make_uint2(__byte_perm(lo, hi, 0x5140), __byte_perm(lo, hi, 0x7362));
+}
+
+// Re-encode a packed tile [ROWS x 64 B] (128 e2m1 per row, row-major) into the e4m3 tile
+// [ROWS x 128 B] with the 128-byte swizzle (16-byte chunk c of row r at chunk c ^ (r % 8)),
+// one warp.  For a group of 8 rows, lane l reads 16 packed bytes (row l / 4 of the group,
+// chunk l % 4: 32 elements) and writes output chunks 2*(l%4) and 2*(l%4)+1; eight
+// consecutive lanes read 128 contiguous bytes and write 8 distinct chunks of two rows.  Four
+// groups' loads are issued before their conversions.
+template <int ROWS>
+__device__ __forceinline__ void convert_fp4_tile(const uint8_t* raw, uint8_t* out,
+                                                 uint32_t lane) {
+  static_assert(ROWS % 32 == 0, "groups of 4 x 8 rows");
+  const uint32_t q = lane & 3;
+#pragma unroll 1
+  for (int g0 = 0; g0 < ROWS / 8; g0 += 4) {
+    uint4 in[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const uint32_t row = (g0 + u) * 8 + (lane >> 2);
+      in[u] = *reinterpret_cast<const uint4*>(raw + row * 64 + q * 16);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const uint32_t row = (g0 + u) * 8 + (lane >> 2);
+      const uint2 a = e2m1x8_to_e4m3x8(in[u].x), b = e2m1x8_to_e4m3x8(in[u].y);
+      const uint2 c = e2m1x8_to_e4m3x8(in[u].z), d = e2m1x8_to_e4m3x8(in[u].w);
+      uint8_t* orow = out + row * 128;
+      *reinterpret_cast<uint4*>(orow + (((2 * q) ^ (row & 7)) << 4)) =
+          make_uint4(a.x, a.y, b.x, b.y);
+      *reinterpret_cast<uint4*>(orow + (((2 * q + 1) ^ (row & 7)) << 4)) =
+          make_uint4(c.x, c.y, d.x, d.y);
+    }
+  }
+}
+
+// Waits of every role but the MMA thread sleep in the barrier (mbar_wait_sleep): polling
+// warps would take issue slots from the warps they share a sub-partition with (the MMA
+// thread, the fp4 converters).  BSMX_SPIN_WAITS restores polling for comparison.
+__device__ __forceinline__ bool role_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
+#ifdef BSMX_SPIN_WAITS
+  return mbar_wait(bar, parity, abort);
+#else
+  return mbar_wait_sleep(bar, parity, abort);
+#endif
+}
+
+// The MMA thread polls: it alone issues the tensor-core work and must see each stage at once.
+__device__ __forceinline__ bool mma_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
+#ifdef BSMX_MMA_SLEEP
+  return mbar_wait_sleep(bar, parity, abort);
+#else
+  return mbar_wait(bar, parity, abort);
+#endif
+}
+
 __device__ __forceinline__ void record_error(int* err, int code, volatile int* abort) {
   atomicCAS(err, 0, code);
   *abort = 1;
@@ -103,7 +231,7 @@ __device__ __forceinline__ uint64_t sf_block_desc(uint32_t saddr) {
 }
 
 template <class C>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__global__ void __launch_bounds__(C::THREADS, 1)
 bsmxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const GemmArgs args) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -142,6 +270,7 @@ bsmxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   auto empty_bar = [&](int s) { return smem_u32(&ctl->empty[s]); };
   auto tfull_bar = [&](int s) { return smem_u32(&ctl->tfull[s]); };
   auto tempty_bar = [&](int s) { return smem_u32(&ctl->tempty[s]); };
+  auto cfull_bar = [&](int s) { return smem_u32(&ctl->cfull[s]); };
 
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
@@ -151,6 +280,7 @@ bsmxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       mbar_init(full_bar(s), packed_b ? 2 : 3);
       mbar_init(empty_bar(s), 1);  // one MMA commit
     }
+    for (int s = 0; s < C::CSTAGES; ++s) mbar_init(cfull_bar(s), 1);  // its converter warp
     for (int s = 0; s < 2; ++s) {
       mbar_init(tfull_bar(s), 1);
       mbar_init(tempty_bar(s), 4);  // the 4 epilogue warps
@@ -184,14 +314,15 @@ bsmxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         const uint8_t* w_sf = static_cast<const uint8_t*>(args.b_scales) +
                               ((int64_t)w_row / WROWS) * KB * SF_BLOCK;
         for (int kb = 0; kb < KB; ++kb) {
-          if (!mbar_wait(empty_bar(stage), phase ^ 1, abort)) {
+          if (!role_wait(empty_bar(stage), phase ^ 1, abort)) {
             record_error(args.err, DEV_TIMEOUT, abort);
             ok = false;
             break;
           }
           mbar_arrive_expect_tx(full_bar(stage), C::STAGE_TX + (packed_b ? SF_BLOCK : 0u));
-          tma_load_2d_hint(sW + stage * C::W_STAGE, &tmB, kb * BK, w_row, full_bar(stage), pol_w);
-          tma_load_2d(sT + stage * C::T_STAGE, &tmA, kb * BK, t_row, full_bar(stage));
+          tma_load_2d_hint(sW + stage * C::W_STAGE, &tmB, kb * C::W_KX, w_row, full_bar(stage),
+                           pol_w);
+          tma_load_2d(sT + stage * C::T_STAGE, &tmA, kb * C::T_KX, t_row, full_bar(stage));
           if (packed_b)  // the stage's weight-scale block is stored ready-made
             bulk_copy_g2s_hint(sSFW + stage * SF_BLOCK, w_sf + (int64_t)kb * SF_BLOCK, SF_BLOCK,
                                full_bar(stage), pol_w);
@@ -214,18 +345,23 @@ bsmxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     if (lane == 0) {
       GroupedScheduler<C::TN, WROWS> sched;
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0, slot = 0;
+      uint32_t cstage = 0, cphase = 0;  // converted ring (fp4 formats)
       bool ok = true;
       TileCoord tc;
       for (int64_t t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
         if (!sched.locate(args, t, tc)) break;
-        if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1, abort)) {
+        if (!mma_wait(tempty_bar(acc), acc_phase ^ 1, abort)) {
           record_error(args.err, DEV_TIMEOUT, abort);
           break;
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * C::TN;
         for (int kb = 0; kb < KB; ++kb) {
-          if (!mbar_wait(full_bar(stage), phase, abort)) {
+          // fp4: the converters have written this stage's e4m3 tiles (after its loads and
+          // scale blocks landed); otherwise the stage's loads themselves
+          const bool got = C::CONVERT ? mma_wait(cfull_bar(cstage), cphase, abort)
+                                      : mma_wait(full_bar(stage), phase, abort);
+          if (!got) {
             record_error(args.err, DEV_TIMEOUT, abort);
             ok = false;
             break;
@@ -235,8 +371,15 @@ bsmxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           const uint32_t sft_t = tmem_base + C::SFT_COL + 4 * slot;
           tmem_cp_32x128b_warpx4<1>(sfw_t, sf_block_desc(sSFW + stage * SF_BLOCK));
           tmem_cp_32x128b_warpx4<1>(sft_t, sf_block_desc(sSFT + stage * SF_BLOCK));
-          const uint64_t wdesc = kmajor_sw128_desc(sW + stage * C::W_STAGE);
-          const uint64_t tdesc = kmajor_sw128_desc(sT + stage * C::T_STAGE);
+          const uint32_t w_tile = C::CONVERT ? smem_u32(smem + C::SMEM_CW) + cstage * C::CW_STAGE
+                                             : sW + stage * C::W_STAGE;
+          const uint32_t t_tile = C::A_FP4 ? smem_u32(smem + C::SMEM_CT) + cstage * C::CT_STAGE
+                                           : sT + stage * C::T_STAGE;
+          const uint64_t wdesc = kmajor_sw128_desc(w_tile);
+          const uint64_t tdesc = kmajor_sw128_desc(t_tile);
+          if constexpr (C::CONVERT) {
+            if (++cstage == C::CSTAGES) { cstage = 0; cphase ^= 1; }
+          }
 #pragma unroll
           for (int k = 0; k < BK / 32; ++k)
             umma_mxf8f6f4<1>(d_tmem, wdesc + (uint64_t)(k * 2), tdesc + (uint64_t)(k * 2),
@@ -260,7 +403,8 @@ bsmxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     // pre-packed with the producer's copies).  Each lane moves 4-byte words (one row's 4
     // codes of the stage) into the packed block, row r at byte (r % 32) * 16 + (r / 32) * 4,
     // and a stage is announced on its full barrier once its copies have landed,
-    // SCALE_LOOKAHEAD stages behind the newest issued one.  Token rows >= TN of every
+    // C::LOOKAHEAD stages (SCALE_LOOKAHEAD, fewer in a short ring) behind the newest issued
+    // one.  Token rows >= TN of every
     // block stay zero (written once here).
     const bool weights = warp == 3;
     const uint8_t* a_sc = static_cast<const uint8_t*>(args.a_scales);
@@ -272,7 +416,7 @@ bsmxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     }
     GroupedScheduler<C::TN, WROWS> sched;
     uint32_t stage = 0, phase = 0;
-    uint32_t ring[SCALE_LOOKAHEAD + 1] = {};
+    uint32_t ring[C::LOOKAHEAD + 1] = {};
     int inflight = 0, head = 0;
     bool ok = true;
     TileCoord tc;
@@ -280,7 +424,7 @@ bsmxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       fence_proxy_async_smem();  // generic-proxy writes -> tcgen05.cp (async proxy)
       __syncwarp();
       if (lane == 0) mbar_arrive(full_bar(ring[head]));
-      head = (head + 1) % (SCALE_LOOKAHEAD + 1);
+      head = (head + 1) % (C::LOOKAHEAD + 1);
       --inflight;
     };
     // Weight rows, grouped: when a row's codes for GROUP consecutive stages form one
@@ -325,7 +469,7 @@ bsmxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           const uint8_t* src = stg + (g % STG_SLOTS) * STG_SLOT;
           for (int j = 0; j < GROUP; ++j) {
             const bool got =
-                __all_sync(0xffffffffu, mbar_wait(empty_bar(stage), phase ^ 1, abort));
+                __all_sync(0xffffffffu, role_wait(empty_bar(stage), phase ^ 1, abort));
             if (!got) {
               if (lane == 0) record_error(args.err, DEV_TIMEOUT, abort);
               ok = false;
@@ -354,7 +498,7 @@ bsmxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       if (!sched.locate(args, t, tc)) break;
       const uint8_t* w_rows = b_sc + ((int64_t)tc.be * args.N + tc.n0) * scale_row;
       for (int kb = 0; kb < KB; ++kb) {
-        const bool got = __all_sync(0xffffffffu, mbar_wait(empty_bar(stage), phase ^ 1, abort));
+        const bool got = __all_sync(0xffffffffu, role_wait(empty_bar(stage), phase ^ 1, abort));
         if (!got) {
           if (lane == 0) record_error(args.err, DEV_TIMEOUT, abort);
           ok = false;
@@ -377,10 +521,10 @@ bsmxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           }
         }
         cp_async_commit();
-        ring[(head + inflight) % (SCALE_LOOKAHEAD + 1)] = stage;
+        ring[(head + inflight) % (C::LOOKAHEAD + 1)] = stage;
         ++inflight;
-        if (inflight > SCALE_LOOKAHEAD) {
-          cp_async_wait_group<SCALE_LOOKAHEAD>();
+        if (inflight > C::LOOKAHEAD) {
+          cp_async_wait_group<C::LOOKAHEAD>();
           announce_oldest();
         }
         if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
@@ -388,7 +532,7 @@ bsmxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     }
     cp_async_wait_group<0>();
     while (inflight > 0) announce_oldest();
-  } else if (warp >= EPI_WARP0) {
+  } else if (warp >= EPI_WARP0 && warp < EPI_WARP0 + 4) {
     // ================================= epilogue =================================
     const uint32_t quarter = warp & 3;
     __nv_bfloat16* Cmat = static_cast<__nv_bfloat16*>(args.C);
@@ -397,7 +541,7 @@ bsmxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     TileCoord tc;
     for (int64_t t = blockIdx.x; t < total_tiles; t += gridDim.x) {
       if (!sched.locate(args, t, tc)) break;
-      const bool got = __all_sync(0xffffffffu, mbar_wait(tfull_bar(acc), acc_phase, abort));
+      const bool got = __all_sync(0xffffffffu, role_wait(tfull_bar(acc), acc_phase, abort));
       if (!got) {
         if (lane == 0) record_error(args.err, DEV_TIMEOUT, abort);
         break;
@@ -419,9 +563,49 @@ bsmxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 #pragma unroll
       for (int j = 0; j < C::TN; ++j) {
         if (j < rows) {
-          const __nv_bfloat16 h = __float2bfloat16_rn(__uint_as_float(v[j]));
-          Cmat[(tc.m0 + j) * (int64_t)args.N + n] = h;
+          float x = __uint_as_float(v[j]);
+          if constexpr (C::POST != 1.0f) x *= C::POST;
+          Cmat[(tc.m0 + j) * (int64_t)args.N + n] = __float2bfloat16_rn(x);
         }
+      }
+    }
+  } else if (C::CONVERT && converter_index(warp) >= 0 && converter_index(warp) < C::NCONV) {
+    // ================================ converters ================================
+    // Converter c takes the stages i = c, c + NCONV, ... (counted over this CTA's tiles):
+    // load slot i % STAGES into converted slot c.  Before reusing slot c it waits for the
+    // MMA's release of stage i - NCONV, the slot's previous occupant (the commit on that
+    // stage's load-slot empty barrier), and only then for stage i's loads: the MMA consumes
+    // in order, so by then the load slot's barrier is in the phase of stage i.
+    const int c = converter_index(warp);
+    GroupedScheduler<C::TN, WROWS> sched;
+    int64_t i = 0;  // stage counter of this CTA
+    bool ok = true;
+    TileCoord tc;
+    for (int64_t t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
+      if (!sched.locate(args, t, tc)) break;
+      for (int kb = 0; kb < KB; ++kb, ++i) {
+        if (i % C::NCONV != c) continue;
+        bool got = true;
+        if (i >= C::NCONV) {
+          const int64_t j = i - C::NCONV;
+          got = role_wait(empty_bar((int)(j % C::STAGES)), (uint32_t)((j / C::STAGES) & 1),
+                          abort);
+        }
+        const int stage = (int)(i % C::STAGES);
+        if (got) got = role_wait(full_bar(stage), (uint32_t)((i / C::STAGES) & 1), abort);
+        if (!__all_sync(0xffffffffu, got)) {
+          if (lane == 0) record_error(args.err, DEV_TIMEOUT, abort);
+          ok = false;
+          break;
+        }
+        convert_fp4_tile<WROWS>(smem + C::SMEM_W + stage * C::W_STAGE,
+                                smem + C::SMEM_CW + c * C::CW_STAGE, lane);
+        if constexpr (C::A_FP4)
+          convert_fp4_tile<C::TN>(smem + C::SMEM_T + stage * C::T_STAGE,
+                                  smem + C::SMEM_CT + c * C::CT_STAGE, lane);
+        fence_proxy_async_smem();  // generic-proxy writes -> tensor-core reads (async proxy)
+        __syncwarp();
+        if (lane == 0) mbar_arrive(cfull_bar(c));
       }
     }
   }
@@ -450,7 +634,8 @@ cudaError_t launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArg
   const int64_t max_row_tiles = (args.M_total + C::TN - 1) / C::TN + args.E;
   const int64_t max_tiles = max_row_tiles * (args.N / WROWS);
   const int grid = (int)(max_tiles < num_sms ? max_tiles : num_sms);
-  bsmxfp8_kernel<C><<<grid, NUM_THREADS, smem_bytes<C>(), stream>>>(tmA, tmB, args);
+  static_assert(smem_bytes<C>() <= SMEM_LIMIT, "shared memory");
+  bsmxfp8_kernel<C><<<grid, C::THREADS, smem_bytes<C>(), stream>>>(tmA, tmB, args);
   return cudaGetLastError();
 }
 
@@ -486,6 +671,27 @@ cudaError_t launch_bsmxfp8(int tn, const CUtensorMap& tmA, const CUtensorMap& tm
     case 32: return mx::launch<mx::Cfg<32>>(tmA, tmB, args, num_sms, stream);
     case 64: return mx::launch<mx::Cfg<64>>(tmA, tmB, args, num_sms, stream);
     case 128: return mx::launch<mx::Cfg<128>>(tmA, tmB, args, num_sms, stream);
+  }
+  return cudaErrorInvalidValue;
+}
+
+// fp4 operands: a_fp4 = tokens packed e2m1 (else e4m3); the weights are packed e2m1; tn is
+// 32 or 64.
+// tmA / tmB map the packed operands with 64-byte boxes and no swizzle (tmA the e4m3 tokens
+// as for MXFP8 when !a_fp4).
+cudaError_t launch_bsmxfp4(int tn, bool a_fp4, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                           const GemmArgs& args, int num_sms, cudaStream_t stream) {
+  using namespace mx;
+  if (a_fp4) {
+    switch (tn) {
+      case 32: return launch<Cfg<32, FMT_MXFP4>>(tmA, tmB, args, num_sms, stream);
+      case 64: return launch<Cfg<64, FMT_MXFP4>>(tmA, tmB, args, num_sms, stream);
+    }
+  } else {
+    switch (tn) {
+      case 32: return launch<Cfg<32, FMT_MXFP8_MXFP4>>(tmA, tmB, args, num_sms, stream);
+      case 64: return launch<Cfg<64, FMT_MXFP8_MXFP4>>(tmA, tmB, args, num_sms, stream);
+    }
   }
   return cudaErrorInvalidValue;
 }

@@ -1,5 +1,6 @@
 // C-ABI entry points: argument checks on the host, tensor-map encoding, kernel launch.
 // Declarations and the contract live in include/bsfp8.h.
+#include <algorithm>
 #include <cstdlib>
 #include <cmath>
 #include <cstring>
@@ -89,9 +90,9 @@ bsfp8_status device_info(DeviceInfo** out) {
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 // 2D uint8 tensor map over a row-major [rows, inner] byte matrix, box [box_rows, box_inner],
-// 128-byte swizzle (box_inner must be 128).
+// 128-byte swizzle (box_inner must be 128), or no swizzle (swizzle == false).
 bool encode_u8_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
-                  uint32_t box_inner, uint32_t box_rows) {
+                  uint32_t box_inner, uint32_t box_rows, bool swizzle = true) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[2] = {inner, rows};
@@ -99,7 +100,8 @@ bool encode_u8_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t r
   const cuuint32_t box[2] = {box_inner, box_rows};
   const cuuint32_t estr[2] = {1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -239,8 +241,54 @@ bsfp8_status mx_gemm(const void* A, const void* B, const uint8_t* a_scales,
                                                                                  : BSFP8_ERR_CUDA;
 }
 
+// Formats per operand.  (MXFP8, MXFP8) is mx_gemm; (MXFP8, MXFP4) and (MXFP4, MXFP4) run
+// the swap-AB kernel with on-chip re-encoding of the packed e2m1 tiles at every size.
+bsfp8_status mx_fmt_gemm(int a_fmt, int b_fmt, const void* A, const void* B,
+                         const uint8_t* a_scales, const uint8_t* b_scales, bool packed_b,
+                         const int32_t* offsets, const int32_t* ids, void* C, int64_t M_total,
+                         int N, int K, int G, int E, cudaStream_t stream) {
+  if (a_fmt == BSMX_MXFP8 && b_fmt == BSMX_MXFP8)
+    return mx_gemm(A, B, a_scales, b_scales, offsets, ids, C, M_total, N, K, G, E, stream,
+                   packed_b);
+  const bool a_fp4 = a_fmt == BSMX_MXFP4;
+  if (b_fmt != BSMX_MXFP4 || (a_fmt != BSMX_MXFP8 && a_fmt != BSMX_MXFP4))
+    return BSFP8_ERR_FORMAT;
+  bsfp8_status st = check_common(A, B, a_scales, b_scales, offsets, ids, C, M_total, N, K, G, E);
+  if (st != BSFP8_OK) return st;
+  if (packed_b && !aligned(b_scales, 16)) return BSFP8_ERR_ALIGN;
+  DeviceInfo* dev = nullptr;
+  if ((st = device_info(&dev)) != BSFP8_OK) return st;
+  if (M_total == 0) return BSFP8_OK;
+  GemmArgs args{offsets, a_scales, b_scales, C, M_total, N, K, G, dev->err_word, ids, E,
+                packed_b ? 1 : 0};
+  const int tn = std::min(choose_mx_token_tile(M_total, G), 64);  // fp4 tiles: tn <= 64
+  CUtensorMap tmA, tmB;
+  const bool ok_a = a_fp4 ? encode_u8_2d(&tmA, A, (uint64_t)K / 2, (uint64_t)M_total, 64,
+                                         (uint32_t)tn, false)
+                          : encode_u8_2d(&tmA, A, (uint64_t)K, (uint64_t)M_total, 128,
+                                         (uint32_t)tn);
+  if (!ok_a || !encode_u8_2d(&tmB, B, (uint64_t)K / 2, (uint64_t)E * N, 64, 128, false))
+    return BSFP8_ERR_CUDA;
+  return launch_bsmxfp4(tn, a_fp4, tmA, tmB, args, dev->num_sms, stream) == cudaSuccess
+             ? BSFP8_OK
+             : BSFP8_ERR_CUDA;
+}
+
 }  // namespace
 }  // namespace bsfp8
+
+extern "C" bsfp8_status bsmx_grouped_gemm(int a_format, int b_format, const void* A,
+                                          const void* B, const uint8_t* a_scales,
+                                          const uint8_t* b_scales, int b_scales_packed,
+                                          const int32_t* group_offsets,
+                                          const int32_t* expert_ids, void* C, int64_t M_total,
+                                          int N, int K, int num_groups, int num_experts,
+                                          cudaStream_t stream) {
+  if (!expert_ids && num_groups != num_experts) return BSFP8_ERR_SHAPE;
+  return mx_fmt_gemm(a_format, b_format, A, B, a_scales, b_scales, b_scales_packed != 0,
+                     group_offsets, expert_ids, C, M_total, N, K, num_groups, num_experts,
+                     stream);
+}
 
 extern "C" bsfp8_status bsfp8_grouped_gemm(const void* A, const void* B, const float* a_scales,
                                            const float* b_scales, const int32_t* expert_offsets,
@@ -373,6 +421,7 @@ extern "C" const char* bsfp8_status_string(bsfp8_status s) {
     case BSFP8_ERR_DEVICE_OFFSETS: return "device: invalid expert offsets";
     case BSFP8_ERR_DEVICE_TIMEOUT: return "device: pipeline wait timed out";
     case BSFP8_ERR_DEVICE_EXPERT_IDS: return "device: expert id out of range";
+    case BSFP8_ERR_FORMAT: return "unsupported operand format pair";
   }
   return "unknown status";
 }

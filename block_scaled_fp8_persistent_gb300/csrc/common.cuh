@@ -58,6 +58,11 @@ cudaError_t launch_bsfp8_blockwise(BlockwiseTile tile, const CUtensorMap& tmA,
 cudaError_t launch_bsmxfp8(int tn, const CUtensorMap& tmA, const CUtensorMap& tmB,
                            const GemmArgs& args, int num_sms, cudaStream_t stream);
 
+// The same kernel with packed e2m1 weights (mxfp4) and e4m3 tokens, or packed e2m1 tokens
+// too (a_fp4): tmA / tmB map packed operands with [64-byte x rows] boxes and no swizzle.
+cudaError_t launch_bsmxfp4(int tn, bool a_fp4, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                           const GemmArgs& args, int num_sms, cudaStream_t stream);
+
 // MXFP8 grouped GEMM with CTA-pair 256 x 256 tiles and overlapping TMEM accumulators.
 cudaError_t launch_bsmxfp8_pair(const CUtensorMap& tmA, const CUtensorMap& tmB,
                                 const GemmArgs& args, int num_sms, cudaStream_t stream);

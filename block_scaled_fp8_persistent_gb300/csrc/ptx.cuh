@@ -102,6 +102,37 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   }
 }
 
+// try_wait with a suspend-time hint: a thread whose phase has not completed may be
+// suspended in the barrier (issuing nothing) until the phase completes or hint_ns passes.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar, uint32_t parity,
+                                                   uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
+// mbar_wait for roles that share a sub-partition with busy warps: the waiting thread sleeps
+// in the barrier instead of polling it, leaving the issue slots to the others.  Same bounds:
+// every try_wait returns within hint_ns, after which *abort and the time limit are checked.
+constexpr uint32_t BSFP8_SUSPEND_HINT_NS = 20000;
+__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity,
+                                                volatile int* abort,
+                                                uint64_t limit_ns = BSFP8_WAIT_LIMIT_NS) {
+  if (mbar_try_wait_hint(bar, parity, BSFP8_SUSPEND_HINT_NS)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (mbar_try_wait_hint(bar, parity, BSFP8_SUSPEND_HINT_NS)) return true;
+    if (*abort) return false;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
+  }
+}
+
 // Bounded wait with the time limit only (used while winding down after an abort).
 __device__ __forceinline__ bool mbar_wait_timed(uint32_t bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;

@@ -63,8 +63,16 @@ typedef enum {
   BSFP8_ERR_CUDA = 5,               /* a CUDA runtime/driver call failed (launch, ...) */
   BSFP8_ERR_DEVICE_OFFSETS = 6,     /* device error word: invalid expert offsets */
   BSFP8_ERR_DEVICE_TIMEOUT = 7,     /* device error word: a pipeline wait gave up */
-  BSFP8_ERR_DEVICE_EXPERT_IDS = 8   /* device error word: an expert id outside [0, num_experts) */
+  BSFP8_ERR_DEVICE_EXPERT_IDS = 8,  /* device error word: an expert id outside [0, num_experts) */
+  BSFP8_ERR_FORMAT = 9              /* bsmx_grouped_gemm: unsupported operand format pair */
 } bsfp8_status;
+
+/* Operand formats of bsmx_grouped_gemm. */
+typedef enum {
+  BSMX_MXFP8 = 0, /* e4m3 elements, one byte each;        UE8M0 scale per 32 elements of K */
+  BSMX_MXFP4 = 1, /* e2m1 elements, two per byte along K; UE8M0 scale per 32 elements of K */
+  BSMX_NVFP4 = 2  /* e2m1 elements, two per byte along K; e4m3 scale per 16 elements of K */
+} bsmx_format;
 
 /*
  * Blockwise FP8 grouped GEMM (1x128 A scales, 128x128 B scales).
@@ -178,6 +186,45 @@ bsfp8_status bsmxfp8_grouped_gemm_prepacked(const void* A, const void* B, const 
                                             const int32_t* expert_offsets, void* C,
                                             int64_t M_total, int N, int K, int num_experts,
                                             cudaStream_t stream);
+
+/*
+ * Block-scaled grouped GEMM with a format per operand: the formats and format pairs of the
+ * Triton Gluon example "Overlapping Accumulator Block-Scaled Matrix Multiplication"
+ * (Fixed Configuration, FORMATS; random_quantized_tensor: scales per VEC_SIZE = 32 K
+ * elements as uint8 UE8M0, or per 16 as float8_e4m3fn for nvfp4; fp4 elements packed along
+ * K, stored as uint8 and read by the MMA as "e2m1").
+ *
+ *   A          [M_total, K] elements in a_format: K bytes per row (MXFP8) or K/2 (fp4: element
+ *              2i of the row in the low nibble of byte i, element 2i+1 in the high nibble)
+ *   B          [num_experts, N, K] elements in b_format, laid out the same way
+ *   a_scales   [M_total, K/vec] codes (vec = 32: UE8M0; vec = 16 for NVFP4: e4m3), row-major
+ *   b_scales   [num_experts, N, K/vec] codes, row-major; with b_scales_packed != 0 (MXFP8 and
+ *              MXFP4 weights only) the 512-byte block layout of bsmxfp8_pack_b_scales,
+ *              16-byte aligned
+ *   group_offsets, C, M_total, N, K, num_groups, num_experts, stream
+ *              as for bsmxfp8_grouped_gemm_ids; expert_ids as there, or NULL for group g ->
+ *              expert g (then num_groups must equal num_experts: BSFP8_ERR_SHAPE)
+ *
+ *   C[m, n] = bf16( sum_k dec(A[m,k]) * sa(m, k/vec_a) * dec(B[x,n,k]) * sb(x, n, k/vec_b) ),
+ *             x the expert of row m's group
+ *
+ * Supported (a_format, b_format) pairs:
+ *   (MXFP8, MXFP8)  bsmxfp8_grouped_gemm(_ids) / _prepacked
+ *   (MXFP8, MXFP4), (MXFP4, MXFP4)
+ *                   swap-AB tiles at every size.  The packed tiles are loaded as they are and
+ *                   re-encoded on chip into e4m3 for the MXFP8 block-scaled MMA: every e2m1
+ *                   value times 2^-6 is an e4m3 value, and the epilogue multiplies the fp32
+ *                   sums by 2^6 per fp4 operand, so the result is that of the same values in
+ *                   MXFP8 (exact unless a product falls below 2^-120 in magnitude).
+ * Any other pair returns BSFP8_ERR_FORMAT with nothing launched.  Requirements, ownership,
+ * asynchrony and the other errors are those of bsmxfp8_grouped_gemm_ids (A, B and C 16-byte
+ * aligned; N and K multiples of 128).
+ */
+bsfp8_status bsmx_grouped_gemm(int a_format, int b_format, const void* A, const void* B,
+                               const uint8_t* a_scales, const uint8_t* b_scales,
+                               int b_scales_packed, const int32_t* group_offsets,
+                               const int32_t* expert_ids, void* C, int64_t M_total, int N, int K,
+                               int num_groups, int num_experts, cudaStream_t stream);
 
 /*
  * TMEM storage plan of double-buffered block-scaled accumulators (host only, no GPU use).

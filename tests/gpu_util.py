@@ -30,6 +30,12 @@ class DeviceProblem:
 
     def run(self, stream=None):
         p = self.p
+        fmts = (getattr(p, "a_fmt", "mxfp8"), getattr(p, "b_fmt", "mxfp8"))
+        if p.mode == "mx" and fmts != ("mxfp8", "mxfp8"):
+            bsfp8.bsmx_grouped_gemm(*fmts, self.A, self.B, self.sa, self.sb, self.off, self.C,
+                                    p.M_total, p.N, p.K, p.E, p.num_experts,
+                                    expert_ids=self.ids, stream=stream)
+            return
         if self.ids is not None:
             fn = (bsfp8.bsfp8_grouped_gemm_ids if p.mode == "blockwise"
                   else bsfp8.bsmxfp8_grouped_gemm_ids)

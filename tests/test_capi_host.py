@@ -37,9 +37,10 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_status_strings(lib):
-    for code in range(9):
+    for code in range(10):
         assert len(bsfp8.status_string(code)) > 0
     assert bsfp8.status_string(8) == "device: expert id out of range"
+    assert bsfp8.status_string(9) == "unsupported operand format pair"
     assert bsfp8.status_string(99) == "unknown status"
 
 
@@ -123,3 +124,37 @@ def test_host_validation_prepacked_gemm(lib):
 @pytest.mark.parametrize("limit", [0, -5, 2_000_000_000])
 def test_host_validation_wait_timeout_check(lib, limit):
     assert lib.bsfp8_check_wait_timeout(limit, None) == 2
+
+
+def _call_fmt(lib, af, bf, **kw):
+    a = dict(A=FAKE, B=FAKE, sa=FAKE, sb=FAKE, packed=0, off=FAKE, ids=None, C=FAKE, M=256,
+             N=256, K=512, G=2, E=2)
+    a.update(kw)
+    return lib.bsmx_grouped_gemm(af, bf, a["A"], a["B"], a["sa"], a["sb"], a["packed"], a["off"],
+                                 a["ids"], a["C"], a["M"], a["N"], a["K"], a["G"], a["E"], None)
+
+
+@pytest.mark.parametrize("af,bf", [(1, 0), (2, 0), (0, 2), (2, 1), (1, 2), (3, 1), (-1, 1),
+                                   (0, 3)])
+def test_fmt_unsupported_pairs(lib, af, bf):
+    # rejected before any other check or GPU use
+    assert _call_fmt(lib, af, bf) == 9
+    assert _call_fmt(lib, af, bf, B=None) == 9
+
+
+@pytest.mark.parametrize("af,bf", [(0, 1), (1, 1)])
+@pytest.mark.parametrize("kw,status", [
+    (dict(B=None), 1), (dict(off=None), 1), (dict(sb=None), 1),
+    (dict(N=192), 2), (dict(K=96), 2), (dict(G=3), 2), (dict(M=-1), 2),
+    (dict(A=FAKE + 8), 3), (dict(B=FAKE + 8), 3), (dict(sb=FAKE + 2), 3),
+    (dict(packed=1, sb=FAKE + 4), 3),
+])
+def test_fmt_host_validation(lib, af, bf, kw, status):
+    assert _call_fmt(lib, af, bf, **kw) == status
+
+
+def test_fmt_binding_raises_on_unsupported_pair():
+    with pytest.raises(bsfp8.BsFp8Error) as ei:
+        bsfp8.bsmx_grouped_gemm("mxfp4", "mxfp8", FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 256, 256,
+                                512, 1, 1, stream=0)
+    assert ei.value.status == 9

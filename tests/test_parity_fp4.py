@@ -1,0 +1,124 @@
+"""GPU parity of the fp4 block-scaled formats (the format pairs mxfp8 x mxfp4 and mxfp4 x
+mxfp4 of the Triton Gluon example "Overlapping Accumulator Block-Scaled Matrix
+Multiplication") against the CPU oracle, through bsmx_grouped_gemm.  Same acceptance bound
+as MXFP8; inputs whose fp32 sums are exact (fp4-grid values, scale codes 126..128) must
+match bit for bit."""
+import numpy as np
+import pytest
+import torch
+
+import gen
+import oracle
+from helpers import parity_report
+
+pytestmark = pytest.mark.gpu
+
+PAIRS = [("mxfp8", "mxfp4"), ("mxfp4", "mxfp4")]
+
+
+@pytest.fixture(params=["32", "64", "128"])
+def tn(request, monkeypatch):
+    """Token rows per swap-AB tile (fp4 tiles hold at most 64: a request for 128 runs 64)."""
+    monkeypatch.setenv("BSFP8_MX_TN", request.param)
+    return int(request.param)
+
+
+def _check_full(p, **kw):
+    from gpu_util import DeviceProblem
+    import block_scaled_fp8_persistent_gb300 as bsfp8
+    d = DeviceProblem(p, c_rows_extra=2, **kw)
+    d.run()
+    got = d.c_bits()
+    assert bsfp8.bsfp8_get_device_error() == 0
+    ref, T = oracle.problem_reference(p)
+    bad, ratio, exact = parity_report(got, ref, T)
+    assert bad == 0, f"{bad} elements outside tolerance (max err/tol {ratio:.3g})"
+    assert np.all(d.guard_bits() == d.sentinel)
+    return got, ref
+
+
+CASES = [
+    ("decode_like", [3, 17, 0, 32, 1, 9], 256, 512),
+    ("many_tiles", [700, 0, 513], 640, 512),
+    ("ragged_k", [40, 0, 7], 384, 640),
+    ("mixed", [0, 129, 64, 65, 2, 0, 31], 256, 384),
+]
+
+
+@pytest.mark.parametrize("a_fmt,b_fmt", PAIRS)
+@pytest.mark.parametrize("name,counts,N,K", CASES, ids=[c[0] for c in CASES])
+def test_small_cases(name, counts, N, K, a_fmt, b_fmt, tn):
+    _check_full(gen.fmt_problem(counts, N, K, seed=300 + len(name), a_fmt=a_fmt, b_fmt=b_fmt))
+
+
+@pytest.mark.parametrize("a_fmt,b_fmt", PAIRS)
+def test_quantized_tokens(a_fmt, b_fmt, tn):
+    # mxfp8 tokens drawn as the decode workload draws them (N(0,1) rows, UE8M0 per 32)
+    if a_fmt != "mxfp8":
+        pytest.skip("quantized recipe is for mxfp8 tokens")
+    _check_full(gen.fmt_problem([5, 30, 0, 12, 64], 512, 1024, seed=41, a_fmt=a_fmt,
+                                b_fmt=b_fmt, a_recipe="quantized"))
+
+
+@pytest.mark.parametrize("a_fmt,b_fmt", PAIRS)
+def test_exact_inputs_bitwise(a_fmt, b_fmt, tn):
+    p = gen.fmt_problem([5, 30, 0, 12], 256, 1024, seed=42, a_fmt=a_fmt, b_fmt=b_fmt)
+    # scale codes 126..128: every partial sum is exact in fp32, so the result is unique
+    p.a_scales[:] = 126 + p.a_scales % 3
+    p.b_scales[:] = 126 + p.b_scales % 3
+    got, ref = _check_full(p)
+    assert np.array_equal(got, ref)
+
+
+@pytest.mark.parametrize("a_fmt,b_fmt", PAIRS)
+def test_expert_ids(a_fmt, b_fmt, tn):
+    p = gen.fmt_problem([9, 0, 33, 4, 17], 256, 512, seed=43, a_fmt=a_fmt, b_fmt=b_fmt,
+                        expert_ids=[3, 1, 3, 0, 2], num_experts=4)
+    _check_full(p)
+
+
+@pytest.mark.parametrize("a_fmt,b_fmt", PAIRS)
+def test_prepacked_weight_scales(a_fmt, b_fmt):
+    import block_scaled_fp8_persistent_gb300 as bsfp8
+    from gpu_util import DeviceProblem
+    p = gen.fmt_problem([12, 0, 40], 384, 1024, seed=44, a_fmt=a_fmt, b_fmt=b_fmt)
+    d = DeviceProblem(p)
+    E, N, K = p.num_experts, p.N, p.K
+    packed = torch.empty(E * N * K // 32, dtype=torch.uint8, device="cuda")
+    bsfp8.bsmxfp8_pack_b_scales(d.sb, packed, E, N, K)
+    bsfp8.bsmx_grouped_gemm(a_fmt, b_fmt, d.A, d.B, d.sa, packed, d.off, d.C, p.M_total, N, K,
+                            p.E, E, b_scales_packed=True)
+    got = d.c_bits()
+    assert bsfp8.bsfp8_get_device_error() == 0
+    ref, T = oracle.problem_reference(p)
+    bad, ratio, _ = parity_report(got, ref, T)
+    assert bad == 0, f"{bad} elements outside tolerance (max err/tol {ratio:.3g})"
+
+
+def test_mxfp8_pair_through_format_entry():
+    # (mxfp8, mxfp8) through bsmx_grouped_gemm is the MXFP8 GEMM
+    from gpu_util import DeviceProblem
+    import block_scaled_fp8_persistent_gb300 as bsfp8
+    p = gen.fmt_problem([7, 0, 50], 256, 512, seed=45, a_fmt="mxfp8", b_fmt="mxfp8")
+    d = DeviceProblem(p)
+    bsfp8.bsmx_grouped_gemm("mxfp8", "mxfp8", d.A, d.B, d.sa, d.sb, d.off, d.C, p.M_total, p.N,
+                            p.K, p.E, p.num_experts)
+    got = d.c_bits()
+    assert bsfp8.bsfp8_get_device_error() == 0
+    ref, T = oracle.problem_reference(p)
+    assert parity_report(got, ref, T)[0] == 0
+
+
+@pytest.mark.parametrize("a_fmt,b_fmt", PAIRS)
+def test_empty_and_degenerate(a_fmt, b_fmt):
+    # no rows at all; one expert with one row; all rows in the last expert
+    from gpu_util import DeviceProblem
+    import block_scaled_fp8_persistent_gb300 as bsfp8
+    p = gen.fmt_problem([0, 0, 0], 128, 128, seed=46, a_fmt=a_fmt, b_fmt=b_fmt)
+    d = DeviceProblem(p, c_rows_extra=1)
+    d.run()
+    torch.cuda.synchronize()
+    assert bsfp8.bsfp8_get_device_error() == 0
+    assert np.all(d.guard_bits() == d.sentinel)
+    _check_full(gen.fmt_problem([1], 128, 128, seed=47, a_fmt=a_fmt, b_fmt=b_fmt))
+    _check_full(gen.fmt_problem([0, 0, 77], 128, 256, seed=48, a_fmt=a_fmt, b_fmt=b_fmt))
