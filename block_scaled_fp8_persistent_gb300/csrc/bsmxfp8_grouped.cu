@@ -72,6 +72,7 @@ enum Format : int {
   FMT_MXFP8 = 0,        // e4m3 x e4m3
   FMT_MXFP8_MXFP4 = 1,  // e4m3 x e2m1
   FMT_MXFP4 = 2,        // e2m1 x e2m1
+  FMT_NVFP4 = 3,        // e2m1 x e2m1 with e4m3 scales per 16 (fp16 MMA on dequantized tiles)
 };
 constexpr int SF_BLOCK = 512;        // packed scale block: 128 rows x 4 codes
 constexpr int SCALE_LOOKAHEAD = 4;   // scale stages in flight per loader warp
@@ -83,11 +84,18 @@ template <int TN_, int FMT_ = FMT_MXFP8>
 struct Cfg {
   static constexpr int TN = TN_;                               // token rows per tile
   static constexpr int FMT = FMT_;
+  static constexpr bool NV = FMT_ == FMT_NVFP4;
   static constexpr bool B_FP4 = FMT_ != FMT_MXFP8;
-  static constexpr bool A_FP4 = FMT_ == FMT_MXFP4;
+  static constexpr bool A_FP4 = FMT_ == FMT_MXFP4 || NV;
   static constexpr bool CONVERT = B_FP4;
-  static constexpr int THREADS = CONVERT ? 512 : 256;
-  static_assert(!CONVERT || TN <= 64, "fp4 tiles: 512 threads leave 128 registers each");
+  static constexpr int THREADS = !CONVERT ? 256 : NV ? 384 : 512;
+  static_assert(!CONVERT || TN <= 64, "fp4 tiles hold at most 64 token rows");
+  // bytes per converted element: e4m3 for the MX formats, fp16 for nvfp4
+  static constexpr uint32_t ESZ = NV ? 2 : 1;
+  // scale bytes per stage: packed UE8M0 blocks (MX), or row-major e4m3 codes per 16 K (nvfp4)
+  static constexpr uint32_t SFW_STAGE = NV ? WROWS * (BK / 16) : SF_BLOCK;
+  static constexpr uint32_t SFT_STAGE = SF_BLOCK;
+  static_assert(!NV || TN * (BK / 16) <= SFT_STAGE, "nvfp4 token scales of a stage");
   // Load ring (STAGES deep): per stage the weight tile, the token tile and the two scale
   // blocks as they arrive -- e4m3 tiles with the 128-byte swizzle, packed e2m1 tiles
   // [rows x 64 B] without swizzle.  Byte offsets of a K block along a row: W_KX, T_KX.
@@ -98,12 +106,12 @@ struct Cfg {
   // Converted ring (fp4 formats): the e4m3 tiles the MMA reads in place of the packed ones,
   // one slot per converter warp; converter c re-encodes the stages i with i % NCONV == c
   // into slot c.  The load ring keeps the HBM requests in flight.
-  static constexpr int NCONV = !CONVERT ? 0 : (A_FP4 && TN > 32) ? 4 : 6;
+  static constexpr int NCONV = !CONVERT ? 0 : NV ? 3 : (A_FP4 && TN > 32) ? 4 : 6;
   static constexpr int CSTAGES = NCONV;
-  static constexpr uint32_t CW_STAGE = CONVERT ? WROWS * BK : 0;  // 16 KB
-  static constexpr uint32_t CT_STAGE = A_FP4 ? TN * BK : 0;
+  static constexpr uint32_t CW_STAGE = CONVERT ? WROWS * BK * ESZ : 0;  // 16 KB (32 KB fp16)
+  static constexpr uint32_t CT_STAGE = A_FP4 ? TN * BK * ESZ : 0;
   static constexpr uint32_t CONV_BYTES = CSTAGES * (CW_STAGE + CT_STAGE);
-  static constexpr uint32_t PER_STAGE = W_STAGE + T_STAGE + 2 * SF_BLOCK;
+  static constexpr uint32_t PER_STAGE = W_STAGE + T_STAGE + SFW_STAGE + SFT_STAGE;
   // fp4: as many load stages as fit next to the converted ring, the staging slots, the
   // barriers and the alignment pad
   static constexpr int FIT =
@@ -112,15 +120,15 @@ struct Cfg {
                                          : (FIT < 16 ? FIT : 16);
   static constexpr int LOOKAHEAD = SCALE_LOOKAHEAD < STAGES - 1 ? SCALE_LOOKAHEAD : STAGES - 1;
   // the epilogue's factor: 2^6 per fp4 operand undoes the re-encoding's 2^-6
-  static constexpr float POST = A_FP4 ? 4096.0f : (B_FP4 ? 64.0f : 1.0f);
+  static constexpr float POST = NV ? 1.0f : A_FP4 ? 4096.0f : (B_FP4 ? 64.0f : 1.0f);
   static constexpr uint32_t SMEM_CW = 0;
   static constexpr uint32_t SMEM_CT = SMEM_CW + CSTAGES * CW_STAGE;
   static constexpr uint32_t SMEM_W = SMEM_CT + CSTAGES * CT_STAGE;
   static constexpr uint32_t SMEM_T = SMEM_W + STAGES * W_STAGE;
   static constexpr uint32_t SMEM_SFW = SMEM_T + STAGES * T_STAGE;
-  static constexpr uint32_t SMEM_SFT = SMEM_SFW + STAGES * SF_BLOCK;
+  static constexpr uint32_t SMEM_SFT = SMEM_SFW + STAGES * SFW_STAGE;
   // weight-scale staging of the grouped loader: STG_SLOTS x (128 rows x 16 bytes)
-  static constexpr uint32_t SMEM_STG = SMEM_SFT + STAGES * SF_BLOCK;
+  static constexpr uint32_t SMEM_STG = SMEM_SFT + STAGES * SFT_STAGE;
   static constexpr uint32_t SMEM_CTL = SMEM_STG + STG_SLOTS * STG_SLOT;
   static constexpr uint32_t STAGE_TX = W_STAGE + T_STAGE;
   // TMEM: 2 accumulators of TN columns, then 2 slots each of weight / token scales (4 cols)
@@ -199,6 +207,78 @@ __device__ __forceinline__ void convert_fp4_tile(const uint8_t* raw, uint8_t* ou
   }
 }
 
+// Eight e2m1 (one 32-bit word of a packed row, element 2i in the low nibble of byte i) times
+// one fp16 scale (replicated in both halves of s): four fp16 pairs, lower element in the
+// lower half.  Both conversions are exact, and so is the product: an e2m1 value has at most
+// 2 significant bits and an e4m3 scale 4, and |value * scale| lies in [2^-10, 2688], inside
+// the normal fp16 range.
+__device__ __forceinline__ uint4 e2m1x8_scaled_f16x8(uint32_t w, uint32_t s) {
+  uint4 o;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t"
+      "mul.rn.f16x2 %0, %0, %5;\n\t"
+      "mul.rn.f16x2 %1, %1, %5;\n\t"
+      "mul.rn.f16x2 %2, %2, %5;\n\t"
+      "mul.rn.f16x2 %3, %3, %5;\n\t}"
+      : "=r"(o.x), "=r"(o.y), "=r"(o.z), "=r"(o.w)
+      : "r"(w), "r"(s));
+  return o;
+}
+
+// Two e4m3 scale codes (low byte first) to an fp16 pair, exact.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t codes16) {
+  uint32_t h;
+  asm("{\n\t.reg .b16 c;\n\tcvt.u16.u32 c, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, c;\n\t}"
+      : "=r"(h)
+      : "r"(codes16));
+  return h;
+}
+
+// Dequantize a packed nvfp4 tile [ROWS x 64 B] with its e4m3 scales [ROWS x 8] (one per 16
+// elements) into the fp16 tile the kind::f16 MMA reads: K-major, 128-byte swizzle, two
+// atoms of 64 elements ([atom][ROWS][128 B], 16-byte chunk c of row r at c ^ (r % 8)).  One
+// warp; for a group of 8 rows lane l takes row l / 4, packed chunk q = l % 4 (elements
+// 32q .. 32q+31, scale groups 2q and 2q+1) and writes its 64 output bytes as chunks
+// 4*(q%2) .. 4*(q%2)+3 of atom q / 2.
+template <int ROWS>
+__device__ __forceinline__ void convert_nvfp4_tile(const uint8_t* raw, const uint8_t* sc,
+                                                   uint8_t* out, uint32_t lane) {
+  static_assert(ROWS % 16 == 0, "groups of 2 x 8 rows");
+  const uint32_t q = lane & 3;
+  uint8_t* atom = out + (q >> 1) * (ROWS * 128);
+#pragma unroll 1
+  for (int g0 = 0; g0 < ROWS / 8; g0 += 2) {
+    uint4 in[2];
+    uint32_t s2[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const uint32_t row = (g0 + u) * 8 + (lane >> 2);
+      in[u] = *reinterpret_cast<const uint4*>(raw + row * 64 + q * 16);
+      s2[u] = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t*>(sc + row * 8 + 2 * q));
+    }
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const uint32_t row = (g0 + u) * 8 + (lane >> 2);
+      const uint32_t s_lo = __byte_perm(s2[u], 0, 0x1010);  // scale of elements 0..15
+      const uint32_t s_hi = __byte_perm(s2[u], 0, 0x3232);  // scale of elements 16..31
+      const uint4 o0 = e2m1x8_scaled_f16x8(in[u].x, s_lo);
+      const uint4 o1 = e2m1x8_scaled_f16x8(in[u].y, s_lo);
+      const uint4 o2 = e2m1x8_scaled_f16x8(in[u].z, s_hi);
+      const uint4 o3 = e2m1x8_scaled_f16x8(in[u].w, s_hi);
+      uint8_t* orow = atom + row * 128;
+      const uint32_t c0 = 4 * (q & 1), r7 = row & 7;
+      *reinterpret_cast<uint4*>(orow + (((c0 + 0) ^ r7) << 4)) = o0;
+      *reinterpret_cast<uint4*>(orow + (((c0 + 1) ^ r7) << 4)) = o1;
+      *reinterpret_cast<uint4*>(orow + (((c0 + 2) ^ r7) << 4)) = o2;
+      *reinterpret_cast<uint4*>(orow + (((c0 + 3) ^ r7) << 4)) = o3;
+    }
+  }
+}
+
 // Waits of every role but the MMA thread sleep in the barrier (mbar_wait_sleep): polling
 // warps would take issue slots from the warps they share a sub-partition with (the MMA
 // thread, the fp4 converters).  BSMX_SPIN_WAITS restores polling for comparison.
@@ -242,7 +322,8 @@ bsmxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   const uint32_t warp = threadIdx.x >> 5;
   const uint32_t lane = threadIdx.x & 31;
   const int KB = args.K / BK;
-  const int scale_row = args.K / 32;  // bytes per row of a row-major UE8M0 scale matrix
+  // bytes per row of a row-major scale matrix: UE8M0 per 32 K, or e4m3 per 16 K (nvfp4)
+  const int scale_row = args.K / (C::NV ? 16 : 32);
   const bool packed_b = args.b_scales_packed != 0;
 
   // Tiles: per expert ceil(M_e / TN) token tiles x N/128 weight tiles (weights fastest).
@@ -324,7 +405,7 @@ bsmxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                            pol_w);
           tma_load_2d(sT + stage * C::T_STAGE, &tmA, kb * C::T_KX, t_row, full_bar(stage));
           if (packed_b)  // the stage's weight-scale block is stored ready-made
-            bulk_copy_g2s_hint(sSFW + stage * SF_BLOCK, w_sf + (int64_t)kb * SF_BLOCK, SF_BLOCK,
+            bulk_copy_g2s_hint(sSFW + stage * C::SFW_STAGE, w_sf + (int64_t)kb * SF_BLOCK, SF_BLOCK,
                                full_bar(stage), pol_w);
           ++issued;
           if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
@@ -369,8 +450,10 @@ bsmxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           tc_fence_after();
           const uint32_t sfw_t = tmem_base + C::SFW_COL + 4 * slot;
           const uint32_t sft_t = tmem_base + C::SFT_COL + 4 * slot;
-          tmem_cp_32x128b_warpx4<1>(sfw_t, sf_block_desc(sSFW + stage * SF_BLOCK));
-          tmem_cp_32x128b_warpx4<1>(sft_t, sf_block_desc(sSFT + stage * SF_BLOCK));
+          if constexpr (!C::NV) {
+            tmem_cp_32x128b_warpx4<1>(sfw_t, sf_block_desc(sSFW + stage * C::SFW_STAGE));
+            tmem_cp_32x128b_warpx4<1>(sft_t, sf_block_desc(sSFT + stage * C::SFT_STAGE));
+          }
           const uint32_t w_tile = C::CONVERT ? smem_u32(smem + C::SMEM_CW) + cstage * C::CW_STAGE
                                              : sW + stage * C::W_STAGE;
           const uint32_t t_tile = C::A_FP4 ? smem_u32(smem + C::SMEM_CT) + cstage * C::CT_STAGE
@@ -380,11 +463,23 @@ bsmxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           if constexpr (C::CONVERT) {
             if (++cstage == C::CSTAGES) { cstage = 0; cphase ^= 1; }
           }
+          if constexpr (C::NV) {
+            // fp16 tiles: two 64-element swizzle atoms per stage, K = 16 per MMA
 #pragma unroll
-          for (int k = 0; k < BK / 32; ++k)
-            umma_mxf8f6f4<1>(d_tmem, wdesc + (uint64_t)(k * 2), tdesc + (uint64_t)(k * 2),
-                             idesc_mxf8f6f4_e4m3(WROWS, C::TN, k, k), sfw_t, sft_t,
-                             (kb > 0 || k > 0) ? 1u : 0u);
+            for (int k = 0; k < BK / 16; ++k) {
+              const uint64_t wd = kmajor_sw128_desc(w_tile + (k >> 2) * (WROWS * 128)) +
+                                  (uint64_t)((k & 3) * 2);
+              const uint64_t td = kmajor_sw128_desc(t_tile + (k >> 2) * (C::TN * 128)) +
+                                  (uint64_t)((k & 3) * 2);
+              umma_f16<1>(d_tmem, wd, td, idesc_f16_f32(WROWS, C::TN), (kb > 0 || k > 0) ? 1u : 0u);
+            }
+          } else {
+#pragma unroll
+            for (int k = 0; k < BK / 32; ++k)
+              umma_mxf8f6f4<1>(d_tmem, wdesc + (uint64_t)(k * 2), tdesc + (uint64_t)(k * 2),
+                               idesc_mxf8f6f4_e4m3(WROWS, C::TN, k, k), sfw_t, sft_t,
+                               (kb > 0 || k > 0) ? 1u : 0u);
+          }
           umma_commit(empty_bar(stage));
           slot ^= 1;
           if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
@@ -409,7 +504,7 @@ bsmxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     const bool weights = warp == 3;
     const uint8_t* a_sc = static_cast<const uint8_t*>(args.a_scales);
     const uint8_t* b_sc = static_cast<const uint8_t*>(args.b_scales);
-    if (!weights && C::TN < WROWS) {
+    if (!C::NV && !weights && C::TN < WROWS) {
       for (int s = 0; s < C::STAGES; ++s)
         for (int rg = C::TN / 32; rg < 4; ++rg)
           *reinterpret_cast<uint32_t*>(smem + C::SMEM_SFT + s * SF_BLOCK + lane * 16 + rg * 4) = 0u;
@@ -431,7 +526,7 @@ bsmxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     // aligned 16-byte chunk (K % 512 == 0, 16-byte aligned b_scales), fetch each row's chunk
     // with one 16-byte copy two groups ahead and transpose each stage's words into its
     // packed block in shared memory.
-    const bool grouped = weights && (args.K % (GROUP * BK) == 0) &&
+    const bool grouped = !C::NV && weights && (args.K % (GROUP * BK) == 0) &&
                          (reinterpret_cast<uintptr_t>(b_sc) % 16 == 0);
     if (grouped) {
       const int G = KB / GROUP;
@@ -504,15 +599,32 @@ bsmxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           ok = false;
           break;
         }
-        if (weights) {
-          const uint32_t dw = sSFW + stage * SF_BLOCK + lane * 16;
+        if (C::NV) {
+          // nvfp4: row r's 8 e4m3 codes of the stage to byte 8r (row-major, as stored)
+          const uint32_t d = weights ? sSFW + stage * C::SFW_STAGE : sSFT + stage * C::SFT_STAGE;
+          const int rows = weights ? WROWS : C::TN;
+#pragma unroll
+          for (int j = 0; j < WROWS / 32; ++j) {
+            const int r = j * 32 + (int)lane;
+            if (r < rows) {
+              if (weights) {
+                cp_async_8(d + 8 * r, w_rows + (int64_t)r * scale_row + 8 * kb, 8);
+              } else {
+                const int64_t m = tc.m0 + r;
+                const bool live = m < args.M_total;
+                cp_async_8(d + 8 * r, live ? a_sc + m * scale_row + 8 * kb : a_sc, live ? 8u : 0u);
+              }
+            }
+          }
+        } else if (weights) {
+          const uint32_t dw = sSFW + stage * C::SFW_STAGE + lane * 16;
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             const int r = j * 32 + (int)lane;
             cp_async_4(dw + 4 * j, w_rows + (int64_t)r * scale_row + 4 * kb, 4);
           }
         } else {
-          const uint32_t dt = sSFT + stage * SF_BLOCK + lane * 16;
+          const uint32_t dt = sSFT + stage * C::SFT_STAGE + lane * 16;
 #pragma unroll
           for (int j = 0; j < C::TN / 32; ++j) {
             const int64_t m = tc.m0 + j * 32 + (int)lane;
@@ -598,11 +710,20 @@ bsmxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           ok = false;
           break;
         }
-        convert_fp4_tile<WROWS>(smem + C::SMEM_W + stage * C::W_STAGE,
-                                smem + C::SMEM_CW + c * C::CW_STAGE, lane);
-        if constexpr (C::A_FP4)
-          convert_fp4_tile<C::TN>(smem + C::SMEM_T + stage * C::T_STAGE,
-                                  smem + C::SMEM_CT + c * C::CT_STAGE, lane);
+        if constexpr (C::NV) {
+          convert_nvfp4_tile<WROWS>(smem + C::SMEM_W + stage * C::W_STAGE,
+                                    smem + C::SMEM_SFW + stage * C::SFW_STAGE,
+                                    smem + C::SMEM_CW + c * C::CW_STAGE, lane);
+          convert_nvfp4_tile<C::TN>(smem + C::SMEM_T + stage * C::T_STAGE,
+                                    smem + C::SMEM_SFT + stage * C::SFT_STAGE,
+                                    smem + C::SMEM_CT + c * C::CT_STAGE, lane);
+        } else {
+          convert_fp4_tile<WROWS>(smem + C::SMEM_W + stage * C::W_STAGE,
+                                  smem + C::SMEM_CW + c * C::CW_STAGE, lane);
+          if constexpr (C::A_FP4)
+            convert_fp4_tile<C::TN>(smem + C::SMEM_T + stage * C::T_STAGE,
+                                    smem + C::SMEM_CT + c * C::CT_STAGE, lane);
+        }
         fence_proxy_async_smem();  // generic-proxy writes -> tensor-core reads (async proxy)
         __syncwarp();
         if (lane == 0) mbar_arrive(cfull_bar(c));
@@ -696,4 +817,17 @@ cudaError_t launch_bsmxfp4(int tn, bool a_fp4, const CUtensorMap& tmA, const CUt
   return cudaErrorInvalidValue;
 }
 
+}  // namespace bsfp8
+
+namespace bsfp8 {
+// nvfp4 x nvfp4: both operands packed e2m1 with e4m3 scales per 16 K; tn is 32 or 64.
+cudaError_t launch_bsnvfp4(int tn, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                           const GemmArgs& args, int num_sms, cudaStream_t stream) {
+  using namespace mx;
+  switch (tn) {
+    case 32: return launch<Cfg<32, FMT_NVFP4>>(tmA, tmB, args, num_sms, stream);
+    case 64: return launch<Cfg<64, FMT_NVFP4>>(tmA, tmB, args, num_sms, stream);
+  }
+  return cudaErrorInvalidValue;
+}
 }  // namespace bsfp8

@@ -241,8 +241,9 @@ bsfp8_status mx_gemm(const void* A, const void* B, const uint8_t* a_scales,
                                                                                  : BSFP8_ERR_CUDA;
 }
 
-// Formats per operand.  (MXFP8, MXFP8) is mx_gemm; (MXFP8, MXFP4) and (MXFP4, MXFP4) run
-// the swap-AB kernel with on-chip re-encoding of the packed e2m1 tiles at every size.
+// Formats per operand.  (MXFP8, MXFP8) is mx_gemm; (MXFP8, MXFP4), (MXFP4, MXFP4) and
+// (NVFP4, NVFP4) run the swap-AB kernel with the packed e2m1 tiles converted on chip, at
+// every size.
 bsfp8_status mx_fmt_gemm(int a_fmt, int b_fmt, const void* A, const void* B,
                          const uint8_t* a_scales, const uint8_t* b_scales, bool packed_b,
                          const int32_t* offsets, const int32_t* ids, void* C, int64_t M_total,
@@ -250,12 +251,15 @@ bsfp8_status mx_fmt_gemm(int a_fmt, int b_fmt, const void* A, const void* B,
   if (a_fmt == BSMX_MXFP8 && b_fmt == BSMX_MXFP8)
     return mx_gemm(A, B, a_scales, b_scales, offsets, ids, C, M_total, N, K, G, E, stream,
                    packed_b);
-  const bool a_fp4 = a_fmt == BSMX_MXFP4;
-  if (b_fmt != BSMX_MXFP4 || (a_fmt != BSMX_MXFP8 && a_fmt != BSMX_MXFP4))
-    return BSFP8_ERR_FORMAT;
+  const bool nv = a_fmt == BSMX_NVFP4 && b_fmt == BSMX_NVFP4;
+  const bool a_fp4 = a_fmt == BSMX_MXFP4 || nv;
+  const bool mx4 = b_fmt == BSMX_MXFP4 && (a_fmt == BSMX_MXFP8 || a_fmt == BSMX_MXFP4);
+  if (!nv && !mx4) return BSFP8_ERR_FORMAT;
+  if (nv && packed_b) return BSFP8_ERR_FORMAT;  // the packed block layout holds UE8M0 codes
   bsfp8_status st = check_common(A, B, a_scales, b_scales, offsets, ids, C, M_total, N, K, G, E);
   if (st != BSFP8_OK) return st;
   if (packed_b && !aligned(b_scales, 16)) return BSFP8_ERR_ALIGN;
+  if (nv && (!aligned(a_scales, 8) || !aligned(b_scales, 8))) return BSFP8_ERR_ALIGN;
   DeviceInfo* dev = nullptr;
   if ((st = device_info(&dev)) != BSFP8_OK) return st;
   if (M_total == 0) return BSFP8_OK;
@@ -269,9 +273,9 @@ bsfp8_status mx_fmt_gemm(int a_fmt, int b_fmt, const void* A, const void* B,
                                          (uint32_t)tn);
   if (!ok_a || !encode_u8_2d(&tmB, B, (uint64_t)K / 2, (uint64_t)E * N, 64, 128, false))
     return BSFP8_ERR_CUDA;
-  return launch_bsmxfp4(tn, a_fp4, tmA, tmB, args, dev->num_sms, stream) == cudaSuccess
-             ? BSFP8_OK
-             : BSFP8_ERR_CUDA;
+  const cudaError_t e = nv ? launch_bsnvfp4(tn, tmA, tmB, args, dev->num_sms, stream)
+                           : launch_bsmxfp4(tn, a_fp4, tmA, tmB, args, dev->num_sms, stream);
+  return e == cudaSuccess ? BSFP8_OK : BSFP8_ERR_CUDA;
 }
 
 }  // namespace

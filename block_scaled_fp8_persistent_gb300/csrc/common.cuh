@@ -63,6 +63,11 @@ cudaError_t launch_bsmxfp8(int tn, const CUtensorMap& tmA, const CUtensorMap& tm
 cudaError_t launch_bsmxfp4(int tn, bool a_fp4, const CUtensorMap& tmA, const CUtensorMap& tmB,
                            const GemmArgs& args, int num_sms, cudaStream_t stream);
 
+// nvfp4 x nvfp4 (packed e2m1, e4m3 scales per 16 K, row-major [rows, K/16]) in the same
+// kernel: the packed tiles are dequantized on chip to fp16 for the kind::f16 MMA.
+cudaError_t launch_bsnvfp4(int tn, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                           const GemmArgs& args, int num_sms, cudaStream_t stream);
+
 // MXFP8 grouped GEMM with CTA-pair 256 x 256 tiles and overlapping TMEM accumulators.
 cudaError_t launch_bsmxfp8_pair(const CUtensorMap& tmA, const CUtensorMap& tmB,
                                 const GemmArgs& args, int num_sms, cudaStream_t stream);

@@ -326,6 +326,18 @@ __device__ __forceinline__ void umma_f8f6f4(uint32_t d_tmem, uint64_t a_desc, ui
         : "memory");
 }
 
+// D[tmem] (+)= A[smem desc] * B[smem desc]^T, fp16 x fp16 -> fp32 (kind::f16, K = 16).
+template <int CG>
+__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t accumulate) {
+  static_assert(CG == 1, "one CTA");
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Block-scaled MMA: e4m3 x e4m3 with UE8M0 scales (one per 32 K) read from TMEM.
 template <int CG>
 __device__ __forceinline__ void umma_mxf8f6f4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
@@ -438,6 +450,12 @@ __host__ __device__ constexpr uint32_t idesc_f8f6f4_e4m3(uint32_t M, uint32_t N)
   return (1u << 4) | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
+// Instruction descriptor for kind::f16 with fp16 A and B (format 0 in bits 7-9 / 10-12) and
+// an fp32 accumulator, both K-major: the bit layout of the kind::f8f6f4 descriptor above.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(uint32_t M, uint32_t N) {
+  return (1u << 4) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+
 // Instruction descriptor for kind::mxf8f6f4 (block scaled), e4m3 operands, UE8M0 scales:
 //   bits 4-5 B scale-factor id, 7-9 A format, 10-12 B format, 17-22 N >> 3,
 //   23 scale type (1 = UE8M0), 24-28 M >> 4, 29-30 A scale-factor id.
@@ -454,6 +472,11 @@ __host__ __device__ constexpr uint32_t idesc_mxf8f6f4_e4m3(uint32_t M, uint32_t 
 // Copies 4 bytes, or writes 4 zero bytes when src_bytes == 0 (the source is not read).
 __device__ __forceinline__ void cp_async_4(uint32_t dst, const void* src, uint32_t src_bytes) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+// 8-byte copy (both addresses 8-byte aligned), or 8 zero bytes when src_bytes == 0.
+__device__ __forceinline__ void cp_async_8(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
                : "memory");
 }
 // 16-byte copy (both addresses 16-byte aligned), or 16 zero bytes when src_bytes == 0.

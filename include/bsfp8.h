@@ -216,6 +216,12 @@ bsfp8_status bsmxfp8_grouped_gemm_prepacked(const void* A, const void* B, const 
  *                   value times 2^-6 is an e4m3 value, and the epilogue multiplies the fp32
  *                   sums by 2^6 per fp4 operand, so the result is that of the same values in
  *                   MXFP8 (exact unless a product falls below 2^-120 in magnitude).
+ *   (NVFP4, NVFP4)  swap-AB tiles at every size.  The packed tiles and their e4m3 scales are
+ *                   dequantized on chip into fp16 (exact: an e2m1 value times an e4m3 scale
+ *                   has at most 6 significant bits and lies in the normal fp16 range) and
+ *                   multiplied by the fp16 tensor-core MMA with fp32 accumulation.  The
+ *                   scales must be 8-byte aligned (BSFP8_ERR_ALIGN); b_scales_packed is not
+ *                   available (BSFP8_ERR_FORMAT).
  * Any other pair returns BSFP8_ERR_FORMAT with nothing launched.  Requirements, ownership,
  * asynchrony and the other errors are those of bsmxfp8_grouped_gemm_ids (A, B and C 16-byte
  * aligned; N and K multiples of 128).

@@ -158,3 +158,13 @@ def test_fmt_binding_raises_on_unsupported_pair():
         bsfp8.bsmx_grouped_gemm("mxfp4", "mxfp8", FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 256, 256,
                                 512, 1, 1, stream=0)
     assert ei.value.status == 9
+
+
+def test_nvfp4_host_rules(lib):
+    # nvfp4 x nvfp4 is supported; the packed UE8M0 scale layout is not (format error), and
+    # its e4m3 scales must be 8-byte aligned
+    assert _call_fmt(lib, 2, 2, packed=1) == 9
+    assert _call_fmt(lib, 2, 2, sa=FAKE + 4) == 3
+    assert _call_fmt(lib, 2, 2, sb=FAKE + 4) == 3
+    assert _call_fmt(lib, 2, 2, N=192) == 2
+    assert _call_fmt(lib, 2, 2, B=None) == 1

@@ -1,8 +1,8 @@
-"""GPU parity of the fp4 block-scaled formats (the format pairs mxfp8 x mxfp4 and mxfp4 x
-mxfp4 of the Triton Gluon example "Overlapping Accumulator Block-Scaled Matrix
+"""GPU parity of the fp4 block-scaled formats (the format pairs mxfp8 x mxfp4, mxfp4 x mxfp4
+and nvfp4 x nvfp4 of the Triton Gluon example "Overlapping Accumulator Block-Scaled Matrix
 Multiplication") against the CPU oracle, through bsmx_grouped_gemm.  Same acceptance bound
-as MXFP8; inputs whose fp32 sums are exact (fp4-grid values, scale codes 126..128) must
-match bit for bit."""
+as MXFP8; inputs whose fp32 sums are exact (fp4-grid values, scales 0.5 / 1 / 2) must match
+bit for bit."""
 import numpy as np
 import pytest
 import torch
@@ -13,7 +13,8 @@ from helpers import parity_report
 
 pytestmark = pytest.mark.gpu
 
-PAIRS = [("mxfp8", "mxfp4"), ("mxfp4", "mxfp4")]
+PAIRS = [("mxfp8", "mxfp4"), ("mxfp4", "mxfp4"), ("nvfp4", "nvfp4")]
+MX_PAIRS = PAIRS[:2]
 
 
 @pytest.fixture(params=["32", "64", "128"])
@@ -63,9 +64,14 @@ def test_quantized_tokens(a_fmt, b_fmt, tn):
 @pytest.mark.parametrize("a_fmt,b_fmt", PAIRS)
 def test_exact_inputs_bitwise(a_fmt, b_fmt, tn):
     p = gen.fmt_problem([5, 30, 0, 12], 256, 1024, seed=42, a_fmt=a_fmt, b_fmt=b_fmt)
-    # scale codes 126..128: every partial sum is exact in fp32, so the result is unique
-    p.a_scales[:] = 126 + p.a_scales % 3
-    p.b_scales[:] = 126 + p.b_scales % 3
+    # scales 0.5 / 1 / 2 (UE8M0 codes 126..128, e4m3 codes 0x30 / 0x38 / 0x40): every
+    # partial sum is exact in fp32, so the result is unique
+    if a_fmt == "nvfp4":
+        p.a_scales[:] = 0x30 + 8 * (p.a_scales % 3)
+        p.b_scales[:] = 0x30 + 8 * (p.b_scales % 3)
+    else:
+        p.a_scales[:] = 126 + p.a_scales % 3
+        p.b_scales[:] = 126 + p.b_scales % 3
     got, ref = _check_full(p)
     assert np.array_equal(got, ref)
 
@@ -77,7 +83,14 @@ def test_expert_ids(a_fmt, b_fmt, tn):
     _check_full(p)
 
 
-@pytest.mark.parametrize("a_fmt,b_fmt", PAIRS)
+@pytest.mark.parametrize("counts,N,K", [([3, 17, 0, 32, 1, 9], 256, 512), ([40, 0, 77], 384, 1024)])
+def test_nvfp4_general_e4m3_scales(counts, N, K, tn):
+    # non-power-of-two e4m3 scales (0.125 .. 3.75), as nvfp4 quantization produces them
+    _check_full(gen.fmt_problem(counts, N, K, seed=49, a_fmt="nvfp4", b_fmt="nvfp4",
+                                scales="e4m3"))
+
+
+@pytest.mark.parametrize("a_fmt,b_fmt", MX_PAIRS)
 def test_prepacked_weight_scales(a_fmt, b_fmt):
     import block_scaled_fp8_persistent_gb300 as bsfp8
     from gpu_util import DeviceProblem
