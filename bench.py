@@ -321,6 +321,58 @@ def time_secondary(cfg, args, flush, stream, peaks, peak_src):
     return out
 
 
+FP4_PAIRS = (("mxfp8", "mxfp4"), ("mxfp4", "mxfp4"), ("nvfp4", "nvfp4"))
+
+
+def time_fp4_formats(args, flush, stream, peaks, ref_ms):
+    """The decode workload's shape (config 4's routing, N=4096, K=7168) with fp4 operands,
+    the format pairs of the block-scaled example (fp4 weights stream half the bytes of e4m3),
+    through bsmx_grouped_gemm with the same protocol.  Inputs: random e2m1 codes and scales
+    as random_quantized_tensor draws them; mxfp8 tokens as the decode workload draws them."""
+    import numpy as np
+    import torch
+    import gen
+    import block_scaled_fp8_persistent_gb300 as bsfp8
+    dev = flush.device
+    counts = gen.config_counts(4)
+    N, K = gen.CONFIG_SHAPES[4]
+    out = {"workload": "config 4's routing and shape (E=128 x U{1..32} rows, N=4096, K=7168) "
+                       "with fp4 operands", "pairs": {}}
+    for af, bf in FP4_PAIRS:
+        p = gen.fmt_problem(counts, N, K, seed=4, a_fmt=af, b_fmt=bf, a_recipe="quantized")
+        d = {k: torch.from_numpy(np.ascontiguousarray(getattr(p, k))).to(dev)
+             for k in ("A", "B", "a_scales", "b_scales", "offsets")}
+        C = torch.empty((p.M_total, N), dtype=torch.bfloat16, device=dev)
+
+        def step():
+            bsfp8.bsmx_grouped_gemm(af, bf, d["A"], d["B"], d["a_scales"], d["b_scales"],
+                                    d["offsets"], C, p.M_total, N, K, p.E, p.num_experts,
+                                    stream=stream)
+
+        for _ in range(args.warmup):
+            step()
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        torch.cuda.synchronize()
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+        ms = statistics.mean(s.elapsed_time(e) for s, e in zip(starts, ends))
+        gbs = p.bytes() / (ms * 1e-3) / 1e9
+        out["pairs"][f"{af} x {bf}"] = {
+            "ms_per_step": ms, "TFLOP/s": p.flops() / (ms * 1e-3) / 1e12,
+            "algorithmic_bytes": p.bytes(), "achieved_gbs": gbs,
+            "hbm_frac": gbs / peaks["hbm_gbs"],
+            "time_vs_mxfp8_decode": (ms / ref_ms) if ref_ms else None,
+            "device_error": bsfp8.bsfp8_get_device_error(stream), "gpu_launches": args.steps}
+        del d, C
+        torch.cuda.empty_cache()
+    return out
+
+
 def time_expert_ids(p, d, C, args, flush, stream):
     """The same workload routed through the expert indirection (group g multiplies expert
     perm[g] of the same B, perm a seeded permutation) with the same protocol."""
@@ -516,6 +568,10 @@ def run_ours(args):
         secondary = time_secondary(4, args, flush, stream, peaks, peak_src)
     if not args.no_secondary and cfg not in (4, 5):
         extra = time_secondary(5, args, flush, stream, peaks, peak_src)
+    fp4 = None
+    if not args.no_secondary:
+        fp4 = time_fp4_formats(args, flush, stream, peaks,
+                               secondary["ms_per_step"] if secondary else None)
 
     clocks = sampler.stop()  # sampled from before the warm-up through the timings above
 
@@ -549,6 +605,8 @@ def run_ours(args):
         line["secondary"] = secondary
     if extra is not None:
         line["extra"] = extra
+    if fp4 is not None:
+        line["fp4_formats"] = fp4
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()

@@ -71,8 +71,8 @@ def _L():
         lib.bsfp8_gen_exact_scales_f32.argtypes = [u64, u64, i64, p]
         lib.bsfp8_gen_exact_scales_ue8m0.argtypes = [u64, u64, i64, p]
         lib.bsfp8_gen_fp4_bytes.argtypes = [u64, u64, i64, p, i32]
-        lib.bsfp8_gen_pow2_scales.argtypes = [u64, u64, i64, i32, p]
-        lib.bsfp8_gen_e4m3_scale_codes.argtypes = [u64, u64, i64, i32, i32, p]
+        lib.bsfp8_gen_pow2_scales.argtypes = [u64, u64, i64, i32, p, i32]
+        lib.bsfp8_gen_e4m3_scale_codes.argtypes = [u64, u64, i64, i32, i32, p, i32]
         lib.bsfp8_gen_route_uniform.argtypes = [u64, i64, i64, p]
         lib.bsfp8_gen_route_zipf.argtypes = [u64, i64, i64, ctypes.c_double, i64, p]
         lib.bsfp8_gen_route_counts.argtypes = [u64, i64, i64, i64, p]
@@ -286,9 +286,10 @@ def _fmt_operand(fmt: str, rows: int, K: int, seed: int, s_elem: int, s_scale: i
         L.bsfp8_gen_fp4_bytes(seed, s_elem, Q.size, _ptr(Q), nthreads)
     S = np.empty((rows, K // vec), np.uint8)
     if fmt == "nvfp4" and scales == "e4m3":
-        L.bsfp8_gen_e4m3_scale_codes(seed, s_scale, S.size, 0x20, 0x47, _ptr(S))
+        L.bsfp8_gen_e4m3_scale_codes(seed, s_scale, S.size, 0x20, 0x47, _ptr(S), nthreads)
     else:
-        L.bsfp8_gen_pow2_scales(seed, s_scale, S.size, 1 if fmt == "nvfp4" else 0, _ptr(S))
+        L.bsfp8_gen_pow2_scales(seed, s_scale, S.size, 1 if fmt == "nvfp4" else 0, _ptr(S),
+                                nthreads)
     return Q, S
 
 

@@ -319,18 +319,24 @@ void bsfp8_gen_fp4_bytes(uint64_t seed, uint64_t stream, int64_t nbytes, uint8_t
 // random_quantized_tensor), as UE8M0 codes (e4m3 == 0) or as e4m3 codes (e4m3 != 0; exact:
 // 2^-7 is the e4m3 subnormal 4/8 * 2^-6).
 void bsfp8_gen_pow2_scales(uint64_t seed, uint64_t stream, int64_t count, int e4m3,
-                           uint8_t* out) {
-  for (int64_t i = 0; i < count; ++i) {
-    const int j = -7 + (int)(hash3(seed, stream, (uint64_t)i) % 9);
-    out[i] = e4m3 ? e4m3_encode(std::ldexp(1.0f, j)) : (uint8_t)(127 + j);
-  }
+                           uint8_t* out, int nthreads) {
+  uint8_t code[9];
+  for (int j = -7; j <= 1; ++j) code[j + 7] = e4m3 ? e4m3_encode(std::ldexp(1.0f, j)) : (uint8_t)(127 + j);
+  const int64_t per = 4096;
+  parallel_for((count + per - 1) / per, nthreads, [&](int64_t c) {
+    for (int64_t i = c * per; i < std::min(count, (c + 1) * per); ++i)
+      out[i] = code[hash3(seed, stream, (uint64_t)i) % 9];
+  });
 }
 
 // General positive e4m3 scale codes, uniform over the codes lo .. hi (finite, > 0).
 void bsfp8_gen_e4m3_scale_codes(uint64_t seed, uint64_t stream, int64_t count, int lo, int hi,
-                                uint8_t* out) {
-  for (int64_t i = 0; i < count; ++i)
-    out[i] = (uint8_t)(lo + (int)(hash3(seed, stream, (uint64_t)i) % (uint64_t)(hi - lo + 1)));
+                                uint8_t* out, int nthreads) {
+  const int64_t per = 4096;
+  parallel_for((count + per - 1) / per, nthreads, [&](int64_t c) {
+    for (int64_t i = c * per; i < std::min(count, (c + 1) * per); ++i)
+      out[i] = (uint8_t)(lo + (int)(hash3(seed, stream, (uint64_t)i) % (uint64_t)(hi - lo + 1)));
+  });
 }
 
 // Routing: counts[E] of rows per expert.
