@@ -424,7 +424,15 @@ def run_ours(args):
 
     cfg = args.config
     t0 = time.time()
-    if args.n_override:
+    fmt = tuple(args.fmt.split(":")) if args.fmt else None
+    if fmt is not None:
+        # fp4 operands on this workload's routing and shape (bsmx_grouped_gemm), for ncu
+        if not args.profile:
+            raise SystemExit("--fmt is for --profile runs only")
+        N = args.n_override or gen.CONFIG_SHAPES[cfg][0]
+        p = gen.fmt_problem(gen.config_counts(cfg), N, gen.CONFIG_SHAPES[cfg][1], seed=cfg,
+                            a_fmt=fmt[0], b_fmt=fmt[1], a_recipe="quantized")
+    elif args.n_override:
         # profiling-sized copy of a workload: same routing, K and kernel, fewer columns
         if not args.profile:
             raise SystemExit("--n-override is for --profile runs only")
@@ -445,6 +453,11 @@ def run_ours(args):
     stream = torch.cuda.current_stream(dev)
 
     def step():
+        if fmt is not None:
+            bsfp8.bsmx_grouped_gemm(fmt[0], fmt[1], d["A"], d["B"], d["a_scales"],
+                                    d["b_scales"], d["offsets"], C, p.M_total, p.N, p.K, p.E,
+                                    p.num_experts, stream=stream)
+            return
         fn(d["A"], d["B"], d["a_scales"], d["b_scales"], d["offsets"], C, p.M_total, p.N, p.K,
            p.E, stream=stream)
 
@@ -628,6 +641,9 @@ def main(argv=None):
                     help="skip the MXFP8 decode workload that is timed after the main one")
     ap.add_argument("--n-override", type=int, default=0,
                     help="with --profile: run the workload with this many columns N")
+    ap.add_argument("--fmt", default="",
+                    help="with --profile: operand formats a:b (e.g. mxfp8:mxfp4, nvfp4:nvfp4) "
+                         "on the workload's routing and shape")
     ap.add_argument("--profile", action="store_true",
                     help="only warm-up + timed steps (for ncu): no soak, e2e, clocks or CPU baseline")
     args = ap.parse_args(argv)
