@@ -44,7 +44,9 @@ KERNEL_SOURCES = {
     "mx_pair": _COMMON_SOURCES + ("bsmxfp8_pair.cu",),
 }
 WORKLOAD_KERNEL = {"config0": "blockwise", "config1": "blockwise", "config2": "blockwise",
-                   "config3": "blockwise", "config4": "mx_swap", "config5": "mx_pair"}
+                   "config3": "blockwise", "config4": "mx_swap", "config5": "mx_pair",
+                   "fp4:mxfp8xmxfp4": "mx_swap", "fp4:mxfp4xmxfp4": "mx_swap",
+                   "fp4:nvfp4xnvfp4": "mx_swap"}
 
 
 def log(*a):
@@ -86,10 +88,13 @@ def traffic_from_profiles(workload_key: str):
         if not name.endswith(".txt"):
             continue
         text = open(os.path.join(pdir, name)).read()
-        if f"workload_key: {workload_key}" not in text:
+        key = f"workload_key: {workload_key}\n"
+        if key not in text:
             continue
+        # the workload's own section: from its key to the next workload's key
+        sect = text[text.index(key) + len(key):].split("workload_key:")[0]
         m_hash = re.search(r"kernel_sources_sha256_12: ([0-9a-f]+)", text)
-        m_bytes = re.search(r"dram_bytes_per_launch: ([0-9.eE+]+)", text)
+        m_bytes = re.search(r"dram_bytes_per_launch: ([0-9.eE+]+)", sect)
         if m_hash and m_bytes and m_hash.group(1) == want:
             return float(m_bytes.group(1)), name
     return None, None
@@ -362,10 +367,12 @@ def time_fp4_formats(args, flush, stream, peaks, ref_ms):
         torch.cuda.synchronize()
         ms = statistics.mean(s.elapsed_time(e) for s, e in zip(starts, ends))
         gbs = p.bytes() / (ms * 1e-3) / 1e9
+        traffic, prof_file = traffic_from_profiles(f"fp4:{af}x{bf}")
         out["pairs"][f"{af} x {bf}"] = {
             "ms_per_step": ms, "TFLOP/s": p.flops() / (ms * 1e-3) / 1e12,
             "algorithmic_bytes": p.bytes(), "achieved_gbs": gbs,
-            "hbm_frac": gbs / peaks["hbm_gbs"],
+            "hbm_frac": gbs / peaks["hbm_gbs"], "traffic": traffic,
+            "traffic_source": f"profiles/{prof_file}" if prof_file else None,
             "time_vs_mxfp8_decode": (ms / ref_ms) if ref_ms else None,
             "device_error": bsfp8.bsfp8_get_device_error(stream), "gpu_launches": args.steps}
         del d, C
