@@ -38,9 +38,10 @@
 //   warps 4-7   epilogue: warp w holds weight rows 32*(w%4).. of the tile, reads the tn
 //               token columns of the accumulator, rounds to bf16 and stores C[m, n] for the
 //               tile's token rows that belong to the expert.
-//   warps 8-15  (fp4 operands, tn <= 64) converters: each takes every NCONV-th stage and
-//               re-encodes its packed weight tile (and packed token tile) from the load
-//               ring into its own slot of e4m3 tiles, which the MMA reads; the load ring
+//   warps 8-15  (fp4 operands, tn <= 64) converters: each converted slot takes every
+//               CSTAGES-th stage, whose packed weight tile (and packed token tile) its warp
+//               (nvfp4: its two warps, half the rows each) re-encodes from the load ring into
+//               the slot's e4m3 (fp16) tiles, which the MMA reads; the load ring
 //               stays deep (up to 16 stages of 8 KB weight tiles) to keep HBM requests in
 //               flight.  Warps 9 and 13 idle: they would share the MMA thread's
 //               sub-partition, whose issue slots its tcgen05 instructions need.
@@ -88,7 +89,7 @@ struct Cfg {
   static constexpr bool B_FP4 = FMT_ != FMT_MXFP8;
   static constexpr bool A_FP4 = FMT_ == FMT_MXFP4 || NV;
   static constexpr bool CONVERT = B_FP4;
-  static constexpr int THREADS = !CONVERT ? 256 : NV ? 384 : 512;
+  static constexpr int THREADS = !CONVERT ? 256 : 512;
   static_assert(!CONVERT || TN <= 64, "fp4 tiles hold at most 64 token rows");
   // bytes per converted element: e4m3 for the MX formats, fp16 for nvfp4
   static constexpr uint32_t ESZ = NV ? 2 : 1;
@@ -103,11 +104,13 @@ struct Cfg {
   static constexpr uint32_t T_STAGE = A_FP4 ? TN * BK / 2 : TN * BK;
   static constexpr int W_KX = B_FP4 ? BK / 2 : BK;
   static constexpr int T_KX = A_FP4 ? BK / 2 : BK;
-  // Converted ring (fp4 formats): the e4m3 tiles the MMA reads in place of the packed ones,
-  // one slot per converter warp; converter c re-encodes the stages i with i % NCONV == c
-  // into slot c.  The load ring keeps the HBM requests in flight.
-  static constexpr int NCONV = !CONVERT ? 0 : NV ? 3 : (A_FP4 && TN > 32) ? 4 : 6;
-  static constexpr int CSTAGES = NCONV;
+  // Converted ring (fp4 formats): the e4m3 (fp16) tiles the MMA reads in place of the packed
+  // ones; slot c takes the stages i with i % CSTAGES == c, converted by SPLIT warps that
+  // share the rows of each stage (nvfp4's dequantization is the heavier, and its 40 KB
+  // slots leave room for three).  The load ring keeps the HBM requests in flight.
+  static constexpr int CSTAGES = !CONVERT ? 0 : NV ? 3 : (A_FP4 && TN > 32) ? 4 : 6;
+  static constexpr int SPLIT = NV ? 2 : 1;
+  static constexpr int NCONV = CSTAGES * SPLIT;  // converter warps (at most 6)
   static constexpr uint32_t CW_STAGE = CONVERT ? WROWS * BK * ESZ : 0;  // 16 KB (32 KB fp16)
   static constexpr uint32_t CT_STAGE = A_FP4 ? TN * BK * ESZ : 0;
   static constexpr uint32_t CONV_BYTES = CSTAGES * (CW_STAGE + CT_STAGE);
@@ -241,17 +244,20 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t codes16) {
 // Dequantize a packed nvfp4 tile [ROWS x 64 B] with its e4m3 scales [ROWS x 8] (one per 16
 // elements) into the fp16 tile the kind::f16 MMA reads: K-major, 128-byte swizzle, two
 // atoms of 64 elements ([atom][ROWS][128 B], 16-byte chunk c of row r at c ^ (r % 8)).  One
-// warp; for a group of 8 rows lane l takes row l / 4, packed chunk q = l % 4 (elements
-// 32q .. 32q+31, scale groups 2q and 2q+1) and writes its 64 output bytes as chunks
-// 4*(q%2) .. 4*(q%2)+3 of atom q / 2.
-template <int ROWS>
+// warp converts rows row0 .. row0 + PART - 1.  For a group of 8 rows lane l takes row l / 4,
+// packed chunk q = l % 4 (elements 32q .. 32q+31, scale groups 2q and 2q+1) and writes its
+// 64 output bytes as chunks 4*(q%2) .. 4*(q%2)+3 of atom q / 2; lanes of atom 1 store their
+// chunks in the order 2, 3, 0, 1, so that each store of a quarter-warp covers 8 distinct
+// chunk positions (32 banks) rather than 4 positions twice.
+template <int ROWS, int PART>
 __device__ __forceinline__ void convert_nvfp4_tile(const uint8_t* raw, const uint8_t* sc,
-                                                   uint8_t* out, uint32_t lane) {
-  static_assert(ROWS % 16 == 0, "groups of 2 x 8 rows");
+                                                   uint8_t* out, uint32_t lane, int row0) {
+  static_assert(PART % 16 == 0 && ROWS % PART == 0, "groups of 2 x 8 rows");
   const uint32_t q = lane & 3;
+  const bool second = (q >> 1) != 0;
   uint8_t* atom = out + (q >> 1) * (ROWS * 128);
 #pragma unroll 1
-  for (int g0 = 0; g0 < ROWS / 8; g0 += 2) {
+  for (int g0 = row0 / 8; g0 < (row0 + PART) / 8; g0 += 2) {
     uint4 in[2];
     uint32_t s2[2];
 #pragma unroll
@@ -265,16 +271,23 @@ __device__ __forceinline__ void convert_nvfp4_tile(const uint8_t* raw, const uin
       const uint32_t row = (g0 + u) * 8 + (lane >> 2);
       const uint32_t s_lo = __byte_perm(s2[u], 0, 0x1010);  // scale of elements 0..15
       const uint32_t s_hi = __byte_perm(s2[u], 0, 0x3232);  // scale of elements 16..31
-      const uint4 o0 = e2m1x8_scaled_f16x8(in[u].x, s_lo);
-      const uint4 o1 = e2m1x8_scaled_f16x8(in[u].y, s_lo);
-      const uint4 o2 = e2m1x8_scaled_f16x8(in[u].z, s_hi);
-      const uint4 o3 = e2m1x8_scaled_f16x8(in[u].w, s_hi);
+      uint4 o0 = e2m1x8_scaled_f16x8(in[u].x, s_lo);
+      uint4 o1 = e2m1x8_scaled_f16x8(in[u].y, s_lo);
+      uint4 o2 = e2m1x8_scaled_f16x8(in[u].z, s_hi);
+      uint4 o3 = e2m1x8_scaled_f16x8(in[u].w, s_hi);
+      uint32_t c0 = 4 * (q & 1), c1 = c0 + 1, c2 = c0 + 2, c3 = c0 + 3;
+      if (second) {  // store order 2, 3, 0, 1
+        const uint4 t0 = o0, t1 = o1;
+        o0 = o2; o1 = o3; o2 = t0; o3 = t1;
+        const uint32_t d0 = c0, d1 = c1;
+        c0 = c2; c1 = c3; c2 = d0; c3 = d1;
+      }
+      const uint32_t r7 = row & 7;
       uint8_t* orow = atom + row * 128;
-      const uint32_t c0 = 4 * (q & 1), r7 = row & 7;
-      *reinterpret_cast<uint4*>(orow + (((c0 + 0) ^ r7) << 4)) = o0;
-      *reinterpret_cast<uint4*>(orow + (((c0 + 1) ^ r7) << 4)) = o1;
-      *reinterpret_cast<uint4*>(orow + (((c0 + 2) ^ r7) << 4)) = o2;
-      *reinterpret_cast<uint4*>(orow + (((c0 + 3) ^ r7) << 4)) = o3;
+      *reinterpret_cast<uint4*>(orow + ((c0 ^ r7) << 4)) = o0;
+      *reinterpret_cast<uint4*>(orow + ((c1 ^ r7) << 4)) = o1;
+      *reinterpret_cast<uint4*>(orow + ((c2 ^ r7) << 4)) = o2;
+      *reinterpret_cast<uint4*>(orow + ((c3 ^ r7) << 4)) = o3;
     }
   }
 }
@@ -361,7 +374,7 @@ bsmxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       mbar_init(full_bar(s), packed_b ? 2 : 3);
       mbar_init(empty_bar(s), 1);  // one MMA commit
     }
-    for (int s = 0; s < C::CSTAGES; ++s) mbar_init(cfull_bar(s), 1);  // its converter warp
+    for (int s = 0; s < C::CSTAGES; ++s) mbar_init(cfull_bar(s), C::SPLIT);  // its converters
     for (int s = 0; s < 2; ++s) {
       mbar_init(tfull_bar(s), 1);
       mbar_init(tempty_bar(s), 4);  // the 4 epilogue warps
@@ -683,12 +696,14 @@ bsmxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     }
   } else if (C::CONVERT && converter_index(warp) >= 0 && converter_index(warp) < C::NCONV) {
     // ================================ converters ================================
-    // Converter c takes the stages i = c, c + NCONV, ... (counted over this CTA's tiles):
-    // load slot i % STAGES into converted slot c.  Before reusing slot c it waits for the
-    // MMA's release of stage i - NCONV, the slot's previous occupant (the commit on that
-    // stage's load-slot empty barrier), and only then for stage i's loads: the MMA consumes
-    // in order, so by then the load slot's barrier is in the phase of stage i.
-    const int c = converter_index(warp);
+    // Slot c takes the stages i = c, c + CSTAGES, ... (counted over this CTA's tiles): load
+    // slot i % STAGES into converted slot c, rows split among its SPLIT warps.  Before
+    // reusing slot c a warp waits for the MMA's release of stage i - CSTAGES, the slot's
+    // previous occupant (the commit on that stage's load-slot empty barrier), and only then
+    // for stage i's loads: the MMA consumes in order, so by then the load slot's barrier is
+    // in the phase of stage i.
+    const int ci = converter_index(warp);
+    const int c = ci / C::SPLIT, h = ci % C::SPLIT;
     GroupedScheduler<C::TN, WROWS> sched;
     int64_t i = 0;  // stage counter of this CTA
     bool ok = true;
@@ -696,10 +711,10 @@ bsmxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     for (int64_t t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
       if (!sched.locate(args, t, tc)) break;
       for (int kb = 0; kb < KB; ++kb, ++i) {
-        if (i % C::NCONV != c) continue;
+        if (i % C::CSTAGES != c) continue;
         bool got = true;
-        if (i >= C::NCONV) {
-          const int64_t j = i - C::NCONV;
+        if (i >= C::CSTAGES) {
+          const int64_t j = i - C::CSTAGES;
           got = role_wait(empty_bar((int)(j % C::STAGES)), (uint32_t)((j / C::STAGES) & 1),
                           abort);
         }
@@ -711,12 +726,13 @@ bsmxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           break;
         }
         if constexpr (C::NV) {
-          convert_nvfp4_tile<WROWS>(smem + C::SMEM_W + stage * C::W_STAGE,
-                                    smem + C::SMEM_SFW + stage * C::SFW_STAGE,
-                                    smem + C::SMEM_CW + c * C::CW_STAGE, lane);
-          convert_nvfp4_tile<C::TN>(smem + C::SMEM_T + stage * C::T_STAGE,
-                                    smem + C::SMEM_SFT + stage * C::SFT_STAGE,
-                                    smem + C::SMEM_CT + c * C::CT_STAGE, lane);
+          constexpr int WPART = WROWS / C::SPLIT, TPART = C::TN / C::SPLIT;
+          convert_nvfp4_tile<WROWS, WPART>(smem + C::SMEM_W + stage * C::W_STAGE,
+                                           smem + C::SMEM_SFW + stage * C::SFW_STAGE,
+                                           smem + C::SMEM_CW + c * C::CW_STAGE, lane, h * WPART);
+          convert_nvfp4_tile<C::TN, TPART>(smem + C::SMEM_T + stage * C::T_STAGE,
+                                           smem + C::SMEM_SFT + stage * C::SFT_STAGE,
+                                           smem + C::SMEM_CT + c * C::CT_STAGE, lane, h * TPART);
         } else {
           convert_fp4_tile<WROWS>(smem + C::SMEM_W + stage * C::W_STAGE,
                                   smem + C::SMEM_CW + c * C::CW_STAGE, lane);
