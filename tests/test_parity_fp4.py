@@ -135,3 +135,57 @@ def test_empty_and_degenerate(a_fmt, b_fmt):
     assert np.all(d.guard_bits() == d.sentinel)
     _check_full(gen.fmt_problem([1], 128, 128, seed=47, a_fmt=a_fmt, b_fmt=b_fmt))
     _check_full(gen.fmt_problem([0, 0, 77], 128, 256, seed=48, a_fmt=a_fmt, b_fmt=b_fmt))
+
+
+@pytest.mark.parametrize("a_fmt,b_fmt", PAIRS)
+def test_invalid_offsets_reported_on_device(a_fmt, b_fmt):
+    # offsets that are not a partition of [0, M_total): device error 6, C untouched
+    from gpu_util import DeviceProblem
+    import block_scaled_fp8_persistent_gb300 as bsfp8
+    p = gen.fmt_problem([10, 10], 128, 256, seed=50, a_fmt=a_fmt, b_fmt=b_fmt)
+    d = DeviceProblem(p)
+    d.off.copy_(torch.tensor([0, 15, 12], dtype=torch.int32))
+    d.run()
+    assert bsfp8.bsfp8_get_device_error() == 6
+    assert np.all(d.c_bits() == d.sentinel)
+
+
+@pytest.mark.parametrize("a_fmt,b_fmt", PAIRS)
+@pytest.mark.parametrize("bad", [-1, 3])
+def test_expert_id_out_of_range_reported_on_device(a_fmt, b_fmt, bad):
+    from gpu_util import DeviceProblem
+    import block_scaled_fp8_persistent_gb300 as bsfp8
+    p = gen.fmt_problem([64, 40], 256, 256, seed=51, a_fmt=a_fmt, b_fmt=b_fmt,
+                        expert_ids=[0, 1], num_experts=3)
+    d = DeviceProblem(p)
+    d.ids.copy_(torch.tensor([0, bad], dtype=torch.int32))
+    d.run()
+    assert bsfp8.bsfp8_get_device_error() == 8
+    assert np.all(d.c_bits() == d.sentinel)
+    assert bsfp8.bsfp8_get_device_error() == 0
+
+
+@pytest.mark.parametrize("a_fmt,b_fmt", PAIRS)
+def test_cuda_graph_capture_and_replay(a_fmt, b_fmt):
+    # the fp4 launch records into a CUDA graph and replays with the inputs changed in place
+    from gpu_util import DeviceProblem
+    import block_scaled_fp8_persistent_gb300 as bsfp8
+    p = gen.fmt_problem([100, 0, 29], 256, 512, seed=52, a_fmt=a_fmt, b_fmt=b_fmt)
+    q = gen.fmt_problem([100, 0, 29], 256, 512, seed=53, a_fmt=a_fmt, b_fmt=b_fmt)
+    d = DeviceProblem(p)
+    d.run()
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            d.run(stream=s)
+    for src in (q, p):
+        d.A.copy_(torch.from_numpy(src.A)); d.B.copy_(torch.from_numpy(src.B))
+        d.sa.copy_(torch.from_numpy(src.a_scales)); d.sb.copy_(torch.from_numpy(src.b_scales))
+        g.replay()
+        torch.cuda.synchronize()
+        assert bsfp8.bsfp8_get_device_error() == 0
+        ref, T = oracle.problem_reference(src)
+        bad, ratio, _ = parity_report(d.c_bits(), ref, T)
+        assert bad == 0
