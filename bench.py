@@ -65,15 +65,44 @@ def load_peaks():
     return dict(FALLBACK), "fallback"
 
 
-def kernel_hash(workload_key: str = "config1") -> str:
-    """First 12 hex digits of the SHA-256 over the sources of this workload's kernel."""
+def strip_comments(src: str) -> str:
+    """C/C++ source without comments and blank lines (string literals kept whole), so that
+    the kernel hash changes with the code and not with its commentary."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c == '"':
+            j = i + 1
+            while j < n and src[j] != '"':
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    lines = ("".join(out)).splitlines()
+    return "\n".join(ln.rstrip() for ln in lines if ln.strip())
+
+
+def kernel_hash(workload_key: str = "config1", sources=None) -> str:
+    """First 12 hex digits of the SHA-256 over the sources of this workload's kernel, comments
+    removed (sources: optional {file name: text} to hash instead of the files on disk)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "block_scaled_fp8_persistent_gb300", "csrc")
     for name in KERNEL_SOURCES[WORKLOAD_KERNEL[workload_key]]:
-        p = os.path.join(csrc, name)
-        if os.path.exists(p):
-            with open(p, "rb") as f:
-                h.update(name.encode() + b"\0" + f.read())
+        if sources is not None:
+            text = sources.get(name)
+        else:
+            p = os.path.join(csrc, name)
+            text = open(p, encoding="utf-8").read() if os.path.exists(p) else None
+        if text is not None:
+            h.update(name.encode() + b"\0" + strip_comments(text).encode())
     return h.hexdigest()[:12]
 
 

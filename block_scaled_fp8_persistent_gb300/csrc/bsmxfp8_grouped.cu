@@ -18,23 +18,30 @@
 // along K, UE8M0 scales per 32): every e2m1 value v is exactly an e4m3 value, and the e4m3
 // code (sign << 7) | (magnitude code << 2) is exactly v * 2^-6 (e2m1's subnormal 0.5 lands
 // on e4m3's subnormal 2^-7, zero on zero).  So the kernel loads the packed tiles with TMA,
-// a converter warpgroup re-encodes them into the 128-byte-swizzled e4m3 tile the MMA
-// reads, the MMA and its scales are those of mxfp8, and the epilogue multiplies by 2^6 per
-// fp4 operand (exact in fp32).  The result is the mxfp8 result of the same values.
+// converter warps re-encode them into the 128-byte-swizzled e4m3 tile the MMA reads, the
+// MMA and its scales are those of mxfp8, and the epilogue multiplies by 2^6 per fp4 operand
+// (exact in fp32).  The result is the mxfp8 result of the same values.
 //
-// Roles (8 warps; 12 with fp4 operands):
+// nvfp4 (the example's third format: e2m1 with e4m3 scales per 16 K) cannot use the UE8M0
+// scale path: the converters dequantize each packed tile with its scales into fp16 (exact:
+// an e2m1 value times an e4m3 scale has at most 6 significant bits and lies inside the
+// normal fp16 range), and the MMA thread issues kind::f16 MMAs (K = 16) with no scale copies.
+//
+// Roles (8 warps; 16 with fp4 operands):
 //   warp 0      TMA producer: per K stage (128 K) the weight tile [128 x 128] and the token
 //               tile [tn x 128] (128-byte swizzle; fp4 operands packed [rows x 64 B],
 //               unswizzled) into a STAGES-deep ring.
 //   warp 1      TMEM owner + MMA thread: per stage tcgen05.cp of both scale blocks into
 //               TMEM, then 4 x tcgen05.mma kind::mxf8f6f4.block_scale (K = 32 each, the
-//               scale-factor id picks the byte of the 4-byte scale word), accumulating over
-//               all of K in a 2-deep TMEM accumulator ring.
+//               scale-factor id picks the byte of the 4-byte scale word; nvfp4: 8 x
+//               kind::f16, K = 16), accumulating over all of K in a 2-deep TMEM
+//               accumulator ring.
 //   warps 2, 3  scale loaders (token rows, weight rows): per stage each row's 4 UE8M0 codes
 //               (one 4-byte word, row-major source) are cp.async'ed into the packed
 //               512-byte block (row r at byte (r%32)*16 + (r/32)*4); a few stages in
 //               flight.  With pre-packed weight scales the producer copies the weight block
-//               and warp 3 idles.
+//               and warp 3 idles.  nvfp4: each row's 8 e4m3 codes of the stage, row-major,
+//               for the converters.
 //   warps 4-7   epilogue: warp w holds weight rows 32*(w%4).. of the tile, reads the tn
 //               token columns of the accumulator, rounds to bf16 and stores C[m, n] for the
 //               tile's token rows that belong to the expert.

@@ -47,3 +47,38 @@ def test_replica_aggregation_two_gloo_ranks():
         assert p.exitcode == 0
     # max of the step times, sum of the work, identical on every rank
     assert out == [(0, 2.0, 30.0), (1, 2.0, 30.0)]
+
+
+def test_kernel_hash_ignores_comments_only():
+    sys.path.insert(0, ROOT)
+    import bench
+    src = 'int a = 1; // one\n/* block\n comment */ const char* s = "x // y";\n\n'
+    assert bench.strip_comments(src) == 'int a = 1;\n const char* s = "x // y";'
+    names = bench.KERNEL_SOURCES[bench.WORKLOAD_KERNEL["config4"]]
+    base = {n: f"int f_{i}() {{ return {i}; }}\n" for i, n in enumerate(names)}
+    commented = {n: "// header\n/* a block\n   comment */\n" + t.replace("\n", "  // why\n")
+                 for n, t in base.items()}
+    changed = dict(base)
+    changed[names[-1]] = base[names[-1]].replace("return", "return 1 +")
+    h = bench.kernel_hash("config4", base)
+    assert bench.kernel_hash("config4", commented) == h
+    assert bench.kernel_hash("config4", changed) != h
+
+
+def test_traffic_read_from_the_workloads_own_section(tmp_path, monkeypatch):
+    sys.path.insert(0, ROOT)
+    import bench
+    h = bench.kernel_hash("fp4:nvfp4xnvfp4")
+    (tmp_path / "profiles").mkdir()
+    (tmp_path / "profiles" / "two.txt").write_text(
+        f"kernel_sources_sha256_12: {h}\n"
+        "workload_key: fp4:mxfp8xmxfp4\ndram_bytes_per_launch: 111\n"
+        "workload_key: fp4:nvfp4xnvfp4\ndram_bytes_per_launch: 222\n")
+    (tmp_path / "profiles" / "stale.txt").write_text(
+        "kernel_sources_sha256_12: 000000000000\nworkload_key: config5\n"
+        "dram_bytes_per_launch: 333\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "kernel_hash", lambda key, sources=None: h)
+    assert bench.traffic_from_profiles("fp4:mxfp8xmxfp4") == (111.0, "two.txt")
+    assert bench.traffic_from_profiles("fp4:nvfp4xnvfp4") == (222.0, "two.txt")
+    assert bench.traffic_from_profiles("config5") == (None, None)   # recorded hash differs
