@@ -189,3 +189,25 @@ def test_cuda_graph_capture_and_replay(a_fmt, b_fmt):
         ref, T = oracle.problem_reference(src)
         bad, ratio, _ = parity_report(d.c_bits(), ref, T)
         assert bad == 0
+
+
+def test_nvfp4_scale_codes_signs_and_subnormals(tn):
+    # e4m3 scale codes over the whole finite range, both signs, subnormals included (NaN
+    # codes 0x7F / 0xFF excluded): the dequantized fp16 products stay exact
+    rng = np.random.default_rng(54)
+    p = gen.fmt_problem([3, 17, 0, 32, 9], 256, 512, seed=54, a_fmt="nvfp4", b_fmt="nvfp4")
+    for s in (p.a_scales, p.b_scales):
+        codes = rng.integers(1, 0x7F, s.shape) | (rng.integers(0, 2, s.shape) << 7)
+        s[:] = codes.astype(np.uint8)
+    _check_full(p)
+
+
+@pytest.mark.parametrize("a_fmt,b_fmt", MX_PAIRS)
+def test_mx_fp4_wide_scale_range(a_fmt, b_fmt, tn):
+    # UE8M0 codes 100..160 (2^-27 .. 2^33): the 2^-6 re-encoding and its 2^6 undo in the
+    # epilogue stay exact across a wide exponent range
+    rng = np.random.default_rng(55)
+    p = gen.fmt_problem([5, 30, 0, 12], 256, 512, seed=55, a_fmt=a_fmt, b_fmt=b_fmt)
+    p.a_scales[:] = rng.integers(100, 161, p.a_scales.shape).astype(np.uint8)
+    p.b_scales[:] = rng.integers(100, 161, p.b_scales.shape).astype(np.uint8)
+    _check_full(p)
