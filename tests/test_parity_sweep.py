@@ -1,6 +1,6 @@
 """Seeded randomized sweep against the oracle: expert sizes around every tile height the
 kernels use (96, 128, 192, 256 rows; 32 / 64 / 128 token rows in MX swap-AB tiles), random
-N and K, every tile form; both modes."""
+N and K, every tile form; both modes, and the fp4 format pairs (32 / 64 token rows)."""
 import numpy as np
 import pytest
 
@@ -56,3 +56,17 @@ def test_mx_sweep(seed, monkeypatch):
     if tn:
         monkeypatch.setenv("BSFP8_MX_TN", tn)
     _check(gen.mx_problem(counts, N, K, seed=2000 + seed, exact=bool(seed % 2)))
+
+
+FP4_FORMS = [(a, b, tn) for (a, b) in (("mxfp8", "mxfp4"), ("mxfp4", "mxfp4"), ("nvfp4", "nvfp4"))
+             for tn in ("32", "64")]
+
+
+@pytest.mark.parametrize("seed", range(2 * len(FP4_FORMS)))
+def test_fp4_sweep(seed, monkeypatch):
+    rng = np.random.default_rng(3000 + seed)
+    counts, N, K = _case(rng)
+    a_fmt, b_fmt, tn = FP4_FORMS[seed % len(FP4_FORMS)]
+    monkeypatch.setenv("BSFP8_MX_TN", tn)
+    _check(gen.fmt_problem(counts, N, K, seed=3000 + seed, a_fmt=a_fmt, b_fmt=b_fmt,
+                           a_recipe="quantized" if seed % 2 else "grid"))
