@@ -419,3 +419,13 @@ def test_fp4_scale_block_width(fmt, vec):
     C2, _ = oracle.problem_reference(p)
     assert np.array_equal(bf16_bits_to_f64(C2), 2.0 * bf16_bits_to_f64(C0))
     assert np.any(C0 != 0)
+
+
+def test_nvfp4_signed_and_subnormal_scales():
+    # e4m3 scale codes of both signs over the whole finite range (subnormals included): the
+    # oracle against dequantize-then-matmul (torch's float8 decode of the scales)
+    rng = np.random.default_rng(36)
+    p = gen.fmt_problem([6, 0, 11], 128, 256, seed=36, a_fmt="nvfp4", b_fmt="nvfp4")
+    for sc in (p.a_scales, p.b_scales):
+        sc[:] = (rng.integers(1, 0x7F, sc.shape) | (rng.integers(0, 2, sc.shape) << 7)).astype(np.uint8)
+    _oracle_vs_bruteforce(p, exact_bits=False)
