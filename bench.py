@@ -608,19 +608,30 @@ def run_ours(args):
     if prof_file:
         roof["traffic_source"] = f"profiles/{prof_file}"
 
+    # The timings after the main one each report a failure in their own entry of the line
+    # instead of losing the main result (a CUDA error that breaks the context still ends
+    # the run: those calls raise again below).
+    def guarded(fn, *a):
+        try:
+            return fn(*a)
+        except Exception as exc:  # noqa: BLE001 -- reported in the JSON line
+            log(f"[bench] {fn.__name__} failed: {exc!r}")
+            return {"error": repr(exc)}
+
     # ---- the same workload through the expert indirection (group -> expert ids) ----
-    routed = None if args.no_secondary else time_expert_ids(p, d, C, args, flush, stream)
+    routed = None if args.no_secondary else guarded(time_expert_ids, p, d, C, args, flush,
+                                                    stream)
 
     # ---- the second mode of the path: the MXFP8 decode workload, timed the same way ----
     secondary = extra = None
     if not args.no_secondary and cfg != 4:
-        secondary = time_secondary(4, args, flush, stream, peaks, peak_src)
+        secondary = guarded(time_secondary, 4, args, flush, stream, peaks, peak_src)
     if not args.no_secondary and cfg not in (4, 5):
-        extra = time_secondary(5, args, flush, stream, peaks, peak_src)
+        extra = guarded(time_secondary, 5, args, flush, stream, peaks, peak_src)
     fp4 = None
     if not args.no_secondary:
-        fp4 = time_fp4_formats(args, flush, stream, peaks,
-                               secondary["ms_per_step"] if secondary else None)
+        ref_ms = secondary.get("ms_per_step") if secondary else None
+        fp4 = guarded(time_fp4_formats, args, flush, stream, peaks, ref_ms)
 
     clocks = sampler.stop()  # sampled from before the warm-up through the timings above
 
