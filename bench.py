@@ -276,9 +276,10 @@ def run_reference(args):
 
 
 def time_secondary(cfg, args, flush, stream, peaks, peak_src):
-    """Time another workload (the MXFP8 decode config 4, or the dense MXFP8 config 5) with
-    the same protocol: warm-up, then args.steps launches, each bracketed by CUDA events,
-    L2 flushed between them."""
+    """Time another workload (the other blockwise configs 0, 2, 3, the MXFP8 decode config 4,
+    or the dense MXFP8 config 5) with the same protocol: warm-up, then args.steps launches,
+    each bracketed by CUDA events, L2 flushed between them.  Config 0 is a launch-latency
+    case: its roofline fraction says how far a 0.4 MB problem is from both roofs."""
     import numpy as np
     import torch
     import gen
@@ -320,8 +321,11 @@ def time_secondary(cfg, args, flush, stream, peaks, peak_src):
                 "frac": gbs / peaks["hbm_gbs"], "peak_source": f"{peak_src} copy bandwidth"}
     roof.update({"traffic": traffic, "algorithmic_bytes": p.bytes()})
     out = {"workload": f"config {cfg}: {gen.CONFIG_NAMES[cfg]}", "M_total": p.M_total,
-           "ms_per_step": ms, "value": tflops, "unit": "TFLOP/s", "roofline": roof,
-           "device_error": err, "gpu_launches": args.steps}
+           "experts": p.E, "N": p.N, "K": p.K, "ms_per_step": ms, "value": tflops,
+           "unit": "TFLOP/s", "roofline": roof, "device_error": err, "gpu_launches": args.steps}
+    if p.mode == "blockwise":
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        out["tile_plan"] = bsfp8.bsfp8_blockwise_plan(p.M_total, p.N, p.E, sms)
     if p.mode == "mx" and cfg == 4:
         # the same decode GEMM on weight scales packed once beforehand (not timed)
         packed = torch.empty_like(d["b_scales"])
@@ -624,6 +628,12 @@ def run_ours(args):
 
     # ---- the second mode of the path: the MXFP8 decode workload, timed the same way ----
     secondary = extra = None
+    others = {}
+    if not args.no_secondary:
+        for c in (3, 2, 0):
+            if c != cfg:
+                others[f"config{c}"] = guarded(time_secondary, c, args, flush, stream, peaks,
+                                               peak_src)
     if not args.no_secondary and cfg != 4:
         secondary = guarded(time_secondary, 4, args, flush, stream, peaks, peak_src)
     if not args.no_secondary and cfg not in (4, 5):
@@ -659,6 +669,8 @@ def run_ours(args):
         "device_error": dev_err,
         "kernel_sources_sha256_12": kernel_hash(f"config{cfg}"),
     }
+    if others:
+        line["blockwise_configs"] = others
     if routed is not None:
         line["expert_ids_variant"] = routed
     if secondary is not None:

@@ -223,8 +223,9 @@ bsfp8_blockwise_kernel(const __grid_constant__ CUtensorMap tmA,
   if (!C::is_epilogue(warp)) {
     // 128 rows: warpgroup 0 (producer, MMA issuer, two idle warps) gives registers away
     if constexpr (!C::SPARE_QUARTER) asm volatile("setmaxnreg.dec.sync.aligned.u32 40;");
-    if (warp == C::PRODUCER_WARP && lane == 0) {
+    if (warp == C::PRODUCER_WARP) {
       // =============================== TMA producer ===============================
+      // The whole warp runs the loop and its waits; one lane issues.
       GroupedScheduler<C::BM, C::BN> sched;
       // B (expert weights) is re-read by every row tile of its expert, possibly in a later
       // wave of tiles: keep it in L2 ahead of the streaming A rows and C output.
@@ -238,22 +239,27 @@ bsfp8_blockwise_kernel(const __grid_constant__ CUtensorMap tmA,
         const int32_t a_row = (int32_t)(tc.m0 + C::ROWS * rank);
         const int32_t b_row = tc.be * args.N + tc.n0 + C::B_ROWS * rank;
         for (int kb = 0; kb < KB; ++kb) {
-          if (!mbar_wait_cg<C::CG>(empty_bar(stage), phase ^ 1, abort)) {
-            record_error(args.err, DEV_TIMEOUT, abort);
+          if (!__all_sync(0xffffffffu,
+                          mbar_wait_cg<C::CG>(empty_bar(stage), phase ^ 1, abort))) {
+            if (lane == 0) record_error(args.err, DEV_TIMEOUT, abort);
             ok = false;
             break;
           }
-          if constexpr (C::CG == 1) {
-            mbar_arrive_expect_tx(full_bar(stage), C::STAGE_TX);
-            tma_load_2d(sA + stage * C::A_STAGE, &tmA, kb * BK, a_row, full_bar(stage));
-            tma_load_2d_hint(sB + stage * C::B_STAGE, &tmB, kb * BK, b_row, full_bar(stage), pol_b);
-          } else {
-            // both CTAs' bytes are counted on the leader's barrier
-            const uint32_t bar = mapa_shared(full_bar(stage), 0);
-            if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), C::STAGE_TX);
-            tma_load_2d_pair(sA + stage * C::A_STAGE, &tmA, kb * BK, a_row, bar);
-            tma_load_2d_pair_hint(sB + stage * C::B_STAGE, &tmB, kb * BK, b_row, bar, pol_b);
+          if (lane == 0) {
+            if constexpr (C::CG == 1) {
+              mbar_arrive_expect_tx(full_bar(stage), C::STAGE_TX);
+              tma_load_2d(sA + stage * C::A_STAGE, &tmA, kb * BK, a_row, full_bar(stage));
+              tma_load_2d_hint(sB + stage * C::B_STAGE, &tmB, kb * BK, b_row, full_bar(stage),
+                               pol_b);
+            } else {
+              // both CTAs' bytes are counted on the leader's barrier
+              const uint32_t bar = mapa_shared(full_bar(stage), 0);
+              if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), C::STAGE_TX);
+              tma_load_2d_pair(sA + stage * C::A_STAGE, &tmA, kb * BK, a_row, bar);
+              tma_load_2d_pair_hint(sB + stage * C::B_STAGE, &tmB, kb * BK, b_row, bar, pol_b);
+            }
           }
+          __syncwarp();
           ++issued;
           if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
         }
@@ -267,8 +273,9 @@ bsfp8_blockwise_kernel(const __grid_constant__ CUtensorMap tmA,
         if (rank == 0) mbar_wait_timed(full_bar(stage), phase);
         else mbar_wait_timed(empty_bar(stage), phase);
       }
-    } else if (warp == C::MMA_WARP && lane == 0 && rank == 0) {
+    } else if (warp == C::MMA_WARP && rank == 0) {
       // ================================ MMA issuer ================================
+      // The whole warp runs the loop and its waits; one lane issues.
       GroupedScheduler<C::BM, C::BN> sched;
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
@@ -277,22 +284,32 @@ bsfp8_blockwise_kernel(const __grid_constant__ CUtensorMap tmA,
         if (!sched.locate(args, t, tc)) break;
         for (int kb = 0; kb < KB; ++kb) {
           // operands first: they are usually in place well before the TMEM stage is free
-          if (!mbar_wait_cg<C::CG>(full_bar(stage), phase, abort) ||
-              !mbar_wait_cg<C::CG>(tempty_bar(acc), acc_phase ^ 1, abort)) {
-            record_error(args.err, DEV_TIMEOUT, abort);
+          const bool got = mbar_wait_cg<C::CG>(full_bar(stage), phase, abort) &&
+                           mbar_wait_cg<C::CG>(tempty_bar(acc), acc_phase ^ 1, abort);
+          if (!__all_sync(0xffffffffu, got)) {
+            if (lane == 0) record_error(args.err, DEV_TIMEOUT, abort);
             ok = false;
             break;
           }
           tc_fence_after();
-          issue_kblock<C>(tmem_base, sA, sB, stage, acc, empty_bar(stage), tfull_bar(acc));
+          if (lane == 0)
+            issue_kblock<C>(tmem_base, sA, sB, stage, acc, empty_bar(stage), tfull_bar(acc));
+          __syncwarp();
           if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
           if (++acc == C::ACC_STAGES) { acc = 0; acc_phase ^= 1; }
         }
       }
-      // Every MMA this thread issued has finished before TMEM is released.
-      if constexpr (C::CG == 1) umma_commit(smem_u32(&ctl->mma_done));
-      else umma_commit_pair(smem_u32(&ctl->mma_done), 0x1);
-      mbar_wait_timed(smem_u32(&ctl->mma_done), 0);
+      // Every MMA this thread issued has finished before TMEM is released.  A wait that
+      // gives up is reported and waited out once more (bounded) before the teardown.
+      if (lane == 0) {
+        if constexpr (C::CG == 1) umma_commit(smem_u32(&ctl->mma_done));
+        else umma_commit_pair(smem_u32(&ctl->mma_done), 0x1);
+      }
+      __syncwarp();
+      if (!__all_sync(0xffffffffu, mbar_wait_timed(smem_u32(&ctl->mma_done), 0))) {
+        if (lane == 0) record_error(args.err, DEV_TIMEOUT, abort);
+        mbar_wait_timed(smem_u32(&ctl->mma_done), 0);
+      }
     }
     __syncwarp();
   } else {

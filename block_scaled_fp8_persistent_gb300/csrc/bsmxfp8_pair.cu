@@ -238,8 +238,13 @@ bsmxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         if (!ok) break;
         umma_commit_pair(accf_bar(buf), 0x3);
       }
+      // every MMA issued has finished before TMEM is released; a wait that gives up is
+      // reported and waited out once more (bounded) before the teardown
       umma_commit_pair(smem_u32(&ctl->mma_done), 0x1);
-      mbar_wait_timed(smem_u32(&ctl->mma_done), 0);
+      if (!mbar_wait_timed(smem_u32(&ctl->mma_done), 0)) {
+        record_error(args.err, DEV_TIMEOUT, abort);
+        mbar_wait_timed(smem_u32(&ctl->mma_done), 0);
+      }
     }
     __syncwarp();
   } else if (warp == 2) {

@@ -264,6 +264,11 @@ bsfp8_status bsfp8_blockwise_plan(int64_t M_total, int N, int num_experts, int n
  * Read the device error word of the current device (after synchronising `stream`) into
  * *code (0, BSFP8_ERR_DEVICE_OFFSETS, BSFP8_ERR_DEVICE_TIMEOUT or BSFP8_ERR_DEVICE_EXPERT_IDS)
  * and reset it to 0.
+ * The word is one per device, not per stream: every kernel of this library on the device
+ * records its first error there, whatever stream it runs on.  Only `stream` is synchronised,
+ * so a kernel still running on another stream can set the word after it is read, or have its
+ * error read (and cleared) by this call on behalf of the wrong caller.  Callers that launch on
+ * several streams synchronise the device (cudaDeviceSynchronize) before reading the word.
  * Returns BSFP8_ERR_NULL for a NULL code, BSFP8_ERR_CUDA if a CUDA call fails.
  */
 bsfp8_status bsfp8_get_device_error(cudaStream_t stream, int* code);

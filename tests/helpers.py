@@ -147,3 +147,15 @@ def parity_report(got_bits: np.ndarray, ref_bits: np.ndarray, T: np.ndarray):
     bad = ~(err <= tol)
     ratio = float(np.max(err / tol)) if err.size else 0.0
     return int(bad.sum()), ratio, int((np.asarray(got_bits) == np.asarray(ref_bits)).sum())
+
+
+def parity_report_chunked(got_bits: np.ndarray, ref_bits: np.ndarray, T: np.ndarray,
+                          rows_per_chunk: int = 2048):
+    """parity_report over row chunks (the full-size outputs hold up to 67 M elements):
+    (n_bad, max_err/tol, n_exact)."""
+    bad, ratio, exact = 0, 0.0, 0
+    for r0 in range(0, got_bits.shape[0], rows_per_chunk):
+        b, q, x = parity_report(got_bits[r0:r0 + rows_per_chunk], ref_bits[r0:r0 + rows_per_chunk],
+                                T[r0:r0 + rows_per_chunk])
+        bad, ratio, exact = bad + b, max(ratio, q), exact + x
+    return bad, ratio, exact

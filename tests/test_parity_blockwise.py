@@ -108,30 +108,3 @@ def test_m_total_zero_is_noop():
     off = torch.zeros(3, dtype=torch.int32, device="cuda")
     bsfp8.bsfp8_grouped_gemm(None, B, None, sb, off, None, 0, 128, 128, 2)
     assert bsfp8.bsfp8_get_device_error() == 0
-
-
-def _sampled_parity(p, n_points=6000, seed=0):
-    """Full-size workload: every output of a few whole rows at expert boundaries plus
-    random sampled elements, each recomputed by the oracle one by one."""
-    from gpu_util import DeviceProblem
-    import block_scaled_fp8_persistent_gb300 as bsfp8
-    d = DeviceProblem(p)
-    d.run()
-    got = d.c_bits()
-    assert bsfp8.bsfp8_get_device_error() == 0
-    rng = np.random.default_rng(seed)
-    off = p.offsets.astype(np.int64)
-    edge_rows = sorted({int(r) for e in range(p.E) if off[e + 1] > off[e]
-                        for r in (off[e], off[e + 1] - 1)})[:16]
-    rows = np.concatenate([np.repeat(edge_rows, p.N), rng.integers(0, p.M_total, n_points)])
-    cols = np.concatenate([np.tile(np.arange(p.N), len(edge_rows)), rng.integers(0, p.N, n_points)])
-    ref, T = oracle.problem_points(p, rows, cols)
-    bad, ratio, exact = parity_report(got[rows, cols], ref, T)
-    assert bad == 0, f"{bad} sampled elements outside tolerance (max err/tol {ratio:.3g})"
-    return got
-
-
-@pytest.mark.parametrize("cfg", [1, 2, 3])
-def test_full_size_config_sampled(cfg, tile):
-    p = gen.config_problem(cfg)
-    _sampled_parity(p, seed=cfg)

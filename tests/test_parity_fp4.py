@@ -52,11 +52,10 @@ def test_small_cases(name, counts, N, K, a_fmt, b_fmt, tn):
     _check_full(gen.fmt_problem(counts, N, K, seed=300 + len(name), a_fmt=a_fmt, b_fmt=b_fmt))
 
 
-@pytest.mark.parametrize("a_fmt,b_fmt", PAIRS)
+@pytest.mark.parametrize("a_fmt,b_fmt", [pr for pr in PAIRS if pr[0] == "mxfp8"])
 def test_quantized_tokens(a_fmt, b_fmt, tn):
-    # mxfp8 tokens drawn as the decode workload draws them (N(0,1) rows, UE8M0 per 32)
-    if a_fmt != "mxfp8":
-        pytest.skip("quantized recipe is for mxfp8 tokens")
+    # mxfp8 tokens drawn as the decode workload draws them (N(0,1) rows, UE8M0 per 32); the
+    # recipe exists for mxfp8 tokens only
     _check_full(gen.fmt_problem([5, 30, 0, 12, 64], 512, 1024, seed=41, a_fmt=a_fmt,
                                 b_fmt=b_fmt, a_recipe="quantized"))
 
@@ -210,4 +209,45 @@ def test_mx_fp4_wide_scale_range(a_fmt, b_fmt, tn):
     p = gen.fmt_problem([5, 30, 0, 12], 256, 512, seed=55, a_fmt=a_fmt, b_fmt=b_fmt)
     p.a_scales[:] = rng.integers(100, 161, p.a_scales.shape).astype(np.uint8)
     p.b_scales[:] = rng.integers(100, 161, p.b_scales.shape).astype(np.uint8)
+    _check_full(p)
+
+
+def _unit_magnitudes(p, a_fmt, rng):
+    """Set every operand element to +-1 or +-1.5 (one octave of products), keeping the
+    layout: packed e2m1 nibbles (codes 2 / 3, sign bit 8) or e4m3 bytes (0x38 / 0x3C)."""
+    def fp4(shape):
+        lo = (rng.integers(2, 4, shape) | (rng.integers(0, 2, shape) << 3)).astype(np.uint8)
+        hi = (rng.integers(2, 4, shape) | (rng.integers(0, 2, shape) << 3)).astype(np.uint8)
+        return lo | (hi << 4)
+    p.B[:] = fp4(p.B.shape)
+    if a_fmt == "mxfp4":
+        p.A[:] = fp4(p.A.shape)
+    else:
+        p.A[:] = (np.where(rng.integers(0, 2, p.A.shape) == 1, 0x3C, 0x38) |
+                  (rng.integers(0, 2, p.A.shape) << 7)).astype(np.uint8)
+
+
+@pytest.mark.parametrize("a_fmt,b_fmt", MX_PAIRS)
+def test_low_scales(a_fmt, b_fmt, tn):
+    # scale codes 65 (tokens) and 66 (weights): every product is 2^-123 times 1 .. 2.25, an fp32
+    # normal number, and the sums stay in bf16's normal range; the fp4 operands' factor 2^6 is
+    # applied through the token scales, so no product the MMA forms falls below 2^-126
+    p = gen.fmt_problem([5, 30, 0, 12], 256, 1024, seed=46, a_fmt=a_fmt, b_fmt=b_fmt)
+    _unit_magnitudes(p, a_fmt, np.random.default_rng(46))
+    p.a_scales[:] = 65
+    p.b_scales[:] = 66
+    _check_full(p)
+
+
+@pytest.mark.parametrize("a_fmt,b_fmt", MX_PAIRS)
+def test_high_token_scales(a_fmt, b_fmt, tn):
+    # token scale codes up to the largest that the fold of 2^6 per fp4 operand leaves
+    # uncapped (248 with e4m3 tokens, 242 with e2m1 tokens), weight codes low enough that the
+    # products stay finite
+    top = 248 if a_fmt == "mxfp8" else 242
+    p = gen.fmt_problem([5, 30, 0, 12], 256, 1024, seed=47, a_fmt=a_fmt, b_fmt=b_fmt)
+    rng = np.random.default_rng(47)
+    _unit_magnitudes(p, a_fmt, rng)
+    p.a_scales[:] = rng.integers(top - 8, top + 1, p.a_scales.shape).astype(np.uint8)
+    p.b_scales[:] = rng.integers(20, 30, p.b_scales.shape).astype(np.uint8)
     _check_full(p)

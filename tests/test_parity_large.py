@@ -80,16 +80,6 @@ def test_cuda_graph_capture_and_replay(mode):
         assert bad == 0
 
 
-@pytest.mark.parametrize("a_fmt,b_fmt", [("mxfp8", "mxfp4"), ("mxfp4", "mxfp4"),
-                                         ("nvfp4", "nvfp4")])
-def test_fp4_formats_full_decode_shape(a_fmt, b_fmt):
-    # the decode workload's routing and shape (128 experts x U{1..32} rows, N=4096, K=7168)
-    # with fp4 operands, as the bench times it, checked on sampled outputs
-    p = gen.fmt_problem(gen.config_counts(4), 4096, 7168, seed=4, a_fmt=a_fmt, b_fmt=b_fmt,
-                        a_recipe="quantized")
-    _sampled(p, n_points=4000, seed=65)
-
-
 def test_fp4_long_k():
     # K = 65536 (512 K blocks of packed e2m1, 2048 nvfp4 scale codes per row)
     for a_fmt, b_fmt in (("mxfp8", "mxfp4"), ("nvfp4", "nvfp4")):

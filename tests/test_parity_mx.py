@@ -76,40 +76,3 @@ def test_invalid_offsets_reported_on_device():
     d.run()
     assert bsfp8.bsfp8_get_device_error() == 6
     assert np.all(d.c_bits() == d.sentinel)
-
-
-def test_decode_config_sampled():
-    """The full decode-shaped workload (128 experts x U{1..32} tokens, N=4096, K=7168)."""
-    from gpu_util import DeviceProblem
-    import block_scaled_fp8_persistent_gb300 as bsfp8
-    p = gen.config_problem(4)
-    d = DeviceProblem(p)
-    d.run()
-    got = d.c_bits()
-    assert bsfp8.bsfp8_get_device_error() == 0
-    rng = np.random.default_rng(4)
-    off = p.offsets.astype(np.int64)
-    rows_full = sorted({int(off[e]) for e in range(0, p.E, 9) if off[e + 1] > off[e]})
-    rows = np.concatenate([np.repeat(rows_full, p.N), rng.integers(0, p.M_total, 8000)])
-    cols = np.concatenate([np.tile(np.arange(p.N), len(rows_full)), rng.integers(0, p.N, 8000)])
-    ref, T = oracle.problem_points(p, rows, cols)
-    bad, ratio, _ = parity_report(got[rows, cols], ref, T)
-    assert bad == 0, f"{bad} sampled elements outside tolerance (max err/tol {ratio:.3g})"
-
-
-def test_dense_large_mx_sampled(monkeypatch):
-    """Dense 8192^3 MXFP8 (one expert), the CTA-pair kernel with overlapping accumulators."""
-    from gpu_util import DeviceProblem
-    import block_scaled_fp8_persistent_gb300 as bsfp8
-    monkeypatch.setenv("BSFP8_MX_KERNEL", "pair")
-    p = gen.config_problem(5)
-    d = DeviceProblem(p)
-    d.run()
-    got = d.c_bits()
-    assert bsfp8.bsfp8_get_device_error() == 0
-    rng = np.random.default_rng(5)
-    rows = np.concatenate([np.repeat([0, 255, 256, 8191], p.N), rng.integers(0, p.M_total, 6000)])
-    cols = np.concatenate([np.tile(np.arange(p.N), 4), rng.integers(0, p.N, 6000)])
-    ref, T = oracle.problem_points(p, rows, cols)
-    bad, ratio, _ = parity_report(got[rows, cols], ref, T)
-    assert bad == 0, f"{bad} sampled elements outside tolerance (max err/tol {ratio:.3g})"
