@@ -102,7 +102,6 @@ template <class C>
 struct Ctl {
   uint64_t full[C::STAGES];
   uint64_t empty[C::STAGES];
-  uint64_t tfull[C::ACC_STAGES];
   uint64_t tempty[C::ACC_STAGES];
   uint64_t mma_done;
   uint32_t tmem_base;
@@ -133,26 +132,19 @@ __device__ __forceinline__ void promote16(float2* acc, const uint32_t* p, float 
 }
 
 // Issue the MMAs of one K block: 4 x tcgen05.mma kind::f8f6f4 (K = 32 e4m3 each, 32 bytes
-// along the swizzled row) from operand stage `stage` into the TMEM partial `acc`, then
-// commit "operands consumed" to empty_bar and "partial ready" to tfull_bar.
+// along the swizzled row; the descriptors advance by 32 bytes >> 4) from an operand stage
+// into the TMEM partial at d_tmem, then one commit to the stage's empty barrier.  That
+// barrier completes when the K block's MMAs have finished: the producer waits on it to
+// refill the stage and the epilogue to read the partial.
 template <class C>
-__device__ __forceinline__ void issue_kblock(uint32_t tmem_base, uint32_t sA, uint32_t sB,
-                                             uint32_t stage, uint32_t acc, uint32_t empty_bar,
-                                             uint32_t tfull_bar) {
-  const uint32_t d_tmem = tmem_base + acc * C::BN;
-  const uint64_t adesc = kmajor_sw128_desc(sA + stage * C::A_STAGE);
-  const uint64_t bdesc = kmajor_sw128_desc(sB + stage * C::B_STAGE);
+__device__ __forceinline__ void issue_kblock(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                             uint32_t empty_bar) {
 #pragma unroll
   for (int k = 0; k < BK / 32; ++k)
     umma_f8f6f4<C::CG>(d_tmem, adesc + (uint64_t)(k * 2), bdesc + (uint64_t)(k * 2), C::IDESC,
                        k > 0 ? 1u : 0u);
-  if constexpr (C::CG == 1) {
-    umma_commit(empty_bar);
-    umma_commit(tfull_bar);
-  } else {
-    umma_commit_pair(empty_bar, 0x3);
-    umma_commit_pair(tfull_bar, 0x3);
-  }
+  if constexpr (C::CG == 1) umma_commit(empty_bar);
+  else umma_commit_pair(empty_bar, 0x3);
 }
 
 template <class C>
@@ -193,7 +185,6 @@ bsfp8_blockwise_kernel(const __grid_constant__ CUtensorMap tmA,
   const uint32_t sB = smem_u32(smem + C::SMEM_B);
   auto full_bar = [&](int s) { return smem_u32(&ctl->full[s]); };
   auto empty_bar = [&](int s) { return smem_u32(&ctl->empty[s]); };
-  auto tfull_bar = [&](int s) { return smem_u32(&ctl->tfull[s]); };
   auto tempty_bar = [&](int s) { return smem_u32(&ctl->tempty[s]); };
 
   if (warp == 0 && lane == 0) {
@@ -201,10 +192,9 @@ bsfp8_blockwise_kernel(const __grid_constant__ CUtensorMap tmA,
     tma_prefetch_desc(&tmB);
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(full_bar(s), 1);   // the leader's producer arrives (+ both CTAs' bytes)
-      mbar_init(empty_bar(s), 1);  // one MMA commit
+      mbar_init(empty_bar(s), 1);  // one MMA commit per K block
     }
     for (int s = 0; s < C::ACC_STAGES; ++s) {
-      mbar_init(tfull_bar(s), 1);                       // one MMA commit
       mbar_init(tempty_bar(s), C::NUM_EPI_WARPS * C::CG);  // every epilogue warp of the pair
     }
     mbar_init(smem_u32(&ctl->mma_done), 1);
@@ -223,9 +213,10 @@ bsfp8_blockwise_kernel(const __grid_constant__ CUtensorMap tmA,
   if (!C::is_epilogue(warp)) {
     // 128 rows: warpgroup 0 (producer, MMA issuer, two idle warps) gives registers away
     if constexpr (!C::SPARE_QUARTER) asm volatile("setmaxnreg.dec.sync.aligned.u32 40;");
-    if (warp == C::PRODUCER_WARP) {
+    if (warp == C::PRODUCER_WARP && lane == 0) {
       // =============================== TMA producer ===============================
-      // The whole warp runs the loop and its waits; one lane issues.
+      // The producer sleeps in its barrier waits (suspend-time hint): it shares its
+      // sub-partition with the MMA thread, whose issue slots set the pace.
       GroupedScheduler<C::BM, C::BN> sched;
       // B (expert weights) is re-read by every row tile of its expert, possibly in a later
       // wave of tiles: keep it in L2 ahead of the streaming A rows and C output.
@@ -239,27 +230,23 @@ bsfp8_blockwise_kernel(const __grid_constant__ CUtensorMap tmA,
         const int32_t a_row = (int32_t)(tc.m0 + C::ROWS * rank);
         const int32_t b_row = tc.be * args.N + tc.n0 + C::B_ROWS * rank;
         for (int kb = 0; kb < KB; ++kb) {
-          if (!__all_sync(0xffffffffu,
-                          mbar_wait_cg<C::CG>(empty_bar(stage), phase ^ 1, abort))) {
-            if (lane == 0) record_error(args.err, DEV_TIMEOUT, abort);
+          if (!mbar_wait_sleep(empty_bar(stage), phase ^ 1, abort)) {
+            record_error(args.err, DEV_TIMEOUT, abort);
             ok = false;
             break;
           }
-          if (lane == 0) {
-            if constexpr (C::CG == 1) {
-              mbar_arrive_expect_tx(full_bar(stage), C::STAGE_TX);
-              tma_load_2d(sA + stage * C::A_STAGE, &tmA, kb * BK, a_row, full_bar(stage));
-              tma_load_2d_hint(sB + stage * C::B_STAGE, &tmB, kb * BK, b_row, full_bar(stage),
-                               pol_b);
-            } else {
-              // both CTAs' bytes are counted on the leader's barrier
-              const uint32_t bar = mapa_shared(full_bar(stage), 0);
-              if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), C::STAGE_TX);
-              tma_load_2d_pair(sA + stage * C::A_STAGE, &tmA, kb * BK, a_row, bar);
-              tma_load_2d_pair_hint(sB + stage * C::B_STAGE, &tmB, kb * BK, b_row, bar, pol_b);
-            }
+          if constexpr (C::CG == 1) {
+            mbar_arrive_expect_tx(full_bar(stage), C::STAGE_TX);
+            tma_load_2d(sA + stage * C::A_STAGE, &tmA, kb * BK, a_row, full_bar(stage));
+            tma_load_2d_hint(sB + stage * C::B_STAGE, &tmB, kb * BK, b_row, full_bar(stage),
+                             pol_b);
+          } else {
+            // both CTAs' bytes are counted on the leader's barrier
+            const uint32_t bar = mapa_shared(full_bar(stage), 0);
+            if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), C::STAGE_TX);
+            tma_load_2d_pair(sA + stage * C::A_STAGE, &tmA, kb * BK, a_row, bar);
+            tma_load_2d_pair_hint(sB + stage * C::B_STAGE, &tmB, kb * BK, b_row, bar, pol_b);
           }
-          __syncwarp();
           ++issued;
           if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
         }
@@ -273,10 +260,13 @@ bsfp8_blockwise_kernel(const __grid_constant__ CUtensorMap tmA,
         if (rank == 0) mbar_wait_timed(full_bar(stage), phase);
         else mbar_wait_timed(empty_bar(stage), phase);
       }
-    } else if (warp == C::MMA_WARP && rank == 0) {
+    } else if (warp == C::MMA_WARP && lane == 0 && rank == 0) {
       // ================================ MMA issuer ================================
-      // The whole warp runs the loop and its waits; one lane issues.
+      // One thread, and the pace of the whole pipeline: per K block two barrier tests,
+      // four MMAs and one commit, with the descriptors of every stage precomputed.
       GroupedScheduler<C::BM, C::BN> sched;
+      const uint64_t adesc0 = kmajor_sw128_desc(sA);
+      const uint64_t bdesc0 = kmajor_sw128_desc(sB);
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
       TileCoord tc;
@@ -284,30 +274,25 @@ bsfp8_blockwise_kernel(const __grid_constant__ CUtensorMap tmA,
         if (!sched.locate(args, t, tc)) break;
         for (int kb = 0; kb < KB; ++kb) {
           // operands first: they are usually in place well before the TMEM stage is free
-          const bool got = mbar_wait_cg<C::CG>(full_bar(stage), phase, abort) &&
-                           mbar_wait_cg<C::CG>(tempty_bar(acc), acc_phase ^ 1, abort);
-          if (!__all_sync(0xffffffffu, got)) {
-            if (lane == 0) record_error(args.err, DEV_TIMEOUT, abort);
+          if (!mbar_wait_cg<C::CG>(full_bar(stage), phase, abort) ||
+              !mbar_wait_cg<C::CG>(tempty_bar(acc), acc_phase ^ 1, abort)) {
+            record_error(args.err, DEV_TIMEOUT, abort);
             ok = false;
             break;
           }
           tc_fence_after();
-          if (lane == 0)
-            issue_kblock<C>(tmem_base, sA, sB, stage, acc, empty_bar(stage), tfull_bar(acc));
-          __syncwarp();
+          issue_kblock<C>(tmem_base + acc * C::BN, adesc0 + ((stage * C::A_STAGE) >> 4),
+                          bdesc0 + ((stage * C::B_STAGE) >> 4), empty_bar(stage));
           if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
           if (++acc == C::ACC_STAGES) { acc = 0; acc_phase ^= 1; }
         }
       }
       // Every MMA this thread issued has finished before TMEM is released.  A wait that
       // gives up is reported and waited out once more (bounded) before the teardown.
-      if (lane == 0) {
-        if constexpr (C::CG == 1) umma_commit(smem_u32(&ctl->mma_done));
-        else umma_commit_pair(smem_u32(&ctl->mma_done), 0x1);
-      }
-      __syncwarp();
-      if (!__all_sync(0xffffffffu, mbar_wait_timed(smem_u32(&ctl->mma_done), 0))) {
-        if (lane == 0) record_error(args.err, DEV_TIMEOUT, abort);
+      if constexpr (C::CG == 1) umma_commit(smem_u32(&ctl->mma_done));
+      else umma_commit_pair(smem_u32(&ctl->mma_done), 0x1);
+      if (!mbar_wait_timed(smem_u32(&ctl->mma_done), 0)) {
+        record_error(args.err, DEV_TIMEOUT, abort);
         mbar_wait_timed(smem_u32(&ctl->mma_done), 0);
       }
     }
@@ -328,7 +313,8 @@ bsfp8_blockwise_kernel(const __grid_constant__ CUtensorMap tmA,
     GroupedScheduler<C::BM, C::BN> sched;
     // C rows go out as one 32-byte sector per lane when C allows it
     const bool c_vec32 = (reinterpret_cast<uintptr_t>(args.C) & 31) == 0;
-    uint32_t acc_stage = 0, acc_phase = 0;
+    uint32_t acc_stage = 0, acc_phase = 0;  // TMEM partial ring
+    uint32_t op_stage = 0, op_phase = 0;    // operand ring (its empty barriers)
     // This warp has finished reading TMEM stage acc_stage: tell the MMA thread (in the MMA
     // CTA of a pair).
     auto release_stage = [&]() {
@@ -372,8 +358,9 @@ bsfp8_blockwise_kernel(const __grid_constant__ CUtensorMap tmA,
           sbl_n = lo_in ? ldg_f32(sb_lo + kb + 1) : 0.0f;
           sbh_n = hi_in ? ldg_f32(sb_hi + kb + 1) : 0.0f;
         }
+        // the K block's MMAs are done when its operand stage's empty barrier completes
         const bool got = __all_sync(
-            0xffffffffu, mbar_wait_cg<C::CG>(tfull_bar(acc_stage), acc_phase, abort));
+            0xffffffffu, mbar_wait_cg<C::CG>(empty_bar(op_stage), op_phase, abort));
         if (!got) {
           if (lane == 0) record_error(args.err, DEV_TIMEOUT, abort);
           ok = false;
@@ -408,6 +395,7 @@ bsfp8_blockwise_kernel(const __grid_constant__ CUtensorMap tmA,
           }
         }
         if (++acc_stage == C::ACC_STAGES) { acc_stage = 0; acc_phase ^= 1; }
+        if (++op_stage == C::STAGES) { op_stage = 0; op_phase ^= 1; }
       }
       if (!ok) break;
       if (row < tc.m_end) {
@@ -489,6 +477,9 @@ using Pair128 = Cfg<2, 128, 8, 4>;
 using Cta1x128 = Cfg<1, 128, 6, 4>;
 using Cta1x96x256 = Cfg<1, 256, 4, 2, 96>;
 using Pair192x256 = Cfg<2, 256, 6, 2, 96>;
+using Cta1x96x192 = Cfg<1, 192, 5, 2, 96>;
+using Pair192x192 = Cfg<2, 192, 7, 2, 96>;
+using Cta1x128x192 = Cfg<1, 192, 5, 2, 128>;
 
 }  // namespace bw
 
@@ -501,6 +492,9 @@ int blockwise_b_rows(BlockwiseTile tile) {
     case TILE_CTA1_128: return bw::Cta1x128::B_ROWS;
     case TILE_CTA1_96: return bw::Cta1x96x256::B_ROWS;
     case TILE_PAIR_192: return bw::Pair192x256::B_ROWS;
+    case TILE_CTA1_96x192: return bw::Cta1x96x192::B_ROWS;
+    case TILE_PAIR_192x192: return bw::Pair192x192::B_ROWS;
+    case TILE_CTA1_128x192: return bw::Cta1x128x192::B_ROWS;
   }
   return 0;
 }
@@ -509,6 +503,8 @@ int blockwise_a_rows(BlockwiseTile tile) {
   switch (tile) {
     case TILE_CTA1_96: return bw::Cta1x96x256::ROWS;
     case TILE_PAIR_192: return bw::Pair192x256::ROWS;
+    case TILE_CTA1_96x192: return bw::Cta1x96x192::ROWS;
+    case TILE_PAIR_192x192: return bw::Pair192x192::ROWS;
     default: return 128;
   }
 }
@@ -524,6 +520,9 @@ cudaError_t launch_bsfp8_blockwise(BlockwiseTile tile, const CUtensorMap& tmA,
     case TILE_CTA1_128: return bw::launch<bw::Cta1x128>(tmA, tmB, args, num_sms, stream);
     case TILE_CTA1_96: return bw::launch<bw::Cta1x96x256>(tmA, tmB, args, num_sms, stream);
     case TILE_PAIR_192: return bw::launch<bw::Pair192x256>(tmA, tmB, args, num_sms, stream);
+    case TILE_CTA1_96x192: return bw::launch<bw::Cta1x96x192>(tmA, tmB, args, num_sms, stream);
+    case TILE_PAIR_192x192: return bw::launch<bw::Pair192x192>(tmA, tmB, args, num_sms, stream);
+    case TILE_CTA1_128x192: return bw::launch<bw::Cta1x128x192>(tmA, tmB, args, num_sms, stream);
   }
   return cudaErrorInvalidValue;
 }

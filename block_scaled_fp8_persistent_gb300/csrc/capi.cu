@@ -149,6 +149,9 @@ BlockwiseTile choose_blockwise_tile(int64_t M_total, int N, int E, int num_sms) 
     if (!std::strcmp(v, "cta1_128")) return TILE_CTA1_128;
     if (!std::strcmp(v, "cta1_96")) return TILE_CTA1_96;
     if (!std::strcmp(v, "pair_192")) return TILE_PAIR_192;
+    if (!std::strcmp(v, "cta1_96x192")) return TILE_CTA1_96x192;
+    if (!std::strcmp(v, "pair_192x192")) return TILE_PAIR_192x192;
+    if (!std::strcmp(v, "cta1_128x192")) return TILE_CTA1_128x192;
   }
   const double single = blockwise_makespan(M_total, N, E, 96, num_sms);
   const double pair = blockwise_makespan(M_total, N, E, 192, num_sms / 2) * kPairTileTime;
@@ -391,7 +394,7 @@ extern "C" bsfp8_status bsfp8_blockwise_plan(int64_t M_total, int N, int num_exp
     return BSFP8_ERR_SHAPE;
   const BlockwiseTile tile = choose_blockwise_tile(M_total, N, num_experts, num_sms);
   const int ctas = (tile == TILE_PAIR_256 || tile == TILE_PAIR_160 || tile == TILE_PAIR_128 ||
-                    tile == TILE_PAIR_192) ? 2 : 1;
+                    tile == TILE_PAIR_192 || tile == TILE_PAIR_192x192) ? 2 : 1;
   out[0] = blockwise_a_rows(tile) * ctas;
   out[1] = blockwise_b_rows(tile) * ctas;
   out[2] = ctas;

@@ -41,6 +41,9 @@ enum BlockwiseTile : int {
   TILE_CTA1_128 = 4,  // one CTA, 128 x 128 tile, 4-deep TMEM ring
   TILE_CTA1_96 = 5,   // one CTA, 96 x 256 tile, role warps on the spare TMEM sub-partition
   TILE_PAIR_192 = 6,  // CTA pair, 192 x 256 tile, the same per CTA
+  TILE_CTA1_96x192 = 7,   // one CTA, 96 x 192 tile: each epilogue warp drains its 96 columns at once
+  TILE_PAIR_192x192 = 8,  // CTA pair, 192 x 192 tile, the same per CTA
+  TILE_CTA1_128x192 = 9,  // one CTA, 128 x 192 tile (12 warps)
 };
 
 // Rows of B each CTA loads per stage (the B tensor map's box height) for a tile config.

@@ -55,7 +55,8 @@ def test_default_is_smaller_estimated_makespan(M, N, E):
 @pytest.mark.parametrize("name,rows,cols,ctas", [
     ("cta1_256", 128, 256, 1), ("pair_256", 256, 256, 2), ("pair_160", 256, 160, 2),
     ("pair_128", 256, 128, 2), ("cta1_128", 128, 128, 1), ("cta1_96", 96, 256, 1),
-    ("pair_192", 192, 256, 2)])
+    ("pair_192", 192, 256, 2), ("cta1_96x192", 96, 192, 1), ("pair_192x192", 192, 192, 2),
+    ("cta1_128x192", 128, 192, 1)])
 def test_environment_override(monkeypatch, name, rows, cols, ctas):
     monkeypatch.setenv("BSFP8_BLOCKWISE_TILE", name)
     assert plan(4096, 4096, 8) == {"tile_rows": rows, "tile_cols": cols, "ctas_per_tile": ctas}

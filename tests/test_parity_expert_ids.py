@@ -12,7 +12,7 @@ from helpers import parity_report
 
 pytestmark = pytest.mark.gpu
 
-BLOCKWISE_TILES = ["cta1_96", "pair_192", "cta1_256", "pair_256"]
+BLOCKWISE_TILES = ["cta1_96", "pair_192", "cta1_256", "pair_256", "cta1_96x192", "pair_192x192"]
 MX_FORMS = ["swap32", "swap128", "pair"]
 
 
