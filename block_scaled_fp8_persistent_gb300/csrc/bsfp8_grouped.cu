@@ -40,12 +40,13 @@
 // the TMA completions of both CTAs are counted on the leader's barrier, and the leader's
 // commits arrive on both CTAs' barriers.  Each CTA promotes and stores its own 128 rows.
 //
-// A and B scales reach the epilogue through the read-only cache one K block ahead, and the
-// A scales' lines are prefetched into L1 SCALE_LOOKAHEAD K blocks ahead.  a_scales is
-// [K/128, M_total], so every K block touches a new line per 32 rows; without the L1
-// prefetch the one-ahead load often missed to DRAM and stalled both warps of that TMEM
-// lane quarter at the sa * sb multiply for 300-1300 cycles, holding up the release of the
-// TMEM stage (B scales of consecutive K blocks share a line and hit L1).
+// A and B scales reach the epilogue through the read-only cache two K blocks ahead of their
+// use, and the A scales' lines are prefetched into L1 SCALE_LOOKAHEAD K blocks ahead.
+// a_scales is [K/128, M_total], so every K block touches a new line per 32 rows; loads issued
+// one K block ahead, or without the L1 prefetch, left the epilogue warps waiting on them.
+// With 256-column tiles each epilogue warp's 128 columns lie in one 128-column B-scale block,
+// so it needs one B scale per K block (and the registers of a second one go to the loads
+// in flight).
 #include <atomic>
 #include <cuda_bf16.h>
 #include "common.cuh"
@@ -80,6 +81,8 @@ struct Cfg {
   static constexpr uint32_t A_STAGE = 128 * BK;  // the MMA reads 128 rows per CTA
   static constexpr uint32_t B_STAGE = B_ROWS * BK;
   static constexpr uint32_t STAGE_TX = (ROWS * BK + B_STAGE) * CG;  // bytes loaded, pair
+  // each epilogue warp's columns lie in one 128-column B-scale block (one B scale per K block)
+  static constexpr bool ONE_BLOCK = COLS == 128 && BN % 256 == 0;
   static constexpr int SCALE_LOOKAHEAD = 6;  // K blocks of A-scale L1 prefetch
   static constexpr uint32_t SMEM_A = 0;
   static constexpr uint32_t SMEM_B = SMEM_A + STAGES * A_STAGE;
@@ -92,6 +95,15 @@ struct Cfg {
   __device__ static uint32_t column_half(uint32_t warp) {
     return SPARE_QUARTER ? warp >> 2 : (warp - 4) >> 2;
   }
+  // One CTA with 128 rows: every sub-partition hosts two epilogue warps, so the producer and
+  // MMA work is split four ways instead of sitting on one of them: warp j of warpgroup 0
+  // owns operand stage j (K blocks kb with kb % 4 == j), loads it and issues its MMAs.
+  static constexpr bool ROLE4 = !SPARE_QUARTER && CG == 1;
+  // TMEM-stage release barriers: one per K block mod 4 with ROLE4 (each has a single waiter,
+  // which sees its phases in order), else one per TMEM stage
+  static constexpr int N_TEMPTY = ROLE4 ? 4 : ACC_STAGES;
+  static_assert(!ROLE4 || (STAGES == 4 && ACC_STAGES <= 4 && 4 % ACC_STAGES == 0),
+                "four role warps own one operand stage each");
   static_assert(ACC_STAGES * BN <= (int)TMEM_COLS, "TMEM ring too large");
   static_assert(COLS % 16 == 0 && BN % 16 == 0 && B_ROWS % 8 == 0, "tile shape");
   static_assert(LOAD_ALL || COLS % 64 == 0, "two-phase epilogue works in 64-column halves");
@@ -102,7 +114,7 @@ template <class C>
 struct Ctl {
   uint64_t full[C::STAGES];
   uint64_t empty[C::STAGES];
-  uint64_t tempty[C::ACC_STAGES];
+  uint64_t tempty[C::N_TEMPTY];
   uint64_t mma_done;
   uint32_t tmem_base;
   int abort;
@@ -194,7 +206,7 @@ bsfp8_blockwise_kernel(const __grid_constant__ CUtensorMap tmA,
       mbar_init(full_bar(s), 1);   // the leader's producer arrives (+ both CTAs' bytes)
       mbar_init(empty_bar(s), 1);  // one MMA commit per K block
     }
-    for (int s = 0; s < C::ACC_STAGES; ++s) {
+    for (int s = 0; s < C::N_TEMPTY; ++s) {
       mbar_init(tempty_bar(s), C::NUM_EPI_WARPS * C::CG);  // every epilogue warp of the pair
     }
     mbar_init(smem_u32(&ctl->mma_done), 1);
@@ -213,7 +225,56 @@ bsfp8_blockwise_kernel(const __grid_constant__ CUtensorMap tmA,
   if (!C::is_epilogue(warp)) {
     // 128 rows: warpgroup 0 (producer, MMA issuer, two idle warps) gives registers away
     if constexpr (!C::SPARE_QUARTER) asm volatile("setmaxnreg.dec.sync.aligned.u32 40;");
-    if (warp == C::PRODUCER_WARP && lane == 0) {
+    if (C::ROLE4 && lane == 0) {
+      // ======================= stage owner j = warp (0..3) =======================
+      // K blocks g = j, j + 4, ... (counted over this CTA's tiles): wait for the stage's
+      // previous MMAs, load A and B into it, wait for the bytes, wait for the TMEM stage
+      // (the epilogue's release of K block g - ACC_STAGES), issue 4 MMAs, commit to the
+      // stage's empty barrier.  Waits sleep (suspend-time hint): the sub-partition is shared
+      // with two epilogue warps.
+      const uint32_t j = warp;
+      GroupedScheduler<C::BM, C::BN> sched;
+      const uint64_t pol_b = l2_policy_evict_last();
+      const uint64_t adesc = kmajor_sw128_desc(sA + j * C::A_STAGE);
+      const uint64_t bdesc = kmajor_sw128_desc(sB + j * C::B_STAGE);
+      int64_t g = 0;
+      uint32_t u = 0;  // uses of stage j so far
+      bool ok = true;
+      TileCoord tc;
+      for (int64_t t = tile0; ok && t < total_tiles; t += tile_stride) {
+        if (!sched.locate(args, t, tc)) break;
+        const int32_t a_row = (int32_t)tc.m0;
+        const int32_t b_row = tc.be * args.N + tc.n0;
+        // this tile's K blocks with g % 4 == j
+        for (int kb = (int)((j - (uint32_t)(g & 3)) & 3); kb < KB; kb += 4) {
+          const int64_t gk = g + kb;
+          bool w = mbar_wait_sleep(empty_bar(j), (u & 1) ^ 1, abort);
+          if (w) {
+            mbar_arrive_expect_tx(full_bar(j), C::STAGE_TX);
+            tma_load_2d(sA + j * C::A_STAGE, &tmA, kb * BK, a_row, full_bar(j));
+            tma_load_2d_hint(sB + j * C::B_STAGE, &tmB, kb * BK, b_row, full_bar(j), pol_b);
+            w = mbar_wait_sleep(full_bar(j), u & 1, abort);
+          }
+          const int64_t gr = gk - C::ACC_STAGES;  // its TMEM stage's previous K block
+          if (w && gr >= 0) w = mbar_wait_sleep(tempty_bar((int)(gr & 3)), (uint32_t)(gr >> 2) & 1, abort);
+          if (!w) {
+            record_error(args.err, DEV_TIMEOUT, abort);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          issue_kblock<C>(tmem_base + (uint32_t)(gk % C::ACC_STAGES) * C::BN, adesc, bdesc,
+                          empty_bar(j));
+          ++u;
+        }
+        g += KB;
+      }
+      // the stage's last MMAs have finished before TMEM is released (bounded, reported)
+      if (u > 0 && !mbar_wait_timed(empty_bar(j), (u - 1) & 1)) {
+        record_error(args.err, DEV_TIMEOUT, abort);
+        mbar_wait_timed(empty_bar(j), (u - 1) & 1);
+      }
+    } else if (!C::ROLE4 && warp == C::PRODUCER_WARP && lane == 0) {
       // =============================== TMA producer ===============================
       // The producer sleeps in its barrier waits (suspend-time hint): it shares its
       // sub-partition with the MMA thread, whose issue slots set the pace.
@@ -260,7 +321,7 @@ bsfp8_blockwise_kernel(const __grid_constant__ CUtensorMap tmA,
         if (rank == 0) mbar_wait_timed(full_bar(stage), phase);
         else mbar_wait_timed(empty_bar(stage), phase);
       }
-    } else if (warp == C::MMA_WARP && lane == 0 && rank == 0) {
+    } else if (!C::ROLE4 && warp == C::MMA_WARP && lane == 0 && rank == 0) {
       // ================================ MMA issuer ================================
       // One thread, and the pace of the whole pipeline: per K block two barrier tests,
       // four MMAs and one commit, with the descriptors of every stage precomputed.
@@ -315,12 +376,14 @@ bsfp8_blockwise_kernel(const __grid_constant__ CUtensorMap tmA,
     const bool c_vec32 = (reinterpret_cast<uintptr_t>(args.C) & 31) == 0;
     uint32_t acc_stage = 0, acc_phase = 0;  // TMEM partial ring
     uint32_t op_stage = 0, op_phase = 0;    // operand ring (its empty barriers)
+    uint32_t rel = 0;                       // K blocks released so far (ROLE4: barrier rel % 4)
     // This warp has finished reading TMEM stage acc_stage: tell the MMA thread (in the MMA
     // CTA of a pair).
     auto release_stage = [&]() {
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive_cluster_or_local<C::CG>(tempty_mma(acc_stage));
+      if (lane == 0)
+        mbar_arrive_cluster_or_local<C::CG>(tempty_mma(C::ROLE4 ? (int)(rel & 3) : (int)acc_stage));
     };
     bool ok = true;
     TileCoord tc;
@@ -332,31 +395,41 @@ bsfp8_blockwise_kernel(const __grid_constant__ CUtensorMap tmA,
       // this warp's columns touch scale blocks col0/128 and (col0+COLS-1)/128 (<= 2)
       const int blk_lo = col0 / 128;
       const int blk_hi = (col0 + C::COLS - 1) / 128;
-      const bool lo_in = blk_lo < nblk, hi_in = blk_hi < nblk;
-      const float* sa_ptr = a_scales + (row_in ? row : 0);
+      const bool lo_in = blk_lo < nblk, hi_in = !C::ONE_BLOCK && blk_hi < nblk;
       // the group's expert, re-read per tile (kept out of the scheduler's live registers)
       const int64_t be = args.expert_ids ? ldg_s32(args.expert_ids + tc.e) : tc.e;
+      // Scales: loaded two K blocks ahead of their use, a_scales[kb, row] (one load per lane,
+      // consecutive K blocks M_total apart, their lines prefetched into L1 SCALE_LOOKAHEAD K
+      // blocks ahead) and b_scales[be, blk, kb] (uniform per warp).
+      const float* sa_ptr = a_scales + (row_in ? row : 0);
       const float* sb_lo = b_scales + (be * nblk + (lo_in ? blk_lo : 0)) * KB;
       const float* sb_hi = b_scales + (be * nblk + (hi_in ? blk_hi : 0)) * KB;
       float2 acc[C::COLS / 2];  // columns 2j, 2j+1
 #pragma unroll
       for (int j = 0; j < C::COLS / 2; ++j) acc[j] = make_float2(0.0f, 0.0f);
       if (row_in) {
-        for (int k = 1; k < C::SCALE_LOOKAHEAD && k < KB; ++k)
+        for (int k = 2; k < C::SCALE_LOOKAHEAD && k < KB; ++k)
           prefetch_l1(sa_ptr + (int64_t)k * args.M_total);
       }
+      // K block kb's values (sa_n, sbl_n, sbh_n) and K block kb + 1's (sa_2, ...)
       float sa_n = row_in ? ldg_f32(sa_ptr) : 0.0f;
       float sbl_n = lo_in ? ldg_f32(sb_lo) : 0.0f;
-      float sbh_n = hi_in ? ldg_f32(sb_hi) : 0.0f;
+      float sbh_n = (!C::ONE_BLOCK && hi_in) ? ldg_f32(sb_hi) : 0.0f;
+      float sa_2 = (row_in && KB > 1) ? ldg_f32(sa_ptr + args.M_total) : 0.0f;
+      float sbl_2 = (lo_in && KB > 1) ? ldg_f32(sb_lo + 1) : 0.0f;
+      float sbh_2 = (!C::ONE_BLOCK && hi_in && KB > 1) ? ldg_f32(sb_hi + 1) : 0.0f;
       for (int kb = 0; kb < KB; ++kb) {
         const float s_lo = sa_n * sbl_n;
-        const float s_hi = sa_n * sbh_n;
+        const float s_hi = C::ONE_BLOCK ? s_lo : sa_n * sbh_n;
+        sa_n = sa_2;
+        sbl_n = sbl_2;
+        sbh_n = sbh_2;
         if (row_in && kb + C::SCALE_LOOKAHEAD < KB)
           prefetch_l1(sa_ptr + (int64_t)(kb + C::SCALE_LOOKAHEAD) * args.M_total);
-        if (kb + 1 < KB) {
-          sa_n = row_in ? ldg_f32(sa_ptr + (int64_t)(kb + 1) * args.M_total) : 0.0f;
-          sbl_n = lo_in ? ldg_f32(sb_lo + kb + 1) : 0.0f;
-          sbh_n = hi_in ? ldg_f32(sb_hi + kb + 1) : 0.0f;
+        if (kb + 2 < KB) {
+          sa_2 = row_in ? ldg_f32(sa_ptr + (int64_t)(kb + 2) * args.M_total) : 0.0f;
+          sbl_2 = lo_in ? ldg_f32(sb_lo + kb + 2) : 0.0f;
+          if constexpr (!C::ONE_BLOCK) sbh_2 = hi_in ? ldg_f32(sb_hi + kb + 2) : 0.0f;
         }
         // the K block's MMAs are done when its operand stage's empty barrier completes
         const bool got = __all_sync(
@@ -396,6 +469,7 @@ bsfp8_blockwise_kernel(const __grid_constant__ CUtensorMap tmA,
         }
         if (++acc_stage == C::ACC_STAGES) { acc_stage = 0; acc_phase ^= 1; }
         if (++op_stage == C::STAGES) { op_stage = 0; op_phase ^= 1; }
+        ++rel;
       }
       if (!ok) break;
       if (row < tc.m_end) {
@@ -474,12 +548,12 @@ using Cta1x256 = Cfg<1, 256, 4, 2>;
 using Pair256 = Cfg<2, 256, 6, 2>;
 using Pair160 = Cfg<2, 160, 8, 3>;
 using Pair128 = Cfg<2, 128, 8, 4>;
-using Cta1x128 = Cfg<1, 128, 6, 4>;
+using Cta1x128 = Cfg<1, 128, 4, 4>;
 using Cta1x96x256 = Cfg<1, 256, 4, 2, 96>;
 using Pair192x256 = Cfg<2, 256, 6, 2, 96>;
 using Cta1x96x192 = Cfg<1, 192, 5, 2, 96>;
 using Pair192x192 = Cfg<2, 192, 7, 2, 96>;
-using Cta1x128x192 = Cfg<1, 192, 5, 2, 128>;
+using Cta1x128x192 = Cfg<1, 192, 4, 2, 128>;
 
 }  // namespace bw
 
