@@ -14,31 +14,36 @@
 //  * Triton Gluon example "Overlapping Accumulator Block-Scaled Matrix Multiplication":
 //    load / MMA / epilogue partitions, persistent static tile stride, 2-CTA tiles.
 //
-// Roles with 128 A rows per CTA (12 warps):
-//   warp 0       TMA producer: per K block, this CTA's A rows [128 x 128] and its share of
-//                B rows [BN/CG x 128] (e4m3, 128-byte swizzle) into a STAGES-deep ring.
-//   warp 1       TMEM owner; in the MMA CTA (rank 0 of the pair) the single issuing thread:
-//                per K block 4 x tcgen05.mma kind::f8f6f4 (K = 32 each) into a fresh TMEM
-//                partial (ACC_STAGES-deep ring of BN columns).
-//   warps 4-11   epilogue: warp w reads TMEM lanes 32*(w%4).. (rows) and columns
-//                (BN/2)*((w-4)/4).. ; per K block it loads its partial, hands the TMEM stage
-//                back, and promotes acc = fma(sa*sb, partial, acc) in registers.  After the
-//                last K block it rounds to bf16 and stores the rows of the tile's expert.
+// Roles with 96 A rows per CTA (8 warps, the layouts the planner picks).  The M = 128 MMA
+// computes TMEM lanes 96..127 from shared-memory rows that nobody reads.  A warp can only
+// read the TMEM lanes of its own SM sub-partition (lanes 32*(w%4)..), so the sub-partition
+// of lanes 96..127 is free for the roles:
+//   warp 3       TMA producer: per K block, A rows [rows x 128] and this CTA's share of B
+//                rows [BN/CG x 128] (e4m3, 128-byte swizzle) into a STAGES-deep ring.
+//   warp 7       TMEM owner; in the MMA CTA (rank 0 of a pair) the single issuing thread: per
+//                K block 4 x tcgen05.mma kind::f8f6f4 (K = 32 each) into a fresh TMEM partial
+//                (ACC_STAGES-deep ring of BN columns), then one commit to the stage's empty
+//                barrier, which both the producer and the epilogue wait on.
+//   warps 0-2,   epilogue: warp w reads TMEM lanes 32*(w%4).. (rows) and columns
+//   4-6          (BN/2)*(w/4).. ; per K block it loads its partial, hands the TMEM stage back
+//                and promotes acc = fma(sa*sb, partial, acc) in registers.  After the last K
+//                block it rounds to bf16 and stores the rows of the tile's expert.
+// A sub-partition that issues TMA loads or tcgen05.mma next to epilogue warps slows those
+// warps down about twofold (clock64 traces: every step of their K-block loop, not one wait),
+// so no epilogue warp shares a sub-partition with a role; a quarter of each single-CTA MMA
+// is the price.  The 128-row single-CTA layouts (12 warps: warps 0-3 each own one operand
+// stage, load it and issue its MMAs; warps 4-11 epilogue) stay selectable and parity-tested
+// but run ~1.4x slower per tile.
 //
-// With 96 A rows per CTA (8 warps) the M = 128 MMA computes TMEM lanes 96..127 from
-// shared-memory rows that are never loaded, and nobody reads them.  A warp can only read
-// the TMEM lanes of its own SM sub-partition (lanes 32*(w%4)..), so the sub-partition of
-// lanes 96..127 is free: warp 3 is the producer and warp 7 the TMEM owner / MMA issuer,
-// and warps 0-2 and 4-6 are the epilogue (columns (BN/2)*(w/4)..).  The role warps' barrier
-// polling and TMA / MMA issue then share no SMSP with a warp that drains a TMEM stage.
-// Measured on the 128-row layout, epilogue warps on the role warps' SMSPs see each
-// TMEM-full barrier 500-1000 cycles after the others, which with two TMEM stages stalls
-// the tensor core every K block; a quarter of the MMA work is the price of removing that.
-//
-// CG = 2 runs a CTA pair (cluster of 2) on a 256 x BN tile: each CTA loads its own 128 A
-// rows and half of the B rows (no multicast), the pair MMA (M = 256) reads both halves,
-// the TMA completions of both CTAs are counted on the leader's barrier, and the leader's
-// commits arrive on both CTAs' barriers.  Each CTA promotes and stores its own 128 rows.
+// CG = 2 runs a CTA pair (cluster of 2) with the pair MMA (M = 256): each CTA's TMEM holds
+// its 128 rows x BN columns; B is split between the CTAs; the TMA completions of both CTAs
+// are counted on the leader's barrier and the leader's commits arrive on both CTAs'
+// barriers.  Each CTA promotes and stores its own rows.  Symmetric pairs run the 96-row
+// layout in both CTAs (192-row tiles).  The asymmetric pair (PEER_ROWS = 128) uses all 128
+// MMA rows of the peer: the leader keeps the 96-row layout and its producer also loads the
+// peer's A rows and half of B, by TMA multicast to the peer alone with the bytes counted on
+// the leader's barrier, so the peer runs epilogue warps only (224-row tiles, 87.5 % of the
+// MMA rows useful).
 //
 // A and B scales reach the epilogue through the read-only cache two K blocks ahead of their
 // use, and the A scales' lines are prefetched into L1 SCALE_LOOKAHEAD K blocks ahead.
@@ -59,17 +64,23 @@ namespace bw {
 constexpr int BK = 128;
 constexpr uint32_t TMEM_COLS = 512;
 
-template <int CG_, int BN_, int STAGES_, int ACC_STAGES_, int ROWS_ = 128>
+template <int CG_, int BN_, int STAGES_, int ACC_STAGES_, int ROWS_ = 128, int PEER_ROWS_ = ROWS_>
 struct Cfg {
   static constexpr int CG = CG_;                  // CTAs per tile (1 or 2)
   static constexpr int BN = BN_;                  // tile columns
   static constexpr int ROWS = ROWS_;              // A rows per CTA (128, or 96: see above)
-  static constexpr int BM = ROWS * CG;            // tile rows
+  // Asymmetric pair: a 96-row leader whose spare sub-partition hosts the producer and the
+  // MMA issuer, and a 128-row peer that runs epilogue warps only; the leader's producer
+  // loads the peer's operands (multicast to the peer alone, bytes counted on the leader).
+  static constexpr int PEER_ROWS = PEER_ROWS_;    // A rows of the pair's second CTA
+  static constexpr bool ASYM = CG_ == 2 && PEER_ROWS_ != ROWS_;
+  static constexpr int BM = CG == 2 ? ROWS + PEER_ROWS : ROWS;  // tile rows
   static constexpr bool SPARE_QUARTER = ROWS == 96;  // TMEM lanes 96..127 unused
   static constexpr int THREADS = SPARE_QUARTER ? 256 : 384;
   static constexpr int PRODUCER_WARP = SPARE_QUARTER ? 3 : 0;
   static constexpr int MMA_WARP = SPARE_QUARTER ? 7 : 1;  // also allocates TMEM
-  static constexpr int NUM_EPI_WARPS = SPARE_QUARTER ? 6 : 8;
+  static constexpr int NUM_EPI_WARPS = SPARE_QUARTER ? 6 : 8;  // (the leader's, with ASYM)
+  static constexpr int PAIR_EPI_WARPS = ASYM ? NUM_EPI_WARPS + 8 : NUM_EPI_WARPS * CG;
   static constexpr int STAGES = STAGES_;          // SMEM ring depth
   static constexpr int ACC_STAGES = ACC_STAGES_;  // TMEM partial ring depth
   static constexpr int B_ROWS = BN / CG;          // B rows loaded by each CTA
@@ -80,7 +91,8 @@ struct Cfg {
   static constexpr bool LOAD_ALL = COLS <= 96;
   static constexpr uint32_t A_STAGE = 128 * BK;  // the MMA reads 128 rows per CTA
   static constexpr uint32_t B_STAGE = B_ROWS * BK;
-  static constexpr uint32_t STAGE_TX = (ROWS * BK + B_STAGE) * CG;  // bytes loaded, pair
+  static constexpr int A_BOX = ASYM ? 128 : ROWS;  // A rows per TMA box
+  static constexpr uint32_t STAGE_TX = (A_BOX * BK + B_STAGE) * CG;  // bytes loaded, pair
   // each epilogue warp's columns lie in one 128-column B-scale block (one B scale per K block)
   static constexpr bool ONE_BLOCK = COLS == 128 && BN % 256 == 0;
   static constexpr int SCALE_LOOKAHEAD = 6;  // K blocks of A-scale L1 prefetch
@@ -89,6 +101,7 @@ struct Cfg {
   static constexpr uint32_t SMEM_CTL = SMEM_B + STAGES * B_STAGE;
   static constexpr uint32_t IDESC = idesc_f8f6f4_e4m3(128 * CG, BN);
   static_assert(ROWS == 128 || ROWS == 96, "A rows per CTA");
+  static_assert(!ASYM || (ROWS == 96 && PEER_ROWS == 128), "asymmetric pair: 96 + 128 rows");
   __device__ static bool is_epilogue(uint32_t warp) {
     return SPARE_QUARTER ? (warp & 3) != 3 : warp >= 4;
   }
@@ -207,7 +220,7 @@ bsfp8_blockwise_kernel(const __grid_constant__ CUtensorMap tmA,
       mbar_init(empty_bar(s), 1);  // one MMA commit per K block
     }
     for (int s = 0; s < C::N_TEMPTY; ++s) {
-      mbar_init(tempty_bar(s), C::NUM_EPI_WARPS * C::CG);  // every epilogue warp of the pair
+      mbar_init(tempty_bar(s), C::PAIR_EPI_WARPS);  // every epilogue warp of the pair
     }
     mbar_init(smem_u32(&ctl->mma_done), 1);
     fence_mbarrier_init();
@@ -222,7 +235,9 @@ bsfp8_blockwise_kernel(const __grid_constant__ CUtensorMap tmA,
   tc_fence_after();
   const uint32_t tmem_base = ctl->tmem_base;
 
-  if (!C::is_epilogue(warp)) {
+  // the asymmetric pair's peer runs epilogue warps only
+  const bool all_epilogue = C::ASYM && rank == 1;
+  if (!all_epilogue && !C::is_epilogue(warp)) {
     // 128 rows: warpgroup 0 (producer, MMA issuer, two idle warps) gives registers away
     if constexpr (!C::SPARE_QUARTER) asm volatile("setmaxnreg.dec.sync.aligned.u32 40;");
     if (C::ROLE4 && lane == 0) {
@@ -307,6 +322,14 @@ bsfp8_blockwise_kernel(const __grid_constant__ CUtensorMap tmA,
             if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), C::STAGE_TX);
             tma_load_2d_pair(sA + stage * C::A_STAGE, &tmA, kb * BK, a_row, bar);
             tma_load_2d_pair_hint(sB + stage * C::B_STAGE, &tmB, kb * BK, b_row, bar, pol_b);
+            if constexpr (C::ASYM) {
+              // the peer's A rows (after the leader's ROWS) and its half of B, into the peer's
+              // shared memory at the same offsets, counted on this barrier
+              tma_load_2d_mc_pair_hint(sA + stage * C::A_STAGE, &tmA, kb * BK, a_row + C::ROWS,
+                                       full_bar(stage), 0x2, pol_b);
+              tma_load_2d_mc_pair_hint(sB + stage * C::B_STAGE, &tmB, kb * BK, b_row + C::B_ROWS,
+                                       full_bar(stage), 0x2, pol_b);
+            }
           }
           ++issued;
           if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
@@ -554,6 +577,7 @@ using Pair192x256 = Cfg<2, 256, 6, 2, 96>;
 using Cta1x96x192 = Cfg<1, 192, 5, 2, 96>;
 using Pair192x192 = Cfg<2, 192, 7, 2, 96>;
 using Cta1x128x192 = Cfg<1, 192, 4, 2, 128>;
+using Pair224x256 = Cfg<2, 256, 6, 2, 96, 128>;
 
 }  // namespace bw
 
@@ -569,6 +593,7 @@ int blockwise_b_rows(BlockwiseTile tile) {
     case TILE_CTA1_96x192: return bw::Cta1x96x192::B_ROWS;
     case TILE_PAIR_192x192: return bw::Pair192x192::B_ROWS;
     case TILE_CTA1_128x192: return bw::Cta1x128x192::B_ROWS;
+    case TILE_PAIR_224: return bw::Pair224x256::B_ROWS;
   }
   return 0;
 }
@@ -579,6 +604,7 @@ int blockwise_a_rows(BlockwiseTile tile) {
     case TILE_PAIR_192: return bw::Pair192x256::ROWS;
     case TILE_CTA1_96x192: return bw::Cta1x96x192::ROWS;
     case TILE_PAIR_192x192: return bw::Pair192x192::ROWS;
+    case TILE_PAIR_224: return bw::Pair224x256::A_BOX;
     default: return 128;
   }
 }
@@ -597,6 +623,7 @@ cudaError_t launch_bsfp8_blockwise(BlockwiseTile tile, const CUtensorMap& tmA,
     case TILE_CTA1_96x192: return bw::launch<bw::Cta1x96x192>(tmA, tmB, args, num_sms, stream);
     case TILE_PAIR_192x192: return bw::launch<bw::Pair192x192>(tmA, tmB, args, num_sms, stream);
     case TILE_CTA1_128x192: return bw::launch<bw::Cta1x128x192>(tmA, tmB, args, num_sms, stream);
+    case TILE_PAIR_224: return bw::launch<bw::Pair224x256>(tmA, tmB, args, num_sms, stream);
   }
   return cudaErrorInvalidValue;
 }

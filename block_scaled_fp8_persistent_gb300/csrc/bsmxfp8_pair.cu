@@ -254,6 +254,9 @@ bsmxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     // scales from each CTA's own TMEM).  Announced on the MMA CTA's full barrier.
     const uint8_t* a_sc = static_cast<const uint8_t*>(args.a_scales);
     const uint8_t* b_sc = static_cast<const uint8_t*>(args.b_scales);
+    // weight scales either row-major [E, N, K/32] or pre-packed [E][N/128][K/128] blocks
+    const bool packed_b = args.b_scales_packed != 0;
+    const int nblk = args.N / 128;
     GroupedScheduler<BM, BN> sched;
     uint32_t stage = 0, phase = 0;
     // Grouped path: when a row's codes for 4 consecutive stages form one aligned 16-byte
@@ -282,13 +285,30 @@ bsmxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             const bool live = m < args.M_total;
             cp_async_16(dst + r * 16, live ? a_sc + m * scale_row + 16 * qp : a_sc, live ? 16u : 0u);
           }
+          if (packed_b) {
+            // pre-packed weight scales: the tile's two 128-row blocks of these 4 K blocks are
+            // two contiguous 2 KB runs (staging: [block h][K block][512 bytes])
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int r = 32 * i + (int)lane;
-            const int n = tp.n0 + r;
-            const bool live = n < args.N;
-            const uint8_t* src = b_sc + ((int64_t)tp.be * args.N + n) * scale_row + 16 * qp;
-            cp_async_16(dst + STG_A + r * 16, live ? src : b_sc, live ? 16u : 0u);
+            for (int h = 0; h < 2; ++h) {
+              const int nb = tp.n0 / 128 + h;
+              const bool live = nb < nblk;
+              const uint8_t* run = b_sc + (((int64_t)tp.be * nblk + nb) * KB + 4 * qp) * SF_BLOCK;
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const int c = 32 * i + (int)lane;
+                cp_async_16(dst + STG_A + h * 4 * SF_BLOCK + c * 16, live ? run + c * 16 : b_sc,
+                            live ? 16u : 0u);
+              }
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int r = 32 * i + (int)lane;
+              const int n = tp.n0 + r;
+              const bool live = n < args.N;
+              const uint8_t* src = b_sc + ((int64_t)tp.be * args.N + n) * scale_row + 16 * qp;
+              cp_async_16(dst + STG_A + r * 16, live ? src : b_sc, live ? 16u : 0u);
+            }
           }
           if (++qp == G) {
             qp = 0;
@@ -327,10 +347,15 @@ bsmxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
               return w;
             };
             *reinterpret_cast<uint4*>(smem + SMEM_SFA + stage * SF_BLOCK + lane * 16) = gather(src);
-            *reinterpret_cast<uint4*>(smem + SMEM_SFB + stage * 2 * SF_BLOCK + lane * 16) =
-                gather(src + STG_A);
-            *reinterpret_cast<uint4*>(smem + SMEM_SFB + stage * 2 * SF_BLOCK + SF_BLOCK +
-                                      lane * 16) = gather(src + STG_A + 128 * 16);
+            uint4* sfb = reinterpret_cast<uint4*>(smem + SMEM_SFB + stage * 2 * SF_BLOCK);
+            if (packed_b) {
+              const uint8_t* pb = src + STG_A + j * SF_BLOCK + lane * 16;
+              sfb[lane] = *reinterpret_cast<const uint4*>(pb);
+              sfb[32 + lane] = *reinterpret_cast<const uint4*>(pb + 4 * SF_BLOCK);
+            } else {
+              sfb[lane] = gather(src + STG_A);
+              sfb[32 + lane] = gather(src + STG_A + 128 * 16);
+            }
             fence_proxy_async_smem();  // generic-proxy writes -> tcgen05.cp (async proxy)
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(mapa_shared(full_bar(stage), 0));
@@ -371,12 +396,24 @@ bsmxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
           const int64_t m = tc.m0 + 128 * rank + r;
           const bool a_live = m < args.M_total;
           cp_async_4(da + 4 * j, a_live ? a_sc + m * scale_row + 4 * kb : a_sc, a_live ? 4u : 0u);
+          if (!packed_b) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int n = tc.n0 + 128 * h + r;
+              const bool b_live = n < args.N;
+              const uint8_t* src = b_sc + ((int64_t)tc.be * args.N + n) * scale_row + 4 * kb;
+              cp_async_4(db + h * SF_BLOCK + 4 * j, b_live ? src : b_sc, b_live ? 4u : 0u);
+            }
+          }
+        }
+        if (packed_b) {
+          // pre-packed weight scales: the stage's two blocks, 16 bytes per lane each
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
-            const int n = tc.n0 + 128 * h + r;
-            const bool b_live = n < args.N;
-            const uint8_t* src = b_sc + ((int64_t)tc.be * args.N + n) * scale_row + 4 * kb;
-            cp_async_4(db + h * SF_BLOCK + 4 * j, b_live ? src : b_sc, b_live ? 4u : 0u);
+            const int nb = tc.n0 / 128 + h;
+            const bool live = nb < nblk;
+            const uint8_t* blk = b_sc + (((int64_t)tc.be * nblk + nb) * KB + kb) * SF_BLOCK;
+            cp_async_16(db + h * SF_BLOCK, live ? blk + lane * 16 : b_sc, live ? 16u : 0u);
           }
         }
         cp_async_commit();

@@ -119,26 +119,31 @@ bsfp8_status check_common(const void* A, const void* B, const void* sa, const vo
   return BSFP8_OK;
 }
 
-// Estimated makespan of a blockwise tile configuration, in tiles: persistent CTAs (or CTA
-// pairs) take tiles with a static stride, so the busiest one runs ceil(tiles / units) of
-// them.  The expert offsets live on the device, so row tiles are estimated from M_total with
-// half a ragged tile per expert.
+// Estimated makespan of a blockwise tile configuration, in tile times: persistent CTAs (or
+// CTA pairs) take tiles with a static stride, so the busiest one runs ceil(tiles / units) of
+// them.  The expert offsets live on the device, so the row tiles are estimated from M_total
+// and E as for an even split of the rows (E * ceil(M_total / (E * rows))).
 double blockwise_makespan(int64_t M_total, int N, int E, int tile_rows, int units) {
-  const double row_tiles =
-      std::ceil((double)M_total / tile_rows) + (E > 1 ? 0.5 * (double)E : 0.0);
+  const double per_expert = std::ceil((double)M_total / ((double)E * tile_rows));
+  const double row_tiles = (double)E * per_expert;
   const double tiles = row_tiles * (double)((N + 255) / 256);
   return std::ceil(tiles / (double)(units > 0 ? units : 1));
 }
 
-// Tile configuration for a launch.  The default is the 96 x 256 tile with the role warps on
-// the spare TMEM sub-partition, on one CTA or on a CTA pair (192 x 256), whichever has the
-// smaller estimated makespan; a pair tile runs about 3 % faster than two single-CTA tiles
-// (half the B bytes per SM) but there are half as many of them to spread over the SMs.
-// Measured on GB300 the 128-row tiles are slower: their epilogue warps share SMSPs with the
-// producer and MMA warps and lag them by up to ~1000 cycles per K block.  The environment
-// variable BSFP8_BLOCKWISE_TILE (cta1_96 | pair_192 | cta1_256 | pair_256 | pair_160 |
-// pair_128 | cta1_128) selects a configuration.
-constexpr double kPairTileTime = 0.97;  // pair 192 x 256 tile time / 1-CTA 96 x 256 tile time
+// Tile configuration for a launch.  Candidates, all with the role warps on a TMEM
+// sub-partition of their own (a sub-partition that runs producer or MMA issue next to
+// epilogue warps slows those warps down about twofold, so the 128-row single-CTA layouts
+// lose): 96 x 256 on one CTA; 192 x 256 on a CTA pair; and 224 x 256 on an asymmetric pair,
+// whose 128-row peer runs epilogue warps only.  Per tile, measured on GB300, a pair tile
+// takes about 0.95 and a 224-row pair tile about 0.97 of a one-CTA 96-row tile's time.  The
+// one-CTA tile is kept unless a pair form's estimated makespan is at least kSwitchMargin
+// smaller (the estimates count whole waves, so an error of one tile can flip them).  The
+// environment variable BSFP8_BLOCKWISE_TILE (cta1_96 | pair_192 | pair_224 | cta1_256 |
+// pair_256 | pair_160 | pair_128 | cta1_128 | cta1_96x192 | pair_192x192 | cta1_128x192)
+// selects a configuration.
+constexpr double kPair192Time = 0.95;  // 192 x 256 pair tile time / 96 x 256 one-CTA tile time
+constexpr double kPair224Time = 0.97;  // 224 x 256 pair tile time / 96 x 256 one-CTA tile time
+constexpr double kSwitchMargin = 0.92;
 
 BlockwiseTile choose_blockwise_tile(int64_t M_total, int N, int E, int num_sms) {
   if (const char* v = std::getenv("BSFP8_BLOCKWISE_TILE")) {
@@ -152,10 +157,14 @@ BlockwiseTile choose_blockwise_tile(int64_t M_total, int N, int E, int num_sms) 
     if (!std::strcmp(v, "cta1_96x192")) return TILE_CTA1_96x192;
     if (!std::strcmp(v, "pair_192x192")) return TILE_PAIR_192x192;
     if (!std::strcmp(v, "cta1_128x192")) return TILE_CTA1_128x192;
+    if (!std::strcmp(v, "pair_224")) return TILE_PAIR_224;
   }
   const double single = blockwise_makespan(M_total, N, E, 96, num_sms);
-  const double pair = blockwise_makespan(M_total, N, E, 192, num_sms / 2) * kPairTileTime;
-  return pair < single ? TILE_PAIR_192 : TILE_CTA1_96;
+  const double pair192 = blockwise_makespan(M_total, N, E, 192, num_sms / 2) * kPair192Time;
+  const double pair224 = blockwise_makespan(M_total, N, E, 224, num_sms / 2) * kPair224Time;
+  const double best_pair = std::min(pair192, pair224);
+  if (best_pair >= kSwitchMargin * single) return TILE_CTA1_96;
+  return pair224 <= pair192 ? TILE_PAIR_224 : TILE_PAIR_192;
 }
 
 // MXFP8 kernel choice: experts averaging at least 256 token rows use the CTA-pair 256 x 256
@@ -212,8 +221,8 @@ bsfp8_status blockwise_gemm(const void* A, const void* B, const float* a_scales,
              : BSFP8_ERR_CUDA;
 }
 
-// packed_b: b_scales are in the 512-byte block layout of bsmxfp8_pack_b_scales (swap-AB
-// tiles only: their weight tile is one 128-row block).
+// packed_b: b_scales are in the 512-byte block layout of bsmxfp8_pack_b_scales (both kernels:
+// a swap-AB tile's weights are one 128-row block, a CTA-pair tile's two).
 bsfp8_status mx_gemm(const void* A, const void* B, const uint8_t* a_scales,
                      const uint8_t* b_scales, const int32_t* offsets, const int32_t* ids,
                      void* C, int64_t M_total, int N, int K, int G, int E, cudaStream_t stream,
@@ -226,7 +235,7 @@ bsfp8_status mx_gemm(const void* A, const void* B, const uint8_t* a_scales,
   if (M_total == 0) return BSFP8_OK;
   GemmArgs args{offsets, a_scales, b_scales, C, M_total, N, K, G, dev->err_word, ids, E,
                 packed_b ? 1 : 0};
-  if (!packed_b && use_mx_pair(M_total, G)) {
+  if (use_mx_pair(M_total, G)) {
     CUtensorMap tmA, tmB;
     if (!encode_u8_2d(&tmA, A, (uint64_t)K, (uint64_t)M_total, 128, 128) ||
         !encode_u8_2d(&tmB, B, (uint64_t)K, (uint64_t)E * N, 128, 128))
@@ -394,8 +403,9 @@ extern "C" bsfp8_status bsfp8_blockwise_plan(int64_t M_total, int N, int num_exp
     return BSFP8_ERR_SHAPE;
   const BlockwiseTile tile = choose_blockwise_tile(M_total, N, num_experts, num_sms);
   const int ctas = (tile == TILE_PAIR_256 || tile == TILE_PAIR_160 || tile == TILE_PAIR_128 ||
-                    tile == TILE_PAIR_192 || tile == TILE_PAIR_192x192) ? 2 : 1;
-  out[0] = blockwise_a_rows(tile) * ctas;
+                    tile == TILE_PAIR_192 || tile == TILE_PAIR_192x192 ||
+                    tile == TILE_PAIR_224) ? 2 : 1;
+  out[0] = tile == TILE_PAIR_224 ? 224 : blockwise_a_rows(tile) * ctas;
   out[1] = blockwise_b_rows(tile) * ctas;
   out[2] = ctas;
   return BSFP8_OK;

@@ -44,6 +44,7 @@ enum BlockwiseTile : int {
   TILE_CTA1_96x192 = 7,   // one CTA, 96 x 192 tile: each epilogue warp drains its 96 columns at once
   TILE_PAIR_192x192 = 8,  // CTA pair, 192 x 192 tile, the same per CTA
   TILE_CTA1_128x192 = 9,  // one CTA, 128 x 192 tile (12 warps)
+  TILE_PAIR_224 = 10,     // CTA pair, 224 x 256 tile: 96-row leader with the role warps, 128-row peer
 };
 
 // Rows of B each CTA loads per stage (the B tensor map's box height) for a tile config.

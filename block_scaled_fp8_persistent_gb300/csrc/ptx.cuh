@@ -242,6 +242,19 @@ __device__ __forceinline__ void tma_load_2d_pair_hint(uint32_t dst, const void* 
       : "memory");
 }
 
+// CTA-pair load into the shared memory of the CTAs in `mask` (at this CTA's offset dst), with
+// the completion of each copy counted on the pair leader's barrier at offset `bar`
+// (.cta_group::2).  Used to fill a peer CTA that runs no producer of its own.
+__device__ __forceinline__ void tma_load_2d_mc_pair_hint(uint32_t dst, const void* tmap, int32_t x,
+                                                         int32_t y, uint32_t bar, uint16_t mask,
+                                                         uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      ".multicast::cluster.cta_group::2.L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5, %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(bar), "h"(mask), "l"(policy)
+      : "memory");
+}
+
 // Non-tensor bulk copy global -> this CTA's shared memory, completion counted on `bar`
 // (bytes).  dst, src and bytes must be multiples of 16.
 __device__ __forceinline__ void bulk_copy_g2s_hint(uint32_t dst, const void* src, uint32_t bytes,

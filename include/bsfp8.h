@@ -175,8 +175,9 @@ bsfp8_status bsmxfp8_grouped_gemm_ids(const void* A, const void* B, const uint8_
  * num_experts * N < 2^31), BSFP8_ERR_ALIGN, BSFP8_ERR_UNSUPPORTED_DEVICE, BSFP8_ERR_CUDA.
  *
  * bsmxfp8_grouped_gemm_prepacked is bsmxfp8_grouped_gemm with b_scales_packed (16-byte
- * aligned) in place of b_scales; it always runs the swap-AB tiles (128 weight rows = one
- * packed block per K block).  Same result, requirements and errors otherwise.
+ * aligned) in place of b_scales, on the kernel the plan picks: swap-AB tiles (128 weight rows
+ * = one packed block per K block) or CTA-pair 256 x 256 tiles (two blocks per K block).  Same
+ * result, requirements and errors otherwise.
  */
 bsfp8_status bsmxfp8_pack_b_scales(const uint8_t* b_scales, uint8_t* b_scales_packed,
                                    int num_experts, int N, int K, cudaStream_t stream);
@@ -253,9 +254,10 @@ bsfp8_status bsmxfp8_tmem_plan(int block_k, int epilogue_n, int vec, int overlap
  * tile rows, out[1] = tile columns, out[2] = CTAs per tile (1, or 2 for a CTA pair).  The
  * persistent kernel gives each CTA (pair) every (SMs / CTAs per tile)-th tile; tiles are
  * ceil(M_e / rows) x ceil(N / columns) per expert e.  The default picks 96 x 256 tiles on
- * one CTA or 192 x 256 on a pair by estimated makespan (the tile rows leave the TMEM lanes
- * of one SM sub-partition to the producer and MMA warps).  This is a performance choice
- * only: every plan computes the same result.  BSFP8_ERR_NULL / BSFP8_ERR_SHAPE on bad input.
+ * one CTA, 192 x 256 on a CTA pair or 224 x 256 on an asymmetric pair (a 96-row CTA with the
+ * producer and MMA warps next to a 128-row CTA of epilogue warps only) by estimated makespan.
+ * This is a performance choice only: every plan computes the same result.  BSFP8_ERR_NULL /
+ * BSFP8_ERR_SHAPE on bad input.
  */
 bsfp8_status bsfp8_blockwise_plan(int64_t M_total, int N, int num_experts, int num_sms,
                                   int32_t* out);

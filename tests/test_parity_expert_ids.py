@@ -12,7 +12,8 @@ from helpers import parity_report
 
 pytestmark = pytest.mark.gpu
 
-BLOCKWISE_TILES = ["cta1_96", "pair_192", "cta1_256", "pair_256", "cta1_96x192", "pair_192x192"]
+BLOCKWISE_TILES = ["cta1_96", "pair_192", "cta1_256", "pair_256", "cta1_96x192", "pair_192x192",
+                   "pair_224"]
 MX_FORMS = ["swap32", "swap128", "pair"]
 
 

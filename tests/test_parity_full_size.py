@@ -19,7 +19,7 @@ from helpers import parity_report_chunked
 pytestmark = pytest.mark.gpu
 
 TILES = ["cta1_256", "pair_256", "pair_160", "pair_128", "cta1_128", "cta1_96", "pair_192",
-         "cta1_96x192", "pair_192x192", "cta1_128x192"]
+         "cta1_96x192", "pair_192x192", "cta1_128x192", "pair_224"]
 FP4_PAIRS = [("mxfp8", "mxfp4"), ("mxfp4", "mxfp4"), ("nvfp4", "nvfp4")]
 
 _REFS = {}

@@ -1,7 +1,8 @@
 """GPU parity of the pre-packed MXFP8 weight scales: the pack kernel against the oracle's
 statement of the packed block layout (swizzle_scales_packed_block, Triton Gluon example
 "Overlapping Accumulator Block-Scaled Matrix Multiplication"), bit for bit, and the GEMM on
-pre-packed scales against the oracle and against the GEMM on row-major scales."""
+pre-packed scales, on the swap-AB and the CTA-pair kernels, against the oracle and against
+the GEMM on row-major scales."""
 import numpy as np
 import pytest
 import torch
@@ -29,20 +30,20 @@ def test_pack_kernel_matches_oracle(E, N, K):
     assert np.array_equal(got, oracle.pack_mx_scales(sb.reshape(E * N, K // 32)))
 
 
-@pytest.fixture(autouse=True)
-def swap_tiles(monkeypatch):
-    """The pre-packed path runs the swap-AB tiles; compare with the same tiles."""
-    monkeypatch.setenv("BSFP8_MX_KERNEL", "swap")
-
-
-@pytest.fixture(params=["32", "64", "128"])
-def tn(request, monkeypatch):
-    monkeypatch.setenv("BSFP8_MX_TN", request.param)
-    return int(request.param)
+@pytest.fixture(params=["swap32", "swap64", "swap128", "pair"])
+def form(request, monkeypatch):
+    """Kernel form: swap-AB tiles of 32 / 64 / 128 token rows, or CTA-pair 256 x 256 tiles
+    (both read pre-packed weight scales); the row-major comparison runs the same form."""
+    if request.param == "pair":
+        monkeypatch.setenv("BSFP8_MX_KERNEL", "pair")
+    else:
+        monkeypatch.setenv("BSFP8_MX_KERNEL", "swap")
+        monkeypatch.setenv("BSFP8_MX_TN", request.param[4:])
+    return request.param
 
 
 def _run_both(p):
-    """(prepacked result, row-major-scale result) as bf16 bits, on the swap-AB tiles."""
+    """(prepacked result, row-major-scale result) as bf16 bits, on the same kernel form."""
     from gpu_util import DeviceProblem
     import block_scaled_fp8_persistent_gb300 as bsfp8
     d = DeviceProblem(p, c_rows_extra=2)
@@ -64,7 +65,7 @@ CASES = [("decode_like", [3, 17, 0, 32, 1, 9], 256, 512),
 
 
 @pytest.mark.parametrize("name,counts,N,K", CASES, ids=[c[0] for c in CASES])
-def test_prepacked_gemm(name, counts, N, K, tn):
+def test_prepacked_gemm(name, counts, N, K, form):
     p = gen.mx_problem(counts, N, K, seed=400 + len(name))
     got, plain = _run_both(p)
     assert np.array_equal(got, plain)
@@ -73,17 +74,18 @@ def test_prepacked_gemm(name, counts, N, K, tn):
     assert bad == 0, f"{bad} elements outside tolerance (max err/tol {ratio:.3g})"
 
 
-def test_prepacked_gemm_exact_bitwise(tn):
+def test_prepacked_gemm_exact_bitwise(form):
     p = gen.mx_problem([5, 30, 0, 12], 256, 1024, seed=410, exact=True)
     got, _ = _run_both(p)
     ref, _ = oracle.problem_reference(p, want_t=False)
     assert np.array_equal(got, ref)
 
 
-def test_full_size_decode_prepacked_equals_row_major():
+def test_full_size_decode_prepacked_equals_row_major(monkeypatch):
     """The decode workload at its full size (128 experts, N=4096, K=7168): the pack kernel
     matches the oracle's layout and the GEMM on packed scales equals, bit for bit, the GEMM
     on row-major scales."""
+    monkeypatch.setenv("BSFP8_MX_KERNEL", "swap")
     p = gen.config_problem(4)
     got, plain = _run_both(p)
     assert np.array_equal(got, plain)
@@ -91,3 +93,11 @@ def test_full_size_decode_prepacked_equals_row_major():
     d = DeviceProblem(p)
     packed = _pack_on_device(d.sb, p.E, p.N, p.K).cpu().numpy()
     assert np.array_equal(packed, oracle.pack_mx_scales(p.b_scales.reshape(p.E * p.N, -1)))
+
+
+def test_full_size_dense_prepacked_pair_equals_row_major(monkeypatch):
+    """The dense 8192^3 MXFP8 workload on the CTA-pair kernel: pre-packed weight scales give
+    the same bits as row-major ones."""
+    monkeypatch.setenv("BSFP8_MX_KERNEL", "pair")
+    got, plain = _run_both(gen.config_problem(5))
+    assert np.array_equal(got, plain)
