@@ -91,6 +91,9 @@ __device__ __forceinline__ uint64_t sf_block_desc(uint32_t saddr) {
   return make_smem_desc(saddr, 0, 128, LAYOUT_NONE);
 }
 
+// PACKED_B: weight scales pre-packed in [E][N/128][K/128] blocks of 512 bytes (else
+// row-major [E, N, K/32]); an instantiation each, so the row-major loader carries no branch.
+template <bool PACKED_B>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 bsmxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const GemmArgs args) {
@@ -255,7 +258,7 @@ bsmxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     const uint8_t* a_sc = static_cast<const uint8_t*>(args.a_scales);
     const uint8_t* b_sc = static_cast<const uint8_t*>(args.b_scales);
     // weight scales either row-major [E, N, K/32] or pre-packed [E][N/128][K/128] blocks
-    const bool packed_b = args.b_scales_packed != 0;
+    constexpr bool packed_b = PACKED_B;
     const int nblk = args.N / 128;
     GroupedScheduler<BM, BN> sched;
     uint32_t stage = 0, phase = 0;
@@ -285,7 +288,7 @@ bsmxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             const bool live = m < args.M_total;
             cp_async_16(dst + r * 16, live ? a_sc + m * scale_row + 16 * qp : a_sc, live ? 16u : 0u);
           }
-          if (packed_b) {
+          if constexpr (packed_b) {
             // pre-packed weight scales: the tile's two 128-row blocks of these 4 K blocks are
             // two contiguous 2 KB runs (staging: [block h][K block][512 bytes])
 #pragma unroll
@@ -348,7 +351,7 @@ bsmxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             };
             *reinterpret_cast<uint4*>(smem + SMEM_SFA + stage * SF_BLOCK + lane * 16) = gather(src);
             uint4* sfb = reinterpret_cast<uint4*>(smem + SMEM_SFB + stage * 2 * SF_BLOCK);
-            if (packed_b) {
+            if constexpr (packed_b) {
               const uint8_t* pb = src + STG_A + j * SF_BLOCK + lane * 16;
               sfb[lane] = *reinterpret_cast<const uint4*>(pb);
               sfb[32 + lane] = *reinterpret_cast<const uint4*>(pb + 4 * SF_BLOCK);
@@ -396,7 +399,7 @@ bsmxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
           const int64_t m = tc.m0 + 128 * rank + r;
           const bool a_live = m < args.M_total;
           cp_async_4(da + 4 * j, a_live ? a_sc + m * scale_row + 4 * kb : a_sc, a_live ? 4u : 0u);
-          if (!packed_b) {
+          if constexpr (!packed_b) {
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
               const int n = tc.n0 + 128 * h + r;
@@ -406,7 +409,7 @@ bsmxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             }
           }
         }
-        if (packed_b) {
+        if constexpr (packed_b) {
           // pre-packed weight scales: the stage's two blocks, 16 bytes per lane each
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
@@ -493,15 +496,17 @@ bsmxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
 
 }  // namespace mxp
 
-cudaError_t launch_bsmxfp8_pair(const CUtensorMap& tmA, const CUtensorMap& tmB,
-                                const GemmArgs& args, int num_sms, cudaStream_t stream) {
+namespace mxp {
+template <bool PACKED_B>
+cudaError_t launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& args,
+                   int num_sms, cudaStream_t stream) {
   static std::atomic<bool> attr_set[64];  // per device; several host threads may launch
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 64 || !attr_set[dev].load(std::memory_order_acquire)) {
-    cudaError_t e = cudaFuncSetAttribute(mxp::bsmxfp8_pair_kernel,
+    cudaError_t e = cudaFuncSetAttribute(bsmxfp8_pair_kernel<PACKED_B>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)mxp::SMEM_BYTES);
+                                         (int)SMEM_BYTES);
     if (e != cudaSuccess) return e;
     if (dev < 64) attr_set[dev].store(true, std::memory_order_release);
   }
@@ -521,7 +526,14 @@ cudaError_t launch_bsmxfp8_pair(const CUtensorMap& tmA, const CUtensorMap& tmB,
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, mxp::bsmxfp8_pair_kernel, tmA, tmB, args);
+  return cudaLaunchKernelEx(&cfg, bsmxfp8_pair_kernel<PACKED_B>, tmA, tmB, args);
+}
+}  // namespace mxp
+
+cudaError_t launch_bsmxfp8_pair(const CUtensorMap& tmA, const CUtensorMap& tmB,
+                                const GemmArgs& args, int num_sms, cudaStream_t stream) {
+  return args.b_scales_packed ? mxp::launch<true>(tmA, tmB, args, num_sms, stream)
+                              : mxp::launch<false>(tmA, tmB, args, num_sms, stream);
 }
 
 TmemPlan mx_pair_tmem_plan() { return mxp::PLAN; }

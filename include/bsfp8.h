@@ -216,7 +216,10 @@ bsfp8_status bsmxfp8_grouped_gemm_prepacked(const void* A, const void* B, const 
  *                   re-encoded on chip into e4m3 for the MXFP8 block-scaled MMA: every e2m1
  *                   value times 2^-6 is an e4m3 value, and the epilogue multiplies the fp32
  *                   sums by 2^6 per fp4 operand, so the result is that of the same values in
- *                   MXFP8 (exact unless a product falls below 2^-120 in magnitude).
+ *                   MXFP8 while the tensor core's products, 2^-6 per fp4 operand below the
+ *                   true ones, stay in fp32's normal range: every non-zero product
+ *                   dec(A)*sa*dec(B)*sb of magnitude at least 2^-120 (one fp4 operand) or
+ *                   2^-114 (two).  Smaller products may be flushed to zero.
  *   (NVFP4, NVFP4)  swap-AB tiles at every size.  The packed tiles and their e4m3 scales are
  *                   dequantized on chip into fp16 (exact: an e2m1 value times an e4m3 scale
  *                   has at most 6 significant bits and lies in the normal fp16 range) and

@@ -229,25 +229,23 @@ def _unit_magnitudes(p, a_fmt, rng):
 
 @pytest.mark.parametrize("a_fmt,b_fmt", MX_PAIRS)
 def test_low_scales(a_fmt, b_fmt, tn):
-    # scale codes 65 (tokens) and 66 (weights): every product is 2^-123 times 1 .. 2.25, an fp32
-    # normal number, and the sums stay in bf16's normal range; the fp4 operands' factor 2^6 is
-    # applied through the token scales, so no product the MMA forms falls below 2^-126
+    # scale codes 72 and 72: every product is 2^-110 times 1 .. 2.25, inside the documented
+    # range (the tensor core sums them 2^-6 per fp4 operand lower, 2^-116 / 2^-122, still
+    # fp32-normal), and the sums are far below 1 but in bf16's normal range
     p = gen.fmt_problem([5, 30, 0, 12], 256, 1024, seed=46, a_fmt=a_fmt, b_fmt=b_fmt)
     _unit_magnitudes(p, a_fmt, np.random.default_rng(46))
-    p.a_scales[:] = 65
-    p.b_scales[:] = 66
+    p.a_scales[:] = 72
+    p.b_scales[:] = 72
     _check_full(p)
 
 
 @pytest.mark.parametrize("a_fmt,b_fmt", MX_PAIRS)
-def test_high_token_scales(a_fmt, b_fmt, tn):
-    # token scale codes up to the largest that the fold of 2^6 per fp4 operand leaves
-    # uncapped (248 with e4m3 tokens, 242 with e2m1 tokens), weight codes low enough that the
-    # products stay finite
-    top = 248 if a_fmt == "mxfp8" else 242
+def test_high_scales(a_fmt, b_fmt, tn):
+    # token scale codes up to 254 (2^127) with weight codes low enough that the products stay
+    # finite: the 2^6 per fp4 operand is applied after the sums, in fp32
     p = gen.fmt_problem([5, 30, 0, 12], 256, 1024, seed=47, a_fmt=a_fmt, b_fmt=b_fmt)
     rng = np.random.default_rng(47)
     _unit_magnitudes(p, a_fmt, rng)
-    p.a_scales[:] = rng.integers(top - 8, top + 1, p.a_scales.shape).astype(np.uint8)
+    p.a_scales[:] = rng.integers(246, 255, p.a_scales.shape).astype(np.uint8)
     p.b_scales[:] = rng.integers(20, 30, p.b_scales.shape).astype(np.uint8)
     _check_full(p)
