@@ -21,10 +21,13 @@
 // the MMA two tiles later waits for the whole accumulator (acc_empty).
 //
 // Roles (12 warps per CTA): warp 0 TMA producer (own 128 token rows, own 128 weight rows);
-// warp 1 TMEM owner and, in CTA 0 of the pair, the MMA thread (tcgen05.cp of the scale
-// blocks, 4 x tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale per 128-K stage, commits
-// multicast to both CTAs); warp 2 scale loader; warps 4-11 epilogue (TMEM lane quarter
-// w%4, column half (w-4)/4, 32-column subtiles).
+// warp 1 TMEM owner and, in CTA 0 of the pair, the MMA thread (per 128-K block tcgen05.cp
+// of its scale blocks and 4 x tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale; one
+// commit per ring stage, multicast to both CTAs); warp 2 scale loader; warps 4-11 epilogue
+// (TMEM lane quarter w%4, column half (w-4)/4, 32-column subtiles).
+// A ring stage holds KG = 2 K blocks (the k_group_size grouping of K iterations per
+// pipeline stage): the full/empty barriers, the scale announce and the commit are paid once
+// per 256 of K.
 #include <atomic>
 #include <cuda_bf16.h>
 #include "common.cuh"
@@ -43,28 +46,41 @@ constexpr int NUM_THREADS = 384;
 constexpr int EPI_WARP0 = 4;
 constexpr int NUM_EPI_WARPS = 8;
 constexpr int SF_BLOCK = 512;  // packed scale block: 128 rows x 4 codes
-constexpr int STAGES = 6;
-constexpr int SCALE_LOOKAHEAD = 3;
+// K blocks of 128 per ring stage (k_group_size of the per-K-stage context, MAX
+// EpilogueWarpContext page, per_k_stage): one full/empty round trip and one commit per KG
+// K blocks instead of per K block
+constexpr int KG = 2;
+constexpr int STAGES = 3;  // ring stages of KG K blocks (64 KB of operands each)
+// Row-major scale copies in flight before the oldest is announced.  A stage's copies start
+// once the MMA has freed it; announcing stage s only after the copies of s + L are issued
+// waits for the MMA to free s + L, so L <= STAGES - 2 keeps that off the MMA's path.
+constexpr int SCALE_LOOKAHEAD = 1;
+static_assert(SCALE_LOOKAHEAD <= STAGES - 2, "scale announce would wait on the MMA");
 constexpr TmemPlan PLAN = tmem_overlap_plan(BK, EPI_N, 32, true, BN, 512);
 static_assert(PLAN.right_offset == 244 && PLAN.a_scale_offset == 500 &&
               PLAN.b_scale_offset == 504 && PLAN.early_release_subtile == 0,
               "plan for BLOCK_K 128, VEC 32");
 
-constexpr uint32_t A_STAGE = 128 * BK;  // this CTA's token rows
-constexpr uint32_t B_STAGE = 128 * BK;  // this CTA's weight rows
+constexpr uint32_t A_SUB = 128 * BK;   // one K block of this CTA's token rows
+constexpr uint32_t B_SUB = 128 * BK;   // one K block of this CTA's weight rows
+constexpr uint32_t A_STAGE = KG * A_SUB;
+constexpr uint32_t B_STAGE = KG * B_SUB;
 constexpr uint32_t SMEM_A = 0;
 constexpr uint32_t SMEM_B = SMEM_A + STAGES * A_STAGE;
-constexpr uint32_t SMEM_SFA = SMEM_B + STAGES * B_STAGE;            // 1 block per stage
-constexpr uint32_t SMEM_SFB = SMEM_SFA + STAGES * SF_BLOCK;         // 2 blocks per stage
+constexpr uint32_t SFA_STAGE = KG * SF_BLOCK;                        // 1 block per K block
+constexpr uint32_t SFB_STAGE = KG * 2 * SF_BLOCK;                    // 2 blocks per K block
+constexpr uint32_t SMEM_SFA = SMEM_B + STAGES * B_STAGE;
+constexpr uint32_t SMEM_SFB = SMEM_SFA + STAGES * SFA_STAGE;
 // Scale staging for the grouped loader: per group of 4 stages, 16 bytes (4 stages x 4
 // codes) of each of this CTA's 128 token rows and the tile's 256 weight rows.
 constexpr int GROUP = 4;
 constexpr uint32_t STG_A = 128 * 16;
 constexpr uint32_t STG_SLOT = STG_A + 256 * 16;
 constexpr int STG_SLOTS = 3;
-constexpr uint32_t SMEM_STG = SMEM_SFB + STAGES * 2 * SF_BLOCK;
+constexpr uint32_t SMEM_STG = SMEM_SFB + STAGES * SFB_STAGE;
 constexpr uint32_t SMEM_CTL = SMEM_STG + STG_SLOTS * STG_SLOT;
-constexpr uint32_t STAGE_TX = 2 * (A_STAGE + B_STAGE);              // both CTAs' bytes
+constexpr uint32_t SUB_TX = 2 * (A_SUB + B_SUB);  // both CTAs' bytes of one K block
+static_assert(GROUP % KG == 0, "a grouped scale fetch covers whole ring stages");
 
 struct Ctl {
   uint64_t full[STAGES];
@@ -174,16 +190,21 @@ bsmxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         if (!sched.locate(args, t, tc)) break;
         const int32_t a_row = (int32_t)(tc.m0 + 128 * rank);
         const int32_t b_row = tc.be * args.N + tc.n0 + 128 * rank;
-        for (int kb = 0; kb < KB; ++kb) {
+        for (int kb0 = 0; kb0 < KB; kb0 += KG) {
+          const int nk = KB - kb0 < KG ? KB - kb0 : KG;  // K blocks in this ring stage
           if (!mbar_wait(empty_bar(stage), phase ^ 1, abort)) {
             record_error(args.err, DEV_TIMEOUT, abort);
             ok = false;
             break;
           }
           const uint32_t bar = mapa_shared(full_bar(stage), 0);
-          if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), STAGE_TX);
-          tma_load_2d_pair(sA + stage * A_STAGE, &tmA, kb * BK, a_row, bar);
-          tma_load_2d_pair_hint(sB + stage * B_STAGE, &tmB, kb * BK, b_row, bar, pol_b);
+          if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), nk * SUB_TX);
+          for (int u = 0; u < nk; ++u) {
+            const int kb = kb0 + u;
+            tma_load_2d_pair(sA + stage * A_STAGE + u * A_SUB, &tmA, kb * BK, a_row, bar);
+            tma_load_2d_pair_hint(sB + stage * B_STAGE + u * B_SUB, &tmB, kb * BK, b_row, bar,
+                                  pol_b);
+          }
           ++issued;
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
         }
@@ -218,23 +239,30 @@ bsmxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         const uint32_t d_tmem = tmem_base + (buf ? PLAN.right_offset : PLAN.left_offset);
         const uint32_t sfa_t = tmem_base + PLAN.a_scale_offset;
         const uint32_t sfb_t = tmem_base + PLAN.b_scale_offset;
-        for (int kb = 0; kb < KB; ++kb) {
+        for (int kb0 = 0; kb0 < KB; kb0 += KG) {
+          const int nk = KB - kb0 < KG ? KB - kb0 : KG;
           if (!mbar_wait(full_bar(stage), phase, abort)) {
             record_error(args.err, DEV_TIMEOUT, abort);
             ok = false;
             break;
           }
           tc_fence_after();
-          tmem_cp_32x128b_warpx4<2>(sfa_t, sf_block_desc(sSFA + stage * SF_BLOCK));
-          tmem_cp_32x128b_warpx4<2>(sfb_t, sf_block_desc(sSFB + stage * 2 * SF_BLOCK));
-          tmem_cp_32x128b_warpx4<2>(sfb_t + 4, sf_block_desc(sSFB + stage * 2 * SF_BLOCK + SF_BLOCK));
-          const uint64_t adesc = kmajor_sw128_desc(sA + stage * A_STAGE);
-          const uint64_t bdesc = kmajor_sw128_desc(sB + stage * B_STAGE);
+          for (int u = 0; u < nk; ++u) {
+            // this K block's scales into the TMEM scale columns (after the previous K block's
+            // MMAs, which read them, in this thread's issue order)
+            const uint32_t sfa_s = sSFA + stage * SFA_STAGE + u * SF_BLOCK;
+            const uint32_t sfb_s = sSFB + stage * SFB_STAGE + u * 2 * SF_BLOCK;
+            tmem_cp_32x128b_warpx4<2>(sfa_t, sf_block_desc(sfa_s));
+            tmem_cp_32x128b_warpx4<2>(sfb_t, sf_block_desc(sfb_s));
+            tmem_cp_32x128b_warpx4<2>(sfb_t + 4, sf_block_desc(sfb_s + SF_BLOCK));
+            const uint64_t adesc = kmajor_sw128_desc(sA + stage * A_STAGE + u * A_SUB);
+            const uint64_t bdesc = kmajor_sw128_desc(sB + stage * B_STAGE + u * B_SUB);
 #pragma unroll
-          for (int k = 0; k < BK / 32; ++k)
-            umma_mxf8f6f4<2>(d_tmem, adesc + (uint64_t)(k * 2), bdesc + (uint64_t)(k * 2),
-                             idesc_mxf8f6f4_e4m3(BM, BN, k, k), sfa_t, sfb_t,
-                             (kb > 0 || k > 0) ? 1u : 0u);
+            for (int k = 0; k < BK / 32; ++k)
+              umma_mxf8f6f4<2>(d_tmem, adesc + (uint64_t)(k * 2), bdesc + (uint64_t)(k * 2),
+                               idesc_mxf8f6f4_e4m3(BM, BN, k, k), sfa_t, sfb_t,
+                               (kb0 + u > 0 || k > 0) ? 1u : 0u);
+          }
           umma_commit_pair(empty_bar(stage), 0x3);
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
         }
@@ -332,7 +360,7 @@ bsmxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
           cp_async_wait_group<1>();  // group g has landed (g + 1 may be in flight)
           __syncwarp();
           const uint8_t* src = stg + (g % STG_SLOTS) * STG_SLOT;
-          for (int j = 0; j < GROUP; ++j) {
+          for (int jg = 0; jg < GROUP; jg += KG) {
             const bool got =
                 __all_sync(0xffffffffu, mbar_wait(empty_bar(stage), phase ^ 1, abort));
             if (!got) {
@@ -340,6 +368,9 @@ bsmxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
               ok = false;
               break;
             }
+#pragma unroll
+            for (int u = 0; u < KG; ++u) {
+            const int j = jg + u;
             // packed block: row r = 32*rg + lane at byte lane*16 + rg*4
             auto gather = [&](const uint8_t* rows) {
               uint4 w;
@@ -349,8 +380,10 @@ bsmxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
               w.w = *reinterpret_cast<const uint32_t*>(rows + (3 * 32 + lane) * 16 + 4 * j);
               return w;
             };
-            *reinterpret_cast<uint4*>(smem + SMEM_SFA + stage * SF_BLOCK + lane * 16) = gather(src);
-            uint4* sfb = reinterpret_cast<uint4*>(smem + SMEM_SFB + stage * 2 * SF_BLOCK);
+            *reinterpret_cast<uint4*>(smem + SMEM_SFA + stage * SFA_STAGE + u * SF_BLOCK +
+                                      lane * 16) = gather(src);
+            uint4* sfb =
+                reinterpret_cast<uint4*>(smem + SMEM_SFB + stage * SFB_STAGE + u * 2 * SF_BLOCK);
             if constexpr (packed_b) {
               const uint8_t* pb = src + STG_A + j * SF_BLOCK + lane * 16;
               sfb[lane] = *reinterpret_cast<const uint4*>(pb);
@@ -358,6 +391,7 @@ bsmxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             } else {
               sfb[lane] = gather(src + STG_A);
               sfb[32 + lane] = gather(src + STG_A + 128 * 16);
+            }
             }
             fence_proxy_async_smem();  // generic-proxy writes -> tcgen05.cp (async proxy)
             __syncwarp();
@@ -384,15 +418,18 @@ bsmxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     };
     for (int64_t t = tile0; ok && t < total_tiles; t += tile_stride) {
       if (!sched.locate(args, t, tc)) break;
-      for (int kb = 0; kb < KB; ++kb) {
+      for (int kb0 = 0; kb0 < KB; kb0 += KG) {
+        const int nk = KB - kb0 < KG ? KB - kb0 : KG;
         const bool got = __all_sync(0xffffffffu, mbar_wait(empty_bar(stage), phase ^ 1, abort));
         if (!got) {
           if (lane == 0) record_error(args.err, DEV_TIMEOUT, abort);
           ok = false;
           break;
         }
-        const uint32_t da = sSFA + stage * SF_BLOCK + lane * 16;
-        const uint32_t db = sSFB + stage * 2 * SF_BLOCK + lane * 16;
+        for (int u = 0; u < nk; ++u) {
+        const int kb = kb0 + u;
+        const uint32_t da = sSFA + stage * SFA_STAGE + u * SF_BLOCK + lane * 16;
+        const uint32_t db = sSFB + stage * SFB_STAGE + u * 2 * SF_BLOCK + lane * 16;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const int r = j * 32 + (int)lane;
@@ -418,6 +455,7 @@ bsmxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             const uint8_t* blk = b_sc + (((int64_t)tc.be * nblk + nb) * KB + kb) * SF_BLOCK;
             cp_async_16(db + h * SF_BLOCK, live ? blk + lane * 16 : b_sc, live ? 16u : 0u);
           }
+        }
         }
         cp_async_commit();
         ring[(head + inflight) % (SCALE_LOOKAHEAD + 1)] = stage;

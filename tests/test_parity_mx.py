@@ -44,6 +44,7 @@ CASES = [
     ("ragged_k", [40, 0, 7], 384, 640),
     ("one_expert_many_rows", [300], 128, 256),
     ("mixed", [0, 129, 64, 65, 2, 0, 31], 256, 384),
+    ("single_k_block", [130, 0, 5], 256, 128),
 ]
 
 
