@@ -89,12 +89,17 @@ struct Cfg {
   // all of a warp's columns fit in registers next to its accumulators: load them all,
   // release the TMEM stage, then promote
   static constexpr bool LOAD_ALL = COLS <= 96;
-  static constexpr uint32_t A_STAGE = 128 * BK;  // the MMA reads 128 rows per CTA
+  // The MMA reads 128 A rows per CTA.  A one-CTA 96-row tile keeps only its 96 rows per
+  // stage: rows 96..127 of the read come from the next 4 KB of shared memory (the next stage,
+  // or the first B stage), land in TMEM lanes 96..127 and are never read, and the ring gets
+  // a fifth stage in the same space.
+  static constexpr uint32_t A_STAGE = (SPARE_QUARTER && CG == 1 ? 96 : 128) * BK;
   static constexpr uint32_t B_STAGE = B_ROWS * BK;
   static constexpr int A_BOX = ASYM ? 128 : ROWS;  // A rows per TMA box
   static constexpr uint32_t STAGE_TX = (A_BOX * BK + B_STAGE) * CG;  // bytes loaded, pair
-  // each epilogue warp's columns lie in one 128-column B-scale block (one B scale per K block)
-  static constexpr bool ONE_BLOCK = COLS == 128 && BN % 256 == 0;
+  // each epilogue warp's columns lie in one 128-column B-scale block (one B scale per K
+  // block): its first column is a multiple of COLS, which divides 128
+  static constexpr bool ONE_BLOCK = 128 % COLS == 0;
   static constexpr int SCALE_LOOKAHEAD = 6;  // K blocks of A-scale L1 prefetch
   static constexpr uint32_t SMEM_A = 0;
   static constexpr uint32_t SMEM_B = SMEM_A + STAGES * A_STAGE;
@@ -533,6 +538,7 @@ bsfp8_blockwise_kernel(const __grid_constant__ CUtensorMap tmA,
 template <class C>
 cudaError_t launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& args,
                    int num_sms, cudaStream_t stream) {
+  static_assert(smem_bytes<C>() <= 227 * 1024, "shared memory per CTA");
   static std::atomic<bool> attr_set[64];  // per device; several host threads may launch
   int dev = 0;
   cudaGetDevice(&dev);
@@ -572,7 +578,7 @@ using Pair256 = Cfg<2, 256, 6, 2>;
 using Pair160 = Cfg<2, 160, 8, 3>;
 using Pair128 = Cfg<2, 128, 8, 4>;
 using Cta1x128 = Cfg<1, 128, 4, 4>;
-using Cta1x96x256 = Cfg<1, 256, 4, 2, 96>;
+using Cta1x96x256 = Cfg<1, 256, 5, 2, 96>;
 using Pair192x256 = Cfg<2, 256, 6, 2, 96>;
 using Cta1x96x192 = Cfg<1, 192, 5, 2, 96>;
 using Pair192x192 = Cfg<2, 192, 7, 2, 96>;

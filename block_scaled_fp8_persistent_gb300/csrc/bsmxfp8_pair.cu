@@ -42,6 +42,9 @@ constexpr int BK = 128;
 constexpr int BM = 256;        // token rows per pair tile (128 per CTA)
 constexpr int BN = 256;        // weight rows per pair tile (MMA N)
 constexpr int EPI_N = 32;      // epilogue subtile columns
+// Tiles are walked in bands of 16 row tiles (row index fastest inside a band): the 76 pairs
+// in flight share ~5 columns of B, and B is read from DRAM about once per band
+constexpr int TILE_BAND = 16;
 constexpr int NUM_THREADS = 384;
 constexpr int EPI_WARP0 = 4;
 constexpr int NUM_EPI_WARPS = 8;
@@ -180,7 +183,7 @@ bsmxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
   if (warp == 0) {
     // =============================== TMA producer ===============================
     if (lane == 0) {
-      GroupedScheduler<BM, BN> sched;
+      GroupedScheduler<BM, BN, TILE_BAND> sched;
       const uint64_t pol_b = l2_policy_evict_last();
       uint32_t stage = 0, phase = 0;
       int64_t issued = 0;
@@ -220,7 +223,7 @@ bsmxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
   } else if (warp == 1) {
     // ================================ MMA thread ================================
     if (lane == 0 && rank == 0) {
-      GroupedScheduler<BM, BN> sched;
+      GroupedScheduler<BM, BN, TILE_BAND> sched;
       uint32_t stage = 0, phase = 0;
       bool ok = true;
       int64_t i = 0;  // tiles issued by this pair
@@ -288,7 +291,7 @@ bsmxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     // weight scales either row-major [E, N, K/32] or pre-packed [E][N/128][K/128] blocks
     constexpr bool packed_b = PACKED_B;
     const int nblk = args.N / 128;
-    GroupedScheduler<BM, BN> sched;
+    GroupedScheduler<BM, BN, TILE_BAND> sched;
     uint32_t stage = 0, phase = 0;
     // Grouped path: when a row's codes for 4 consecutive stages form one aligned 16-byte
     // chunk (K % 512 == 0, 16-byte aligned scale arrays), fetch a 4-stage group per row with
@@ -301,7 +304,7 @@ bsmxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
       const int G = KB / GROUP;  // groups per tile
       const uint32_t sSTG = smem_u32(smem + SMEM_STG);
       const uint8_t* stg = smem + SMEM_STG;
-      GroupedScheduler<BM, BN> pre;
+      GroupedScheduler<BM, BN, TILE_BAND> pre;
       TileCoord tp;
       int64_t tp_t = tile0;
       bool pre_ok = pre.locate(args, tp_t, tp);
@@ -476,7 +479,7 @@ bsmxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     const uint32_t quarter = warp & 3;
     const uint32_t half = ew >> 2;  // accumulator columns half*128 .. +127
     __nv_bfloat16* Cmat = static_cast<__nv_bfloat16*>(args.C);
-    GroupedScheduler<BM, BN> sched;
+    GroupedScheduler<BM, BN, TILE_BAND> sched;
     const uint64_t pol_c = l2_policy_evict_first();
     int64_t i = 0;
     TileCoord tc;

@@ -1,7 +1,11 @@
 // Grouped persistent tile scheduler (device side).
 //
 // Tiles are numbered expert by expert; inside expert e there are ceil(M_e / BM) row
-// tiles times N / BN column tiles, column index fastest.  A persistent CTA takes tiles
+// tiles times N / BN column tiles, walked in bands of BAND row tiles: inside a band the row
+// index is fastest, so the tiles in flight at one time share a few columns of B (read from
+// DRAM once per band instead of once per wave) while the band's rows of A stay in L2 as
+// its columns go by.  BAND = 1 is the plain order, column index fastest.  A persistent CTA
+// takes tiles
 // blockIdx.x, blockIdx.x + gridDim.x, ... (the static stride of the SpsTileScheduler in
 // the Triton Gluon example "Overlapping Accumulator Block-Scaled Matrix Multiplication",
 // Partitions section), and maps a tile id to (expert, first row, first column) by walking
@@ -25,7 +29,7 @@ struct TileCoord {
   int64_t m_end;   // one past the expert's last row (rows >= m_end are not this tile's)
 };
 
-template <int BM, int BN>
+template <int BM, int BN, int BAND = 1>
 struct GroupedScheduler {
   // Only the cursor lives here; offsets, expert ids, group count and N are read from the
   // kernel's parameter block (constant memory) at each call, so they cost no registers.
@@ -34,6 +38,7 @@ struct GroupedScheduler {
   int64_t base = 0;     // id of the first tile of group e
   int64_t e_tiles = 0;  // tiles of group e
   int64_t r0 = 0, r1 = 0;  // rows of group e
+  int64_t rt = 0;          // row tiles of group e
 
   // t must not decrease between calls.  Returns false past the last tile.  Args has
   // offsets [E+1], expert_ids [E] (or nullptr), E (groups) and N.
@@ -46,14 +51,18 @@ struct GroupedScheduler {
       if (e >= a.E) return false;
       r0 = ldg_s32(a.offsets + e);
       r1 = ldg_s32(a.offsets + e + 1);
-      e_tiles = ((r1 - r0 + BM - 1) / BM) * (int64_t)n_tiles;
+      rt = (r1 - r0 + BM - 1) / BM;
+      e_tiles = rt * (int64_t)n_tiles;
       be = a.expert_ids ? ldg_s32(a.expert_ids + e) : e;
     }
     const int64_t local = t - base;
+    const int64_t band = local / ((int64_t)BAND * n_tiles);
+    const int64_t in_band = local - band * BAND * n_tiles;
+    const int64_t band_rows = rt - band * BAND < BAND ? rt - band * BAND : BAND;
     c.e = e;
     c.be = be;
-    c.m0 = r0 + (local / n_tiles) * BM;
-    c.n0 = (int)(local % n_tiles) * BN;
+    c.m0 = r0 + (band * BAND + in_band % band_rows) * BM;
+    c.n0 = (int)(in_band / band_rows) * BN;
     c.m_end = r1;
     return true;
   }
