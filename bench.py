@@ -359,6 +359,66 @@ def time_secondary(cfg, args, flush, stream, peaks, peak_src):
     return out
 
 
+def time_mx_skewed(args, flush, stream, peaks, peak_src):
+    """MXFP8 on config 2's routing and shape (64 experts, 16384 token rows by Zipf(1.2),
+    N=2048, K=7168): the library's own kernel choice and each forced form (CTA-pair tiles for
+    every expert, swap-AB tiles for every expert, and the split by expert size), same
+    protocol.  The MXFP8 kernels pick one form per launch; this line shows what that costs on
+    skewed routing."""
+    import os
+    import numpy as np
+    import torch
+    import gen
+    import block_scaled_fp8_persistent_gb300 as bsfp8
+    dev = flush.device
+    counts = gen.config_counts(2)
+    N, K = gen.CONFIG_SHAPES[2]
+    p = gen.mx_problem(counts, N, K, seed=2)
+    d = {k: torch.from_numpy(np.ascontiguousarray(getattr(p, k))).to(dev)
+         for k in ("A", "B", "a_scales", "b_scales", "offsets")}
+    C = torch.empty((p.M_total, N), dtype=torch.bfloat16, device=dev)
+    out = {"workload": "MXFP8 on config 2's routing: E=64 M_total=16384 (Zipf 1.2) N=2048 K=7168",
+           "experts_with_256_rows_or_more": int(sum(int(c) >= 256 for c in counts)),
+           "algorithmic_bytes": p.bytes(), "forms": {}}
+    saved = os.environ.get("BSFP8_MX_KERNEL")
+    try:
+        for form in ("plan", "pair", "swap", "split"):
+            if form == "plan":
+                os.environ.pop("BSFP8_MX_KERNEL", None)
+            else:
+                os.environ["BSFP8_MX_KERNEL"] = form
+
+            def step():
+                bsfp8.bsmxfp8_grouped_gemm(d["A"], d["B"], d["a_scales"], d["b_scales"],
+                                           d["offsets"], C, p.M_total, N, K, p.E, stream=stream)
+
+            for _ in range(args.warmup):
+                step()
+            starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+            ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+            torch.cuda.synchronize()
+            for i in range(args.steps):
+                flush.fill_(i & 0xFF)
+                starts[i].record(stream)
+                step()
+                ends[i].record(stream)
+            torch.cuda.synchronize()
+            ms = statistics.mean(s.elapsed_time(e) for s, e in zip(starts, ends))
+            gbs = p.bytes() / (ms * 1e-3) / 1e9
+            out["forms"][form] = {"ms_per_step": ms, "TFLOP/s": p.flops() / (ms * 1e-3) / 1e12,
+                                  "achieved_gbs": gbs, "hbm_frac": gbs / peaks["hbm_gbs"],
+                                  "device_error": bsfp8.bsfp8_get_device_error(stream)}
+    finally:
+        if saved is None:
+            os.environ.pop("BSFP8_MX_KERNEL", None)
+        else:
+            os.environ["BSFP8_MX_KERNEL"] = saved
+    out["hbm_peak_source"] = f"{peak_src} copy bandwidth"
+    del d, C
+    torch.cuda.empty_cache()
+    return out
+
+
 FP4_PAIRS = (("mxfp8", "mxfp4"), ("mxfp4", "mxfp4"), ("nvfp4", "nvfp4"))
 
 
@@ -642,6 +702,8 @@ def run_ours(args):
     if not args.no_secondary:
         ref_ms = secondary.get("ms_per_step") if secondary else None
         fp4 = guarded(time_fp4_formats, args, flush, stream, peaks, ref_ms)
+    mx_skewed = None if args.no_secondary else guarded(time_mx_skewed, args, flush, stream,
+                                                       peaks, peak_src)
 
     clocks = sampler.stop()  # sampled from before the warm-up through the timings above
 
@@ -679,6 +741,8 @@ def run_ours(args):
         line["extra"] = extra
     if fp4 is not None:
         line["fp4_formats"] = fp4
+    if mx_skewed is not None:
+        line["mx_skewed_routing"] = mx_skewed
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()

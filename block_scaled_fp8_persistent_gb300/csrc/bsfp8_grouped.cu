@@ -198,7 +198,7 @@ bsfp8_blockwise_kernel(const __grid_constant__ CUtensorMap tmA,
     int status;
     int64_t row_tiles;
     validate_offsets<C::BM>(args.offsets, args.expert_ids, args.E, args.num_experts, args.M_total,
-                            DEV_BAD_OFFSETS, DEV_BAD_EXPERT_IDS, status, row_tiles);
+                            args.min_group_rows, args.max_group_rows, DEV_BAD_OFFSETS, DEV_BAD_EXPERT_IDS, status, row_tiles);
     if (lane == 0) {
       ctl->valid = status == 0;
       ctl->total_tiles = row_tiles * ((args.N + C::BN - 1) / C::BN);
@@ -428,37 +428,38 @@ bsfp8_blockwise_kernel(const __grid_constant__ CUtensorMap tmA,
       const int64_t be = args.expert_ids ? ldg_s32(args.expert_ids + tc.e) : tc.e;
       // Scales: loaded two K blocks ahead of their use, a_scales[kb, row] (one load per lane,
       // consecutive K blocks M_total apart, their lines prefetched into L1 SCALE_LOOKAHEAD K
-      // blocks ahead) and b_scales[be, blk, kb] (uniform per warp).
+      // blocks ahead) and b_scales[be, blk, kb] (uniform per warp).  Every lane loads from a
+      // valid address without a predicate: rows past M_total read row 0 and scale blocks past
+      // N read block 0 (those results are never stored), and K blocks past the last re-read it.
       const float* sa_ptr = a_scales + (row_in ? row : 0);
       const float* sb_lo = b_scales + (be * nblk + (lo_in ? blk_lo : 0)) * KB;
       const float* sb_hi = b_scales + (be * nblk + (hi_in ? blk_hi : 0)) * KB;
       float2 acc[C::COLS / 2];  // columns 2j, 2j+1
 #pragma unroll
       for (int j = 0; j < C::COLS / 2; ++j) acc[j] = make_float2(0.0f, 0.0f);
-      if (row_in) {
-        for (int k = 2; k < C::SCALE_LOOKAHEAD && k < KB; ++k)
-          prefetch_l1(sa_ptr + (int64_t)k * args.M_total);
-      }
+      for (int k = 2; k < C::SCALE_LOOKAHEAD && k < KB; ++k)
+        prefetch_l1(sa_ptr + (int64_t)k * args.M_total);
       // K block kb's values (sa_n, sbl_n, sbh_n) and K block kb + 1's (sa_2, ...)
-      float sa_n = row_in ? ldg_f32(sa_ptr) : 0.0f;
-      float sbl_n = lo_in ? ldg_f32(sb_lo) : 0.0f;
-      float sbh_n = (!C::ONE_BLOCK && hi_in) ? ldg_f32(sb_hi) : 0.0f;
-      float sa_2 = (row_in && KB > 1) ? ldg_f32(sa_ptr + args.M_total) : 0.0f;
-      float sbl_2 = (lo_in && KB > 1) ? ldg_f32(sb_lo + 1) : 0.0f;
-      float sbh_2 = (!C::ONE_BLOCK && hi_in && KB > 1) ? ldg_f32(sb_hi + 1) : 0.0f;
+      const int kb1 = KB > 1 ? 1 : 0;
+      float sa_n = ldg_f32(sa_ptr);
+      float sbl_n = ldg_f32(sb_lo);
+      float sbh_n = C::ONE_BLOCK ? 0.0f : ldg_f32(sb_hi);
+      float sa_2 = ldg_f32(sa_ptr + (int64_t)kb1 * args.M_total);
+      float sbl_2 = ldg_f32(sb_lo + kb1);
+      float sbh_2 = C::ONE_BLOCK ? 0.0f : ldg_f32(sb_hi + kb1);
+      const uint32_t taddr0 = tmem_base + ((quarter * 32) << 16) + half * C::COLS;
       for (int kb = 0; kb < KB; ++kb) {
         const float s_lo = sa_n * sbl_n;
         const float s_hi = C::ONE_BLOCK ? s_lo : sa_n * sbh_n;
         sa_n = sa_2;
         sbl_n = sbl_2;
         sbh_n = sbh_2;
-        if (row_in && kb + C::SCALE_LOOKAHEAD < KB)
-          prefetch_l1(sa_ptr + (int64_t)(kb + C::SCALE_LOOKAHEAD) * args.M_total);
-        if (kb + 2 < KB) {
-          sa_2 = row_in ? ldg_f32(sa_ptr + (int64_t)(kb + 2) * args.M_total) : 0.0f;
-          sbl_2 = lo_in ? ldg_f32(sb_lo + kb + 2) : 0.0f;
-          if constexpr (!C::ONE_BLOCK) sbh_2 = hi_in ? ldg_f32(sb_hi + kb + 2) : 0.0f;
-        }
+        const int kp = kb + C::SCALE_LOOKAHEAD < KB ? kb + C::SCALE_LOOKAHEAD : KB - 1;
+        prefetch_l1(sa_ptr + (int64_t)kp * args.M_total);
+        const int k2 = kb + 2 < KB ? kb + 2 : KB - 1;
+        sa_2 = ldg_f32(sa_ptr + (int64_t)k2 * args.M_total);
+        sbl_2 = ldg_f32(sb_lo + k2);
+        if constexpr (!C::ONE_BLOCK) sbh_2 = ldg_f32(sb_hi + k2);
         // the K block's MMAs are done when its operand stage's empty barrier completes
         const bool got = __all_sync(
             0xffffffffu, mbar_wait_cg<C::CG>(empty_bar(op_stage), op_phase, abort));
@@ -468,8 +469,7 @@ bsfp8_blockwise_kernel(const __grid_constant__ CUtensorMap tmA,
           break;
         }
         tc_fence_after();
-        const uint32_t taddr =
-            tmem_base + ((quarter * 32) << 16) + acc_stage * C::BN + half * C::COLS;
+        const uint32_t taddr = taddr0 + acc_stage * C::BN;
         // 16-column chunks never straddle a 128-column scale block
         auto chunk_scale = [&](int c) { return ((col0 + 16 * c) / 128 == blk_lo) ? s_lo : s_hi; };
         if constexpr (C::LOAD_ALL) {

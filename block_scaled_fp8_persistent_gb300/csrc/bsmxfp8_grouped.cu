@@ -354,7 +354,7 @@ bsmxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     int status;
     int64_t row_tiles;
     validate_offsets<C::TN>(args.offsets, args.expert_ids, args.E, args.num_experts, args.M_total,
-                            DEV_BAD_OFFSETS, DEV_BAD_EXPERT_IDS, status, row_tiles);
+                            args.min_group_rows, args.max_group_rows, DEV_BAD_OFFSETS, DEV_BAD_EXPERT_IDS, status, row_tiles);
     if (lane == 0) {
       ctl->valid = status == 0;
       ctl->total_tiles = row_tiles * (args.N / WROWS);

@@ -167,15 +167,31 @@ BlockwiseTile choose_blockwise_tile(int64_t M_total, int N, int E, int num_sms) 
   return pair224 <= pair192 ? TILE_PAIR_224 : TILE_PAIR_192;
 }
 
-// MXFP8 kernel choice: experts averaging at least 256 token rows use the CTA-pair 256 x 256
-// tiles with overlapping accumulators; smaller ones the swap-AB tiles.  BSFP8_MX_KERNEL
-// (pair | swap) overrides it.
-bool use_mx_pair(int64_t M_total, int E) {
+// MXFP8 kernel choice from the average token rows per expert (the per-expert counts live on
+// the device).  Measured on GB300 (K = 7168, N = 2048 / 4096, L2 flushed):
+//  - balanced routing favours the swap-AB tiles up to ~50 rows per expert (128 experts x
+//    16-32 rows: 597 us against 692 us on the CTA-pair kernel; x 32-64 rows: 613 against
+//    707) and the CTA-pair kernel from ~60 (64 experts x 48-80 rows: 373 against 404);
+//  - Zipf-skewed routing favours the CTA-pair kernel already at 32 rows per expert (64
+//    experts x 2048 rows: 189 us against 235; 128 x 4096: 676 against 904), its heavy
+//    experts' tiles sharing each wave with the light experts' weight-streaming tiles;
+//  - the split (experts with >= kMxPairMinRows rows on the CTA-pair kernel, then the others
+//    on 64-row swap-AB tiles, two launches one after the other) stays near the better of the
+//    two between 24 and 56 rows per expert: balanced 611 / 618 us (swap-AB 607 / 613),
+//    skewed 201 / 663 / 225 us (CTA-pair 190 / 684 / 196, swap-AB 235 / 903 / 225).
+// So: swap-AB up to 24 rows per expert, the split up to 56, the CTA-pair kernel above.
+// BSFP8_MX_KERNEL (pair | swap | split) overrides the choice.
+constexpr int64_t kMxPairMinRows = 256;
+enum class MxPlan { Swap, Pair, Split };
+MxPlan choose_mx_plan(int64_t M_total, int E) {
   if (const char* v = std::getenv("BSFP8_MX_KERNEL")) {
-    if (!std::strcmp(v, "pair")) return true;
-    if (!std::strcmp(v, "swap")) return false;
+    if (!std::strcmp(v, "pair")) return MxPlan::Pair;
+    if (!std::strcmp(v, "swap")) return MxPlan::Swap;
+    if (!std::strcmp(v, "split")) return MxPlan::Split;
   }
-  return M_total >= (int64_t)256 * E;
+  if (M_total <= (int64_t)24 * E) return MxPlan::Swap;
+  if (E > 1 && M_total <= (int64_t)56 * E) return MxPlan::Split;
+  return MxPlan::Pair;
 }
 
 // Token rows per MXFP8 tile: the smallest of 32 / 64 / 128 that holds the average expert
@@ -235,19 +251,26 @@ bsfp8_status mx_gemm(const void* A, const void* B, const uint8_t* a_scales,
   if (M_total == 0) return BSFP8_OK;
   GemmArgs args{offsets, a_scales, b_scales, C, M_total, N, K, G, dev->err_word, ids, E,
                 packed_b ? 1 : 0};
-  if (use_mx_pair(M_total, G)) {
-    CUtensorMap tmA, tmB;
-    if (!encode_u8_2d(&tmA, A, (uint64_t)K, (uint64_t)M_total, 128, 128) ||
-        !encode_u8_2d(&tmB, B, (uint64_t)K, (uint64_t)E * N, 128, 128))
+  const MxPlan plan = choose_mx_plan(M_total, G);
+  CUtensorMap tmB;
+  if (!encode_u8_2d(&tmB, B, (uint64_t)K, (uint64_t)E * N, 128, 128)) return BSFP8_ERR_CUDA;
+  if (plan != MxPlan::Swap) {
+    CUtensorMap tmA;
+    if (!encode_u8_2d(&tmA, A, (uint64_t)K, (uint64_t)M_total, 128, 128)) return BSFP8_ERR_CUDA;
+    GemmArgs heavy = args;
+    if (plan == MxPlan::Split) heavy.min_group_rows = kMxPairMinRows;
+    if (launch_bsmxfp8_pair(tmA, tmB, heavy, dev->num_sms, stream) != cudaSuccess)
       return BSFP8_ERR_CUDA;
-    return launch_bsmxfp8_pair(tmA, tmB, args, dev->num_sms, stream) == cudaSuccess
-               ? BSFP8_OK
-               : BSFP8_ERR_CUDA;
+    if (plan == MxPlan::Pair) return BSFP8_OK;
+    args.max_group_rows = kMxPairMinRows;
   }
-  const int tn = choose_mx_token_tile(M_total, G);
-  CUtensorMap tmA, tmB;
-  if (!encode_u8_2d(&tmA, A, (uint64_t)K, (uint64_t)M_total, 128, (uint32_t)tn) ||
-      !encode_u8_2d(&tmB, B, (uint64_t)K, (uint64_t)E * N, 128, 128))
+  // the groups below kMxPairMinRows rows under Split run 64-row token tiles (measured faster
+  // than 32 or 128 rows there)
+  const int tn = plan == MxPlan::Split && !std::getenv("BSFP8_MX_TN")
+                     ? 64
+                     : choose_mx_token_tile(M_total, G);
+  CUtensorMap tmA;
+  if (!encode_u8_2d(&tmA, A, (uint64_t)K, (uint64_t)M_total, 128, (uint32_t)tn))
     return BSFP8_ERR_CUDA;
   return launch_bsmxfp8(tn, tmA, tmB, args, dev->num_sms, stream) == cudaSuccess ? BSFP8_OK
                                                                                  : BSFP8_ERR_CUDA;

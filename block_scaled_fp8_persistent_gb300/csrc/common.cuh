@@ -30,6 +30,10 @@ struct GemmArgs {
   const int32_t* expert_ids;  // [E] group -> expert (rows of B and B scales); nullptr: identity
   int num_experts;         // experts in B (bound of expert_ids)
   int b_scales_packed;     // MX swap-AB kernel: b_scales in the 512-byte block layout
+  // Groups this launch computes: those with min_group_rows <= rows < max_group_rows (the
+  // others own no tiles here; a second launch with the complementary range takes them).
+  int64_t min_group_rows = 0;
+  int64_t max_group_rows = INT64_MAX;
 };
 
 // Tile configurations of the blockwise kernel.

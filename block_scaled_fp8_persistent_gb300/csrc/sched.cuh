@@ -11,7 +11,9 @@
 // Partitions section), and maps a tile id to (expert, first row, first column) by walking
 // the expert row offsets forward -- the ids a CTA visits only grow, so each role keeps a
 // cursor and the walk costs O(E + tiles) per CTA without any table in memory.  Experts
-// with no rows own no tiles.  Row segments are groups; group g multiplies the weights (B
+// with no rows own no tiles, and so do groups whose row count lies outside the launch's
+// [min_group_rows, max_group_rows) (two launches of different tile forms split the groups
+// by size).  Row segments are groups; group g multiplies the weights (B
 // rows and B scales) of expert expert_ids[g], the mapping from group index to expert rows of
 // B in promote_accumulators (MAX kernels, grouped_matmul_sm100_blockwise_fp8, Args); without
 // an expert_ids array group g uses expert g.
@@ -41,7 +43,7 @@ struct GroupedScheduler {
   int64_t rt = 0;          // row tiles of group e
 
   // t must not decrease between calls.  Returns false past the last tile.  Args has
-  // offsets [E+1], expert_ids [E] (or nullptr), E (groups) and N.
+  // offsets [E+1], expert_ids [E] (or nullptr), E (groups), N and the group row range.
   template <class Args>
   __device__ bool locate(const Args& a, int64_t t, TileCoord& c) {
     const int n_tiles = (a.N + BN - 1) / BN;  // the last column tile may be partial
@@ -51,7 +53,8 @@ struct GroupedScheduler {
       if (e >= a.E) return false;
       r0 = ldg_s32(a.offsets + e);
       r1 = ldg_s32(a.offsets + e + 1);
-      rt = (r1 - r0 + BM - 1) / BM;
+      const int64_t rows = r1 - r0;
+      rt = (rows >= a.min_group_rows && rows < a.max_group_rows) ? (rows + BM - 1) / BM : 0;
       e_tiles = rt * (int64_t)n_tiles;
       be = a.expert_ids ? ldg_s32(a.expert_ids + e) : e;
     }
@@ -69,11 +72,13 @@ struct GroupedScheduler {
 };
 
 // Validate the group offsets (and the expert ids, when given) and count the row tiles (sum
-// over groups of ceil(M_g / BM)).  Executed by one full warp; every lane gets the results:
-// status 0, or the device error code (bad_offsets_code / bad_ids_code) to report.
+// over the groups with min_rows <= M_g < max_rows of ceil(M_g / BM)).  Executed by one full
+// warp; every lane gets the results: status 0, or the device error code (bad_offsets_code /
+// bad_ids_code) to report.
 template <int BM>
 __device__ __forceinline__ void validate_offsets(const int32_t* off, const int32_t* ids, int E,
                                                  int num_experts, int64_t M_total,
+                                                 int64_t min_rows, int64_t max_rows,
                                                  int bad_offsets_code, int bad_ids_code,
                                                  int& status, int64_t& row_tiles) {
   const uint32_t lane = lane_id();
@@ -82,7 +87,7 @@ __device__ __forceinline__ void validate_offsets(const int32_t* off, const int32
   for (int e = (int)lane; e < E; e += 32) {
     const int a = ldg_s32(off + e), b = ldg_s32(off + e + 1);
     if (b < a) good = 0;
-    else tiles += (b - a + BM - 1) / BM;
+    else if (b - a >= min_rows && b - a < max_rows) tiles += (b - a + BM - 1) / BM;
     if (ids) {
       const int x = ldg_s32(ids + e);
       if (x < 0 || x >= num_experts) good_ids = 0;

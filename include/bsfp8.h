@@ -108,12 +108,16 @@ bsfp8_status bsfp8_grouped_gemm(const void* A, const void* B, const float* a_sca
  *   expert_offsets int32 [num_experts+1]         as for bsfp8_grouped_gemm
  *   C              bf16 [M_total, N]             output
  *
- * Same requirements, ownership and error behaviour as bsfp8_grouped_gemm.  When experts
- * average fewer than 256 token rows, tiles pair 128 rows of an expert's weights with up to
- * 32 / 64 / 128 of its token rows ("swap-AB"; the height follows M_total / num_experts,
- * environment variable BSFP8_MX_TN = 32 | 64 | 128 overrides it); otherwise CTA-pair
- * 256 x 256 tiles with overlapping double-buffered TMEM accumulators are used (environment
- * variable BSFP8_MX_KERNEL = swap | pair overrides the choice).
+ * Same requirements, ownership and error behaviour as bsfp8_grouped_gemm.  Tile forms:
+ * "swap-AB" tiles pair 128 rows of an expert's weights with up to 32 / 64 / 128 of its token
+ * rows (the height follows M_total / num_experts); CTA-pair 256 x 256 tiles have overlapping
+ * double-buffered TMEM accumulators.  With at most 24 token rows per expert on average the
+ * call runs swap-AB tiles, above 56 the CTA-pair tiles, and in between both kernels one after
+ * the other on `stream`: experts with at least 256 rows on the CTA-pair tiles, the others on
+ * swap-AB tiles of 64 token rows, each kernel writing its own experts' rows of C (the
+ * per-expert counts are only known on the device).  Environment variables override the
+ * choice: BSFP8_MX_KERNEL = swap | pair | split, BSFP8_MX_TN = 32 | 64 | 128 (swap-AB
+ * height).  Every form meets the same accuracy bound.
  */
 bsfp8_status bsmxfp8_grouped_gemm(const void* A, const void* B, const uint8_t* a_scales,
                                   const uint8_t* b_scales, const int32_t* expert_offsets,

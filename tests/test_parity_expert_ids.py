@@ -14,14 +14,14 @@ pytestmark = pytest.mark.gpu
 
 BLOCKWISE_TILES = ["cta1_96", "pair_192", "cta1_256", "pair_256", "cta1_96x192", "pair_192x192",
                    "pair_224"]
-MX_FORMS = ["swap32", "swap128", "pair"]
+MX_FORMS = ["swap32", "swap128", "pair", "split"]
 
 
 def _set_form(monkeypatch, mode, form):
     if mode == "blockwise":
         monkeypatch.setenv("BSFP8_BLOCKWISE_TILE", form)
-    elif form == "pair":
-        monkeypatch.setenv("BSFP8_MX_KERNEL", "pair")
+    elif form in ("pair", "split"):
+        monkeypatch.setenv("BSFP8_MX_KERNEL", form)
     else:
         monkeypatch.setenv("BSFP8_MX_KERNEL", "swap")
         monkeypatch.setenv("BSFP8_MX_TN", form[4:])

@@ -12,12 +12,12 @@ from helpers import parity_report
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(params=["swap32", "swap64", "swap128", "pair"])
+@pytest.fixture(params=["swap32", "swap64", "swap128", "pair", "split"])
 def tn(request, monkeypatch):
-    """The MXFP8 kernel form: swap-AB with 32/64/128 token rows per tile, or CTA-pair
-    256 x 256 tiles with overlapping accumulators."""
-    if request.param == "pair":
-        monkeypatch.setenv("BSFP8_MX_KERNEL", "pair")
+    """The MXFP8 kernel form: swap-AB with 32/64/128 token rows per tile, CTA-pair 256 x 256
+    tiles with overlapping accumulators, or both launches with the groups split by size."""
+    if request.param in ("pair", "split"):
+        monkeypatch.setenv("BSFP8_MX_KERNEL", request.param)
     else:
         monkeypatch.setenv("BSFP8_MX_KERNEL", "swap")
         monkeypatch.setenv("BSFP8_MX_TN", request.param[4:])
@@ -45,6 +45,7 @@ CASES = [
     ("one_expert_many_rows", [300], 128, 256),
     ("mixed", [0, 129, 64, 65, 2, 0, 31], 256, 384),
     ("single_k_block", [130, 0, 5], 256, 128),
+    ("sizes_both_sides", [300, 7, 0, 45, 260, 129, 1, 256, 255], 256, 512),
 ]
 
 

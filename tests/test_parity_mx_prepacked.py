@@ -30,12 +30,13 @@ def test_pack_kernel_matches_oracle(E, N, K):
     assert np.array_equal(got, oracle.pack_mx_scales(sb.reshape(E * N, K // 32)))
 
 
-@pytest.fixture(params=["swap32", "swap64", "swap128", "pair"])
+@pytest.fixture(params=["swap32", "swap64", "swap128", "pair", "split"])
 def form(request, monkeypatch):
-    """Kernel form: swap-AB tiles of 32 / 64 / 128 token rows, or CTA-pair 256 x 256 tiles
-    (both read pre-packed weight scales); the row-major comparison runs the same form."""
-    if request.param == "pair":
-        monkeypatch.setenv("BSFP8_MX_KERNEL", "pair")
+    """Kernel form: swap-AB tiles of 32 / 64 / 128 token rows, CTA-pair 256 x 256 tiles, or
+    both with the groups split by size (all read pre-packed weight scales); the row-major
+    comparison runs the same form."""
+    if request.param in ("pair", "split"):
+        monkeypatch.setenv("BSFP8_MX_KERNEL", request.param)
     else:
         monkeypatch.setenv("BSFP8_MX_KERNEL", "swap")
         monkeypatch.setenv("BSFP8_MX_TN", request.param[4:])
@@ -61,7 +62,8 @@ def _run_both(p):
 
 CASES = [("decode_like", [3, 17, 0, 32, 1, 9], 256, 512),
          ("ragged", [40, 0, 7, 130], 384, 640),
-         ("many_tiles", [700, 0, 513], 640, 512)]
+         ("many_tiles", [700, 0, 513], 640, 512),
+         ("sizes_both_sides", [300, 7, 0, 45, 260, 129], 256, 1024)]
 
 
 @pytest.mark.parametrize("name,counts,N,K", CASES, ids=[c[0] for c in CASES])
