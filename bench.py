@@ -363,8 +363,7 @@ def time_mx_skewed(args, flush, stream, peaks, peak_src):
     """MXFP8 on config 2's routing and shape (64 experts, 16384 token rows by Zipf(1.2),
     N=2048, K=7168): the library's own kernel choice and each forced form (CTA-pair tiles for
     every expert, swap-AB tiles for every expert, and the split by expert size), same
-    protocol.  The MXFP8 kernels pick one form per launch; this line shows what that costs on
-    skewed routing."""
+    protocol: the library's choice against each form on skewed routing."""
     import os
     import numpy as np
     import torch
