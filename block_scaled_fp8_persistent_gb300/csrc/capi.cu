@@ -224,17 +224,32 @@ bsfp8_status blockwise_gemm(const void* A, const void* B, const float* a_scales,
   DeviceInfo* dev = nullptr;
   if ((st = device_info(&dev)) != BSFP8_OK) return st;
   if (M_total == 0) return BSFP8_OK;
-  const BlockwiseTile tile = choose_blockwise_tile(M_total, N, G, dev->num_sms);
-  CUtensorMap tmA, tmB;
-  if (!encode_u8_2d(&tmA, A, (uint64_t)K, (uint64_t)M_total, 128,
-                    (uint32_t)blockwise_a_rows(tile)) ||
-      !encode_u8_2d(&tmB, B, (uint64_t)K, (uint64_t)E * N, 128,
-                    (uint32_t)blockwise_b_rows(tile)))
-    return BSFP8_ERR_CUDA;
   GemmArgs args{offsets, a_scales, b_scales, C, M_total, N, K, G, dev->err_word, ids, E, 0};
-  return launch_bsfp8_blockwise(tile, tmA, tmB, args, dev->num_sms, stream) == cudaSuccess
-             ? BSFP8_OK
-             : BSFP8_ERR_CUDA;
+  auto run = [&](BlockwiseTile tile, const GemmArgs& a) {
+    CUtensorMap tmA, tmB;
+    if (!encode_u8_2d(&tmA, A, (uint64_t)K, (uint64_t)M_total, 128,
+                      (uint32_t)blockwise_a_rows(tile)) ||
+        !encode_u8_2d(&tmB, B, (uint64_t)K, (uint64_t)E * N, 128,
+                      (uint32_t)blockwise_b_rows(tile)))
+      return BSFP8_ERR_CUDA;
+    return launch_bsfp8_blockwise(tile, tmA, tmB, a, dev->num_sms, stream) == cudaSuccess
+               ? BSFP8_OK
+               : BSFP8_ERR_CUDA;
+  };
+  if (const char* v = std::getenv("BSFP8_BLOCKWISE_TILE")) {
+    if (!std::strcmp(v, "split")) {
+      // groups of at least split_rows rows on 224-row CTA-pair tiles, then the others on
+      // 96-row tiles (two launches on `stream`, each over its own groups)
+      const char* r = std::getenv("BSFP8_BLOCKWISE_SPLIT_ROWS");
+      const int64_t split_rows = r ? std::atoll(r) : 448;
+      GemmArgs heavy = args, light = args;
+      heavy.min_group_rows = split_rows;
+      light.max_group_rows = split_rows;
+      const bsfp8_status s1 = run(TILE_PAIR_224, heavy);
+      return s1 != BSFP8_OK ? s1 : run(TILE_CTA1_96, light);
+    }
+  }
+  return run(choose_blockwise_tile(M_total, N, G, dev->num_sms), args);
 }
 
 // packed_b: b_scales are in the 512-byte block layout of bsmxfp8_pack_b_scales (both kernels:

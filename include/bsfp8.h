@@ -263,8 +263,12 @@ bsfp8_status bsmxfp8_tmem_plan(int block_k, int epilogue_n, int vec, int overlap
  * ceil(M_e / rows) x ceil(N / columns) per expert e.  The default picks 96 x 256 tiles on
  * one CTA, 192 x 256 on a CTA pair or 224 x 256 on an asymmetric pair (a 96-row CTA with the
  * producer and MMA warps next to a 128-row CTA of epilogue warps only) by estimated makespan.
- * This is a performance choice only: every plan computes the same result.  BSFP8_ERR_NULL /
- * BSFP8_ERR_SHAPE on bad input.
+ * This is a performance choice only: every plan computes the same result.  The environment
+ * variable BSFP8_BLOCKWISE_TILE names a tile form for the GEMM to use instead (cta1_96,
+ * pair_192, pair_224, cta1_256, pair_256, ...), or "split": groups with at least
+ * BSFP8_BLOCKWISE_SPLIT_ROWS rows (default 448) on 224 x 256 pair tiles, then the others on
+ * 96 x 256 tiles, as two kernels on the GEMM's stream; this function then reports the default
+ * plan.  BSFP8_ERR_NULL / BSFP8_ERR_SHAPE on bad input.
  */
 bsfp8_status bsfp8_blockwise_plan(int64_t M_total, int N, int num_experts, int num_sms,
                                   int32_t* out);

@@ -15,7 +15,7 @@ from helpers import parity_report
 pytestmark = pytest.mark.gpu
 
 TILES = ["cta1_256", "pair_256", "pair_160", "pair_128", "cta1_128", "cta1_96", "pair_192",
-         "cta1_96x192", "pair_192x192", "cta1_128x192", "pair_224"]
+         "cta1_96x192", "pair_192x192", "cta1_128x192", "pair_224", "split"]
 
 
 @pytest.fixture(params=TILES)
@@ -46,6 +46,7 @@ SMALL_CASES = [
     ("single_row", [1], 128, 128),
     ("many_small_experts", [5, 0, 0, 33, 128, 127, 129, 2, 0, 64], 256, 256),
     ("tail_rows_not_mult4", [3, 250, 7], 512, 384),
+    ("sizes_both_sides_of_448", [500, 3, 0, 447, 448, 130, 900], 256, 384),
 ]
 
 

@@ -13,7 +13,8 @@ pytestmark = pytest.mark.gpu
 SIZES = [0, 1, 7, 31, 32, 33, 63, 64, 65, 95, 96, 97, 127, 128, 129, 191, 192, 193, 223, 224,
          225, 255, 256, 257]
 BLOCKWISE_TILES = ["cta1_96", "pair_192", "cta1_256", "pair_256", "pair_160", "pair_128",
-                   "cta1_128", "cta1_96x192", "pair_192x192", "cta1_128x192", "pair_224"]
+                   "cta1_128", "cta1_96x192", "pair_192x192", "cta1_128x192", "pair_224",
+                   "split"]
 MX_FORMS = [("swap", "32"), ("swap", "64"), ("swap", "128"), ("pair", None), ("split", None)]
 
 
