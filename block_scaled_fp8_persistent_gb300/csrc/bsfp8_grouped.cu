@@ -482,17 +482,16 @@ bsfp8_blockwise_kernel(const __grid_constant__ CUtensorMap tmA,
           for (int c = 0; c < C::CHUNKS; ++c) promote16(acc + 8 * c, p[c], chunk_scale(c));
         } else {
           // 64-column halves: load, promote, ..., load the last half, release, promote
-          uint32_t p0[32], p1[32];
+          uint32_t p[64];
 #pragma unroll
           for (int h = 0; h < C::COLS / 64; ++h) {
-            tmem_ld_32x32b_x32(taddr + 64 * h, p0);
-            tmem_ld_32x32b_x32(taddr + 64 * h + 32, p1);
+            tmem_ld_32x32b_x64(taddr + 64 * h, p);
             tmem_ld_wait();
             if (h == C::COLS / 64 - 1) release_stage();
-            promote16(acc + 32 * h + 0, p0, chunk_scale(4 * h + 0));
-            promote16(acc + 32 * h + 8, p0 + 16, chunk_scale(4 * h + 1));
-            promote16(acc + 32 * h + 16, p1, chunk_scale(4 * h + 2));
-            promote16(acc + 32 * h + 24, p1 + 16, chunk_scale(4 * h + 3));
+            promote16(acc + 32 * h + 0, p, chunk_scale(4 * h + 0));
+            promote16(acc + 32 * h + 8, p + 16, chunk_scale(4 * h + 1));
+            promote16(acc + 32 * h + 16, p + 32, chunk_scale(4 * h + 2));
+            promote16(acc + 32 * h + 24, p + 48, chunk_scale(4 * h + 3));
           }
         }
         if (++acc_stage == C::ACC_STAGES) { acc_stage = 0; acc_phase ^= 1; }
