@@ -184,7 +184,10 @@ bsmxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     // =============================== TMA producer ===============================
     if (lane == 0) {
       GroupedScheduler<BM, BN, TILE_BAND> sched;
-      const uint64_t pol_b = l2_policy_evict_last();
+      // The band of row strips walked together keeps its rows of A in L2 while the columns of
+      // B stream past (each B column is read by the band's tiles in the same wave): A is the
+      // operand to keep.
+      const uint64_t pol_a = l2_policy_evict_last();
       uint32_t stage = 0, phase = 0;
       int64_t issued = 0;
       bool ok = true;
@@ -204,9 +207,9 @@ bsmxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
           if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), nk * SUB_TX);
           for (int u = 0; u < nk; ++u) {
             const int kb = kb0 + u;
-            tma_load_2d_pair(sA + stage * A_STAGE + u * A_SUB, &tmA, kb * BK, a_row, bar);
-            tma_load_2d_pair_hint(sB + stage * B_STAGE + u * B_SUB, &tmB, kb * BK, b_row, bar,
-                                  pol_b);
+            tma_load_2d_pair_hint(sA + stage * A_STAGE + u * A_SUB, &tmA, kb * BK, a_row, bar,
+                                  pol_a);
+            tma_load_2d_pair(sB + stage * B_STAGE + u * B_SUB, &tmB, kb * BK, b_row, bar);
           }
           ++issued;
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
