@@ -105,6 +105,10 @@ struct Cfg {
   static constexpr uint32_t SMEM_B = SMEM_A + STAGES * A_STAGE;
   static constexpr uint32_t SMEM_CTL = SMEM_B + STAGES * B_STAGE;
   static constexpr uint32_t IDESC = idesc_f8f6f4_e4m3(128 * CG, BN);
+  // Tile walk: CTA pairs take bands of 16 row tiles (row index fastest inside a band) and keep
+  // the band's A rows in L2 while B streams; one-CTA tiles take the plain order (column index
+  // fastest) and keep B, which the row tiles of an expert share within a wave.
+  static constexpr int TILE_BAND = CG == 2 ? 16 : 1;
   static_assert(ROWS == 128 || ROWS == 96, "A rows per CTA");
   static_assert(!ASYM || (ROWS == 96 && PEER_ROWS == 128), "asymmetric pair: 96 + 128 rows");
   __device__ static bool is_epilogue(uint32_t warp) {
@@ -253,7 +257,7 @@ bsfp8_blockwise_kernel(const __grid_constant__ CUtensorMap tmA,
       // stage's empty barrier.  Waits sleep (suspend-time hint): the sub-partition is shared
       // with two epilogue warps.
       const uint32_t j = warp;
-      GroupedScheduler<C::BM, C::BN> sched;
+      GroupedScheduler<C::BM, C::BN, C::TILE_BAND> sched;
       const uint64_t pol_b = l2_policy_evict_last();
       const uint64_t adesc = kmajor_sw128_desc(sA + j * C::A_STAGE);
       const uint64_t bdesc = kmajor_sw128_desc(sB + j * C::B_STAGE);
@@ -298,10 +302,12 @@ bsfp8_blockwise_kernel(const __grid_constant__ CUtensorMap tmA,
       // =============================== TMA producer ===============================
       // The producer sleeps in its barrier waits (suspend-time hint): it shares its
       // sub-partition with the MMA thread, whose issue slots set the pace.
-      GroupedScheduler<C::BM, C::BN> sched;
-      // B (expert weights) is re-read by every row tile of its expert, possibly in a later
-      // wave of tiles: keep it in L2 ahead of the streaming A rows and C output.
+      GroupedScheduler<C::BM, C::BN, C::TILE_BAND> sched;
+      // One-CTA tiles: B (expert weights) is re-read by every row tile of its expert,
+      // possibly in a later wave of tiles: keep it in L2 ahead of the streaming A rows and C
+      // output.  CTA pairs (banded walk): keep A with this policy, B at normal priority.
       const uint64_t pol_b = l2_policy_evict_last();
+      const uint64_t pol_n = l2_policy_evict_normal();
       uint32_t stage = 0, phase = 0;
       int64_t issued = 0;
       bool ok = true;
@@ -325,15 +331,16 @@ bsfp8_blockwise_kernel(const __grid_constant__ CUtensorMap tmA,
             // both CTAs' bytes are counted on the leader's barrier
             const uint32_t bar = mapa_shared(full_bar(stage), 0);
             if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), C::STAGE_TX);
-            tma_load_2d_pair(sA + stage * C::A_STAGE, &tmA, kb * BK, a_row, bar);
-            tma_load_2d_pair_hint(sB + stage * C::B_STAGE, &tmB, kb * BK, b_row, bar, pol_b);
+            // (banded walk: A is the operand the tiles in flight reuse, B streams)
+            tma_load_2d_pair_hint(sA + stage * C::A_STAGE, &tmA, kb * BK, a_row, bar, pol_b);
+            tma_load_2d_pair_hint(sB + stage * C::B_STAGE, &tmB, kb * BK, b_row, bar, pol_n);
             if constexpr (C::ASYM) {
               // the peer's A rows (after the leader's ROWS) and its half of B, into the peer's
               // shared memory at the same offsets, counted on this barrier
               tma_load_2d_mc_pair_hint(sA + stage * C::A_STAGE, &tmA, kb * BK, a_row + C::ROWS,
                                        full_bar(stage), 0x2, pol_b);
               tma_load_2d_mc_pair_hint(sB + stage * C::B_STAGE, &tmB, kb * BK, b_row + C::B_ROWS,
-                                       full_bar(stage), 0x2, pol_b);
+                                       full_bar(stage), 0x2, pol_n);
             }
           }
           ++issued;
@@ -353,7 +360,7 @@ bsfp8_blockwise_kernel(const __grid_constant__ CUtensorMap tmA,
       // ================================ MMA issuer ================================
       // One thread, and the pace of the whole pipeline: per K block two barrier tests,
       // four MMAs and one commit, with the descriptors of every stage precomputed.
-      GroupedScheduler<C::BM, C::BN> sched;
+      GroupedScheduler<C::BM, C::BN, C::TILE_BAND> sched;
       const uint64_t adesc0 = kmajor_sw128_desc(sA);
       const uint64_t bdesc0 = kmajor_sw128_desc(sB);
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
@@ -399,7 +406,7 @@ bsfp8_blockwise_kernel(const __grid_constant__ CUtensorMap tmA,
     auto tempty_mma = [&](int s) {
       return (C::CG == 2) ? mapa_shared(tempty_bar(s), 0) : tempty_bar(s);
     };
-    GroupedScheduler<C::BM, C::BN> sched;
+    GroupedScheduler<C::BM, C::BN, C::TILE_BAND> sched;
     // C rows go out as one 32-byte sector per lane when C allows it
     const bool c_vec32 = (reinterpret_cast<uintptr_t>(args.C) & 31) == 0;
     uint32_t acc_stage = 0, acc_phase = 0;  // TMEM partial ring
