@@ -35,7 +35,7 @@ FORMATS = {"mxfp8": 0, "mxfp4": 1, "nvfp4": 2}
 # Every symbol include/bsfp8.h declares (the CPU test checks the library exports them).
 EXPORTED = ("bsfp8_grouped_gemm", "bsmxfp8_grouped_gemm", "bsfp8_grouped_gemm_ids",
             "bsmxfp8_grouped_gemm_ids", "bsmxfp8_pack_b_scales", "bsmxfp8_grouped_gemm_prepacked",
-            "bsmxfp8_tmem_plan", "bsfp8_blockwise_plan",
+            "bsmxfp8_tmem_plan", "bsfp8_blockwise_plan", "bsmxfp8_plan",
             "bsmx_grouped_gemm", "bsfp8_get_device_error", "bsfp8_check_wait_timeout",
             "bsfp8_status_string")
 
@@ -78,6 +78,8 @@ def load_library() -> ctypes.CDLL:
         lib.bsfp8_blockwise_plan.argtypes = [ctypes.c_int64, i32, i32, i32,
                                              ctypes.POINTER(ctypes.c_int32)]
         lib.bsfp8_blockwise_plan.restype = i32
+        lib.bsmxfp8_plan.argtypes = [ctypes.c_int64, i32, ctypes.POINTER(ctypes.c_int32)]
+        lib.bsmxfp8_plan.restype = i32
         lib.bsfp8_get_device_error.argtypes = [p, ctypes.POINTER(ctypes.c_int)]
         lib.bsfp8_get_device_error.restype = i32
         lib.bsfp8_check_wait_timeout.argtypes = [ctypes.c_int64, p]
@@ -214,6 +216,17 @@ def bsfp8_blockwise_plan(M_total: int, N: int, num_experts: int, num_sms: int) -
     if st != BSFP8_OK:
         raise BsFp8Error(st, "bsfp8_blockwise_plan")
     return {"tile_rows": out[0], "tile_cols": out[1], "ctas_per_tile": out[2]}
+
+
+def bsmxfp8_plan(M_total: int, num_experts: int) -> dict:
+    """Kernel plan of the MXFP8 GEMM for M_total token rows over num_experts groups (host
+    only): which kernel(s) run, the swap-AB tile height and the split's row threshold."""
+    out = (ctypes.c_int32 * 3)()
+    st = load_library().bsmxfp8_plan(int(M_total), int(num_experts), out)
+    if st != BSFP8_OK:
+        raise BsFp8Error(st, "bsmxfp8_plan")
+    return {"kernel": ("swap", "pair", "split")[out[0]], "token_rows": out[1],
+            "split_rows": out[2]}
 
 
 def bsfp8_check_wait_timeout(limit_ns: int, stream=None) -> None:

@@ -449,6 +449,19 @@ extern "C" bsfp8_status bsfp8_blockwise_plan(int64_t M_total, int N, int num_exp
   return BSFP8_OK;
 }
 
+extern "C" bsfp8_status bsmxfp8_plan(int64_t M_total, int num_experts, int32_t* out) {
+  if (!out) return BSFP8_ERR_NULL;
+  if (M_total < 0 || num_experts < 1) return BSFP8_ERR_SHAPE;
+  const MxPlan plan = choose_mx_plan(M_total, num_experts);
+  out[0] = plan == MxPlan::Swap ? 0 : plan == MxPlan::Pair ? 1 : 2;
+  out[1] = plan == MxPlan::Pair ? 0
+           : plan == MxPlan::Split && !std::getenv("BSFP8_MX_TN")
+               ? 64
+               : choose_mx_token_tile(M_total, num_experts);
+  out[2] = plan == MxPlan::Split ? (int32_t)kMxPairMinRows : 0;
+  return BSFP8_OK;
+}
+
 extern "C" bsfp8_status bsfp8_get_device_error(cudaStream_t stream, int* code) {
   if (!code) return BSFP8_ERR_NULL;
   DeviceInfo* dev = nullptr;

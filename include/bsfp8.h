@@ -274,6 +274,17 @@ bsfp8_status bsfp8_blockwise_plan(int64_t M_total, int N, int num_experts, int n
                                   int32_t* out);
 
 /*
+ * Kernel plan bsmxfp8_grouped_gemm (and its _ids / _prepacked forms) uses for M_total token
+ * rows over num_experts row groups (host only, no GPU use; BSFP8_MX_KERNEL and BSFP8_MX_TN
+ * are honoured as in the GEMM): out[0] = 0 for swap-AB tiles, 1 for CTA-pair 256 x 256 tiles,
+ * 2 for both (split by rows per group); out[1] = token rows per swap-AB tile (0 when only the
+ * CTA-pair kernel runs); out[2] = the split's row threshold (groups with at least this many
+ * rows run on the CTA-pair tiles; 0 without a split).  A performance choice only: every plan
+ * meets the same accuracy bound.  BSFP8_ERR_NULL / BSFP8_ERR_SHAPE on bad input.
+ */
+bsfp8_status bsmxfp8_plan(int64_t M_total, int num_experts, int32_t* out);
+
+/*
  * Read the device error word of the current device (after synchronising `stream`) into
  * *code (0, BSFP8_ERR_DEVICE_OFFSETS, BSFP8_ERR_DEVICE_TIMEOUT or BSFP8_ERR_DEVICE_EXPERT_IDS)
  * and reset it to 0.
