@@ -20,13 +20,16 @@ import ctypes
 import os
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "lib", "libbsfp8.so")
+# The library: lib/libbsfp8.so, or the build named by BSFP8_LIBRARY (for example the
+# bounds-checking lib/libbsfp8_debug.so that build.build(debug=True) makes).
+LIB_PATH = os.environ.get("BSFP8_LIBRARY") or os.path.join(_PKG, "lib", "libbsfp8.so")
 
 BSFP8_OK = 0
 STATUS_NAMES = {
     0: "BSFP8_OK", 1: "BSFP8_ERR_NULL", 2: "BSFP8_ERR_SHAPE", 3: "BSFP8_ERR_ALIGN",
     4: "BSFP8_ERR_UNSUPPORTED_DEVICE", 5: "BSFP8_ERR_CUDA", 6: "BSFP8_ERR_DEVICE_OFFSETS",
     7: "BSFP8_ERR_DEVICE_TIMEOUT", 8: "BSFP8_ERR_DEVICE_EXPERT_IDS", 9: "BSFP8_ERR_FORMAT",
+    10: "BSFP8_ERR_DEVICE_BOUNDS",
 }
 
 # bsmx_format values of include/bsfp8.h

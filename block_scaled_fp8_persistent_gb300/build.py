@@ -3,6 +3,10 @@
 Each translation unit is compiled for sm_103a only (nvcc -gencode
 arch=compute_103a,code=sm_103a), in parallel, then linked into one shared library with
 the CUDA runtime linked statically (the driver itself is found at run time).
+
+build(debug=True) makes lib/libbsfp8_debug.so instead: the same sources with
+-DBSFP8_DEBUG=1, whose kernels check every tile's coordinates against the problem and
+record BSFP8_ERR_DEVICE_BOUNDS in the device error word instead of going out of range.
 """
 from __future__ import annotations
 
@@ -18,6 +22,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OBJDIR = os.path.join(PKG, "_build")
 LIBDIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIBDIR, "libbsfp8.so")
+DEBUG_LIB = os.path.join(LIBDIR, "libbsfp8_debug.so")
 
 SOURCES = ["capi.cu", "bsfp8_grouped.cu", "bsmxfp8_grouped.cu", "bsmxfp8_pair.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -35,23 +40,28 @@ def _deps() -> list[str]:
     return out
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(d) <= t for d in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
-    if not force and up_to_date():
-        return LIB
-    os.makedirs(OBJDIR, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False,
+          debug: bool = False) -> str:
+    lib = DEBUG_LIB if debug else LIB
+    objdir = OBJDIR + ("_debug" if debug else "")
+    if not force and up_to_date(lib):
+        return lib
+    os.makedirs(objdir, exist_ok=True)
     os.makedirs(LIBDIR, exist_ok=True)
     nvcc = _nvcc()
     extra = ["-Xptxas", "-v"] if ptxas_info else []
+    if debug:
+        extra.append("-DBSFP8_DEBUG=1")
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(OBJDIR, src.replace(".cu", ".o"))
+        obj = os.path.join(objdir, src.replace(".cu", ".o"))
         cmd = [nvcc, *ARCH, *NVCC_FLAGS, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -62,15 +72,15 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
 
     with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    build(force="--force" in sys.argv, ptxas_info="-v" in sys.argv)
-    print(LIB)
+    print(build(force="--force" in sys.argv, ptxas_info="-v" in sys.argv,
+                debug="--debug" in sys.argv))

@@ -490,6 +490,7 @@ extern "C" const char* bsfp8_status_string(bsfp8_status s) {
     case BSFP8_ERR_DEVICE_TIMEOUT: return "device: pipeline wait timed out";
     case BSFP8_ERR_DEVICE_EXPERT_IDS: return "device: expert id out of range";
     case BSFP8_ERR_FORMAT: return "unsupported operand format pair";
+    case BSFP8_ERR_DEVICE_BOUNDS: return "device (debug build): tile outside the problem";
   }
   return "unknown status";
 }

@@ -14,7 +14,16 @@ enum DeviceError : int {
   DEV_BAD_OFFSETS = 6,  // offsets[0] != 0, offsets[E] != M_total or not non-decreasing
   DEV_TIMEOUT = 7,      // a pipeline wait gave up (the kernel wound down cleanly)
   DEV_BAD_EXPERT_IDS = 8,  // an expert id outside [0, num_experts)
+  DEV_BOUNDS = 10,  // debug builds: a tile's rows, columns or expert fell outside the problem
 };
+
+// Debug builds (-DBSFP8_DEBUG=1) check every tile's coordinates against the problem before
+// any role uses them (GroupedScheduler::locate): a tile outside it records DEV_BOUNDS and
+// ends the kernel's tile walk in every role at once, instead of touching memory out of
+// range.  Release builds compile the checks away.
+#ifndef BSFP8_DEBUG
+#define BSFP8_DEBUG 0
+#endif
 
 // Plain pointers and sizes handed to every kernel (tensor maps travel separately as
 // __grid_constant__ parameters).

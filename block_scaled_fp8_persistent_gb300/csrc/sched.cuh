@@ -19,6 +19,7 @@
 // an expert_ids array group g uses expert g.
 #pragma once
 #include <cstdint>
+#include "common.cuh"
 #include "ptx.cuh"
 
 namespace bsfp8 {
@@ -67,6 +68,14 @@ struct GroupedScheduler {
     c.m0 = r0 + (band * BAND + in_band % band_rows) * BM;
     c.n0 = (int)(in_band / band_rows) * BN;
     c.m_end = r1;
+    if constexpr (BSFP8_DEBUG) {
+      const bool inside = c.m0 >= r0 && c.m0 < r1 && r1 <= a.M_total && c.n0 >= 0 &&
+                          c.n0 < a.N && c.be >= 0 && c.be < a.num_experts;
+      if (!inside) {
+        atomicCAS(a.err, 0, (int)DEV_BOUNDS);
+        return false;
+      }
+    }
     return true;
   }
 };

@@ -64,7 +64,9 @@ typedef enum {
   BSFP8_ERR_DEVICE_OFFSETS = 6,     /* device error word: invalid expert offsets */
   BSFP8_ERR_DEVICE_TIMEOUT = 7,     /* device error word: a pipeline wait gave up */
   BSFP8_ERR_DEVICE_EXPERT_IDS = 8,  /* device error word: an expert id outside [0, num_experts) */
-  BSFP8_ERR_FORMAT = 9              /* bsmx_grouped_gemm: unsupported operand format pair */
+  BSFP8_ERR_FORMAT = 9,             /* bsmx_grouped_gemm: unsupported operand format pair */
+  BSFP8_ERR_DEVICE_BOUNDS = 10      /* device error word, debug builds only: a tile's rows,
+                                       columns or expert fell outside the problem */
 } bsfp8_status;
 
 /* Operand formats of bsmx_grouped_gemm. */
@@ -286,7 +288,8 @@ bsfp8_status bsmxfp8_plan(int64_t M_total, int num_experts, int32_t* out);
 
 /*
  * Read the device error word of the current device (after synchronising `stream`) into
- * *code (0, BSFP8_ERR_DEVICE_OFFSETS, BSFP8_ERR_DEVICE_TIMEOUT or BSFP8_ERR_DEVICE_EXPERT_IDS)
+ * *code (0, BSFP8_ERR_DEVICE_OFFSETS, BSFP8_ERR_DEVICE_TIMEOUT, BSFP8_ERR_DEVICE_EXPERT_IDS, or
+ * in a debug build BSFP8_ERR_DEVICE_BOUNDS)
  * and reset it to 0.
  * The word is one per device, not per stream: every kernel of this library on the device
  * records its first error there, whatever stream it runs on.  Only `stream` is synchronised,
