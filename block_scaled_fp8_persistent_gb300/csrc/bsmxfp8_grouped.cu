@@ -14,41 +14,49 @@
 // per-expert token counts of decode (the swapAB mode of the TileScheduler in the MAX
 // grouped_matmul_sm100_blockwise_fp8 kernels).
 //
-// fp4 operands (the mxfp4 format of the same example: e2m1 elements packed two per byte
-// along K, UE8M0 scales per 32): every e2m1 value v is exactly an e4m3 value, and the e4m3
-// code (sign << 7) | (magnitude code << 2) is exactly v * 2^-6 (e2m1's subnormal 0.5 lands
-// on e4m3's subnormal 2^-7, zero on zero).  So the kernel loads the packed tiles with TMA,
-// converter warps re-encode them into the 128-byte-swizzled e4m3 tile the MMA reads, the
-// MMA and its scales are those of mxfp8, and the epilogue multiplies by 2^6 per fp4 operand
-// (exact in fp32).  The result is the mxfp8 result of the same values as long as the MMA's
-// products, 2^-6 per fp4 operand below the true ones, stay in fp32's normal range: true
-// products of magnitude at least 2^-120 (one fp4 operand) or 2^-114 (two).  (Folding 2^6
-// into the token scale codes instead measured 6-12 % slower on the decode shape.)
+// fp4 operands (the example's mxfp4 and nvfp4 formats: e2m1 elements packed two per byte
+// along K; UE8M0 scales per 32, or e4m3 scales per 16 for nvfp4), both operands fp4: the
+// packed tiles feed the fp4 block-scaled MMA kinds as TMA loads them (64-byte rows of 128 K,
+// 64-byte swizzle), two K = 64 MMAs per stage -- kind::mxf4 (scale_vec::2X: the scale-factor
+// id, 0 or 2, picks the byte pair of the stage's scale word) and kind::mxf4nvf4 with
+// scale_vec::4X (unsigned e4m3 scales; each MMA reads a whole word, so a stage has two
+// 4-column scale groups per operand).  As the example does for these pairs.
 //
-// nvfp4 (the example's third format: e2m1 with e4m3 scales per 16 K) cannot use the UE8M0
-// scale path: the converters dequantize each packed tile with its scales into fp16 (exact:
-// an e2m1 value times an e4m3 scale has at most 6 significant bits and lies inside the
-// normal fp16 range), and the MMA thread issues kind::f16 MMAs (K = 16) with no scale copies.
+// Converting forms (mxfp8 tokens with mxfp4 weights, whose only MMA kind takes K = 32 per
+// instruction; and the both-fp4 pairs on request, for comparison).  mxfp4: every e2m1 value
+// v is exactly an e4m3 value, and the e4m3 code (sign << 7) | (magnitude code << 2) is
+// exactly v * 2^-6 (e2m1's subnormal 0.5 lands on e4m3's subnormal 2^-7, zero on zero).  So
+// the kernel loads the packed tiles with TMA, converter warps re-encode them into the
+// 128-byte-swizzled e4m3 tile the MMA reads, the MMA and its scales are those of mxfp8, and
+// the epilogue multiplies by 2^6 per fp4 operand (exact in fp32).  The result is the mxfp8
+// result of the same values as long as the MMA's products, 2^-6 per fp4 operand below the
+// true ones, stay in fp32's normal range: true products of magnitude at least 2^-120 (one
+// fp4 operand) or 2^-114 (two).  (Folding 2^6 into the token scale codes instead measured
+// 6-12 % slower on the decode shape.)  nvfp4: the converters dequantize each packed tile
+// with its scales into fp16 (exact: an e2m1 value times an e4m3 scale has at most 6
+// significant bits and lies inside the normal fp16 range), and the MMA thread issues
+// kind::f16 MMAs (K = 16) with no scale copies.
 //
-// Roles (8 warps; 16 with fp4 operands):
+// Roles (8 warps; 16 in the converting forms):
 //   warp 0      TMA producer: per K stage (128 K) the weight tile [128 x 128] and the token
 //               tile [tn x 128] (128-byte swizzle; fp4 operands packed [rows x 64 B],
 //               unswizzled) into a STAGES-deep ring.
 //   warp 1      TMEM owner + MMA thread: per stage tcgen05.cp of both scale blocks into
 //               TMEM, then 4 x tcgen05.mma kind::mxf8f6f4.block_scale (K = 32 each, the
-//               scale-factor id picks the byte of the 4-byte scale word; nvfp4: 8 x
-//               kind::f16, K = 16), accumulating over all of K in a 2-deep TMEM
-//               accumulator ring.
+//               scale-factor id picks the byte of the 4-byte scale word; fp4 kinds: 2 x
+//               K = 64; converted nvfp4: 8 x kind::f16, K = 16), accumulating over all of
+//               K in a 2-deep TMEM accumulator ring.
 //   warps 2, 3  scale loaders (token rows, weight rows): per stage each row's 4 UE8M0 codes
 //               (one 4-byte word, row-major source) are cp.async'ed into the packed
 //               512-byte block (row r at byte (r%32)*16 + (r/32)*4); a few stages in
 //               flight.  With pre-packed weight scales the producer copies the weight block
-//               and warp 3 idles.  nvfp4: each row's 8 e4m3 codes of the stage, row-major,
-//               for the converters.
+//               and warp 3 idles.  nvfp4: each row's 8 e4m3 codes of the stage, as two
+//               packed blocks (codes 0-3 and 4-7) for the MMA kind, or row-major for the
+//               converters.
 //   warps 4-7   epilogue: warp w holds weight rows 32*(w%4).. of the tile, reads the tn
 //               token columns of the accumulator, rounds to bf16 and stores C[m, n] for the
 //               tile's token rows that belong to the expert.
-//   warps 8-15  (fp4 operands, tn <= 64) converters: each converted slot takes every
+//   warps 8-15  (converting forms, tn <= 64) converters: each converted slot takes every
 //               CSTAGES-th stage, whose packed weight tile (and packed token tile) its warp
 //               (nvfp4: its two warps, half the rows each) re-encodes from the load ring into
 //               the slot's e4m3 (fp16) tiles, which the MMA reads; the load ring
@@ -84,6 +92,8 @@ enum Format : int {
   FMT_MXFP8_MXFP4 = 1,  // e4m3 x e2m1
   FMT_MXFP4 = 2,        // e2m1 x e2m1
   FMT_NVFP4 = 3,        // e2m1 x e2m1 with e4m3 scales per 16 (fp16 MMA on dequantized tiles)
+  FMT_MXFP4_MMA = 4,    // e2m1 x e2m1, kind::mxf4 on the packed tiles as loaded
+  FMT_NVFP4_MMA = 5,    // e2m1 x e2m1 with UE4M3 scales per 16, kind::mxf4nvf4 (scale_vec::4X)
 };
 constexpr int SF_BLOCK = 512;        // packed scale block: 128 rows x 4 codes
 constexpr int SCALE_LOOKAHEAD = 4;   // scale stages in flight per loader warp
@@ -95,18 +105,24 @@ template <int TN_, int FMT_ = FMT_MXFP8>
 struct Cfg {
   static constexpr int TN = TN_;                               // token rows per tile
   static constexpr int FMT = FMT_;
-  static constexpr bool NV = FMT_ == FMT_NVFP4;
+  // fp4 MMA kinds: the packed tiles feed the tensor core as loaded (64-byte swizzle, K = 64
+  // per MMA), no converter warps
+  static constexpr bool NATIVE = FMT_ == FMT_MXFP4_MMA || FMT_ == FMT_NVFP4_MMA;
+  static constexpr bool NV = FMT_ == FMT_NVFP4 || FMT_ == FMT_NVFP4_MMA;
   static constexpr bool B_FP4 = FMT_ != FMT_MXFP8;
-  static constexpr bool A_FP4 = FMT_ == FMT_MXFP4 || NV;
-  static constexpr bool CONVERT = B_FP4;
+  static constexpr bool A_FP4 = FMT_ != FMT_MXFP8 && FMT_ != FMT_MXFP8_MXFP4;
+  static constexpr bool CONVERT = B_FP4 && !NATIVE;
+  static constexpr bool NV_F16 = NV && CONVERT;  // nvfp4 dequantized for the fp16 MMA
   static constexpr int THREADS = !CONVERT ? 256 : 512;
   static_assert(!CONVERT || TN <= 64, "fp4 tiles hold at most 64 token rows");
   // bytes per converted element: e4m3 for the MX formats, fp16 for nvfp4
   static constexpr uint32_t ESZ = NV ? 2 : 1;
-  // scale bytes per stage: packed UE8M0 blocks (MX), or row-major e4m3 codes per 16 K (nvfp4)
-  static constexpr uint32_t SFW_STAGE = NV ? WROWS * (BK / 16) : SF_BLOCK;
-  static constexpr uint32_t SFT_STAGE = SF_BLOCK;
-  static_assert(!NV || TN * (BK / 16) <= SFT_STAGE, "nvfp4 token scales of a stage");
+  // scale bytes per stage: packed UE8M0 blocks (MX), row-major e4m3 codes per 16 K (nvfp4 for
+  // the fp16 MMA), or two packed UE4M3 blocks, one per K = 64 MMA (nvfp4 MMA kind)
+  static constexpr int SF_GROUPS = (NV && NATIVE) ? 2 : 1;  // 4-column TMEM scale groups
+  static constexpr uint32_t SFW_STAGE = NV_F16 ? WROWS * (BK / 16) : SF_GROUPS * SF_BLOCK;
+  static constexpr uint32_t SFT_STAGE = SF_GROUPS * SF_BLOCK;
+  static_assert(!NV_F16 || TN * (BK / 16) <= SFT_STAGE, "nvfp4 token scales of a stage");
   // Load ring (STAGES deep): per stage the weight tile, the token tile and the two scale
   // blocks as they arrive -- e4m3 tiles with the 128-byte swizzle, packed e2m1 tiles
   // [rows x 64 B] without swizzle.  Byte offsets of a K block along a row: W_KX, T_KX.
@@ -125,15 +141,15 @@ struct Cfg {
   static constexpr uint32_t CT_STAGE = A_FP4 ? TN * BK * ESZ : 0;
   static constexpr uint32_t CONV_BYTES = CSTAGES * (CW_STAGE + CT_STAGE);
   static constexpr uint32_t PER_STAGE = W_STAGE + T_STAGE + SFW_STAGE + SFT_STAGE;
-  // fp4: as many load stages as fit next to the converted ring, the staging slots, the
-  // barriers and the alignment pad
+  // fp4: as many load stages as fit next to the converted ring (if any), the staging slots,
+  // the barriers and the alignment pad, at most 16 (128 KB of packed weights in flight)
   static constexpr int FIT =
       (int)((SMEM_LIMIT - CONV_BYTES - STG_SLOTS * STG_SLOT - 2048) / PER_STAGE);
-  static constexpr int STAGES = !CONVERT ? ((TN <= 32) ? 10 : (TN <= 64) ? 8 : 6)
-                                         : (FIT < 16 ? FIT : 16);
+  static constexpr int STAGES = !B_FP4 ? ((TN <= 32) ? 10 : (TN <= 64) ? 8 : 6)
+                                       : (FIT < 16 ? FIT : 16);
   static constexpr int LOOKAHEAD = SCALE_LOOKAHEAD < STAGES - 1 ? SCALE_LOOKAHEAD : STAGES - 1;
   // the epilogue's factor: 2^6 per fp4 operand undoes the re-encoding's 2^-6 (exact in fp32)
-  static constexpr float POST = NV ? 1.0f : A_FP4 ? 4096.0f : (B_FP4 ? 64.0f : 1.0f);
+  static constexpr float POST = (NV || NATIVE) ? 1.0f : A_FP4 ? 4096.0f : (B_FP4 ? 64.0f : 1.0f);
   static constexpr uint32_t SMEM_CW = 0;
   static constexpr uint32_t SMEM_CT = SMEM_CW + CSTAGES * CW_STAGE;
   static constexpr uint32_t SMEM_W = SMEM_CT + CSTAGES * CT_STAGE;
@@ -144,17 +160,22 @@ struct Cfg {
   static constexpr uint32_t SMEM_STG = SMEM_SFT + STAGES * SFT_STAGE;
   static constexpr uint32_t SMEM_CTL = SMEM_STG + STG_SLOTS * STG_SLOT;
   static constexpr uint32_t STAGE_TX = W_STAGE + T_STAGE;
-  // TMEM: 2 accumulators of TN columns, then 2 slots each of weight / token scales (4 cols)
+  // TMEM: 2 accumulators of TN columns, then 2 slots each of weight / token scales (4 columns
+  // per scale group, every group on a 4-column boundary)
   static constexpr uint32_t ACC_COLS = 2 * TN;
+  static constexpr uint32_t SF_COLS = 4 * SF_GROUPS;  // columns of one slot
   static constexpr uint32_t SFW_COL = ACC_COLS;
-  static constexpr uint32_t SFT_COL = ACC_COLS + 8;
-  static constexpr uint32_t TMEM_COLS = (ACC_COLS + 16 <= 64) ? 64 : (ACC_COLS + 16 <= 128) ? 128
-                                        : (ACC_COLS + 16 <= 256) ? 256 : 512;
+  static constexpr uint32_t SFT_COL = ACC_COLS + 2 * SF_COLS;
+  static constexpr uint32_t TMEM_USED = ACC_COLS + 4 * SF_COLS;
+  static constexpr uint32_t TMEM_COLS = (TMEM_USED <= 64) ? 64 : (TMEM_USED <= 128) ? 128
+                                        : (TMEM_USED <= 256) ? 256 : 512;
   static_assert(LOOKAHEAD >= 1 && LOOKAHEAD < STAGES, "scale look-ahead must leave a free stage");
   static_assert(STAGES > CSTAGES, "the load ring is deeper than the converted ring");
   // 128-byte-swizzled tiles start on 1024-byte boundaries
   static_assert(SMEM_W % 1024 == 0 && SMEM_T % 1024 == 0 && CT_STAGE % 1024 == 0, "swizzle");
   static_assert(A_FP4 || T_STAGE % 1024 == 0, "token tiles keep the 1024-byte alignment");
+  // 64-byte-swizzled packed tiles (fp4 MMA kinds) start on 512-byte boundaries
+  static_assert(!NATIVE || (W_STAGE % 512 == 0 && T_STAGE % 512 == 0), "64-byte swizzle");
   static_assert(B_FP4 || W_STAGE % 1024 == 0, "weight tiles keep the 1024-byte alignment");
 };
 
@@ -471,11 +492,16 @@ bsmxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             break;
           }
           tc_fence_after();
-          const uint32_t sfw_t = tmem_base + C::SFW_COL + 4 * slot;
-          const uint32_t sft_t = tmem_base + C::SFT_COL + 4 * slot;
-          if constexpr (!C::NV) {
-            tmem_cp_32x128b_warpx4<1>(sfw_t, sf_block_desc(sSFW + stage * C::SFW_STAGE));
-            tmem_cp_32x128b_warpx4<1>(sft_t, sf_block_desc(sSFT + stage * C::SFT_STAGE));
+          const uint32_t sfw_t = tmem_base + C::SFW_COL + C::SF_COLS * slot;
+          const uint32_t sft_t = tmem_base + C::SFT_COL + C::SF_COLS * slot;
+          if constexpr (!C::NV_F16) {
+#pragma unroll
+            for (int g = 0; g < C::SF_GROUPS; ++g) {
+              tmem_cp_32x128b_warpx4<1>(sfw_t + 4 * g,
+                                        sf_block_desc(sSFW + stage * C::SFW_STAGE + g * SF_BLOCK));
+              tmem_cp_32x128b_warpx4<1>(sft_t + 4 * g,
+                                        sf_block_desc(sSFT + stage * C::SFT_STAGE + g * SF_BLOCK));
+            }
           }
           const uint32_t w_tile = C::CONVERT ? smem_u32(smem + C::SMEM_CW) + cstage * C::CW_STAGE
                                              : sW + stage * C::W_STAGE;
@@ -486,7 +512,22 @@ bsmxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           if constexpr (C::CONVERT) {
             if (++cstage == C::CSTAGES) { cstage = 0; cphase ^= 1; }
           }
-          if constexpr (C::NV) {
+          if constexpr (C::NATIVE) {
+            // packed e2m1 tiles of 64-byte rows: two K = 64 MMAs per stage, 32 bytes apart
+            const uint64_t wd = kmajor_sw64_desc(sW + stage * C::W_STAGE);
+            const uint64_t td = kmajor_sw64_desc(sT + stage * C::T_STAGE);
+#pragma unroll
+            for (int k = 0; k < BK / 64; ++k) {
+              if constexpr (C::NV)  // UE4M3 per 16: the k-th scale group of each operand
+                umma_mxf4nvf4_4x(d_tmem, wd + (uint64_t)(k * 2), td + (uint64_t)(k * 2),
+                                 idesc_nvf4_e2m1_ue4m3(WROWS, C::TN), sfw_t + 4 * k, sft_t + 4 * k,
+                                 (kb > 0 || k > 0) ? 1u : 0u);
+              else  // UE8M0 per 32: bytes 2k, 2k + 1 of the stage's scale word
+                umma_mxf4(d_tmem, wd + (uint64_t)(k * 2), td + (uint64_t)(k * 2),
+                          idesc_mxf4_e2m1(WROWS, C::TN, 2 * k, 2 * k), sfw_t, sft_t,
+                          (kb > 0 || k > 0) ? 1u : 0u);
+            }
+          } else if constexpr (C::NV_F16) {
             // fp16 tiles: two 64-element swizzle atoms per stage, K = 16 per MMA
 #pragma unroll
             for (int k = 0; k < BK / 16; ++k) {
@@ -532,8 +573,8 @@ bsmxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     const bool weights = warp == 3;
     const uint8_t* a_sc = static_cast<const uint8_t*>(args.a_scales);
     const uint8_t* b_sc = static_cast<const uint8_t*>(args.b_scales);
-    if (!C::NV && !weights && C::TN < WROWS) {
-      for (int s = 0; s < C::STAGES; ++s)
+    if (!C::NV_F16 && !weights && C::TN < WROWS) {
+      for (int s = 0; s < C::STAGES * C::SF_GROUPS; ++s)
         for (int rg = C::TN / 32; rg < 4; ++rg)
           *reinterpret_cast<uint32_t*>(smem + C::SMEM_SFT + s * SF_BLOCK + lane * 16 + rg * 4) = 0u;
     }
@@ -627,7 +668,29 @@ bsmxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           ok = false;
           break;
         }
-        if (C::NV) {
+        if (C::NV && C::NATIVE) {
+          // nvfp4, MMA kind: row r's 8 UE4M3 codes of the stage, codes 0-3 (the first K = 64
+          // MMA) into block 0 and codes 4-7 into block 1, each at byte (r % 32) * 16 + (r / 32) * 4
+          const uint32_t d =
+              (weights ? sSFW + stage * C::SFW_STAGE : sSFT + stage * C::SFT_STAGE) + lane * 16;
+          if (weights) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const uint8_t* src = w_rows + (int64_t)(j * 32 + (int)lane) * scale_row + 8 * kb;
+              cp_async_4(d + 4 * j, src, 4);
+              cp_async_4(d + SF_BLOCK + 4 * j, src + 4, 4);
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < C::TN / 32; ++j) {
+              const int64_t m = tc.m0 + j * 32 + (int)lane;
+              const bool live = m < args.M_total;
+              const uint8_t* src = live ? a_sc + m * scale_row + 8 * kb : a_sc;
+              cp_async_4(d + 4 * j, src, live ? 4u : 0u);
+              cp_async_4(d + SF_BLOCK + 4 * j, live ? src + 4 : a_sc, live ? 4u : 0u);
+            }
+          }
+        } else if (C::NV) {
           // nvfp4: row r's 8 e4m3 codes of the stage to byte 8r (row-major, as stored)
           const uint32_t d = weights ? sSFW + stage * C::SFW_STAGE : sSFT + stage * C::SFT_STAGE;
           const int rows = weights ? WROWS : C::TN;
@@ -740,7 +803,7 @@ bsmxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           ok = false;
           break;
         }
-        if constexpr (C::NV) {
+        if constexpr (C::NV_F16) {
           constexpr int WPART = WROWS / C::SPLIT, TPART = C::TN / C::SPLIT;
           convert_nvfp4_tile<WROWS, WPART>(smem + C::SMEM_W + stage * C::W_STAGE,
                                            smem + C::SMEM_SFW + stage * C::SFW_STAGE,
@@ -828,13 +891,17 @@ cudaError_t launch_bsmxfp8(int tn, const CUtensorMap& tmA, const CUtensorMap& tm
 }
 
 // fp4 operands: a_fp4 = tokens packed e2m1 (else e4m3); the weights are packed e2m1; tn is
-// 32 or 64.
-// tmA / tmB map the packed operands with 64-byte boxes and no swizzle (tmA the e4m3 tokens
-// as for MXFP8 when !a_fp4).
-cudaError_t launch_bsmxfp4(int tn, bool a_fp4, const CUtensorMap& tmA, const CUtensorMap& tmB,
-                           const GemmArgs& args, int num_sms, cudaStream_t stream) {
+// 32 or 64.  mma_kind (with a_fp4): kind::mxf4 on the packed tiles.
+cudaError_t launch_bsmxfp4(int tn, bool a_fp4, bool mma_kind, const CUtensorMap& tmA,
+                           const CUtensorMap& tmB, const GemmArgs& args, int num_sms,
+                           cudaStream_t stream) {
   using namespace mx;
-  if (a_fp4) {
+  if (a_fp4 && mma_kind) {
+    switch (tn) {
+      case 32: return launch<Cfg<32, FMT_MXFP4_MMA>>(tmA, tmB, args, num_sms, stream);
+      case 64: return launch<Cfg<64, FMT_MXFP4_MMA>>(tmA, tmB, args, num_sms, stream);
+    }
+  } else if (a_fp4) {
     switch (tn) {
       case 32: return launch<Cfg<32, FMT_MXFP4>>(tmA, tmB, args, num_sms, stream);
       case 64: return launch<Cfg<64, FMT_MXFP4>>(tmA, tmB, args, num_sms, stream);
@@ -852,9 +919,17 @@ cudaError_t launch_bsmxfp4(int tn, bool a_fp4, const CUtensorMap& tmA, const CUt
 
 namespace bsfp8 {
 // nvfp4 x nvfp4: both operands packed e2m1 with e4m3 scales per 16 K; tn is 32 or 64.
-cudaError_t launch_bsnvfp4(int tn, const CUtensorMap& tmA, const CUtensorMap& tmB,
+// mma_kind: kind::mxf4nvf4 (scale_vec::4X) on the packed tiles.
+cudaError_t launch_bsnvfp4(int tn, bool mma_kind, const CUtensorMap& tmA, const CUtensorMap& tmB,
                            const GemmArgs& args, int num_sms, cudaStream_t stream) {
   using namespace mx;
+  if (mma_kind) {
+    switch (tn) {
+      case 32: return launch<Cfg<32, FMT_NVFP4_MMA>>(tmA, tmB, args, num_sms, stream);
+      case 64: return launch<Cfg<64, FMT_NVFP4_MMA>>(tmA, tmB, args, num_sms, stream);
+    }
+    return cudaErrorInvalidValue;
+  }
   switch (tn) {
     case 32: return launch<Cfg<32, FMT_NVFP4>>(tmA, tmB, args, num_sms, stream);
     case 64: return launch<Cfg<64, FMT_NVFP4>>(tmA, tmB, args, num_sms, stream);

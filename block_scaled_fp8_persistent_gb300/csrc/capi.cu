@@ -90,7 +90,8 @@ bsfp8_status device_info(DeviceInfo** out) {
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 // 2D uint8 tensor map over a row-major [rows, inner] byte matrix, box [box_rows, box_inner],
-// 128-byte swizzle (box_inner must be 128), or no swizzle (swizzle == false).
+// swizzled over box_inner bytes (128 or 64: the 128- or 64-byte swizzle), or with no swizzle
+// (swizzle == false).
 bool encode_u8_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
                   uint32_t box_inner, uint32_t box_rows, bool swizzle = true) {
   EncodeTiledFn fn = encode_fn();
@@ -101,7 +102,8 @@ bool encode_u8_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t r
   const cuuint32_t estr[2] = {1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+            !swizzle ? CU_TENSOR_MAP_SWIZZLE_NONE
+                     : box_inner == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -291,9 +293,16 @@ bsfp8_status mx_gemm(const void* A, const void* B, const uint8_t* a_scales,
                                                                                  : BSFP8_ERR_CUDA;
 }
 
-// Formats per operand.  (MXFP8, MXFP8) is mx_gemm; (MXFP8, MXFP4), (MXFP4, MXFP4) and
-// (NVFP4, NVFP4) run the swap-AB kernel with the packed e2m1 tiles converted on chip, at
-// every size.
+// Formats per operand.  (MXFP8, MXFP8) is mx_gemm; (MXFP4, MXFP4) and (NVFP4, NVFP4) run
+// the swap-AB kernel with the fp4 MMA kinds on the packed tiles as loaded; (MXFP8, MXFP4)
+// has no such kind (kind::mxf8f6f4 takes K = 32 per instruction either way) and converts the
+// packed weight tiles on chip to e4m3.  BSFP8_FP4_MMA=convert runs the converting kernels for
+// every pair (the forms before the fp4 kinds, kept for comparison).
+bool fp4_mma_kind() {
+  const char* v = std::getenv("BSFP8_FP4_MMA");
+  return !(v && std::strcmp(v, "convert") == 0);
+}
+
 bsfp8_status mx_fmt_gemm(int a_fmt, int b_fmt, const void* A, const void* B,
                          const uint8_t* a_scales, const uint8_t* b_scales, bool packed_b,
                          const int32_t* offsets, const int32_t* ids, void* C, int64_t M_total,
@@ -316,15 +325,18 @@ bsfp8_status mx_fmt_gemm(int a_fmt, int b_fmt, const void* A, const void* B,
   GemmArgs args{offsets, a_scales, b_scales, C, M_total, N, K, G, dev->err_word, ids, E,
                 packed_b ? 1 : 0};
   const int tn = std::min(choose_mx_token_tile(M_total, G), 64);  // fp4 tiles: tn <= 64
+  // both operands fp4: the MMA kinds read the packed tiles 64-byte swizzled
+  const bool kind = a_fp4 && fp4_mma_kind();
   CUtensorMap tmA, tmB;
   const bool ok_a = a_fp4 ? encode_u8_2d(&tmA, A, (uint64_t)K / 2, (uint64_t)M_total, 64,
-                                         (uint32_t)tn, false)
+                                         (uint32_t)tn, kind)
                           : encode_u8_2d(&tmA, A, (uint64_t)K, (uint64_t)M_total, 128,
                                          (uint32_t)tn);
-  if (!ok_a || !encode_u8_2d(&tmB, B, (uint64_t)K / 2, (uint64_t)E * N, 64, 128, false))
+  if (!ok_a || !encode_u8_2d(&tmB, B, (uint64_t)K / 2, (uint64_t)E * N, 64, 128, kind))
     return BSFP8_ERR_CUDA;
-  const cudaError_t e = nv ? launch_bsnvfp4(tn, tmA, tmB, args, dev->num_sms, stream)
-                           : launch_bsmxfp4(tn, a_fp4, tmA, tmB, args, dev->num_sms, stream);
+  const cudaError_t e =
+      nv ? launch_bsnvfp4(tn, kind, tmA, tmB, args, dev->num_sms, stream)
+         : launch_bsmxfp4(tn, a_fp4, kind, tmA, tmB, args, dev->num_sms, stream);
   return e == cudaSuccess ? BSFP8_OK : BSFP8_ERR_CUDA;
 }
 

@@ -378,6 +378,34 @@ __device__ __forceinline__ void umma_mxf8f6f4(uint32_t d_tmem, uint64_t a_desc, 
         : "memory");
 }
 
+// Block-scaled fp4 MMA, kind::mxf4: packed e2m1 x packed e2m1 (two elements per byte along
+// K, K = 64 per instruction) with UE8M0 scales per 32 K, two per row per instruction
+// (scale_vec::2X: the scale-factor id, 0 or 2, picks the byte pair of the TMEM scale word).
+__device__ __forceinline__ void umma_mxf4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Block-scaled fp4 MMA, kind::mxf4nvf4 with scale_vec::4X: packed e2m1 operands (K = 64 per
+// instruction) and UE4M3 scales per 16 K, four per row per instruction (the whole TMEM scale
+// word; scale-factor id 0).
+__device__ __forceinline__ void umma_mxf4nvf4_4x(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                 uint32_t idesc, uint32_t sfa_tmem,
+                                                 uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+          d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive on an mbarrier once every tcgen05 operation issued so far by this thread is done.
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
@@ -447,7 +475,7 @@ __device__ __forceinline__ void tmem_ld_wait() {
 //   bits 32-45 stride byte offset >> 4 bits 46-48 fixed 0b001
 //   bits 49-51 base offset (0: atoms 1024-byte aligned)   bit 52 LBO mode (0)
 //   bits 61-63 layout: 0 none, 2 128-byte swizzle, 4 64-byte, 6 32-byte
-enum : uint32_t { LAYOUT_NONE = 0, LAYOUT_SW128 = 2 };
+enum : uint32_t { LAYOUT_NONE = 0, LAYOUT_SW128 = 2, LAYOUT_SW64 = 4 };
 
 __device__ __forceinline__ uint64_t make_smem_desc(uint32_t saddr, uint32_t lbo_bytes,
                                                    uint32_t sbo_bytes, uint32_t layout) {
@@ -465,6 +493,12 @@ __device__ __forceinline__ uint64_t make_smem_desc(uint32_t saddr, uint32_t lbo_
 // address by 32 bytes.
 __device__ __forceinline__ uint64_t kmajor_sw128_desc(uint32_t saddr) {
   return make_smem_desc(saddr, 16, 1024, LAYOUT_SW128);
+}
+
+// K-major operand tile whose rows are 64 bytes, 64-byte swizzled by TMA: 8-row atoms of 512
+// bytes.  Packed e2m1 tiles of 128 K per row: one K = 64 MMA step is 32 bytes (>> 4 = 2).
+__device__ __forceinline__ uint64_t kmajor_sw64_desc(uint32_t saddr) {
+  return make_smem_desc(saddr, 16, 512, LAYOUT_SW64);
 }
 
 // Instruction descriptor for kind::f8f6f4, e4m3 x e4m3 -> fp32, both operands K-major:
@@ -488,6 +522,20 @@ __host__ __device__ constexpr uint32_t idesc_mxf8f6f4_e4m3(uint32_t M, uint32_t 
                                                           uint32_t sfb_id) {
   return ((sfb_id & 3u) << 4) | ((N >> 3) << 17) | (1u << 23) | ((M >> 4) << 24) |
          ((sfa_id & 3u) << 29);
+}
+
+// Instruction descriptors for the fp4 block-scaled kinds, both operands packed e2m1 (format
+// code 1 in bits 7-9 and 10-12 for kind::mxf4 and kind::mxf4nvf4), K-major, the field layout
+// of the kind::mxf8f6f4 descriptor above:
+//   kind::mxf4, UE8M0 scales (bit 23 = 1); scale-factor ids 0 or 2 (a byte pair per K = 64);
+//   kind::mxf4nvf4 with scale_vec::4X, UE4M3 scales (bit 23 = 0); scale-factor ids 0.
+__host__ __device__ constexpr uint32_t idesc_mxf4_e2m1(uint32_t M, uint32_t N, uint32_t sfa_id,
+                                                      uint32_t sfb_id) {
+  return ((sfb_id & 3u) << 4) | (1u << 7) | (1u << 10) | ((N >> 3) << 17) | (1u << 23) |
+         ((M >> 4) << 24) | ((sfa_id & 3u) << 29);
+}
+__host__ __device__ constexpr uint32_t idesc_nvf4_e2m1_ue4m3(uint32_t M, uint32_t N) {
+  return (1u << 7) | (1u << 10) | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
 // ---------------------------------------------------------------------------

@@ -204,7 +204,8 @@ bsfp8_status bsmxfp8_grouped_gemm_prepacked(const void* A, const void* B, const 
  *   A          [M_total, K] elements in a_format: K bytes per row (MXFP8) or K/2 (fp4: element
  *              2i of the row in the low nibble of byte i, element 2i+1 in the high nibble)
  *   B          [num_experts, N, K] elements in b_format, laid out the same way
- *   a_scales   [M_total, K/vec] codes (vec = 32: UE8M0; vec = 16 for NVFP4: e4m3), row-major
+ *   a_scales   [M_total, K/vec] codes (vec = 32: UE8M0; vec = 16 for NVFP4: unsigned e4m3,
+ *              codes 0x00..0x7E, bit 7 zero: the example draws them positive), row-major
  *   b_scales   [num_experts, N, K/vec] codes, row-major; with b_scales_packed != 0 (MXFP8 and
  *              MXFP4 weights only) the 512-byte block layout of bsmxfp8_pack_b_scales,
  *              16-byte aligned
@@ -217,21 +218,33 @@ bsfp8_status bsmxfp8_grouped_gemm_prepacked(const void* A, const void* B, const 
  *
  * Supported (a_format, b_format) pairs:
  *   (MXFP8, MXFP8)  bsmxfp8_grouped_gemm(_ids) / _prepacked
- *   (MXFP8, MXFP4), (MXFP4, MXFP4)
- *                   swap-AB tiles at every size.  The packed tiles are loaded as they are and
- *                   re-encoded on chip into e4m3 for the MXFP8 block-scaled MMA: every e2m1
- *                   value times 2^-6 is an e4m3 value, and the epilogue multiplies the fp32
- *                   sums by 2^6 per fp4 operand, so the result is that of the same values in
- *                   MXFP8 while the tensor core's products, 2^-6 per fp4 operand below the
- *                   true ones, stay in fp32's normal range: every non-zero product
- *                   dec(A)*sa*dec(B)*sb of magnitude at least 2^-120 (one fp4 operand) or
- *                   2^-114 (two).  Smaller products may be flushed to zero.
- *   (NVFP4, NVFP4)  swap-AB tiles at every size.  The packed tiles and their e4m3 scales are
- *                   dequantized on chip into fp16 (exact: an e2m1 value times an e4m3 scale
- *                   has at most 6 significant bits and lies in the normal fp16 range) and
- *                   multiplied by the fp16 tensor-core MMA with fp32 accumulation.  The
- *                   scales must be 8-byte aligned (BSFP8_ERR_ALIGN); b_scales_packed is not
- *                   available (BSFP8_ERR_FORMAT).
+ *   (MXFP4, MXFP4)  swap-AB tiles at every size; the packed tiles feed the fp4 block-scaled
+ *                   MMA (tcgen05.mma kind::mxf4, K = 64 per instruction, UE8M0 per 32) as
+ *                   loaded.  Every product is taken exactly and summed in fp32.
+ *   (NVFP4, NVFP4)  swap-AB tiles at every size; the packed tiles feed tcgen05.mma
+ *                   kind::mxf4nvf4 with scale_vec::4X (UE4M3 per 16) as loaded.  The scales
+ *                   must be 8-byte aligned (BSFP8_ERR_ALIGN); b_scales_packed is not
+ *                   available (BSFP8_ERR_FORMAT).  A scale code with bit 7 set is outside the
+ *                   format (the tensor core's scale type is unsigned): its result is not
+ *                   specified.
+ *   (MXFP8, MXFP4)  swap-AB tiles at every size.  No fp4 MMA kind takes e4m3 with e2m1 at more
+ *                   than K = 32 per instruction, so the packed weight tiles are loaded as
+ *                   they are and re-encoded on chip into e4m3 for the MXFP8 block-scaled MMA
+ *                   (the "converting" form below).
+ * Converting forms (environment variable BSFP8_FP4_MMA=convert selects them for the two
+ * both-fp4 pairs too; kept for comparison):
+ *   MX pairs        the packed tiles are re-encoded on chip into e4m3 for the MXFP8
+ *                   block-scaled MMA: every e2m1 value times 2^-6 is an e4m3 value, and the
+ *                   epilogue multiplies the fp32 sums by 2^6 per fp4 operand, so the result
+ *                   is that of the same values in MXFP8 while the tensor core's products,
+ *                   2^-6 per fp4 operand below the true ones, stay in fp32's normal range:
+ *                   every non-zero product dec(A)*sa*dec(B)*sb of magnitude at least 2^-120
+ *                   (one fp4 operand) or 2^-114 (two).  Smaller products may be flushed to
+ *                   zero.
+ *   NVFP4           the packed tiles and their e4m3 scales are dequantized on chip into
+ *                   fp16 (exact: an e2m1 value times an e4m3 scale has at most 6 significant
+ *                   bits and lies in the normal fp16 range) and multiplied by the fp16
+ *                   tensor-core MMA with fp32 accumulation.
  * Any other pair returns BSFP8_ERR_FORMAT with nothing launched.  Requirements, ownership,
  * asynchrony and the other errors are those of bsmxfp8_grouped_gemm_ids (A, B and C 16-byte
  * aligned; N and K multiples of 128).

@@ -15,6 +15,19 @@ pytestmark = pytest.mark.gpu
 
 PAIRS = [("mxfp8", "mxfp4"), ("mxfp4", "mxfp4"), ("nvfp4", "nvfp4")]
 MX_PAIRS = PAIRS[:2]
+# (a format, b format, path): both-fp4 pairs run the fp4 MMA kinds by default ("mma") and the
+# converting kernels on request ("convert"); mxfp8 x mxfp4 always converts its weight tiles
+FORMS = [("mxfp8", "mxfp4", "convert"), ("mxfp4", "mxfp4", "mma"), ("mxfp4", "mxfp4", "convert"),
+         ("nvfp4", "nvfp4", "mma"), ("nvfp4", "nvfp4", "convert")]
+MX_FORMS = [f for f in FORMS if f[0] != "nvfp4"]
+NV_PATHS = ["mma", "convert"]
+
+
+@pytest.fixture
+def path_env(monkeypatch):
+    def use(path):
+        monkeypatch.setenv("BSFP8_FP4_MMA", path)
+    return use
 
 
 @pytest.fixture(params=["32", "64", "128"])
@@ -46,9 +59,10 @@ CASES = [
 ]
 
 
-@pytest.mark.parametrize("a_fmt,b_fmt", PAIRS)
+@pytest.mark.parametrize("a_fmt,b_fmt,path", FORMS)
 @pytest.mark.parametrize("name,counts,N,K", CASES, ids=[c[0] for c in CASES])
-def test_small_cases(name, counts, N, K, a_fmt, b_fmt, tn):
+def test_small_cases(name, counts, N, K, a_fmt, b_fmt, tn, path, path_env):
+    path_env(path)
     _check_full(gen.fmt_problem(counts, N, K, seed=300 + len(name), a_fmt=a_fmt, b_fmt=b_fmt))
 
 
@@ -60,8 +74,9 @@ def test_quantized_tokens(a_fmt, b_fmt, tn):
                                 b_fmt=b_fmt, a_recipe="quantized"))
 
 
-@pytest.mark.parametrize("a_fmt,b_fmt", PAIRS)
-def test_exact_inputs_bitwise(a_fmt, b_fmt, tn):
+@pytest.mark.parametrize("a_fmt,b_fmt,path", FORMS)
+def test_exact_inputs_bitwise(a_fmt, b_fmt, tn, path, path_env):
+    path_env(path)
     p = gen.fmt_problem([5, 30, 0, 12], 256, 1024, seed=42, a_fmt=a_fmt, b_fmt=b_fmt)
     # scales 0.5 / 1 / 2 (UE8M0 codes 126..128, e4m3 codes 0x30 / 0x38 / 0x40): every
     # partial sum is exact in fp32, so the result is unique
@@ -75,22 +90,26 @@ def test_exact_inputs_bitwise(a_fmt, b_fmt, tn):
     assert np.array_equal(got, ref)
 
 
-@pytest.mark.parametrize("a_fmt,b_fmt", PAIRS)
-def test_expert_ids(a_fmt, b_fmt, tn):
+@pytest.mark.parametrize("a_fmt,b_fmt,path", FORMS)
+def test_expert_ids(a_fmt, b_fmt, tn, path, path_env):
+    path_env(path)
     p = gen.fmt_problem([9, 0, 33, 4, 17], 256, 512, seed=43, a_fmt=a_fmt, b_fmt=b_fmt,
                         expert_ids=[3, 1, 3, 0, 2], num_experts=4)
     _check_full(p)
 
 
+@pytest.mark.parametrize("path", NV_PATHS)
 @pytest.mark.parametrize("counts,N,K", [([3, 17, 0, 32, 1, 9], 256, 512), ([40, 0, 77], 384, 1024)])
-def test_nvfp4_general_e4m3_scales(counts, N, K, tn):
+def test_nvfp4_general_e4m3_scales(counts, N, K, tn, path, path_env):
+    path_env(path)
     # non-power-of-two e4m3 scales (0.125 .. 3.75), as nvfp4 quantization produces them
     _check_full(gen.fmt_problem(counts, N, K, seed=49, a_fmt="nvfp4", b_fmt="nvfp4",
                                 scales="e4m3"))
 
 
-@pytest.mark.parametrize("a_fmt,b_fmt", MX_PAIRS)
-def test_prepacked_weight_scales(a_fmt, b_fmt):
+@pytest.mark.parametrize("a_fmt,b_fmt,path", MX_FORMS)
+def test_prepacked_weight_scales(a_fmt, b_fmt, path, path_env):
+    path_env(path)
     import block_scaled_fp8_persistent_gb300 as bsfp8
     from gpu_util import DeviceProblem
     p = gen.fmt_problem([12, 0, 40], 384, 1024, seed=44, a_fmt=a_fmt, b_fmt=b_fmt)
@@ -121,8 +140,9 @@ def test_mxfp8_pair_through_format_entry():
     assert parity_report(got, ref, T)[0] == 0
 
 
-@pytest.mark.parametrize("a_fmt,b_fmt", PAIRS)
-def test_empty_and_degenerate(a_fmt, b_fmt):
+@pytest.mark.parametrize("a_fmt,b_fmt,path", FORMS)
+def test_empty_and_degenerate(a_fmt, b_fmt, path, path_env):
+    path_env(path)
     # no rows at all; one expert with one row; all rows in the last expert
     from gpu_util import DeviceProblem
     import block_scaled_fp8_persistent_gb300 as bsfp8
@@ -136,8 +156,9 @@ def test_empty_and_degenerate(a_fmt, b_fmt):
     _check_full(gen.fmt_problem([0, 0, 77], 128, 256, seed=48, a_fmt=a_fmt, b_fmt=b_fmt))
 
 
-@pytest.mark.parametrize("a_fmt,b_fmt", PAIRS)
-def test_invalid_offsets_reported_on_device(a_fmt, b_fmt):
+@pytest.mark.parametrize("a_fmt,b_fmt,path", FORMS)
+def test_invalid_offsets_reported_on_device(a_fmt, b_fmt, path, path_env):
+    path_env(path)
     # offsets that are not a partition of [0, M_total): device error 6, C untouched
     from gpu_util import DeviceProblem
     import block_scaled_fp8_persistent_gb300 as bsfp8
@@ -149,9 +170,10 @@ def test_invalid_offsets_reported_on_device(a_fmt, b_fmt):
     assert np.all(d.c_bits() == d.sentinel)
 
 
-@pytest.mark.parametrize("a_fmt,b_fmt", PAIRS)
+@pytest.mark.parametrize("a_fmt,b_fmt,path", FORMS)
 @pytest.mark.parametrize("bad", [-1, 3])
-def test_expert_id_out_of_range_reported_on_device(a_fmt, b_fmt, bad):
+def test_expert_id_out_of_range_reported_on_device(a_fmt, b_fmt, bad, path, path_env):
+    path_env(path)
     from gpu_util import DeviceProblem
     import block_scaled_fp8_persistent_gb300 as bsfp8
     p = gen.fmt_problem([64, 40], 256, 256, seed=51, a_fmt=a_fmt, b_fmt=b_fmt,
@@ -164,8 +186,9 @@ def test_expert_id_out_of_range_reported_on_device(a_fmt, b_fmt, bad):
     assert bsfp8.bsfp8_get_device_error() == 0
 
 
-@pytest.mark.parametrize("a_fmt,b_fmt", PAIRS)
-def test_cuda_graph_capture_and_replay(a_fmt, b_fmt):
+@pytest.mark.parametrize("a_fmt,b_fmt,path", FORMS)
+def test_cuda_graph_capture_and_replay(a_fmt, b_fmt, path, path_env):
+    path_env(path)
     # the fp4 launch records into a CUDA graph and replays with the inputs changed in place
     from gpu_util import DeviceProblem
     import block_scaled_fp8_persistent_gb300 as bsfp8
@@ -190,19 +213,35 @@ def test_cuda_graph_capture_and_replay(a_fmt, b_fmt):
         assert bad == 0
 
 
-def test_nvfp4_scale_codes_signs_and_subnormals(tn):
-    # e4m3 scale codes over the whole finite range, both signs, subnormals included (NaN
-    # codes 0x7F / 0xFF excluded): the dequantized fp16 products stay exact
+@pytest.mark.parametrize("path", NV_PATHS)
+def test_nvfp4_scale_codes_and_subnormals(tn, path, path_env):
+    # nvfp4 scale codes over the whole finite unsigned e4m3 (UE4M3) range, 0x00 .. 0x7E,
+    # subnormals (0x01 .. 0x07) and zero included: the Gluon example draws its nvfp4 scales
+    # positive (1/128 .. 2, converted to float8_e4m3fn), and the tensor core's scale type is
+    # unsigned, so codes with bit 7 set are outside the format
+    path_env(path)
     rng = np.random.default_rng(54)
     p = gen.fmt_problem([3, 17, 0, 32, 9], 256, 512, seed=54, a_fmt="nvfp4", b_fmt="nvfp4")
     for s in (p.a_scales, p.b_scales):
-        codes = rng.integers(1, 0x7F, s.shape) | (rng.integers(0, 2, s.shape) << 7)
-        s[:] = codes.astype(np.uint8)
+        s[:] = rng.integers(0, 0x7F, s.shape).astype(np.uint8)
     _check_full(p)
 
 
-@pytest.mark.parametrize("a_fmt,b_fmt", MX_PAIRS)
-def test_mx_fp4_wide_scale_range(a_fmt, b_fmt, tn):
+@pytest.mark.parametrize("path", NV_PATHS)
+def test_nvfp4_subnormal_scales(tn, path, path_env):
+    # every scale code subnormal or zero (0x00 .. 0x07: 0 .. 7 * 2^-9), the low end of the
+    # Gluon example's range (its 1/128 is the subnormal 0x04)
+    path_env(path)
+    rng = np.random.default_rng(56)
+    p = gen.fmt_problem([3, 17, 0, 32, 9], 256, 512, seed=56, a_fmt="nvfp4", b_fmt="nvfp4")
+    for s in (p.a_scales, p.b_scales):
+        s[:] = rng.integers(0, 8, s.shape).astype(np.uint8)
+    _check_full(p)
+
+
+@pytest.mark.parametrize("a_fmt,b_fmt,path", MX_FORMS)
+def test_mx_fp4_wide_scale_range(a_fmt, b_fmt, tn, path, path_env):
+    path_env(path)
     # UE8M0 codes 100..160 (2^-27 .. 2^33): the 2^-6 re-encoding and its 2^6 undo in the
     # epilogue stay exact across a wide exponent range
     rng = np.random.default_rng(55)
@@ -227,8 +266,9 @@ def _unit_magnitudes(p, a_fmt, rng):
                   (rng.integers(0, 2, p.A.shape) << 7)).astype(np.uint8)
 
 
-@pytest.mark.parametrize("a_fmt,b_fmt", MX_PAIRS)
-def test_low_scales(a_fmt, b_fmt, tn):
+@pytest.mark.parametrize("a_fmt,b_fmt,path", MX_FORMS)
+def test_low_scales(a_fmt, b_fmt, tn, path, path_env):
+    path_env(path)
     # scale codes 72 and 72: every product is 2^-110 times 1 .. 2.25, inside the documented
     # range (the tensor core sums them 2^-6 per fp4 operand lower, 2^-116 / 2^-122, still
     # fp32-normal), and the sums are far below 1 but in bf16's normal range
@@ -239,8 +279,9 @@ def test_low_scales(a_fmt, b_fmt, tn):
     _check_full(p)
 
 
-@pytest.mark.parametrize("a_fmt,b_fmt", MX_PAIRS)
-def test_high_scales(a_fmt, b_fmt, tn):
+@pytest.mark.parametrize("a_fmt,b_fmt,path", MX_FORMS)
+def test_high_scales(a_fmt, b_fmt, tn, path, path_env):
+    path_env(path)
     # token scale codes up to 254 (2^127) with weight codes low enough that the products stay
     # finite: the 2^6 per fp4 operand is applied after the sums, in fp32
     p = gen.fmt_problem([5, 30, 0, 12], 256, 1024, seed=47, a_fmt=a_fmt, b_fmt=b_fmt)

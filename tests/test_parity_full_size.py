@@ -5,7 +5,8 @@ cores) and compared with the GPU output of every kernel form that runs it: the s
 configurations of the blockwise kernel for the three blockwise workloads, the swap-AB
 kernel (row-major and pre-packed weight scales) for the decode-shaped MXFP8 workload, the
 CTA-pair kernel for the dense MXFP8 one, and the three fp4 format pairs on the decode
-workload's routing and shape.  Acceptance per element as everywhere:
+workload's routing and shape (the both-fp4 pairs on the fp4 MMA kinds and on the converting
+kernels).  Acceptance per element as everywhere:
 |gpu - oracle| <= 2 ulp_bf16(oracle) + 1e-6 * sum|scaled terms|.
 """
 import numpy as np
@@ -93,9 +94,15 @@ def test_dense_mxfp8_every_element(kernel, monkeypatch):
     _run_and_compare(p, ref, T)
 
 
-@pytest.mark.parametrize("a_fmt,b_fmt", FP4_PAIRS)
-def test_fp4_decode_shape_every_element(a_fmt, b_fmt):
-    # the decode workload's routing and shape with fp4 operands, as the bench times it
+@pytest.mark.parametrize("a_fmt,b_fmt,path", [("mxfp8", "mxfp4", "convert"),
+                                                ("mxfp4", "mxfp4", "mma"),
+                                                ("mxfp4", "mxfp4", "convert"),
+                                                ("nvfp4", "nvfp4", "mma"),
+                                                ("nvfp4", "nvfp4", "convert")])
+def test_fp4_decode_shape_every_element(a_fmt, b_fmt, path, monkeypatch):
+    # the decode workload's routing and shape with fp4 operands, as the bench times it (the
+    # both-fp4 pairs on the fp4 MMA kinds, and on the converting kernels)
+    monkeypatch.setenv("BSFP8_FP4_MMA", path)
     p, ref, T = _reference(("fp4", a_fmt, b_fmt), lambda: gen.fmt_problem(
         gen.config_counts(4), 4096, 7168, seed=4, a_fmt=a_fmt, b_fmt=b_fmt,
         a_recipe="quantized"))

@@ -80,7 +80,9 @@ def test_cuda_graph_capture_and_replay(mode):
         assert bad == 0
 
 
-def test_fp4_long_k():
+@pytest.mark.parametrize("path", ["mma", "convert"])
+def test_fp4_long_k(path, monkeypatch):
     # K = 65536 (512 K blocks of packed e2m1, 2048 nvfp4 scale codes per row)
-    for a_fmt, b_fmt in (("mxfp8", "mxfp4"), ("nvfp4", "nvfp4")):
+    monkeypatch.setenv("BSFP8_FP4_MMA", path)
+    for a_fmt, b_fmt in (("mxfp8", "mxfp4"), ("mxfp4", "mxfp4"), ("nvfp4", "nvfp4")):
         _sampled(gen.fmt_problem([40, 0, 9], 256, 65536, seed=66, a_fmt=a_fmt, b_fmt=b_fmt))

@@ -60,7 +60,12 @@ def test_mx_sweep(seed, monkeypatch):
     _check(gen.mx_problem(counts, N, K, seed=2000 + seed, exact=bool(seed % 2)))
 
 
-FP4_FORMS = [(a, b, tn) for (a, b) in (("mxfp8", "mxfp4"), ("mxfp4", "mxfp4"), ("nvfp4", "nvfp4"))
+# (a format, b format, token tile, path): the both-fp4 pairs on the fp4 MMA kinds and on the
+# converting kernels
+FP4_FORMS = [(a, b, tn, path)
+             for (a, b, path) in (("mxfp8", "mxfp4", "convert"), ("mxfp4", "mxfp4", "mma"),
+                                  ("mxfp4", "mxfp4", "convert"), ("nvfp4", "nvfp4", "mma"),
+                                  ("nvfp4", "nvfp4", "convert"))
              for tn in ("32", "64")]
 
 
@@ -68,7 +73,8 @@ FP4_FORMS = [(a, b, tn) for (a, b) in (("mxfp8", "mxfp4"), ("mxfp4", "mxfp4"), (
 def test_fp4_sweep(seed, monkeypatch):
     rng = np.random.default_rng(3000 + seed)
     counts, N, K = _case(rng)
-    a_fmt, b_fmt, tn = FP4_FORMS[seed % len(FP4_FORMS)]
+    a_fmt, b_fmt, tn, path = FP4_FORMS[seed % len(FP4_FORMS)]
     monkeypatch.setenv("BSFP8_MX_TN", tn)
+    monkeypatch.setenv("BSFP8_FP4_MMA", path)
     _check(gen.fmt_problem(counts, N, K, seed=3000 + seed, a_fmt=a_fmt, b_fmt=b_fmt,
                            a_recipe="quantized" if seed % 2 else "grid"))
