@@ -37,7 +37,7 @@
 // significant bits and lies inside the normal fp16 range), and the MMA thread issues
 // kind::f16 MMAs (K = 16) with no scale copies.
 //
-// Roles (8 warps; 16 in the converting forms):
+// Roles (8 warps; 12 with the fp4 kinds; 16 in the converting forms):
 //   warp 0      TMA producer: per K stage (128 K) the weight tile [128 x 128] and the token
 //               tile [tn x 128] (128-byte swizzle; fp4 operands packed [rows x 64 B],
 //               unswizzled) into a STAGES-deep ring.
@@ -56,6 +56,13 @@
 //   warps 4-7   epilogue: warp w holds weight rows 32*(w%4).. of the tile, reads the tn
 //               token columns of the accumulator, rounds to bf16 and stores C[m, n] for the
 //               tile's token rows that belong to the expert.
+//   warps 8-11  (fp4 kinds) scale writers: warp 8 + q stores TMEM lane quarter q of each
+//               stage's scale slot with tcgen05.st (one slot per ring stage), so the MMA
+//               thread issues only MMAs and the commit.  With chunkable scale rows (16
+//               aligned bytes = 4 stages of UE8M0 or 2 of UE4M3 codes) each writer fetches its
+//               own weight row's and all token rows' chunks, several groups ahead, into
+//               private staging slots, and warps 2 and 3 idle; otherwise they relay the
+//               loaders' packed blocks.
 //   warps 8-15  (converting forms, tn <= 64) converters: each converted slot takes every
 //               CSTAGES-th stage, whose packed weight tile (and packed token tile) its warp
 //               (nvfp4: its two warps, half the rows each) re-encodes from the load ring into
@@ -75,7 +82,8 @@ namespace mx {
 constexpr int BK = 128;              // K per stage
 constexpr int WROWS = 128;           // weight rows per tile (MMA M)
 constexpr int EPI_WARP0 = 4;
-constexpr int CONV_WARP0 = 8;        // converter warps 8..15 but 9, 13 (fp4 operands)
+constexpr int CONV_WARP0 = 8;        // converter warps 8..15 but 9, 13 (converting forms)
+constexpr int SFW_WARP0 = 8;         // scale writer warps 8..11 (fp4 MMA kinds)
 
 // Converter index of warp 8..15 (0..5), or -1 for warps 9 and 13 (sub-partition 1, the MMA
 // thread's: its tcgen05 instructions need that sub-partition's issue slots).
@@ -97,7 +105,6 @@ enum Format : int {
 };
 constexpr int SF_BLOCK = 512;        // packed scale block: 128 rows x 4 codes
 constexpr int SCALE_LOOKAHEAD = 4;   // scale stages in flight per loader warp
-constexpr int GROUP = 4;             // stages whose 4 codes per row form one 16-byte chunk
 constexpr int STG_SLOTS = 3;         // staged 16-byte groups: one in use, two in flight
 constexpr uint32_t STG_SLOT = WROWS * 16;
 
@@ -113,7 +120,11 @@ struct Cfg {
   static constexpr bool A_FP4 = FMT_ != FMT_MXFP8 && FMT_ != FMT_MXFP8_MXFP4;
   static constexpr bool CONVERT = B_FP4 && !NATIVE;
   static constexpr bool NV_F16 = NV && CONVERT;  // nvfp4 dequantized for the fp16 MMA
-  static constexpr int THREADS = !CONVERT ? 256 : 512;
+  // Scale feed: the MMA thread copies each stage's scale blocks into TMEM (tcgen05.cp), or
+  // (SF_ST) four writer warps, one per TMEM lane quarter, store them (tcgen05.st) into a
+  // per-stage TMEM slot and the MMA thread issues only MMAs and the commit.
+  static constexpr bool SF_ST = NATIVE;
+  static constexpr int THREADS = CONVERT ? 512 : SF_ST ? 384 : 256;
   static_assert(!CONVERT || TN <= 64, "fp4 tiles hold at most 64 token rows");
   // bytes per converted element: e4m3 for the MX formats, fp16 for nvfp4
   static constexpr uint32_t ESZ = NV ? 2 : 1;
@@ -141,10 +152,18 @@ struct Cfg {
   static constexpr uint32_t CT_STAGE = A_FP4 ? TN * BK * ESZ : 0;
   static constexpr uint32_t CONV_BYTES = CSTAGES * (CW_STAGE + CT_STAGE);
   static constexpr uint32_t PER_STAGE = W_STAGE + T_STAGE + SFW_STAGE + SFT_STAGE;
+  // staged scale loads (both operands): STG_AHEAD groups of 16-byte row chunks in flight,
+  // 8 stages ahead for e4m3 and mxf4 tiles, 12 for the 8 KB mxf4 / nvf4 stages
+  static constexpr int STG_AHEAD = NATIVE ? (NV ? 6 : 3) : STG_SLOTS - 1;
+  static constexpr int STG_N = STG_AHEAD + 1;
+  // staging per slot: 128 weight rows and the token rows (x4 with the scale writers, each of
+  // which keeps its own copy of the token rows)
+  static constexpr uint32_t STGT_SLOT = (SF_ST ? 4 : 1) * TN * 16;
+  static constexpr uint32_t STG_BYTES = STG_N * (STG_SLOT + STGT_SLOT);
   // fp4: as many load stages as fit next to the converted ring (if any), the staging slots,
   // the barriers and the alignment pad, at most 16 (128 KB of packed weights in flight)
   static constexpr int FIT =
-      (int)((SMEM_LIMIT - CONV_BYTES - STG_SLOTS * STG_SLOT - 2048) / PER_STAGE);
+      (int)((SMEM_LIMIT - CONV_BYTES - STG_BYTES - 2048) / PER_STAGE);
   static constexpr int STAGES = !B_FP4 ? ((TN <= 32) ? 10 : (TN <= 64) ? 8 : 6)
                                        : (FIT < 16 ? FIT : 16);
   static constexpr int LOOKAHEAD = SCALE_LOOKAHEAD < STAGES - 1 ? SCALE_LOOKAHEAD : STAGES - 1;
@@ -156,9 +175,11 @@ struct Cfg {
   static constexpr uint32_t SMEM_T = SMEM_W + STAGES * W_STAGE;
   static constexpr uint32_t SMEM_SFW = SMEM_T + STAGES * T_STAGE;
   static constexpr uint32_t SMEM_SFT = SMEM_SFW + STAGES * SFW_STAGE;
-  // weight-scale staging of the grouped loader: STG_SLOTS x (128 rows x 16 bytes)
+  // weight-scale staging of the grouped loader: STG_N x (128 rows x 16 bytes), STG_AHEAD
+  // groups in flight
   static constexpr uint32_t SMEM_STG = SMEM_SFT + STAGES * SFT_STAGE;
-  static constexpr uint32_t SMEM_CTL = SMEM_STG + STG_SLOTS * STG_SLOT;
+  static constexpr uint32_t SMEM_STGT = SMEM_STG + STG_N * STG_SLOT;  // token staging
+  static constexpr uint32_t SMEM_CTL = SMEM_STGT + STG_N * STGT_SLOT;
   static constexpr uint32_t STAGE_TX = W_STAGE + T_STAGE;
   // TMEM: 2 accumulators of TN columns, then 2 slots each of weight / token scales (4 columns
   // per scale group, every group on a 4-column boundary)
@@ -166,7 +187,10 @@ struct Cfg {
   static constexpr uint32_t SF_COLS = 4 * SF_GROUPS;  // columns of one slot
   static constexpr uint32_t SFW_COL = ACC_COLS;
   static constexpr uint32_t SFT_COL = ACC_COLS + 2 * SF_COLS;
-  static constexpr uint32_t TMEM_USED = ACC_COLS + 4 * SF_COLS;
+  // SF_ST: one slot pair per operand-ring stage (weights, then tokens)
+  static constexpr uint32_t SF_STAGE_COLS = 2 * SF_COLS;
+  static constexpr uint32_t TMEM_USED =
+      SF_ST ? ACC_COLS + STAGES * SF_STAGE_COLS : ACC_COLS + 4 * SF_COLS;
   static constexpr uint32_t TMEM_COLS = (TMEM_USED <= 64) ? 64 : (TMEM_USED <= 128) ? 128
                                         : (TMEM_USED <= 256) ? 256 : 512;
   static_assert(LOOKAHEAD >= 1 && LOOKAHEAD < STAGES, "scale look-ahead must leave a free stage");
@@ -184,6 +208,7 @@ struct Ctl {
   uint64_t full[C::STAGES];
   uint64_t empty[C::STAGES];
   uint64_t cfull[C::CSTAGES > 0 ? C::CSTAGES : 1];  // converted tiles written (fp4 formats)
+  uint64_t sfull[C::SF_ST ? C::STAGES : 1];          // stage's scales stored in TMEM (SF_ST)
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t mma_done;
@@ -369,6 +394,15 @@ bsmxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   // bytes per row of a row-major scale matrix: UE8M0 per 32 K, or e4m3 per 16 K (nvfp4)
   const int scale_row = args.K / (C::NV ? 16 : 32);
   const bool packed_b = args.b_scales_packed != 0;
+  // Scale writers fetching their own scale chunks (SF_ST, chunkable rows: each row's codes of
+  // 16 / CPS consecutive stages form one aligned 16-byte chunk); otherwise the loader warps
+  // pack each stage's blocks in shared memory and the writers relay them into TMEM.
+  constexpr int CPS = C::NV ? 8 : 4;  // scale codes per row per stage
+  constexpr int GS = 16 / CPS;        // stages per 16-byte chunk
+  const bool sf_direct =
+      C::SF_ST && KB % GS == 0 && scale_row % 16 == 0 &&
+      reinterpret_cast<uintptr_t>(args.a_scales) % 16 == 0 &&
+      (packed_b || reinterpret_cast<uintptr_t>(args.b_scales) % 16 == 0);
 
   // Tiles: per expert ceil(M_e / TN) token tiles x N/128 weight tiles (weights fastest).
   if (warp == 0) {
@@ -396,16 +430,19 @@ bsmxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   auto tfull_bar = [&](int s) { return smem_u32(&ctl->tfull[s]); };
   auto tempty_bar = [&](int s) { return smem_u32(&ctl->tempty[s]); };
   auto cfull_bar = [&](int s) { return smem_u32(&ctl->cfull[s]); };
+  auto sfull_bar = [&](int s) { return smem_u32(&ctl->sfull[s]); };
 
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
     for (int s = 0; s < C::STAGES; ++s) {
       // producer (with bytes) + token-scale loader (+ weight-scale loader)
-      mbar_init(full_bar(s), packed_b ? 2 : 3);
+      mbar_init(full_bar(s), sf_direct ? 1 : packed_b ? 2 : 3);
       mbar_init(empty_bar(s), 1);  // one MMA commit
     }
     for (int s = 0; s < C::CSTAGES; ++s) mbar_init(cfull_bar(s), C::SPLIT);  // its converters
+    if constexpr (C::SF_ST)
+      for (int s = 0; s < C::STAGES; ++s) mbar_init(sfull_bar(s), 4);  // the 4 scale writers
     for (int s = 0; s < 2; ++s) {
       mbar_init(tfull_bar(s), 1);
       mbar_init(tempty_bar(s), 4);  // the 4 epilogue warps
@@ -485,6 +522,7 @@ bsmxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           // fp4: the converters have written this stage's e4m3 tiles (after its loads and
           // scale blocks landed); otherwise the stage's loads themselves
           const bool got = C::CONVERT ? mma_wait(cfull_bar(cstage), cphase, abort)
+                           : C::SF_ST ? mma_wait(sfull_bar(stage), phase, abort)
                                       : mma_wait(full_bar(stage), phase, abort);
           if (!got) {
             record_error(args.err, DEV_TIMEOUT, abort);
@@ -492,9 +530,11 @@ bsmxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             break;
           }
           tc_fence_after();
-          const uint32_t sfw_t = tmem_base + C::SFW_COL + C::SF_COLS * slot;
-          const uint32_t sft_t = tmem_base + C::SFT_COL + C::SF_COLS * slot;
-          if constexpr (!C::NV_F16) {
+          const uint32_t sfw_t = C::SF_ST ? tmem_base + C::ACC_COLS + stage * C::SF_STAGE_COLS
+                                          : tmem_base + C::SFW_COL + C::SF_COLS * slot;
+          const uint32_t sft_t = C::SF_ST ? sfw_t + C::SF_COLS
+                                          : tmem_base + C::SFT_COL + C::SF_COLS * slot;
+          if constexpr (!C::NV_F16 && !C::SF_ST) {
 #pragma unroll
             for (int g = 0; g < C::SF_GROUPS; ++g) {
               tmem_cp_32x128b_warpx4<1>(sfw_t + 4 * g,
@@ -561,15 +601,16 @@ bsmxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       }
     }
     __syncwarp();
-  } else if (warp == 2 || (warp == 3 && !packed_b)) {
+  } else if (!sf_direct && (warp == 2 || (warp == 3 && !packed_b))) {
     // =============================== scale loaders ===============================
     // Warp 2 gathers the token rows' scales, warp 3 the weight rows' (unless they arrive
-    // pre-packed with the producer's copies).  Each lane moves 4-byte words (one row's 4
-    // codes of the stage) into the packed block, row r at byte (r % 32) * 16 + (r / 32) * 4,
-    // and a stage is announced on its full barrier once its copies have landed,
-    // C::LOOKAHEAD stages (SCALE_LOOKAHEAD, fewer in a short ring) behind the newest issued
-    // one.  Token rows >= TN of every
-    // block stay zero (written once here).
+    // pre-packed with the producer's copies), into each stage's packed block(s): row r's 4
+    // codes at byte (r % 32) * 16 + (r / 32) * 4.  Staged (below) when the rows' codes come
+    // in aligned 16-byte chunks; otherwise each lane cp.async's 4-byte words (8 bytes per row
+    // for the fp16 nvfp4 form) into the stage once its ring slot is free, and a stage is
+    // announced on its full barrier once its copies have landed, C::LOOKAHEAD stages
+    // (SCALE_LOOKAHEAD, fewer in a short ring) behind the newest issued one; token rows >= TN
+    // of every block stay zero (written once here).
     const bool weights = warp == 3;
     const uint8_t* a_sc = static_cast<const uint8_t*>(args.a_scales);
     const uint8_t* b_sc = static_cast<const uint8_t*>(args.b_scales);
@@ -591,16 +632,23 @@ bsmxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       head = (head + 1) % (C::LOOKAHEAD + 1);
       --inflight;
     };
-    // Weight rows, grouped: when a row's codes for GROUP consecutive stages form one
-    // aligned 16-byte chunk (K % 512 == 0, 16-byte aligned b_scales), fetch each row's chunk
-    // with one 16-byte copy two groups ahead and transpose each stage's words into its
-    // packed block in shared memory.
-    const bool grouped = !C::NV && weights && (args.K % (GROUP * BK) == 0) &&
-                         (reinterpret_cast<uintptr_t>(b_sc) % 16 == 0);
+    // Staged: when a row's codes for GS consecutive stages form one aligned 16-byte chunk
+    // (4 stages of 4 UE8M0 codes, or 2 stages of 8 UE4M3 codes), fetch each row's chunk with
+    // one 16-byte copy STG_AHEAD groups ahead into a staging slot, and when a stage's ring
+    // slot is free transpose its words into the stage's packed block(s): the DRAM latency of
+    // the scales is covered by the staging slots, not by the ring.  Token rows past M_total
+    // read as zero; rows >= TN of a token block are written zero.
+    const uint8_t* sc_base = weights ? b_sc : a_sc;
+    const bool grouped = !C::NV_F16 && (KB % GS == 0) && (scale_row % 16 == 0) &&
+                         (reinterpret_cast<uintptr_t>(sc_base) % 16 == 0);
     if (grouped) {
-      const int G = KB / GROUP;
-      const uint32_t sSTG = smem_u32(smem + C::SMEM_STG);
-      const uint8_t* stg = smem + C::SMEM_STG;
+      const int G = KB / GS;
+      const int R = weights ? WROWS : C::TN;  // rows of the operand tile
+      const uint32_t slot_bytes = (uint32_t)R * 16;
+      const uint32_t sSTG = smem_u32(smem + (weights ? C::SMEM_STG : C::SMEM_STGT));
+      const uint8_t* stg = smem + (weights ? C::SMEM_STG : C::SMEM_STGT);
+      const uint32_t blk0 = weights ? C::SMEM_SFW : C::SMEM_SFT;
+      const uint32_t blk_stage = weights ? C::SFW_STAGE : C::SFT_STAGE;
       GroupedScheduler<C::TN, WROWS> pre;
       TileCoord tp;
       int64_t tp_t = blockIdx.x;
@@ -608,11 +656,21 @@ bsmxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       int qp = 0;
       auto issue_group = [&](int slot) {
         if (pre_ok) {
-          const uint8_t* rows = b_sc + ((int64_t)tp.be * args.N + tp.n0) * scale_row + 16 * qp;
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int r = 32 * j + (int)lane;
-            cp_async_16(sSTG + slot * STG_SLOT + r * 16, rows + (int64_t)r * scale_row, 16u);
+          for (int jr = 0; jr < 4; ++jr) {
+            const int r = 32 * jr + (int)lane;
+            if (r < R) {
+              const uint8_t* src;
+              uint32_t n = 16u;
+              if (weights) {
+                src = b_sc + ((int64_t)tp.be * args.N + tp.n0 + r) * scale_row + 16 * qp;
+              } else {
+                const int64_t m = tp.m0 + r;
+                n = m < args.M_total ? 16u : 0u;
+                src = n ? a_sc + m * scale_row + 16 * qp : a_sc;
+              }
+              cp_async_16(sSTG + slot * slot_bytes + r * 16, src, n);
+            }
           }
           if (++qp == G) {
             qp = 0;
@@ -622,16 +680,15 @@ bsmxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         }
         cp_async_commit();  // an empty group keeps the group count in step
       };
-      issue_group(0);
-      issue_group(1);
+      for (int a = 0; a < C::STG_AHEAD; ++a) issue_group(a);
       int64_t g = 0;
       for (int64_t t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
         if (!sched.locate(args, t, tc)) break;
         for (int q = 0; ok && q < G; ++q, ++g) {
-          cp_async_wait_group<1>();  // group g has landed (g + 1 may be in flight)
+          cp_async_wait_group<C::STG_AHEAD - 1>();  // group g has landed (later ones in flight)
           __syncwarp();
-          const uint8_t* src = stg + (g % STG_SLOTS) * STG_SLOT;
-          for (int j = 0; j < GROUP; ++j) {
+          const uint8_t* src = stg + (g % C::STG_N) * slot_bytes;
+          for (int j = 0; j < GS; ++j) {
             const bool got =
                 __all_sync(0xffffffffu, role_wait(empty_bar(stage), phase ^ 1, abort));
             if (!got) {
@@ -639,13 +696,19 @@ bsmxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
               ok = false;
               break;
             }
-            // packed block: row 32*rg + lane at byte lane*16 + rg*4
-            uint4 w;
-            w.x = *reinterpret_cast<const uint32_t*>(src + (0 * 32 + lane) * 16 + 4 * j);
-            w.y = *reinterpret_cast<const uint32_t*>(src + (1 * 32 + lane) * 16 + 4 * j);
-            w.z = *reinterpret_cast<const uint32_t*>(src + (2 * 32 + lane) * 16 + 4 * j);
-            w.w = *reinterpret_cast<const uint32_t*>(src + (3 * 32 + lane) * 16 + 4 * j);
-            *reinterpret_cast<uint4*>(smem + C::SMEM_SFW + stage * SF_BLOCK + lane * 16) = w;
+            // packed block b (the stage's codes 4b..4b+3): row 32*rg + lane at byte
+            // lane*16 + rg*4
+#pragma unroll
+            for (int b = 0; b < CPS / 4; ++b) {
+              uint32_t w[4];
+#pragma unroll
+              for (int rg = 0; rg < 4; ++rg)
+                w[rg] = 32 * rg < R ? *reinterpret_cast<const uint32_t*>(
+                                          src + (32 * rg + lane) * 16 + CPS * j + 4 * b)
+                                    : 0u;
+              *reinterpret_cast<uint4*>(smem + blk0 + stage * blk_stage + b * SF_BLOCK +
+                                        lane * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+            }
             fence_proxy_async_smem();  // generic-proxy writes -> tcgen05.cp (async proxy)
             __syncwarp();
             if (lane == 0) mbar_arrive(full_bar(stage));
@@ -653,7 +716,7 @@ bsmxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           }
           if (!ok) break;
           __syncwarp();
-          issue_group((int)((g + 2) % STG_SLOTS));  // the slot group g - 1 used is free
+          issue_group((int)((g + C::STG_AHEAD) % C::STG_N));  // the slot group g - 1 used is free
         }
       }
       cp_async_wait_group<0>();
@@ -769,6 +832,136 @@ bsmxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           float x = __uint_as_float(v[j]);
           if constexpr (C::POST != 1.0f) x *= C::POST;
           Cmat[(tc.m0 + j) * (int64_t)args.N + n] = __float2bfloat16_rn(x);
+        }
+      }
+    }
+  } else if (C::SF_ST && warp >= SFW_WARP0 && warp < SFW_WARP0 + 4) {
+    // ============================== scale writers ===============================
+    // Warp 8 + q stores TMEM lanes 32q..32q+31 of each stage's scale slot (the slot of stage
+    // s is rewritten after the stage's loads of its next use landed, which followed the MMAs
+    // that read the slot).  What the MMA reads there (pinned by the parity tests): for the
+    // weights (its M operand) lane quarter q reads only column q of a 4-column group, row
+    // 32q + i's codes at lane i; for the tokens (its N operand) every lane quarter reads
+    // token row 32j + i's codes at lane i of column j, so each writer stores all token rows.
+    const uint32_t q = warp & 3;
+    GroupedScheduler<C::TN, WROWS> sched;
+    uint32_t stage = 0, phase = 0;
+    bool ok = true;
+    TileCoord tc;
+    auto stage_ready = [&]() {
+      if (!__all_sync(0xffffffffu, role_wait(full_bar(stage), phase, abort))) {
+        if (lane == 0) record_error(args.err, DEV_TIMEOUT, abort);
+        return false;
+      }
+      return true;
+    };
+    auto stage_done = [&]() {
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sfull_bar(stage));
+      if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
+    };
+    if (sf_direct) {
+      // Each lane fetches, STG_AHEAD groups of GS stages ahead, the 16-byte chunks of weight
+      // row 32q + lane (unless the weight blocks come pre-packed with the stage) and of token
+      // rows 32j + lane, into this warp's staging slots; nothing is shared between lanes.
+      const uint8_t* a_sc = static_cast<const uint8_t*>(args.a_scales);
+      const uint8_t* b_sc = static_cast<const uint8_t*>(args.b_scales);
+      const int G = KB / GS;
+      const uint32_t sWs = smem_u32(smem + C::SMEM_STG) + q * 512 + lane * 16;
+      const uint32_t sTs = smem_u32(smem + C::SMEM_STGT) + q * (C::TN * 16) + lane * 16;
+      const uint8_t* pWs = smem + C::SMEM_STG + q * 512 + lane * 16;
+      const uint8_t* pTs = smem + C::SMEM_STGT + q * (C::TN * 16) + lane * 16;
+      GroupedScheduler<C::TN, WROWS> pre;
+      TileCoord tp;
+      int64_t tp_t = blockIdx.x;
+      bool pre_ok = pre.locate(args, tp_t, tp);
+      int qp = 0;
+      auto issue_group = [&](int slot) {
+        if (pre_ok) {
+          if (!packed_b)
+            cp_async_16(sWs + slot * STG_SLOT,
+                        b_sc + ((int64_t)tp.be * args.N + tp.n0 + 32 * q + lane) * scale_row +
+                            16 * qp,
+                        16u);
+#pragma unroll
+          for (int jt = 0; jt < C::TN / 32; ++jt) {
+            const int64_t m = tp.m0 + 32 * jt + lane;
+            const bool live = m < args.M_total;
+            cp_async_16(sTs + slot * C::STGT_SLOT + jt * 512,
+                        live ? a_sc + m * scale_row + 16 * qp : a_sc, live ? 16u : 0u);
+          }
+          if (++qp == G) {
+            qp = 0;
+            tp_t += gridDim.x;
+            pre_ok = tp_t < total_tiles && pre.locate(args, tp_t, tp);
+          }
+        }
+        cp_async_commit();  // an empty group keeps the group count in step
+      };
+      for (int a = 0; a < C::STG_AHEAD; ++a) issue_group(a);
+      int64_t g = 0;
+      for (int64_t t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
+        if (!sched.locate(args, t, tc)) break;
+        for (int qg = 0; ok && qg < G; ++qg, ++g) {
+          cp_async_wait_group<C::STG_AHEAD - 1>();  // this lane's chunks of group g landed
+          // the slot group g - 1 used is free (this lane read only its own chunks)
+          issue_group((int)((g + C::STG_AHEAD) % C::STG_N));
+          const uint32_t slot = (uint32_t)(g % C::STG_N);
+          for (int j = 0; j < GS; ++j) {
+            if (!stage_ready()) {
+              ok = false;
+              break;
+            }
+            const uint32_t tcol =
+                tmem_base + ((q * 32) << 16) + C::ACC_COLS + stage * C::SF_STAGE_COLS;
+#pragma unroll
+            for (int b = 0; b < CPS / 4; ++b) {
+              const uint32_t w =
+                  packed_b ? *reinterpret_cast<const uint32_t*>(
+                                 smem + C::SMEM_SFW + stage * C::SFW_STAGE + lane * 16 + 4 * q)
+                           : *reinterpret_cast<const uint32_t*>(pWs + slot * STG_SLOT +
+                                                                CPS * j + 4 * b);
+              tmem_st_32x32b_x1(tcol + 4 * b + q, w);
+              const uint32_t x0 = *reinterpret_cast<const uint32_t*>(
+                  pTs + slot * C::STGT_SLOT + CPS * j + 4 * b);
+              if constexpr (C::TN >= 64) {
+                const uint32_t x1 = *reinterpret_cast<const uint32_t*>(
+                    pTs + slot * C::STGT_SLOT + 512 + CPS * j + 4 * b);
+                tmem_st_32x32b_x2(tcol + C::SF_COLS + 4 * b, x0, x1);
+              } else {
+                tmem_st_32x32b_x1(tcol + C::SF_COLS + 4 * b, x0);
+              }
+            }
+            stage_done();
+          }
+        }
+      }
+      cp_async_wait_group<0>();
+    } else {
+      // relay: lane i takes the 16-byte row i of every packed 512-byte block (the loaders'
+      // or the producer's) and writes it to 4 columns, as tcgen05.cp.32x128b.warpx4
+      // replicates a block into all four lane quarters
+      for (int64_t t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
+        if (!sched.locate(args, t, tc)) break;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!stage_ready()) {
+            ok = false;
+            break;
+          }
+          const uint32_t tcol =
+              tmem_base + ((q * 32) << 16) + C::ACC_COLS + stage * C::SF_STAGE_COLS;
+#pragma unroll
+          for (int b = 0; b < C::SF_GROUPS; ++b) {
+            const uint4 w = *reinterpret_cast<const uint4*>(
+                smem + C::SMEM_SFW + stage * C::SFW_STAGE + b * SF_BLOCK + lane * 16);
+            const uint4 x = *reinterpret_cast<const uint4*>(
+                smem + C::SMEM_SFT + stage * C::SFT_STAGE + b * SF_BLOCK + lane * 16);
+            tmem_st_32x32b_x4(tcol + 4 * b, w.x, w.y, w.z, w.w);
+            tmem_st_32x32b_x4(tcol + C::SF_COLS + 4 * b, x.x, x.y, x.z, x.w);
+          }
+          stage_done();
         }
       }
     }
