@@ -108,13 +108,18 @@ constexpr int SCALE_LOOKAHEAD = 4;   // scale stages in flight per loader warp
 constexpr int STG_SLOTS = 3;         // staged 16-byte groups: one in use, two in flight
 constexpr uint32_t STG_SLOT = WROWS * 16;
 
-template <int TN_, int FMT_ = FMT_MXFP8>
+template <int TN_, int FMT_ = FMT_MXFP8, int SK_ = 128>
 struct Cfg {
   static constexpr int TN = TN_;                               // token rows per tile
   static constexpr int FMT = FMT_;
   // fp4 MMA kinds: the packed tiles feed the tensor core as loaded (64-byte swizzle, K = 64
   // per MMA), no converter warps
   static constexpr bool NATIVE = FMT_ == FMT_MXFP4_MMA || FMT_ == FMT_NVFP4_MMA;
+  // K per stage: 128, or 256 for the fp4 kinds on chunkable scale rows (16 KB weight stages of
+  // 128-byte rows, 128-byte swizzle, four K = 64 MMAs and one commit per stage)
+  static constexpr int SK = SK_;
+  static constexpr bool WIDE = SK_ == 256;
+  static_assert(SK_ == 128 || (NATIVE && SK_ == 256), "256-K stages for the fp4 kinds only");
   static constexpr bool NV = FMT_ == FMT_NVFP4 || FMT_ == FMT_NVFP4_MMA;
   static constexpr bool B_FP4 = FMT_ != FMT_MXFP8;
   static constexpr bool A_FP4 = FMT_ != FMT_MXFP8 && FMT_ != FMT_MXFP8_MXFP4;
@@ -130,17 +135,22 @@ struct Cfg {
   static constexpr uint32_t ESZ = NV ? 2 : 1;
   // scale bytes per stage: packed UE8M0 blocks (MX), row-major e4m3 codes per 16 K (nvfp4 for
   // the fp16 MMA), or two packed UE4M3 blocks, one per K = 64 MMA (nvfp4 MMA kind)
-  static constexpr int SF_GROUPS = (NV && NATIVE) ? 2 : 1;  // 4-column TMEM scale groups
-  static constexpr uint32_t SFW_STAGE = NV_F16 ? WROWS * (BK / 16) : SF_GROUPS * SF_BLOCK;
-  static constexpr uint32_t SFT_STAGE = SF_GROUPS * SF_BLOCK;
+  // 4-column TMEM scale groups per operand and stage: one per 128 K of UE8M0 codes, one per
+  // K = 64 MMA of UE4M3 codes
+  static constexpr int SF_GROUPS = !NATIVE ? 1 : NV ? SK / 64 : SK / 128;
+  // (wide stages: the scale writers fetch the codes themselves; the weight blocks stay for
+  // pre-packed MX weight scales, which the producer copies with the stage)
+  static constexpr uint32_t SFW_STAGE =
+      NV_F16 ? WROWS * (BK / 16) : (WIDE && NV) ? 0 : SF_GROUPS * SF_BLOCK;
+  static constexpr uint32_t SFT_STAGE = WIDE ? 0 : SF_GROUPS * SF_BLOCK;
   static_assert(!NV_F16 || TN * (BK / 16) <= SFT_STAGE, "nvfp4 token scales of a stage");
   // Load ring (STAGES deep): per stage the weight tile, the token tile and the two scale
   // blocks as they arrive -- e4m3 tiles with the 128-byte swizzle, packed e2m1 tiles
   // [rows x 64 B] without swizzle.  Byte offsets of a K block along a row: W_KX, T_KX.
-  static constexpr uint32_t W_STAGE = B_FP4 ? WROWS * BK / 2 : WROWS * BK;  // 8 / 16 KB
-  static constexpr uint32_t T_STAGE = A_FP4 ? TN * BK / 2 : TN * BK;
-  static constexpr int W_KX = B_FP4 ? BK / 2 : BK;
-  static constexpr int T_KX = A_FP4 ? BK / 2 : BK;
+  static constexpr uint32_t W_STAGE = B_FP4 ? WROWS * SK / 2 : WROWS * SK;  // 8 / 16 KB
+  static constexpr uint32_t T_STAGE = A_FP4 ? TN * SK / 2 : TN * SK;
+  static constexpr int W_KX = B_FP4 ? SK / 2 : SK;
+  static constexpr int T_KX = A_FP4 ? SK / 2 : SK;
   // Converted ring (fp4 formats): the e4m3 (fp16) tiles the MMA reads in place of the packed
   // ones; slot c takes the stages i with i % CSTAGES == c, converted by SPLIT warps that
   // share the rows of each stage (nvfp4's dequantization is the heavier, and its 40 KB
@@ -152,9 +162,11 @@ struct Cfg {
   static constexpr uint32_t CT_STAGE = A_FP4 ? TN * BK * ESZ : 0;
   static constexpr uint32_t CONV_BYTES = CSTAGES * (CW_STAGE + CT_STAGE);
   static constexpr uint32_t PER_STAGE = W_STAGE + T_STAGE + SFW_STAGE + SFT_STAGE;
-  // staged scale loads (both operands): STG_AHEAD groups of 16-byte row chunks in flight,
-  // 8 stages ahead for e4m3 and mxf4 tiles, 12 for the 8 KB mxf4 / nvf4 stages
-  static constexpr int STG_AHEAD = NATIVE ? (NV ? 6 : 3) : STG_SLOTS - 1;
+  // staged scale loads (both operands): STG_AHEAD groups of 16-byte row chunks in flight:
+  // 8 stages ahead for e4m3 tiles; 1536 K (12 stages of 128 K, 6 of 256 K) for the fp4 kinds
+  static constexpr int CPS = NV ? SK / 16 : SK / 32;  // scale codes per row and stage
+  static constexpr int GS = 16 / CPS;                 // stages per 16-byte chunk
+  static constexpr int STG_AHEAD = NATIVE ? (1536 / SK) / GS : STG_SLOTS - 1;
   static constexpr int STG_N = STG_AHEAD + 1;
   // staging per slot: 128 weight rows and the token rows (x4 with the scale writers, each of
   // which keeps its own copy of the token rows)
@@ -198,8 +210,11 @@ struct Cfg {
   // 128-byte-swizzled tiles start on 1024-byte boundaries
   static_assert(SMEM_W % 1024 == 0 && SMEM_T % 1024 == 0 && CT_STAGE % 1024 == 0, "swizzle");
   static_assert(A_FP4 || T_STAGE % 1024 == 0, "token tiles keep the 1024-byte alignment");
-  // 64-byte-swizzled packed tiles (fp4 MMA kinds) start on 512-byte boundaries
+  // 64-byte-swizzled packed tiles (fp4 MMA kinds) start on 512-byte boundaries, 128-byte-
+  // swizzled ones (wide stages) on 1024-byte boundaries
   static_assert(!NATIVE || (W_STAGE % 512 == 0 && T_STAGE % 512 == 0), "64-byte swizzle");
+  static_assert(!WIDE || (W_STAGE % 1024 == 0 && T_STAGE % 1024 == 0), "128-byte swizzle");
+  static_assert(!NATIVE || CPS * GS == 16, "a 16-byte chunk holds whole stages of codes");
   static_assert(B_FP4 || W_STAGE % 1024 == 0, "weight tiles keep the 1024-byte alignment");
 };
 
@@ -390,19 +405,27 @@ bsmxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   volatile int* abort = &ctl->abort;
   const uint32_t warp = threadIdx.x >> 5;
   const uint32_t lane = threadIdx.x & 31;
-  const int KB = args.K / BK;
+  const int KB = args.K / C::SK;  // stages per tile
   // bytes per row of a row-major scale matrix: UE8M0 per 32 K, or e4m3 per 16 K (nvfp4)
   const int scale_row = args.K / (C::NV ? 16 : 32);
   const bool packed_b = args.b_scales_packed != 0;
   // Scale writers fetching their own scale chunks (SF_ST, chunkable rows: each row's codes of
   // 16 / CPS consecutive stages form one aligned 16-byte chunk); otherwise the loader warps
   // pack each stage's blocks in shared memory and the writers relay them into TMEM.
-  constexpr int CPS = C::NV ? 8 : 4;  // scale codes per row per stage
-  constexpr int GS = 16 / CPS;        // stages per 16-byte chunk
+  constexpr int CPS = C::NATIVE ? C::CPS : C::NV ? 8 : 4;  // scale codes per row per stage
+  constexpr int GS = 16 / CPS;                               // stages per 16-byte chunk
   const bool sf_direct =
       C::SF_ST && KB % GS == 0 && scale_row % 16 == 0 &&
       reinterpret_cast<uintptr_t>(args.a_scales) % 16 == 0 &&
       (packed_b || reinterpret_cast<uintptr_t>(args.b_scales) % 16 == 0);
+  // pre-packed weight-scale bytes per stage (one 512-byte block per 128 K)
+  constexpr uint32_t PB_BYTES = (C::SK / 128) * SF_BLOCK;
+  // Wide stages run with fetching writers only (the host launches them on chunkable rows):
+  // anything else winds down before any barrier is used, with the error recorded.
+  if (C::WIDE && !sf_direct) {
+    if (threadIdx.x == 0) atomicCAS(args.err, 0, DEV_TIMEOUT);
+    return;
+  }
 
   // Tiles: per expert ceil(M_e / TN) token tiles x N/128 weight tiles (weights fastest).
   if (warp == 0) {
@@ -472,22 +495,23 @@ bsmxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         if (!sched.locate(args, t, tc)) break;
         const int32_t w_row = tc.be * args.N + tc.n0;
         const int32_t t_row = (int32_t)tc.m0;
-        // packed weight scales: this tile's 128 rows, K block 0 (blocks of a row are adjacent)
+        // packed weight scales: this tile's 128 rows, K block 0 (blocks of a row are adjacent,
+        // one per 128 K)
         const uint8_t* w_sf = static_cast<const uint8_t*>(args.b_scales) +
-                              ((int64_t)w_row / WROWS) * KB * SF_BLOCK;
+                              ((int64_t)w_row / WROWS) * (args.K / 128) * SF_BLOCK;
         for (int kb = 0; kb < KB; ++kb) {
           if (!role_wait(empty_bar(stage), phase ^ 1, abort)) {
             record_error(args.err, DEV_TIMEOUT, abort);
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(full_bar(stage), C::STAGE_TX + (packed_b ? SF_BLOCK : 0u));
+          mbar_arrive_expect_tx(full_bar(stage), C::STAGE_TX + (packed_b ? PB_BYTES : 0u));
           tma_load_2d_hint(sW + stage * C::W_STAGE, &tmB, kb * C::W_KX, w_row, full_bar(stage),
                            pol_w);
           tma_load_2d(sT + stage * C::T_STAGE, &tmA, kb * C::T_KX, t_row, full_bar(stage));
           if (packed_b)  // the stage's weight-scale block is stored ready-made
-            bulk_copy_g2s_hint(sSFW + stage * C::SFW_STAGE, w_sf + (int64_t)kb * SF_BLOCK, SF_BLOCK,
-                               full_bar(stage), pol_w);
+            bulk_copy_g2s_hint(sSFW + stage * C::SFW_STAGE, w_sf + (int64_t)kb * PB_BYTES,
+                               PB_BYTES, full_bar(stage), pol_w);
           ++issued;
           if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
         }
@@ -553,18 +577,22 @@ bsmxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             if (++cstage == C::CSTAGES) { cstage = 0; cphase ^= 1; }
           }
           if constexpr (C::NATIVE) {
-            // packed e2m1 tiles of 64-byte rows: two K = 64 MMAs per stage, 32 bytes apart
-            const uint64_t wd = kmajor_sw64_desc(sW + stage * C::W_STAGE);
-            const uint64_t td = kmajor_sw64_desc(sT + stage * C::T_STAGE);
+            // packed e2m1 tiles of 64-byte rows (64-byte swizzle) or 128-byte rows (wide
+            // stages, 128-byte swizzle): a K = 64 MMA every 32 bytes
+            const uint64_t wd = C::WIDE ? kmajor_sw128_desc(sW + stage * C::W_STAGE)
+                                        : kmajor_sw64_desc(sW + stage * C::W_STAGE);
+            const uint64_t td = C::WIDE ? kmajor_sw128_desc(sT + stage * C::T_STAGE)
+                                        : kmajor_sw64_desc(sT + stage * C::T_STAGE);
 #pragma unroll
-            for (int k = 0; k < BK / 64; ++k) {
+            for (int k = 0; k < C::SK / 64; ++k) {
               if constexpr (C::NV)  // UE4M3 per 16: the k-th scale group of each operand
                 umma_mxf4nvf4_4x(d_tmem, wd + (uint64_t)(k * 2), td + (uint64_t)(k * 2),
                                  idesc_nvf4_e2m1_ue4m3(WROWS, C::TN), sfw_t + 4 * k, sft_t + 4 * k,
                                  (kb > 0 || k > 0) ? 1u : 0u);
-              else  // UE8M0 per 32: bytes 2k, 2k + 1 of the stage's scale word
+              else  // UE8M0 per 32: group k / 2, bytes 2 (k % 2), +1 of its scale word
                 umma_mxf4(d_tmem, wd + (uint64_t)(k * 2), td + (uint64_t)(k * 2),
-                          idesc_mxf4_e2m1(WROWS, C::TN, 2 * k, 2 * k), sfw_t, sft_t,
+                          idesc_mxf4_e2m1(WROWS, C::TN, 2 * (k & 1), 2 * (k & 1)),
+                          sfw_t + 4 * (k >> 1), sft_t + 4 * (k >> 1),
                           (kb > 0 || k > 0) ? 1u : 0u);
             }
           } else if constexpr (C::NV_F16) {
@@ -601,7 +629,7 @@ bsmxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       }
     }
     __syncwarp();
-  } else if (!sf_direct && (warp == 2 || (warp == 3 && !packed_b))) {
+  } else if (!C::WIDE && !sf_direct && (warp == 2 || (warp == 3 && !packed_b))) {
     // =============================== scale loaders ===============================
     // Warp 2 gathers the token rows' scales, warp 3 the weight rows' (unless they arrive
     // pre-packed with the producer's copies), into each stage's packed block(s): row r's 4
@@ -919,8 +947,9 @@ bsmxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 #pragma unroll
             for (int b = 0; b < CPS / 4; ++b) {
               const uint32_t w =
-                  packed_b ? *reinterpret_cast<const uint32_t*>(
-                                 smem + C::SMEM_SFW + stage * C::SFW_STAGE + lane * 16 + 4 * q)
+                  packed_b ? *reinterpret_cast<const uint32_t*>(smem + C::SMEM_SFW +
+                                                               stage * C::SFW_STAGE +
+                                                               b * SF_BLOCK + lane * 16 + 4 * q)
                            : *reinterpret_cast<const uint32_t*>(pWs + slot * STG_SLOT +
                                                                 CPS * j + 4 * b);
               tmem_st_32x32b_x1(tcol + 4 * b + q, w);
@@ -1084,12 +1113,17 @@ cudaError_t launch_bsmxfp8(int tn, const CUtensorMap& tmA, const CUtensorMap& tm
 }
 
 // fp4 operands: a_fp4 = tokens packed e2m1 (else e4m3); the weights are packed e2m1; tn is
-// 32 or 64.  mma_kind (with a_fp4): kind::mxf4 on the packed tiles.
-cudaError_t launch_bsmxfp4(int tn, bool a_fp4, bool mma_kind, const CUtensorMap& tmA,
+// 32 or 64.  mma_kind (with a_fp4): kind::mxf4 on the packed tiles, stage_k K per stage.
+cudaError_t launch_bsmxfp4(int tn, bool a_fp4, bool mma_kind, int stage_k, const CUtensorMap& tmA,
                            const CUtensorMap& tmB, const GemmArgs& args, int num_sms,
                            cudaStream_t stream) {
   using namespace mx;
-  if (a_fp4 && mma_kind) {
+  if (a_fp4 && mma_kind && stage_k == 256) {
+    switch (tn) {
+      case 32: return launch<Cfg<32, FMT_MXFP4_MMA, 256>>(tmA, tmB, args, num_sms, stream);
+      case 64: return launch<Cfg<64, FMT_MXFP4_MMA, 256>>(tmA, tmB, args, num_sms, stream);
+    }
+  } else if (a_fp4 && mma_kind) {
     switch (tn) {
       case 32: return launch<Cfg<32, FMT_MXFP4_MMA>>(tmA, tmB, args, num_sms, stream);
       case 64: return launch<Cfg<64, FMT_MXFP4_MMA>>(tmA, tmB, args, num_sms, stream);
@@ -1113,9 +1147,17 @@ cudaError_t launch_bsmxfp4(int tn, bool a_fp4, bool mma_kind, const CUtensorMap&
 namespace bsfp8 {
 // nvfp4 x nvfp4: both operands packed e2m1 with e4m3 scales per 16 K; tn is 32 or 64.
 // mma_kind: kind::mxf4nvf4 (scale_vec::4X) on the packed tiles.
-cudaError_t launch_bsnvfp4(int tn, bool mma_kind, const CUtensorMap& tmA, const CUtensorMap& tmB,
-                           const GemmArgs& args, int num_sms, cudaStream_t stream) {
+cudaError_t launch_bsnvfp4(int tn, bool mma_kind, int stage_k, const CUtensorMap& tmA,
+                           const CUtensorMap& tmB, const GemmArgs& args, int num_sms,
+                           cudaStream_t stream) {
   using namespace mx;
+  if (mma_kind && stage_k == 256) {
+    switch (tn) {
+      case 32: return launch<Cfg<32, FMT_NVFP4_MMA, 256>>(tmA, tmB, args, num_sms, stream);
+      case 64: return launch<Cfg<64, FMT_NVFP4_MMA, 256>>(tmA, tmB, args, num_sms, stream);
+    }
+    return cudaErrorInvalidValue;
+  }
   if (mma_kind) {
     switch (tn) {
       case 32: return launch<Cfg<32, FMT_NVFP4_MMA>>(tmA, tmB, args, num_sms, stream);

@@ -325,18 +325,27 @@ bsfp8_status mx_fmt_gemm(int a_fmt, int b_fmt, const void* A, const void* B,
   GemmArgs args{offsets, a_scales, b_scales, C, M_total, N, K, G, dev->err_word, ids, E,
                 packed_b ? 1 : 0};
   const int tn = std::min(choose_mx_token_tile(M_total, G), 64);  // fp4 tiles: tn <= 64
-  // both operands fp4: the MMA kinds read the packed tiles 64-byte swizzled
+  // Both operands fp4: the MMA kinds read the packed tiles as loaded, 256 K per stage
+  // (128-byte rows, 128-byte swizzle) when every scale row's codes come in aligned 16-byte
+  // chunks of whole stages, else 128 K (64-byte rows, 64-byte swizzle).
+  // BSFP8_FP4_STAGE_K=128 keeps 128 K.
   const bool kind = a_fp4 && fp4_mma_kind();
+  const char* sk_env = std::getenv("BSFP8_FP4_STAGE_K");
+  const bool wide = kind && !(sk_env && std::strcmp(sk_env, "128") == 0) &&
+                    K % (nv ? 256 : 512) == 0 && aligned(a_scales, 16) &&
+                    (packed_b || aligned(b_scales, 16));
+  const uint32_t box = wide ? 128 : 64;  // bytes of packed e2m1 per row and stage
   CUtensorMap tmA, tmB;
-  const bool ok_a = a_fp4 ? encode_u8_2d(&tmA, A, (uint64_t)K / 2, (uint64_t)M_total, 64,
+  const bool ok_a = a_fp4 ? encode_u8_2d(&tmA, A, (uint64_t)K / 2, (uint64_t)M_total, box,
                                          (uint32_t)tn, kind)
                           : encode_u8_2d(&tmA, A, (uint64_t)K, (uint64_t)M_total, 128,
                                          (uint32_t)tn);
-  if (!ok_a || !encode_u8_2d(&tmB, B, (uint64_t)K / 2, (uint64_t)E * N, 64, 128, kind))
+  if (!ok_a || !encode_u8_2d(&tmB, B, (uint64_t)K / 2, (uint64_t)E * N, box, 128, kind))
     return BSFP8_ERR_CUDA;
+  const int stage_k = wide ? 256 : 128;
   const cudaError_t e =
-      nv ? launch_bsnvfp4(tn, kind, tmA, tmB, args, dev->num_sms, stream)
-         : launch_bsmxfp4(tn, a_fp4, kind, tmA, tmB, args, dev->num_sms, stream);
+      nv ? launch_bsnvfp4(tn, kind, stage_k, tmA, tmB, args, dev->num_sms, stream)
+         : launch_bsmxfp4(tn, a_fp4, kind, stage_k, tmA, tmB, args, dev->num_sms, stream);
   return e == cudaSuccess ? BSFP8_OK : BSFP8_ERR_CUDA;
 }
 

@@ -76,20 +76,23 @@ cudaError_t launch_bsmxfp8(int tn, const CUtensorMap& tmA, const CUtensorMap& tm
                            const GemmArgs& args, int num_sms, cudaStream_t stream);
 
 // The same kernel with packed e2m1 weights (mxfp4) and e4m3 tokens, or packed e2m1 tokens
-// too (a_fp4).  mma_kind (a_fp4 only): the packed tiles feed kind::mxf4 as loaded, and tmA /
-// tmB map them with [64-byte x rows] boxes and the 64-byte swizzle; otherwise the tiles are
-// re-encoded on chip as e4m3 for kind::mxf8f6f4 and the packed operands are mapped with
-// [64-byte x rows] boxes and no swizzle.
-cudaError_t launch_bsmxfp4(int tn, bool a_fp4, bool mma_kind, const CUtensorMap& tmA,
+// too (a_fp4).  mma_kind (a_fp4 only): the packed tiles feed kind::mxf4 as loaded, stage_k
+// (128 or 256) K per stage, and tmA / tmB map them with [stage_k/2-byte x rows] boxes swizzled
+// over the box width.  stage_k = 256 requires chunkable scale rows: K % 512 == 0 and 16-byte
+// aligned scales (b_scales unless pre-packed).  Otherwise the tiles are re-encoded on chip as
+// e4m3 for kind::mxf8f6f4 and the packed operands are mapped with [64-byte x rows] boxes and
+// no swizzle.
+cudaError_t launch_bsmxfp4(int tn, bool a_fp4, bool mma_kind, int stage_k, const CUtensorMap& tmA,
                            const CUtensorMap& tmB, const GemmArgs& args, int num_sms,
                            cudaStream_t stream);
 
 // nvfp4 x nvfp4 (packed e2m1, e4m3 scales per 16 K, row-major [rows, K/16]) in the same
-// kernel.  mma_kind: kind::mxf4nvf4 with scale_vec::4X on the packed tiles (64-byte swizzle
-// boxes, as above); otherwise the tiles are dequantized on chip to fp16 for kind::f16 (boxes
-// without swizzle).
-cudaError_t launch_bsnvfp4(int tn, bool mma_kind, const CUtensorMap& tmA, const CUtensorMap& tmB,
-                           const GemmArgs& args, int num_sms, cudaStream_t stream);
+// kernel.  mma_kind: kind::mxf4nvf4 with scale_vec::4X on the packed tiles (boxes as above;
+// stage_k = 256 requires K % 256 == 0 and 16-byte aligned scales); otherwise the tiles are
+// dequantized on chip to fp16 for kind::f16 (boxes without swizzle).
+cudaError_t launch_bsnvfp4(int tn, bool mma_kind, int stage_k, const CUtensorMap& tmA,
+                           const CUtensorMap& tmB, const GemmArgs& args, int num_sms,
+                           cudaStream_t stream);
 
 // MXFP8 grouped GEMM with CTA-pair 256 x 256 tiles and overlapping TMEM accumulators.
 cudaError_t launch_bsmxfp8_pair(const CUtensorMap& tmA, const CUtensorMap& tmB,
