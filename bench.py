@@ -460,10 +460,11 @@ def time_fp4_formats(args, flush, stream, peaks, ref_ms):
         ms = statistics.mean(s.elapsed_time(e) for s, e in zip(starts, ends))
         gbs = p.bytes() / (ms * 1e-3) / 1e9
         traffic, prof_file = traffic_from_profiles(f"fp4:{af}x{bf}")
-        both_fp4 = af != "mxfp8" and os.environ.get("BSFP8_FP4_MMA") != "convert"
+        kinds = os.environ.get("BSFP8_FP4_MMA") != "convert"
         out["pairs"][f"{af} x {bf}"] = {
-            "mma": ("kind::mxf4nvf4 scale_vec::4X" if af == "nvfp4" else "kind::mxf4")
-                   if both_fp4 else "packed weights converted on chip for kind::mxf8f6f4",
+            "mma": ({"nvfp4": "kind::mxf4nvf4 scale_vec::4X", "mxfp4": "kind::mxf4",
+                     "mxfp8": "kind::mxf8f6f4, e2m1 weights loaded padded"}[af]
+                    if kinds else "packed fp4 tiles converted on chip"),
             "ms_per_step": ms, "TFLOP/s": p.flops() / (ms * 1e-3) / 1e12,
             "algorithmic_bytes": p.bytes(), "achieved_gbs": gbs,
             "hbm_frac": gbs / peaks["hbm_gbs"], "traffic": traffic,

@@ -102,6 +102,8 @@ enum Format : int {
   FMT_NVFP4 = 3,        // e2m1 x e2m1 with e4m3 scales per 16 (fp16 MMA on dequantized tiles)
   FMT_MXFP4_MMA = 4,    // e2m1 x e2m1, kind::mxf4 on the packed tiles as loaded
   FMT_NVFP4_MMA = 5,    // e2m1 x e2m1 with UE4M3 scales per 16, kind::mxf4nvf4 (scale_vec::4X)
+  FMT_MXFP8_MXFP4_MMA = 6,  // e4m3 x e2m1, kind::mxf8f6f4 on e2m1 weight tiles that TMA loads
+                            // padded (16 codes in each 16 bytes' first 8)
 };
 constexpr int SF_BLOCK = 512;        // packed scale block: 128 rows x 4 codes
 constexpr int SCALE_LOOKAHEAD = 4;   // scale stages in flight per loader warp
@@ -114,15 +116,19 @@ struct Cfg {
   static constexpr int FMT = FMT_;
   // fp4 MMA kinds: the packed tiles feed the tensor core as loaded (64-byte swizzle, K = 64
   // per MMA), no converter warps
-  static constexpr bool NATIVE = FMT_ == FMT_MXFP4_MMA || FMT_ == FMT_NVFP4_MMA;
+  static constexpr bool NATIVE =
+      FMT_ == FMT_MXFP4_MMA || FMT_ == FMT_NVFP4_MMA || FMT_ == FMT_MXFP8_MXFP4_MMA;
+  // e4m3 tokens with e2m1 weights on kind::mxf8f6f4: the weight tile in shared memory has a
+  // byte per element (the padded layout), K = 32 per MMA as for e4m3
+  static constexpr bool MIXED = FMT_ == FMT_MXFP8_MXFP4_MMA;
   // K per stage: 128, or 256 for the fp4 kinds on chunkable scale rows (16 KB weight stages of
   // 128-byte rows, 128-byte swizzle, four K = 64 MMAs and one commit per stage)
   static constexpr int SK = SK_;
   static constexpr bool WIDE = SK_ == 256;
-  static_assert(SK_ == 128 || (NATIVE && SK_ == 256), "256-K stages for the fp4 kinds only");
+  static_assert(SK_ == 128 || (NATIVE && !MIXED && SK_ == 256), "256-K stages: fp4 x fp4 kinds");
   static constexpr bool NV = FMT_ == FMT_NVFP4 || FMT_ == FMT_NVFP4_MMA;
   static constexpr bool B_FP4 = FMT_ != FMT_MXFP8;
-  static constexpr bool A_FP4 = FMT_ != FMT_MXFP8 && FMT_ != FMT_MXFP8_MXFP4;
+  static constexpr bool A_FP4 = FMT_ != FMT_MXFP8 && FMT_ != FMT_MXFP8_MXFP4 && !MIXED;
   static constexpr bool CONVERT = B_FP4 && !NATIVE;
   static constexpr bool NV_F16 = NV && CONVERT;  // nvfp4 dequantized for the fp16 MMA
   // Scale feed: the MMA thread copies each stage's scale blocks into TMEM (tcgen05.cp), or
@@ -147,9 +153,10 @@ struct Cfg {
   // Load ring (STAGES deep): per stage the weight tile, the token tile and the two scale
   // blocks as they arrive -- e4m3 tiles with the 128-byte swizzle, packed e2m1 tiles
   // [rows x 64 B] without swizzle.  Byte offsets of a K block along a row: W_KX, T_KX.
-  static constexpr uint32_t W_STAGE = B_FP4 ? WROWS * SK / 2 : WROWS * SK;  // 8 / 16 KB
+  static constexpr uint32_t W_STAGE = (B_FP4 && !MIXED) ? WROWS * SK / 2 : WROWS * SK;
   static constexpr uint32_t T_STAGE = A_FP4 ? TN * SK / 2 : TN * SK;
-  static constexpr int W_KX = B_FP4 ? SK / 2 : SK;
+  // TMA x of a stage: bytes, or e2m1 elements for the padded weight map
+  static constexpr int W_KX = (B_FP4 && !MIXED) ? SK / 2 : SK;
   static constexpr int T_KX = A_FP4 ? SK / 2 : SK;
   // Converted ring (fp4 formats): the e4m3 (fp16) tiles the MMA reads in place of the packed
   // ones; slot c takes the stages i with i % CSTAGES == c, converted by SPLIT warps that
@@ -192,7 +199,9 @@ struct Cfg {
   static constexpr uint32_t SMEM_STG = SMEM_SFT + STAGES * SFT_STAGE;
   static constexpr uint32_t SMEM_STGT = SMEM_STG + STG_N * STG_SLOT;  // token staging
   static constexpr uint32_t SMEM_CTL = SMEM_STGT + STG_N * STGT_SLOT;
-  static constexpr uint32_t STAGE_TX = W_STAGE + T_STAGE;
+  // bytes a stage's loads complete on its barrier (the padded e2m1 weight load counts the
+  // packed bytes it reads, half the shared-memory tile)
+  static constexpr uint32_t STAGE_TX = (MIXED ? W_STAGE / 2 : W_STAGE) + T_STAGE;
   // TMEM: 2 accumulators of TN columns, then 2 slots each of weight / token scales (4 columns
   // per scale group, every group on a 4-column boundary)
   static constexpr uint32_t ACC_COLS = 2 * TN;
@@ -576,7 +585,15 @@ bsmxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           if constexpr (C::CONVERT) {
             if (++cstage == C::CSTAGES) { cstage = 0; cphase ^= 1; }
           }
-          if constexpr (C::NATIVE) {
+          if constexpr (C::MIXED) {
+            // e2m1 weights (padded: a byte per element, 128-byte rows, 128-byte swizzle) and
+            // e4m3 tokens: 4 x K = 32, the scale-factor id picks the byte of the scale word
+#pragma unroll
+            for (int k = 0; k < C::SK / 32; ++k)
+              umma_mxf8f6f4<1>(d_tmem, wdesc + (uint64_t)(k * 2), tdesc + (uint64_t)(k * 2),
+                               idesc_mxf8f6f4(WROWS, C::TN, MXF_E2M1, MXF_E4M3, k, k), sfw_t,
+                               sft_t, (kb > 0 || k > 0) ? 1u : 0u);
+          } else if constexpr (C::NATIVE) {
             // packed e2m1 tiles of 64-byte rows (64-byte swizzle) or 128-byte rows (wide
             // stages, 128-byte swizzle): a K = 64 MMA every 32 bytes
             const uint64_t wd = C::WIDE ? kmajor_sw128_desc(sW + stage * C::W_STAGE)
@@ -1113,12 +1130,18 @@ cudaError_t launch_bsmxfp8(int tn, const CUtensorMap& tmA, const CUtensorMap& tm
 }
 
 // fp4 operands: a_fp4 = tokens packed e2m1 (else e4m3); the weights are packed e2m1; tn is
-// 32 or 64.  mma_kind (with a_fp4): kind::mxf4 on the packed tiles, stage_k K per stage.
+// 32 or 64.  mma_kind: kind::mxf4 on the packed tiles, stage_k K per stage (a_fp4), or
+// kind::mxf8f6f4 on e2m1 weight tiles loaded padded (e4m3 tokens).
 cudaError_t launch_bsmxfp4(int tn, bool a_fp4, bool mma_kind, int stage_k, const CUtensorMap& tmA,
                            const CUtensorMap& tmB, const GemmArgs& args, int num_sms,
                            cudaStream_t stream) {
   using namespace mx;
-  if (a_fp4 && mma_kind && stage_k == 256) {
+  if (!a_fp4 && mma_kind) {
+    switch (tn) {
+      case 32: return launch<Cfg<32, FMT_MXFP8_MXFP4_MMA>>(tmA, tmB, args, num_sms, stream);
+      case 64: return launch<Cfg<64, FMT_MXFP8_MXFP4_MMA>>(tmA, tmB, args, num_sms, stream);
+    }
+  } else if (a_fp4 && mma_kind && stage_k == 256) {
     switch (tn) {
       case 32: return launch<Cfg<32, FMT_MXFP4_MMA, 256>>(tmA, tmB, args, num_sms, stream);
       case 64: return launch<Cfg<64, FMT_MXFP4_MMA, 256>>(tmA, tmB, args, num_sms, stream);

@@ -107,6 +107,22 @@ bool encode_u8_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t r
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2D tensor map over packed e2m1 [rows, K] (K/2 bytes per row, 32-byte aligned base and
+// rows) that lands each element in a byte of shared memory, the padded layout kind::mxf8f6f4
+// reads e2m1 in: boxes of 128 elements x box_rows, 128-byte swizzle.
+bool encode_e2m1_padded_2d(CUtensorMap* map, const void* base, uint64_t K, uint64_t rows,
+                           uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {K, rows};
+  const cuuint64_t strides[1] = {K / 2};
+  const cuuint32_t box[2] = {128, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 2, const_cast<void*>(base), dims, strides,
+            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bsfp8_status check_common(const void* A, const void* B, const void* sa, const void* sb,
                           const int32_t* off, const int32_t* ids, void* C, int64_t M_total,
                           int N, int K, int G, int E) {
@@ -295,9 +311,9 @@ bsfp8_status mx_gemm(const void* A, const void* B, const uint8_t* a_scales,
 
 // Formats per operand.  (MXFP8, MXFP8) is mx_gemm; (MXFP4, MXFP4) and (NVFP4, NVFP4) run
 // the swap-AB kernel with the fp4 MMA kinds on the packed tiles as loaded; (MXFP8, MXFP4)
-// has no such kind (kind::mxf8f6f4 takes K = 32 per instruction either way) and converts the
-// packed weight tiles on chip to e4m3.  BSFP8_FP4_MMA=convert runs the converting kernels for
-// every pair (the forms before the fp4 kinds, kept for comparison).
+// runs kind::mxf8f6f4 on e2m1 weight tiles that the tensor map loads padded.
+// BSFP8_FP4_MMA=convert runs the converting kernels for every pair (the forms before the fp4
+// kinds, kept for comparison).
 bool fp4_mma_kind() {
   const char* v = std::getenv("BSFP8_FP4_MMA");
   return !(v && std::strcmp(v, "convert") == 0);
@@ -335,17 +351,23 @@ bsfp8_status mx_fmt_gemm(int a_fmt, int b_fmt, const void* A, const void* B,
                     K % (nv ? 256 : 512) == 0 && aligned(a_scales, 16) &&
                     (packed_b || aligned(b_scales, 16));
   const uint32_t box = wide ? 128 : 64;  // bytes of packed e2m1 per row and stage
+  // e4m3 tokens with e2m1 weights: kind::mxf8f6f4 on weight tiles loaded padded (the map
+  // needs a 32-byte aligned base), else converted on chip
+  const bool mixed_kind = !a_fp4 && fp4_mma_kind() && aligned(B, 32);
   CUtensorMap tmA, tmB;
   const bool ok_a = a_fp4 ? encode_u8_2d(&tmA, A, (uint64_t)K / 2, (uint64_t)M_total, box,
                                          (uint32_t)tn, kind)
                           : encode_u8_2d(&tmA, A, (uint64_t)K, (uint64_t)M_total, 128,
                                          (uint32_t)tn);
-  if (!ok_a || !encode_u8_2d(&tmB, B, (uint64_t)K / 2, (uint64_t)E * N, box, 128, kind))
-    return BSFP8_ERR_CUDA;
+  const bool ok_b = mixed_kind
+                        ? encode_e2m1_padded_2d(&tmB, B, (uint64_t)K, (uint64_t)E * N, 128)
+                        : encode_u8_2d(&tmB, B, (uint64_t)K / 2, (uint64_t)E * N, box, 128, kind);
+  if (!ok_a || !ok_b) return BSFP8_ERR_CUDA;
   const int stage_k = wide ? 256 : 128;
   const cudaError_t e =
       nv ? launch_bsnvfp4(tn, kind, stage_k, tmA, tmB, args, dev->num_sms, stream)
-         : launch_bsmxfp4(tn, a_fp4, kind, stage_k, tmA, tmB, args, dev->num_sms, stream);
+         : launch_bsmxfp4(tn, a_fp4, kind || mixed_kind, stage_k, tmA, tmB, args, dev->num_sms,
+                          stream);
   return e == cudaSuccess ? BSFP8_OK : BSFP8_ERR_CUDA;
 }
 

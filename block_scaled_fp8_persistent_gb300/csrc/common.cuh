@@ -79,9 +79,11 @@ cudaError_t launch_bsmxfp8(int tn, const CUtensorMap& tmA, const CUtensorMap& tm
 // too (a_fp4).  mma_kind (a_fp4 only): the packed tiles feed kind::mxf4 as loaded, stage_k
 // (128 or 256) K per stage, and tmA / tmB map them with [stage_k/2-byte x rows] boxes swizzled
 // over the box width.  stage_k = 256 requires chunkable scale rows: K % 512 == 0 and 16-byte
-// aligned scales (b_scales unless pre-packed).  Otherwise the tiles are re-encoded on chip as
-// e4m3 for kind::mxf8f6f4 and the packed operands are mapped with [64-byte x rows] boxes and
-// no swizzle.
+// aligned scales (b_scales unless pre-packed).  mma_kind with e4m3 tokens: kind::mxf8f6f4 on
+// e2m1 weights that tmB loads padded (CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, [128 elements x
+// 128 rows] boxes, 128-byte swizzle), tmA as for MXFP8.  Otherwise the tiles are re-encoded
+// on chip as e4m3 for kind::mxf8f6f4 and the packed operands are mapped with [64-byte x rows]
+// boxes and no swizzle.
 cudaError_t launch_bsmxfp4(int tn, bool a_fp4, bool mma_kind, int stage_k, const CUtensorMap& tmA,
                            const CUtensorMap& tmB, const GemmArgs& args, int num_sms,
                            cudaStream_t stream);

@@ -548,6 +548,14 @@ __host__ __device__ constexpr uint32_t idesc_mxf8f6f4_e4m3(uint32_t M, uint32_t 
   return ((sfb_id & 3u) << 4) | ((N >> 3) << 17) | (1u << 23) | ((M >> 4) << 24) |
          ((sfa_id & 3u) << 29);
 }
+// The same with the operand formats of kind::mxf8f6f4 (bits 7-9 A, 10-12 B): e4m3 0, e2m1 5
+// (e2m1 tiles in the padded shared layout, 16 codes in the first 8 of every 16 bytes).
+enum : uint32_t { MXF_E4M3 = 0, MXF_E2M1 = 5 };
+__host__ __device__ constexpr uint32_t idesc_mxf8f6f4(uint32_t M, uint32_t N, uint32_t a_fmt,
+                                                     uint32_t b_fmt, uint32_t sfa_id,
+                                                     uint32_t sfb_id) {
+  return idesc_mxf8f6f4_e4m3(M, N, sfa_id, sfb_id) | ((a_fmt & 7u) << 7) | ((b_fmt & 7u) << 10);
+}
 
 // Instruction descriptors for the fp4 block-scaled kinds, both operands packed e2m1 (format
 // code 1 in bits 7-9 and 10-12 for kind::mxf4 and kind::mxf4nvf4), K-major, the field layout

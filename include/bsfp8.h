@@ -227,12 +227,13 @@ bsfp8_status bsmxfp8_grouped_gemm_prepacked(const void* A, const void* B, const 
  *                   available (BSFP8_ERR_FORMAT).  A scale code with bit 7 set is outside the
  *                   format (the tensor core's scale type is unsigned): its result is not
  *                   specified.
- *   (MXFP8, MXFP4)  swap-AB tiles at every size.  No fp4 MMA kind takes e4m3 with e2m1 at more
- *                   than K = 32 per instruction, so the packed weight tiles are loaded as
- *                   they are and re-encoded on chip into e4m3 for the MXFP8 block-scaled MMA
- *                   (the "converting" form below).
- * Converting forms (environment variable BSFP8_FP4_MMA=convert selects them for the two
- * both-fp4 pairs too; kept for comparison):
+ *   (MXFP8, MXFP4)  swap-AB tiles at every size; tcgen05.mma kind::mxf8f6f4 with e4m3 tokens
+ *                   and e2m1 weights (K = 32 per instruction, UE8M0 per 32), the packed
+ *                   weight tiles landing in shared memory padded (a byte per element) as
+ *                   the tensor memory access unit expands them.  B must be 32-byte aligned
+ *                   for that load; a B that is only 16-byte aligned runs the converting form.
+ * Converting forms (environment variable BSFP8_FP4_MMA=convert selects them for every pair;
+ * kept for comparison):
  *   MX pairs        the packed tiles are re-encoded on chip into e4m3 for the MXFP8
  *                   block-scaled MMA: every e2m1 value times 2^-6 is an e4m3 value, and the
  *                   epilogue multiplies the fp32 sums by 2^6 per fp4 operand, so the result

@@ -15,10 +15,10 @@ pytestmark = pytest.mark.gpu
 
 PAIRS = [("mxfp8", "mxfp4"), ("mxfp4", "mxfp4"), ("nvfp4", "nvfp4")]
 MX_PAIRS = PAIRS[:2]
-# (a format, b format, path): both-fp4 pairs run the fp4 MMA kinds by default ("mma") and the
-# converting kernels on request ("convert"); mxfp8 x mxfp4 always converts its weight tiles
-FORMS = [("mxfp8", "mxfp4", "convert"), ("mxfp4", "mxfp4", "mma"), ("mxfp4", "mxfp4", "convert"),
-         ("nvfp4", "nvfp4", "mma"), ("nvfp4", "nvfp4", "convert")]
+# (a format, b format, path): every pair runs an fp4 MMA kind by default ("mma") and the
+# converting kernels on request ("convert")
+FORMS = [("mxfp8", "mxfp4", "mma"), ("mxfp8", "mxfp4", "convert"), ("mxfp4", "mxfp4", "mma"),
+         ("mxfp4", "mxfp4", "convert"), ("nvfp4", "nvfp4", "mma"), ("nvfp4", "nvfp4", "convert")]
 MX_FORMS = [f for f in FORMS if f[0] != "nvfp4"]
 NV_PATHS = ["mma", "convert"]
 

@@ -94,7 +94,8 @@ def test_dense_mxfp8_every_element(kernel, monkeypatch):
     _run_and_compare(p, ref, T)
 
 
-@pytest.mark.parametrize("a_fmt,b_fmt,path", [("mxfp8", "mxfp4", "convert"),
+@pytest.mark.parametrize("a_fmt,b_fmt,path", [("mxfp8", "mxfp4", "mma"),
+                                                ("mxfp8", "mxfp4", "convert"),
                                                 ("mxfp4", "mxfp4", "mma"),
                                                 ("mxfp4", "mxfp4", "convert"),
                                                 ("nvfp4", "nvfp4", "mma"),

@@ -60,10 +60,11 @@ def test_mx_sweep(seed, monkeypatch):
     _check(gen.mx_problem(counts, N, K, seed=2000 + seed, exact=bool(seed % 2)))
 
 
-# (a format, b format, token tile, path): the both-fp4 pairs on the fp4 MMA kinds and on the
-# converting kernels
+# (a format, b format, token tile, path): every pair on its fp4 MMA kind and on the converting
+# kernels
 FP4_FORMS = [(a, b, tn, path)
-             for (a, b, path) in (("mxfp8", "mxfp4", "convert"), ("mxfp4", "mxfp4", "mma"),
+             for (a, b, path) in (("mxfp8", "mxfp4", "mma"), ("mxfp8", "mxfp4", "convert"),
+                                  ("mxfp4", "mxfp4", "mma"),
                                   ("mxfp4", "mxfp4", "convert"), ("nvfp4", "nvfp4", "mma"),
                                   ("nvfp4", "nvfp4", "convert"))
              for tn in ("32", "64")]
