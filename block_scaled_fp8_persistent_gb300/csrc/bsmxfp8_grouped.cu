@@ -125,7 +125,7 @@ struct Cfg {
   // 128-byte rows, 128-byte swizzle, four K = 64 MMAs and one commit per stage)
   static constexpr int SK = SK_;
   static constexpr bool WIDE = SK_ == 256;
-  static_assert(SK_ == 128 || (NATIVE && !MIXED && SK_ == 256), "256-K stages: fp4 x fp4 kinds");
+  static_assert(SK_ == 128 || (NATIVE && SK_ == 256), "256-K stages for the fp4 kinds only");
   static constexpr bool NV = FMT_ == FMT_NVFP4 || FMT_ == FMT_NVFP4_MMA;
   static constexpr bool B_FP4 = FMT_ != FMT_MXFP8;
   static constexpr bool A_FP4 = FMT_ != FMT_MXFP8 && FMT_ != FMT_MXFP8_MXFP4 && !MIXED;
@@ -158,6 +158,9 @@ struct Cfg {
   // TMA x of a stage: bytes, or e2m1 elements for the padded weight map
   static constexpr int W_KX = (B_FP4 && !MIXED) ? SK / 2 : SK;
   static constexpr int T_KX = A_FP4 ? SK / 2 : SK;
+  // TMA boxes per operand and stage: a box is 128 bytes (or 128 padded e2m1 elements) wide
+  static constexpr int W_BOXES = MIXED ? SK / 128 : 1;
+  static constexpr int T_BOXES = A_FP4 ? 1 : SK / 128;
   // Converted ring (fp4 formats): the e4m3 (fp16) tiles the MMA reads in place of the packed
   // ones; slot c takes the stages i with i % CSTAGES == c, converted by SPLIT warps that
   // share the rows of each stage (nvfp4's dequantization is the heavier, and its 40 KB
@@ -515,9 +518,14 @@ bsmxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             break;
           }
           mbar_arrive_expect_tx(full_bar(stage), C::STAGE_TX + (packed_b ? PB_BYTES : 0u));
-          tma_load_2d_hint(sW + stage * C::W_STAGE, &tmB, kb * C::W_KX, w_row, full_bar(stage),
-                           pol_w);
-          tma_load_2d(sT + stage * C::T_STAGE, &tmA, kb * C::T_KX, t_row, full_bar(stage));
+#pragma unroll
+          for (int h = 0; h < C::W_BOXES; ++h)  // 128-element boxes into 128-row sub-tiles
+            tma_load_2d_hint(sW + stage * C::W_STAGE + h * (WROWS * 128), &tmB,
+                             kb * C::W_KX + h * 128, w_row, full_bar(stage), pol_w);
+#pragma unroll
+          for (int h = 0; h < C::T_BOXES; ++h)
+            tma_load_2d(sT + stage * C::T_STAGE + h * (C::TN * 128), &tmA, kb * C::T_KX + h * 128,
+                        t_row, full_bar(stage));
           if (packed_b)  // the stage's weight-scale block is stored ready-made
             bulk_copy_g2s_hint(sSFW + stage * C::SFW_STAGE, w_sf + (int64_t)kb * PB_BYTES,
                                PB_BYTES, full_bar(stage), pol_w);
@@ -587,12 +595,16 @@ bsmxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           }
           if constexpr (C::MIXED) {
             // e2m1 weights (padded: a byte per element, 128-byte rows, 128-byte swizzle) and
-            // e4m3 tokens: 4 x K = 32, the scale-factor id picks the byte of the scale word
+            // e4m3 tokens, in 128-K sub-tiles: K = 32 per MMA, the scale-factor id picks the
+            // byte of the sub-tile's scale word
 #pragma unroll
-            for (int k = 0; k < C::SK / 32; ++k)
-              umma_mxf8f6f4<1>(d_tmem, wdesc + (uint64_t)(k * 2), tdesc + (uint64_t)(k * 2),
-                               idesc_mxf8f6f4(WROWS, C::TN, MXF_E2M1, MXF_E4M3, k, k), sfw_t,
-                               sft_t, (kb > 0 || k > 0) ? 1u : 0u);
+            for (int k = 0; k < C::SK / 32; ++k) {
+              const int sub = k >> 2, kk = k & 3;
+              umma_mxf8f6f4<1>(d_tmem, wdesc + (uint64_t)((sub * WROWS * 128) >> 4) + kk * 2,
+                               tdesc + (uint64_t)((sub * C::TN * 128) >> 4) + kk * 2,
+                               idesc_mxf8f6f4(WROWS, C::TN, MXF_E2M1, MXF_E4M3, kk, kk),
+                               sfw_t + 4 * sub, sft_t + 4 * sub, (kb > 0 || k > 0) ? 1u : 0u);
+            }
           } else if constexpr (C::NATIVE) {
             // packed e2m1 tiles of 64-byte rows (64-byte swizzle) or 128-byte rows (wide
             // stages, 128-byte swizzle): a K = 64 MMA every 32 bytes
@@ -1136,7 +1148,12 @@ cudaError_t launch_bsmxfp4(int tn, bool a_fp4, bool mma_kind, int stage_k, const
                            const CUtensorMap& tmB, const GemmArgs& args, int num_sms,
                            cudaStream_t stream) {
   using namespace mx;
-  if (!a_fp4 && mma_kind) {
+  if (!a_fp4 && mma_kind && stage_k == 256) {
+    switch (tn) {
+      case 32: return launch<Cfg<32, FMT_MXFP8_MXFP4_MMA, 256>>(tmA, tmB, args, num_sms, stream);
+      case 64: return launch<Cfg<64, FMT_MXFP8_MXFP4_MMA, 256>>(tmA, tmB, args, num_sms, stream);
+    }
+  } else if (!a_fp4 && mma_kind) {
     switch (tn) {
       case 32: return launch<Cfg<32, FMT_MXFP8_MXFP4_MMA>>(tmA, tmB, args, num_sms, stream);
       case 64: return launch<Cfg<64, FMT_MXFP8_MXFP4_MMA>>(tmA, tmB, args, num_sms, stream);

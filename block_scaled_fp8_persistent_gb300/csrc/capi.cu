@@ -346,14 +346,14 @@ bsfp8_status mx_fmt_gemm(int a_fmt, int b_fmt, const void* A, const void* B,
   // chunks of whole stages, else 128 K (64-byte rows, 64-byte swizzle).
   // BSFP8_FP4_STAGE_K=128 keeps 128 K.
   const bool kind = a_fp4 && fp4_mma_kind();
-  const char* sk_env = std::getenv("BSFP8_FP4_STAGE_K");
-  const bool wide = kind && !(sk_env && std::strcmp(sk_env, "128") == 0) &&
-                    K % (nv ? 256 : 512) == 0 && aligned(a_scales, 16) &&
-                    (packed_b || aligned(b_scales, 16));
-  const uint32_t box = wide ? 128 : 64;  // bytes of packed e2m1 per row and stage
   // e4m3 tokens with e2m1 weights: kind::mxf8f6f4 on weight tiles loaded padded (the map
   // needs a 32-byte aligned base), else converted on chip
   const bool mixed_kind = !a_fp4 && fp4_mma_kind() && aligned(B, 32);
+  const char* sk_env = std::getenv("BSFP8_FP4_STAGE_K");
+  const bool wide = (kind || mixed_kind) && !(sk_env && std::strcmp(sk_env, "128") == 0) &&
+                    K % (nv ? 256 : 512) == 0 && aligned(a_scales, 16) &&
+                    (packed_b || aligned(b_scales, 16));
+  const uint32_t box = wide ? 128 : 64;  // bytes of packed e2m1 per row and stage
   CUtensorMap tmA, tmB;
   const bool ok_a = a_fp4 ? encode_u8_2d(&tmA, A, (uint64_t)K / 2, (uint64_t)M_total, box,
                                          (uint32_t)tn, kind)
