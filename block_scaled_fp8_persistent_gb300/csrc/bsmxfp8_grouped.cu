@@ -56,7 +56,8 @@
 //   warps 4-7   epilogue: warp w holds weight rows 32*(w%4).. of the tile, reads the tn
 //               token columns of the accumulator, rounds to bf16 and stores C[m, n] for the
 //               tile's token rows that belong to the expert.
-//   warps 8-11  (fp4 kinds) scale writers: warp 8 + q stores TMEM lane quarter q of each
+//   warps 8-11  (fp4 kinds, and MXFP8 tiles of up to 64 token rows) scale writers: warp
+//               8 + q stores TMEM lane quarter q of each
 //               stage's scale slot with tcgen05.st (one slot per ring stage), so the MMA
 //               thread issues only MMAs and the commit.  With chunkable scale rows (16
 //               aligned bytes = 4 stages of UE8M0 or 2 of UE4M3 codes) each writer fetches its
@@ -133,8 +134,10 @@ struct Cfg {
   static constexpr bool NV_F16 = NV && CONVERT;  // nvfp4 dequantized for the fp16 MMA
   // Scale feed: the MMA thread copies each stage's scale blocks into TMEM (tcgen05.cp), or
   // (SF_ST) four writer warps, one per TMEM lane quarter, store them (tcgen05.st) into a
-  // per-stage TMEM slot and the MMA thread issues only MMAs and the commit.
-  static constexpr bool SF_ST = NATIVE;
+  // per-stage TMEM slot and the MMA thread issues only MMAs and the commit.  128-row MXFP8
+  // tiles keep the copies: the writers' token staging (every writer holds all token rows)
+  // would cost a ring stage there.
+  static constexpr bool SF_ST = NATIVE || (FMT_ == FMT_MXFP8 && TN_ <= 64);
   static constexpr int THREADS = CONVERT ? 512 : SF_ST ? 384 : 256;
   static_assert(!CONVERT || TN <= 64, "fp4 tiles hold at most 64 token rows");
   // bytes per converted element: e4m3 for the MX formats, fp16 for nvfp4
@@ -144,6 +147,7 @@ struct Cfg {
   // 4-column TMEM scale groups per operand and stage: one per 128 K of UE8M0 codes, one per
   // K = 64 MMA of UE4M3 codes
   static constexpr int SF_GROUPS = !NATIVE ? 1 : NV ? SK / 64 : SK / 128;
+  static_assert(!SF_ST || NATIVE || SK == 128, "e4m3 stages hold 128 K");
   // (wide stages: the scale writers fetch the codes themselves; the weight blocks stay for
   // pre-packed MX weight scales, which the producer copies with the stage)
   static constexpr uint32_t SFW_STAGE =
