@@ -290,3 +290,59 @@ def test_high_scales(a_fmt, b_fmt, tn, path, path_env):
     p.a_scales[:] = rng.integers(246, 255, p.a_scales.shape).astype(np.uint8)
     p.b_scales[:] = rng.integers(20, 30, p.b_scales.shape).astype(np.uint8)
     _check_full(p)
+
+
+def _shifted(t, offset_bytes):
+    """A copy of device tensor t whose data starts offset_bytes into a fresh allocation."""
+    flat = torch.empty(t.numel() * t.element_size() + offset_bytes, dtype=torch.uint8,
+                       device=t.device)
+    view = flat[offset_bytes:offset_bytes + t.numel() * t.element_size()].view(t.dtype)
+    view.copy_(t.reshape(-1))
+    return view.view(t.shape)
+
+
+@pytest.mark.parametrize("a_fmt,b_fmt", PAIRS)
+def test_stage_k_128_forced(a_fmt, b_fmt, tn, monkeypatch):
+    # K % 512 == 0 and aligned scales pick 256-K stages; BSFP8_FP4_STAGE_K=128 keeps the
+    # 128-K form (64-byte rows, or one padded box per stage) on the same inputs
+    monkeypatch.setenv("BSFP8_FP4_STAGE_K", "128")
+    _check_full(gen.fmt_problem([9, 0, 33, 64, 1], 384, 1024, seed=57, a_fmt=a_fmt, b_fmt=b_fmt))
+
+
+def test_mixed_weights_only_16_byte_aligned():
+    # the padded e2m1 load needs a 32-byte aligned B: a B 16 bytes past such a boundary runs
+    # the converting form, with the same results
+    from gpu_util import DeviceProblem
+    import block_scaled_fp8_persistent_gb300 as bsfp8
+    p = gen.fmt_problem([12, 0, 40, 7], 384, 1024, seed=58, a_fmt="mxfp8", b_fmt="mxfp4")
+    d = DeviceProblem(p, c_rows_extra=2)
+    B16 = _shifted(d.B, 16)
+    assert B16.data_ptr() % 32 == 16
+    bsfp8.bsmx_grouped_gemm("mxfp8", "mxfp4", d.A, B16, d.sa, d.sb, d.off, d.C, p.M_total, p.N,
+                            p.K, p.E, p.num_experts)
+    got = d.c_bits()
+    assert bsfp8.bsfp8_get_device_error() == 0
+    ref, T = oracle.problem_reference(p)
+    bad, ratio, _ = parity_report(got, ref, T)
+    assert bad == 0, f"{bad} elements outside tolerance (max err/tol {ratio:.3g})"
+    assert np.all(d.guard_bits() == d.sentinel)
+
+
+@pytest.mark.parametrize("a_fmt,b_fmt", PAIRS)
+def test_scales_not_16_byte_aligned(a_fmt, b_fmt, tn):
+    # scale arrays 8 bytes past a 16-byte boundary: the scale writers cannot fetch 16-byte
+    # chunks, so the loader warps pack each stage and the writers relay (128-K stages)
+    from gpu_util import DeviceProblem
+    import block_scaled_fp8_persistent_gb300 as bsfp8
+    p = gen.fmt_problem([5, 30, 0, 12, 64], 256, 1024, seed=59, a_fmt=a_fmt, b_fmt=b_fmt)
+    d = DeviceProblem(p, c_rows_extra=2)
+    sa8, sb8 = _shifted(d.sa, 8), _shifted(d.sb, 8)
+    assert sa8.data_ptr() % 16 == 8 and sb8.data_ptr() % 16 == 8
+    bsfp8.bsmx_grouped_gemm(a_fmt, b_fmt, d.A, d.B, sa8, sb8, d.off, d.C, p.M_total, p.N, p.K,
+                            p.E, p.num_experts)
+    got = d.c_bits()
+    assert bsfp8.bsfp8_get_device_error() == 0
+    ref, T = oracle.problem_reference(p)
+    bad, ratio, _ = parity_report(got, ref, T)
+    assert bad == 0, f"{bad} elements outside tolerance (max err/tol {ratio:.3g})"
+    assert np.all(d.guard_bits() == d.sentinel)
