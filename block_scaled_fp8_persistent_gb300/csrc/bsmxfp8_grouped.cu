@@ -37,15 +37,18 @@
 // significant bits and lies inside the normal fp16 range), and the MMA thread issues
 // kind::f16 MMAs (K = 16) with no scale copies.
 //
-// Roles (8 warps; 12 with the fp4 kinds; 16 in the converting forms):
-//   warp 0      TMA producer: per K stage (128 K) the weight tile [128 x 128] and the token
-//               tile [tn x 128] (128-byte swizzle; fp4 operands packed [rows x 64 B],
-//               unswizzled) into a STAGES-deep ring.
-//   warp 1      TMEM owner + MMA thread: per stage tcgen05.cp of both scale blocks into
-//               TMEM, then 4 x tcgen05.mma kind::mxf8f6f4.block_scale (K = 32 each, the
-//               scale-factor id picks the byte of the 4-byte scale word; fp4 kinds: 2 x
-//               K = 64; converted nvfp4: 8 x kind::f16, K = 16), accumulating over all of
-//               K in a 2-deep TMEM accumulator ring.
+// Roles (8 warps; 12 with the scale writers; 16 in the converting forms):
+//   warp 0      TMA producer: per K stage (128 K, or 256 K for the fp4 kinds on chunkable
+//               scale rows) the weight tile [128 x K] and the token tile [tn x K] into a
+//               STAGES-deep ring: e4m3 (and padded e2m1) rows of 128 bytes per box, 128-byte
+//               swizzle; packed e2m1 rows of 64 bytes (64-byte swizzle) or 128 bytes for the
+//               fp4 kinds; packed rows of 64 bytes unswizzled for the converting forms.
+//   warp 1      TMEM owner + MMA thread: per stage (without scale writers) tcgen05.cp of
+//               both scale blocks into TMEM, then 4 x tcgen05.mma kind::mxf8f6f4.block_scale
+//               per 128 K (K = 32 each, the scale-factor id picks the byte of the 4-byte
+//               scale word; kind::mxf4 / kind::mxf4nvf4: 2 x K = 64; converted nvfp4: 8 x
+//               kind::f16, K = 16), accumulating over all of K in a 2-deep TMEM
+//               accumulator ring.
 //   warps 2, 3  scale loaders (token rows, weight rows): per stage each row's 4 UE8M0 codes
 //               (one 4-byte word, row-major source) are cp.async'ed into the packed
 //               512-byte block (row r at byte (r%32)*16 + (r/32)*4); a few stages in
@@ -154,9 +157,9 @@ struct Cfg {
       NV_F16 ? WROWS * (BK / 16) : (WIDE && NV) ? 0 : SF_GROUPS * SF_BLOCK;
   static constexpr uint32_t SFT_STAGE = WIDE ? 0 : SF_GROUPS * SF_BLOCK;
   static_assert(!NV_F16 || TN * (BK / 16) <= SFT_STAGE, "nvfp4 token scales of a stage");
-  // Load ring (STAGES deep): per stage the weight tile, the token tile and the two scale
-  // blocks as they arrive -- e4m3 tiles with the 128-byte swizzle, packed e2m1 tiles
-  // [rows x 64 B] without swizzle.  Byte offsets of a K block along a row: W_KX, T_KX.
+  // Load ring (STAGES deep): per stage the weight tile, the token tile and the scale
+  // blocks as they arrive (the row layouts of the producer's comment at the top).  Offsets
+  // of a stage along a row: W_KX, T_KX.
   static constexpr uint32_t W_STAGE = (B_FP4 && !MIXED) ? WROWS * SK / 2 : WROWS * SK;
   static constexpr uint32_t T_STAGE = A_FP4 ? TN * SK / 2 : TN * SK;
   // TMA x of a stage: bytes, or e2m1 elements for the padded weight map

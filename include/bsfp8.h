@@ -232,6 +232,10 @@ bsfp8_status bsmxfp8_grouped_gemm_prepacked(const void* A, const void* B, const 
  *                   weight tiles landing in shared memory padded (a byte per element) as
  *                   the tensor memory access unit expands them.  B must be 32-byte aligned
  *                   for that load; a B that is only 16-byte aligned runs the converting form.
+ * Stages of 256 K run where every scale row's codes come in aligned 16-byte chunks (K % 512
+ * == 0 for the mx formats, K % 256 for nvfp4, a_scales and b_scales 16-byte aligned), else
+ * stages of 128 K; environment variable BSFP8_FP4_STAGE_K=128 keeps 128 K.  Results do not
+ * depend on the stage size.
  * Converting forms (environment variable BSFP8_FP4_MMA=convert selects them for every pair;
  * kept for comparison):
  *   MX pairs        the packed tiles are re-encoded on chip into e4m3 for the MXFP8
