@@ -1,7 +1,8 @@
 """The bounds-checking debug build (build(debug=True), -DBSFP8_DEBUG=1): its kernels check
 every tile's coordinates against the problem and would record BSFP8_ERR_DEVICE_BOUNDS
 instead of going out of range.  On correct inputs it must report nothing and compute what
-the release build computes.  Runs in a child process that loads only the debug library."""
+the release build computes (every blockwise and MX tile form, and the fp4 MMA kinds with
+256-K and 128-K stages).  Runs in a child process that loads only the debug library."""
 import os
 import subprocess
 import sys
@@ -26,11 +27,18 @@ cases = [("blockwise", "cta1_96", [130, 0, 77, 1], 384, 640),
          ("blockwise", "split", [500, 3, 0, 447, 448, 900], 256, 256),
          ("mx", "swap", [3, 17, 0, 32, 1, 9], 256, 512),
          ("mx", "pair", [700, 0, 513], 256, 640),
-         ("mx", "split", [300, 7, 0, 45, 260, 129], 256, 512)]
+         ("mx", "split", [300, 7, 0, 45, 260, 129], 256, 512),
+         ("fp4", "mxfp8:mxfp4", [3, 17, 0, 32, 1, 9], 256, 1024),
+         ("fp4", "mxfp4:mxfp4", [40, 0, 7, 64], 384, 1024),
+         ("fp4", "nvfp4:nvfp4", [3, 17, 0, 32, 1, 9], 256, 768),
+         ("fp4", "mxfp4:mxfp4", [40, 0, 7], 256, 640)]
 for mode, form, counts, N, K in cases:
     if mode == "blockwise":
         os.environ["BSFP8_BLOCKWISE_TILE"] = form
         p = gen.blockwise_problem(counts, N, K, seed=77)
+    elif mode == "fp4":
+        a_fmt, b_fmt = form.split(":")
+        p = gen.fmt_problem(counts, N, K, seed=79, a_fmt=a_fmt, b_fmt=b_fmt)
     else:
         os.environ["BSFP8_MX_KERNEL"] = form
         p = gen.mx_problem(counts, N, K, seed=78)
