@@ -142,7 +142,7 @@ struct Cfg {
   // would cost a ring stage there.
   static constexpr bool SF_ST = NATIVE || (FMT_ == FMT_MXFP8 && TN_ <= 64);
   static constexpr int THREADS = CONVERT ? 512 : SF_ST ? 384 : 256;
-  static_assert(!CONVERT || TN <= 64, "fp4 tiles hold at most 64 token rows");
+  static_assert(!CONVERT || TN <= 64, "converting fp4 tiles hold at most 64 token rows");
   // bytes per converted element: e4m3 for the MX formats, fp16 for nvfp4
   static constexpr uint32_t ESZ = NV ? 2 : 1;
   // scale bytes per stage: packed UE8M0 blocks (MX), row-major e4m3 codes per 16 K (nvfp4 for
@@ -183,7 +183,9 @@ struct Cfg {
   // 8 stages ahead for e4m3 tiles; 1536 K (12 stages of 128 K, 6 of 256 K) for the fp4 kinds
   static constexpr int CPS = NV ? SK / 16 : SK / 32;  // scale codes per row and stage
   static constexpr int GS = 16 / CPS;                 // stages per 16-byte chunk
-  static constexpr int STG_AHEAD = NATIVE ? (1536 / SK) / GS : STG_SLOTS - 1;
+  // (128-row token tiles: at most 3 groups, each writer keeping 2 KB of token chunks per slot)
+  static constexpr int STG_AHEAD_K = NATIVE ? (1536 / SK) / GS : STG_SLOTS - 1;
+  static constexpr int STG_AHEAD = (TN >= 128 && STG_AHEAD_K > 3) ? 3 : STG_AHEAD_K;
   static constexpr int STG_N = STG_AHEAD + 1;
   // staging per slot: 128 weight rows and the token rows (x4 with the scale writers, each of
   // which keeps its own copy of the token rows)
@@ -193,8 +195,11 @@ struct Cfg {
   // the barriers and the alignment pad, at most 16 (128 KB of packed weights in flight)
   static constexpr int FIT =
       (int)((SMEM_LIMIT - CONV_BYTES - STG_BYTES - 2048) / PER_STAGE);
+  // the scale writers' per-stage TMEM slots share the 512 columns with the accumulators
+  static constexpr int TMEM_FIT = SF_ST ? (int)((512 - 2 * TN) / (8 * SF_GROUPS)) : 16;
+  static constexpr int FIT_ALL = FIT < TMEM_FIT ? FIT : TMEM_FIT;
   static constexpr int STAGES = !B_FP4 ? ((TN <= 32) ? 10 : (TN <= 64) ? 8 : 6)
-                                       : (FIT < 16 ? FIT : 16);
+                                       : (FIT_ALL < 16 ? FIT_ALL : 16);
   static constexpr int LOOKAHEAD = SCALE_LOOKAHEAD < STAGES - 1 ? SCALE_LOOKAHEAD : STAGES - 1;
   // the epilogue's factor: 2^6 per fp4 operand undoes the re-encoding's 2^-6 (exact in fp32)
   static constexpr float POST = (NV || NATIVE) ? 1.0f : A_FP4 ? 4096.0f : (B_FP4 ? 64.0f : 1.0f);
@@ -224,6 +229,7 @@ struct Cfg {
       SF_ST ? ACC_COLS + STAGES * SF_STAGE_COLS : ACC_COLS + 4 * SF_COLS;
   static constexpr uint32_t TMEM_COLS = (TMEM_USED <= 64) ? 64 : (TMEM_USED <= 128) ? 128
                                         : (TMEM_USED <= 256) ? 256 : 512;
+  static_assert(TMEM_USED <= 512, "accumulators and scale slots fit the 512 TMEM columns");
   static_assert(LOOKAHEAD >= 1 && LOOKAHEAD < STAGES, "scale look-ahead must leave a free stage");
   static_assert(STAGES > CSTAGES, "the load ring is deeper than the converted ring");
   // 128-byte-swizzled tiles start on 1024-byte boundaries
@@ -989,15 +995,18 @@ bsmxfp8_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                            : *reinterpret_cast<const uint32_t*>(pWs + slot * STG_SLOT +
                                                                 CPS * j + 4 * b);
               tmem_st_32x32b_x1(tcol + 4 * b + q, w);
-              const uint32_t x0 = *reinterpret_cast<const uint32_t*>(
-                  pTs + slot * C::STGT_SLOT + CPS * j + 4 * b);
-              if constexpr (C::TN >= 64) {
-                const uint32_t x1 = *reinterpret_cast<const uint32_t*>(
-                    pTs + slot * C::STGT_SLOT + 512 + CPS * j + 4 * b);
-                tmem_st_32x32b_x2(tcol + C::SF_COLS + 4 * b, x0, x1);
-              } else {
-                tmem_st_32x32b_x1(tcol + C::SF_COLS + 4 * b, x0);
-              }
+              // token rows 32 jt + lane at column jt of the group
+              uint32_t x[C::TN / 32];
+#pragma unroll
+              for (int jt = 0; jt < C::TN / 32; ++jt)
+                x[jt] = *reinterpret_cast<const uint32_t*>(pTs + slot * C::STGT_SLOT + jt * 512 +
+                                                           CPS * j + 4 * b);
+              if constexpr (C::TN >= 128)
+                tmem_st_32x32b_x4(tcol + C::SF_COLS + 4 * b, x[0], x[1], x[2], x[3]);
+              else if constexpr (C::TN >= 64)
+                tmem_st_32x32b_x2(tcol + C::SF_COLS + 4 * b, x[0], x[1]);
+              else
+                tmem_st_32x32b_x1(tcol + C::SF_COLS + 4 * b, x[0]);
             }
             stage_done();
           }
@@ -1149,7 +1158,7 @@ cudaError_t launch_bsmxfp8(int tn, const CUtensorMap& tmA, const CUtensorMap& tm
 }
 
 // fp4 operands: a_fp4 = tokens packed e2m1 (else e4m3); the weights are packed e2m1; tn is
-// 32 or 64.  mma_kind: kind::mxf4 on the packed tiles, stage_k K per stage (a_fp4), or
+// 32 or 64 (and 128 with mma_kind).  mma_kind: kind::mxf4 on the packed tiles, stage_k K per stage (a_fp4), or
 // kind::mxf8f6f4 on e2m1 weight tiles loaded padded (e4m3 tokens).
 cudaError_t launch_bsmxfp4(int tn, bool a_fp4, bool mma_kind, int stage_k, const CUtensorMap& tmA,
                            const CUtensorMap& tmB, const GemmArgs& args, int num_sms,
@@ -1164,16 +1173,19 @@ cudaError_t launch_bsmxfp4(int tn, bool a_fp4, bool mma_kind, int stage_k, const
     switch (tn) {
       case 32: return launch<Cfg<32, FMT_MXFP8_MXFP4_MMA>>(tmA, tmB, args, num_sms, stream);
       case 64: return launch<Cfg<64, FMT_MXFP8_MXFP4_MMA>>(tmA, tmB, args, num_sms, stream);
+      case 128: return launch<Cfg<128, FMT_MXFP8_MXFP4_MMA>>(tmA, tmB, args, num_sms, stream);
     }
   } else if (a_fp4 && mma_kind && stage_k == 256) {
     switch (tn) {
       case 32: return launch<Cfg<32, FMT_MXFP4_MMA, 256>>(tmA, tmB, args, num_sms, stream);
       case 64: return launch<Cfg<64, FMT_MXFP4_MMA, 256>>(tmA, tmB, args, num_sms, stream);
+      case 128: return launch<Cfg<128, FMT_MXFP4_MMA, 256>>(tmA, tmB, args, num_sms, stream);
     }
   } else if (a_fp4 && mma_kind) {
     switch (tn) {
       case 32: return launch<Cfg<32, FMT_MXFP4_MMA>>(tmA, tmB, args, num_sms, stream);
       case 64: return launch<Cfg<64, FMT_MXFP4_MMA>>(tmA, tmB, args, num_sms, stream);
+      case 128: return launch<Cfg<128, FMT_MXFP4_MMA>>(tmA, tmB, args, num_sms, stream);
     }
   } else if (a_fp4) {
     switch (tn) {
@@ -1202,6 +1214,7 @@ cudaError_t launch_bsnvfp4(int tn, bool mma_kind, int stage_k, const CUtensorMap
     switch (tn) {
       case 32: return launch<Cfg<32, FMT_NVFP4_MMA, 256>>(tmA, tmB, args, num_sms, stream);
       case 64: return launch<Cfg<64, FMT_NVFP4_MMA, 256>>(tmA, tmB, args, num_sms, stream);
+      case 128: return launch<Cfg<128, FMT_NVFP4_MMA, 256>>(tmA, tmB, args, num_sms, stream);
     }
     return cudaErrorInvalidValue;
   }
@@ -1209,6 +1222,7 @@ cudaError_t launch_bsnvfp4(int tn, bool mma_kind, int stage_k, const CUtensorMap
     switch (tn) {
       case 32: return launch<Cfg<32, FMT_NVFP4_MMA>>(tmA, tmB, args, num_sms, stream);
       case 64: return launch<Cfg<64, FMT_NVFP4_MMA>>(tmA, tmB, args, num_sms, stream);
+      case 128: return launch<Cfg<128, FMT_NVFP4_MMA>>(tmA, tmB, args, num_sms, stream);
     }
     return cudaErrorInvalidValue;
   }

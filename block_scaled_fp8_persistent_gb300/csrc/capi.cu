@@ -340,7 +340,6 @@ bsfp8_status mx_fmt_gemm(int a_fmt, int b_fmt, const void* A, const void* B,
   if (M_total == 0) return BSFP8_OK;
   GemmArgs args{offsets, a_scales, b_scales, C, M_total, N, K, G, dev->err_word, ids, E,
                 packed_b ? 1 : 0};
-  const int tn = std::min(choose_mx_token_tile(M_total, G), 64);  // fp4 tiles: tn <= 64
   // Both operands fp4: the MMA kinds read the packed tiles as loaded, 256 K per stage
   // (128-byte rows, 128-byte swizzle) when every scale row's codes come in aligned 16-byte
   // chunks of whole stages, else 128 K (64-byte rows, 64-byte swizzle).
@@ -349,10 +348,14 @@ bsfp8_status mx_fmt_gemm(int a_fmt, int b_fmt, const void* A, const void* B,
   // e4m3 tokens with e2m1 weights: kind::mxf8f6f4 on weight tiles loaded padded (the map
   // needs a 32-byte aligned base), else converted on chip
   const bool mixed_kind = !a_fp4 && fp4_mma_kind() && aligned(B, 32);
+  // token rows per tile: the planner's choice; the converting forms hold at most 64
+  const int tn = std::min(choose_mx_token_tile(M_total, G), (kind || mixed_kind) ? 128 : 64);
+  // (mxfp8 x mxfp4 with 128 token rows keeps 128-K stages: a 256-K stage of e4m3 tokens and
+  // padded weights takes 64 KB, two stages only)
   const char* sk_env = std::getenv("BSFP8_FP4_STAGE_K");
   const bool wide = (kind || mixed_kind) && !(sk_env && std::strcmp(sk_env, "128") == 0) &&
-                    K % (nv ? 256 : 512) == 0 && aligned(a_scales, 16) &&
-                    (packed_b || aligned(b_scales, 16));
+                    !(mixed_kind && tn >= 128) && K % (nv ? 256 : 512) == 0 &&
+                    aligned(a_scales, 16) && (packed_b || aligned(b_scales, 16));
   const uint32_t box = wide ? 128 : 64;  // bytes of packed e2m1 per row and stage
   CUtensorMap tmA, tmB;
   const bool ok_a = a_fp4 ? encode_u8_2d(&tmA, A, (uint64_t)K / 2, (uint64_t)M_total, box,

@@ -32,7 +32,8 @@ def path_env(monkeypatch):
 
 @pytest.fixture(params=["32", "64", "128"])
 def tn(request, monkeypatch):
-    """Token rows per swap-AB tile (fp4 tiles hold at most 64: a request for 128 runs 64)."""
+    """Token rows per swap-AB tile (the converting forms hold at most 64: a request for 128
+    runs 64 there)."""
     monkeypatch.setenv("BSFP8_MX_TN", request.param)
     return int(request.param)
 
