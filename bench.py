@@ -476,6 +476,57 @@ def time_fp4_formats(args, flush, stream, peaks, ref_ms):
     return out
 
 
+FP4_PER_BF16 = 4.0  # nominal dense fp4 / bf16 tensor throughput ratio (9 / 2.25 PFLOP/s)
+
+
+def time_fp4_dense(args, flush, stream, peaks):
+    """The fp4 format pairs on a dense prefill-sized problem (one expert, M = N = K = 8192, the
+    block-scaled example's benchmark shape), through bsmx_grouped_gemm: compute-bound, so
+    against the tensor peak of the MMA kind (fp4 kinds twice the fp8 rate; mxfp8 x mxfp4 runs
+    kind::mxf8f6f4 at the fp8 rate)."""
+    import numpy as np
+    import torch
+    import gen
+    import block_scaled_fp8_persistent_gb300 as bsfp8
+    dev = flush.device
+    M = N = K = 8192
+    out = {"workload": "dense fp4, one expert, M=N=K=8192 (prefill-sized; 128-token swap-AB "
+                       "tiles)", "pairs": {}}
+    for af, bf in FP4_PAIRS:
+        p = gen.fmt_problem([M], N, K, seed=5, a_fmt=af, b_fmt=bf)
+        d = {k: torch.from_numpy(np.ascontiguousarray(getattr(p, k))).to(dev)
+             for k in ("A", "B", "a_scales", "b_scales", "offsets")}
+        C = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+
+        def step():
+            bsfp8.bsmx_grouped_gemm(af, bf, d["A"], d["B"], d["a_scales"], d["b_scales"],
+                                    d["offsets"], C, M, N, K, 1, 1, stream=stream)
+
+        for _ in range(args.warmup):
+            step()
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        torch.cuda.synchronize()
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+        ms = statistics.mean(s.elapsed_time(e) for s, e in zip(starts, ends))
+        tflops = p.flops() / (ms * 1e-3) / 1e12
+        ratio = FP8_PER_BF16 if af == "mxfp8" else FP4_PER_BF16
+        peak = peaks["bf16_tflops"] * ratio
+        out["pairs"][f"{af} x {bf}"] = {
+            "ms_per_step": ms, "TFLOP/s": tflops, "peak_tflops": peak,
+            "peak_source": f"measured bf16 burst x {ratio} (nominal ratio of the MMA kind)",
+            "frac": tflops / peak,
+            "device_error": bsfp8.bsfp8_get_device_error(stream), "gpu_launches": args.steps}
+        del d, C
+        torch.cuda.empty_cache()
+    return out
+
+
 def time_expert_ids(p, d, C, args, flush, stream):
     """The same workload routed through the expert indirection (group g multiplies expert
     perm[g] of the same B, perm a seeded permutation) with the same protocol."""
@@ -717,6 +768,8 @@ def run_ours(args):
         fp4 = guarded(time_fp4_formats, args, flush, stream, peaks, ref_ms)
     mx_skewed = None if args.no_secondary else guarded(time_mx_skewed, args, flush, stream,
                                                        peaks, peak_src)
+    fp4_dense = None if args.no_secondary else guarded(time_fp4_dense, args, flush, stream,
+                                                       peaks)
 
     clocks = sampler.stop()  # sampled from before the warm-up through the timings above
 
@@ -762,6 +815,8 @@ def run_ours(args):
         line["fp4_formats"] = fp4
     if mx_skewed is not None:
         line["mx_skewed_routing"] = mx_skewed
+    if fp4_dense is not None:
+        line["fp4_dense"] = fp4_dense
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()

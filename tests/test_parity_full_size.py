@@ -108,3 +108,12 @@ def test_fp4_decode_shape_every_element(a_fmt, b_fmt, path, monkeypatch):
         gen.config_counts(4), 4096, 7168, seed=4, a_fmt=a_fmt, b_fmt=b_fmt,
         a_recipe="quantized"))
     _run_and_compare(p, ref, T)
+
+
+@pytest.mark.parametrize("a_fmt,b_fmt", FP4_PAIRS)
+def test_fp4_dense_prefill_every_element(a_fmt, b_fmt):
+    # a dense prefill-sized fp4 problem (one expert, 4096 x 4096 x 7168): 128-token tiles of
+    # the fp4 kinds, 256-K stages for the fp4 x fp4 pairs
+    p, ref, T = _reference(("fp4 dense", a_fmt, b_fmt), lambda: gen.fmt_problem(
+        [4096], 4096, 7168, seed=6, a_fmt=a_fmt, b_fmt=b_fmt))
+    _run_and_compare(p, ref, T)
