@@ -490,8 +490,8 @@ def time_fp4_dense(args, flush, stream, peaks):
     import block_scaled_fp8_persistent_gb300 as bsfp8
     dev = flush.device
     M = N = K = 8192
-    out = {"workload": "dense fp4, one expert, M=N=K=8192 (prefill-sized; 128-token swap-AB "
-                       "tiles)", "pairs": {}}
+    out = {"workload": "dense fp4, one expert, M=N=K=8192 (prefill-sized; the plan's CTA-pair "
+                       "256x256 tiles on the fp4 kinds)", "pairs": {}}
     for af, bf in FP4_PAIRS:
         p = gen.fmt_problem([M], N, K, seed=5, a_fmt=af, b_fmt=bf)
         d = {k: torch.from_numpy(np.ascontiguousarray(getattr(p, k))).to(dev)

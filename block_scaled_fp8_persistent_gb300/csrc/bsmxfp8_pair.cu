@@ -49,45 +49,79 @@ constexpr int NUM_THREADS = 384;
 constexpr int EPI_WARP0 = 4;
 constexpr int NUM_EPI_WARPS = 8;
 constexpr int SF_BLOCK = 512;  // packed scale block: 128 rows x 4 codes
-// K blocks of 128 per ring stage (k_group_size of the per-K-stage context, MAX
-// EpilogueWarpContext page, per_k_stage): one full/empty round trip and one commit per KG
-// K blocks instead of per K block
-constexpr int KG = 2;
-constexpr int STAGES = 3;  // ring stages of KG K blocks (64 KB of operands each)
-// Row-major scale copies in flight before the oldest is announced.  A stage's copies start
-// once the MMA has freed it; announcing stage s only after the copies of s + L are issued
-// waits for the MMA to free s + L, so L <= STAGES - 2 keeps that off the MMA's path.
-constexpr int SCALE_LOOKAHEAD = 1;
-static_assert(SCALE_LOOKAHEAD <= STAGES - 2, "scale announce would wait on the MMA");
-constexpr TmemPlan PLAN = tmem_overlap_plan(BK, EPI_N, 32, true, BN, 512);
-static_assert(PLAN.right_offset == 244 && PLAN.a_scale_offset == 500 &&
-              PLAN.b_scale_offset == 504 && PLAN.early_release_subtile == 0,
+// Operand formats (A = tokens, B = weights): MXFP8 e4m3 x e4m3; MIXED e4m3 x e2m1 (the weights
+// loaded padded, a byte per element, for kind::mxf8f6f4); MXF4 e2m1 x e2m1 (kind::mxf4, UE8M0
+// per 32); NVF4 e2m1 x e2m1 with UE4M3 scales per 16 (kind::mxf4nvf4, scale_vec::4X).
+enum PairFormat : int { PF_MXFP8 = 0, PF_MIXED = 1, PF_MXF4 = 2, PF_NVF4 = 3 };
+
+template <int FMT_>
+struct PCfg {
+  static constexpr int FMT = FMT_;
+  static constexpr bool FP4 = FMT_ >= PF_MXF4;  // both operands packed e2m1
+  // K per K block: a 128-byte row of the operand tile (128 e4m3 or padded e2m1, 256 packed
+  // e2m1), four MMAs (K = 32, or K = 64 for the fp4 kinds)
+  static constexpr int KBLK = FP4 ? 256 : 128;
+  static constexpr int VEC = FMT_ == PF_NVF4 ? 16 : 32;  // K per scale code
+  static constexpr int CPK = KBLK / VEC;  // scale codes per row and K block: 4, 8 or 16
+  static constexpr int G = CPK / 4;       // 4-column TMEM scale groups per 128 rows
+  // K blocks per ring stage (the k_group_size grouping of K iterations per pipeline stage,
+  // MAX EpilogueWarpContext page, per_k_stage): one full/empty round trip and one commit
+  // per KG K blocks
+  static constexpr int KG = FP4 ? 1 : 2;
+  static constexpr int STAGES = FP4 ? 5 : 3;  // ring stages (64 or 32 KB of operands each)
+  static constexpr TmemPlan PLAN = tmem_overlap_plan(KBLK, EPI_N, VEC, true, BN, 512);
+  static constexpr uint32_t A_SUB = 128 * 128;  // one K block of this CTA's token rows
+  static constexpr uint32_t B_SUB = 128 * 128;  // one K block of this CTA's weight rows
+  static constexpr uint32_t A_STAGE = KG * A_SUB;
+  static constexpr uint32_t B_STAGE = KG * B_SUB;
+  static constexpr uint32_t SMEM_A = 0;
+  static constexpr uint32_t SMEM_B = SMEM_A + STAGES * A_STAGE;
+  static constexpr uint32_t SFA_STAGE = KG * G * SF_BLOCK;      // G blocks per K block
+  static constexpr uint32_t SFB_STAGE = KG * 2 * G * SF_BLOCK;  // 2 G blocks per K block
+  static constexpr uint32_t SMEM_SFA = SMEM_B + STAGES * B_STAGE;
+  static constexpr uint32_t SMEM_SFB = SMEM_SFA + STAGES * SFA_STAGE;
+  // Scale staging for the grouped loader: per group of GROUP K blocks, one 16-byte chunk
+  // (16 / CPK K blocks of codes) of each of this CTA's 128 token rows and the tile's 256
+  // weight rows.
+  static constexpr int KPC = 16 / CPK;  // K blocks per 16-byte chunk
+  static constexpr int GROUP = KPC > KG ? KPC : KG;
+  static_assert(GROUP == KPC && GROUP % KG == 0, "a chunk covers whole ring stages");
+  static constexpr uint32_t STG_A = 128 * 16;
+  static constexpr uint32_t STG_SLOT = STG_A + 256 * 16;
+  // groups fetched ahead: 8 K blocks of 128 (4 of 256 for nvfp4's one-block groups)
+  static constexpr int STG_AHEAD = GROUP == 1 ? 4 : 2;
+  static constexpr int STG_SLOTS = STG_AHEAD + 1;
+  static constexpr uint32_t SMEM_STG = SMEM_SFB + STAGES * SFB_STAGE;
+  static constexpr uint32_t SMEM_CTL = SMEM_STG + STG_SLOTS * STG_SLOT;
+  // both CTAs' bytes of one K block (the padded weight load counts the packed bytes it reads)
+  static constexpr uint32_t SUB_TX = 2 * (A_SUB + (FMT_ == PF_MIXED ? B_SUB / 2 : B_SUB));
+  // Row-major scale copies in flight before the oldest is announced.  A stage's copies start
+  // once the MMA has freed it; announcing stage s only after the copies of s + L are issued
+  // waits for the MMA to free s + L, so L <= STAGES - 2 keeps that off the MMA's path.
+  static constexpr int SCALE_LOOKAHEAD = 1;
+  static_assert(SCALE_LOOKAHEAD <= STAGES - 2, "scale announce would wait on the MMA");
+  // scale-factor TMEM addresses on 4-column boundaries
+  static_assert(PLAN.a_scale_offset % 4 == 0 && PLAN.b_scale_offset % 4 == 0 &&
+                    PLAN.b_scale_offset + 8 * G <= 512 && PLAN.a_scale_cols == 4 * G &&
+                    PLAN.b_scale_cols == 8 * G,
+                "scale columns of the plan");
+};
+// the plan of the MXFP8 form, pinned to the example's values for BLOCK_K 128, VEC 32
+static_assert(PCfg<PF_MXFP8>::PLAN.right_offset == 244 &&
+              PCfg<PF_MXFP8>::PLAN.a_scale_offset == 500 &&
+              PCfg<PF_MXFP8>::PLAN.b_scale_offset == 504 &&
+              PCfg<PF_MXFP8>::PLAN.early_release_subtile == 0,
               "plan for BLOCK_K 128, VEC 32");
+// nvfp4: the example's first worked plan (BLOCK_K 256, VEC 16)
+static_assert(PCfg<PF_NVF4>::PLAN.right_offset == 208 && PCfg<PF_NVF4>::PLAN.a_scale_offset == 464 &&
+              PCfg<PF_NVF4>::PLAN.b_scale_offset == 480 &&
+              PCfg<PF_NVF4>::PLAN.early_release_subtile == 1,
+              "plan for BLOCK_K 256, VEC 16");
 
-constexpr uint32_t A_SUB = 128 * BK;   // one K block of this CTA's token rows
-constexpr uint32_t B_SUB = 128 * BK;   // one K block of this CTA's weight rows
-constexpr uint32_t A_STAGE = KG * A_SUB;
-constexpr uint32_t B_STAGE = KG * B_SUB;
-constexpr uint32_t SMEM_A = 0;
-constexpr uint32_t SMEM_B = SMEM_A + STAGES * A_STAGE;
-constexpr uint32_t SFA_STAGE = KG * SF_BLOCK;                        // 1 block per K block
-constexpr uint32_t SFB_STAGE = KG * 2 * SF_BLOCK;                    // 2 blocks per K block
-constexpr uint32_t SMEM_SFA = SMEM_B + STAGES * B_STAGE;
-constexpr uint32_t SMEM_SFB = SMEM_SFA + STAGES * SFA_STAGE;
-// Scale staging for the grouped loader: per group of 4 stages, 16 bytes (4 stages x 4
-// codes) of each of this CTA's 128 token rows and the tile's 256 weight rows.
-constexpr int GROUP = 4;
-constexpr uint32_t STG_A = 128 * 16;
-constexpr uint32_t STG_SLOT = STG_A + 256 * 16;
-constexpr int STG_SLOTS = 3;
-constexpr uint32_t SMEM_STG = SMEM_SFB + STAGES * SFB_STAGE;
-constexpr uint32_t SMEM_CTL = SMEM_STG + STG_SLOTS * STG_SLOT;
-constexpr uint32_t SUB_TX = 2 * (A_SUB + B_SUB);  // both CTAs' bytes of one K block
-static_assert(GROUP % KG == 0, "a grouped scale fetch covers whole ring stages");
-
+template <class C>
 struct Ctl {
-  uint64_t full[STAGES];
-  uint64_t empty[STAGES];
+  uint64_t full[C::STAGES];
+  uint64_t empty[C::STAGES];
   uint64_t acc_full[2];
   uint64_t acc_empty[2];
   uint64_t overlap;
@@ -98,8 +132,10 @@ struct Ctl {
   int pad;
   long long total_tiles;
 };
-constexpr uint32_t SMEM_BYTES = SMEM_CTL + sizeof(Ctl) + 1024;
-static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+template <class C>
+constexpr uint32_t smem_bytes() {
+  return C::SMEM_CTL + sizeof(Ctl<C>) + 1024;
+}
 
 __device__ __forceinline__ void record_error(int* err, int code, volatile int* abort) {
   atomicCAS(err, 0, code);
@@ -112,23 +148,42 @@ __device__ __forceinline__ uint64_t sf_block_desc(uint32_t saddr) {
 
 // PACKED_B: weight scales pre-packed in [E][N/128][K/128] blocks of 512 bytes (else
 // row-major [E, N, K/32]); an instantiation each, so the row-major loader carries no branch.
-template <bool PACKED_B>
+template <int FMT, bool PACKED_B>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 bsmxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const GemmArgs args) {
+  using C = PCfg<FMT>;
+  constexpr int STAGES = C::STAGES, KG = C::KG, GROUP = C::GROUP, STG_SLOTS = C::STG_SLOTS;
+  constexpr int SCALE_LOOKAHEAD = C::SCALE_LOOKAHEAD;
+  constexpr uint32_t A_SUB = C::A_SUB, B_SUB = C::B_SUB, A_STAGE = C::A_STAGE,
+                     B_STAGE = C::B_STAGE, SFA_STAGE = C::SFA_STAGE, SFB_STAGE = C::SFB_STAGE;
+  constexpr uint32_t SMEM_A = C::SMEM_A, SMEM_B = C::SMEM_B, SMEM_SFA = C::SMEM_SFA,
+                     SMEM_SFB = C::SMEM_SFB, SMEM_STG = C::SMEM_STG, SMEM_CTL = C::SMEM_CTL;
+  constexpr uint32_t STG_A = C::STG_A, STG_SLOT = C::STG_SLOT, SUB_TX = C::SUB_TX;
+  constexpr TmemPlan PLAN = C::PLAN;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  Ctl* ctl = reinterpret_cast<Ctl*>(smem + SMEM_CTL);
+  Ctl<C>* ctl = reinterpret_cast<Ctl<C>*>(smem + SMEM_CTL);
   volatile int* abort = &ctl->abort;
   const uint32_t warp = threadIdx.x >> 5;
   const uint32_t lane = threadIdx.x & 31;
-  const int KB = args.K / BK;
-  const int scale_row = args.K / 32;
+  const int KB = args.K / C::KBLK;      // K blocks (a 128-byte operand row each)
+  const int scale_row = args.K / C::VEC;  // scale codes per row
   const uint32_t rank = cluster_ctarank();
   const int64_t tile0 = blockIdx.x / 2;
   const int64_t tile_stride = gridDim.x / 2;
 
+  // The fp4 forms take their scales through the grouped loader only (the host launches them
+  // on chunkable rows: KB % GROUP == 0, scale rows of whole 16-byte chunks, aligned arrays).
+  if constexpr (C::FP4) {
+    if (KB % GROUP != 0 || scale_row % 16 != 0 ||
+        reinterpret_cast<uintptr_t>(args.a_scales) % 16 != 0 ||
+        reinterpret_cast<uintptr_t>(args.b_scales) % 16 != 0 || PACKED_B) {
+      if (threadIdx.x == 0) atomicCAS(args.err, 0, DEV_TIMEOUT);
+      return;
+    }
+  }
   if (warp == 0) {
     int status;
     int64_t row_tiles;
@@ -256,18 +311,38 @@ bsmxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
           for (int u = 0; u < nk; ++u) {
             // this K block's scales into the TMEM scale columns (after the previous K block's
             // MMAs, which read them, in this thread's issue order)
-            const uint32_t sfa_s = sSFA + stage * SFA_STAGE + u * SF_BLOCK;
-            const uint32_t sfb_s = sSFB + stage * SFB_STAGE + u * 2 * SF_BLOCK;
-            tmem_cp_32x128b_warpx4<2>(sfa_t, sf_block_desc(sfa_s));
-            tmem_cp_32x128b_warpx4<2>(sfb_t, sf_block_desc(sfb_s));
-            tmem_cp_32x128b_warpx4<2>(sfb_t + 4, sf_block_desc(sfb_s + SF_BLOCK));
+            // scale group g: this CTA's token rows into 4 columns at sfa_t + 4g, the tile's
+            // 256 weight rows into 8 columns at sfb_t + 8g (two 128-row blocks)
+            const uint32_t sfa_s = sSFA + stage * SFA_STAGE + u * C::G * SF_BLOCK;
+            const uint32_t sfb_s = sSFB + stage * SFB_STAGE + u * 2 * C::G * SF_BLOCK;
+#pragma unroll
+            for (int g = 0; g < C::G; ++g) {
+              tmem_cp_32x128b_warpx4<2>(sfa_t + 4 * g, sf_block_desc(sfa_s + g * SF_BLOCK));
+              tmem_cp_32x128b_warpx4<2>(sfb_t + 8 * g, sf_block_desc(sfb_s + 2 * g * SF_BLOCK));
+              tmem_cp_32x128b_warpx4<2>(sfb_t + 8 * g + 4,
+                                        sf_block_desc(sfb_s + (2 * g + 1) * SF_BLOCK));
+            }
             const uint64_t adesc = kmajor_sw128_desc(sA + stage * A_STAGE + u * A_SUB);
             const uint64_t bdesc = kmajor_sw128_desc(sB + stage * B_STAGE + u * B_SUB);
+            // four MMAs per 128-byte row: K = 32 (e4m3, padded e2m1) or 64 (packed e2m1)
 #pragma unroll
-            for (int k = 0; k < BK / 32; ++k)
-              umma_mxf8f6f4<2>(d_tmem, adesc + (uint64_t)(k * 2), bdesc + (uint64_t)(k * 2),
-                               idesc_mxf8f6f4_e4m3(BM, BN, k, k), sfa_t, sfb_t,
-                               (kb0 + u > 0 || k > 0) ? 1u : 0u);
+            for (int k = 0; k < 4; ++k) {
+              const uint32_t acc = (kb0 + u > 0 || k > 0) ? 1u : 0u;
+              const uint64_t ad = adesc + (uint64_t)(k * 2), bd = bdesc + (uint64_t)(k * 2);
+              if constexpr (FMT == PF_MXFP8)
+                umma_mxf8f6f4<2>(d_tmem, ad, bd, idesc_mxf8f6f4_e4m3(BM, BN, k, k), sfa_t, sfb_t,
+                                 acc);
+              else if constexpr (FMT == PF_MIXED)
+                umma_mxf8f6f4<2>(d_tmem, ad, bd,
+                                 idesc_mxf8f6f4(BM, BN, MXF_E4M3, MXF_E2M1, k, k), sfa_t, sfb_t,
+                                 acc);
+              else if constexpr (FMT == PF_MXF4)  // group k / 2, byte pair 2 (k % 2)
+                umma_mxf4<2>(d_tmem, ad, bd, idesc_mxf4_e2m1(BM, BN, 2 * (k & 1), 2 * (k & 1)),
+                             sfa_t + 4 * (k >> 1), sfb_t + 8 * (k >> 1), acc);
+              else  // UE4M3 per 16: group k
+                umma_mxf4nvf4_4x<2>(d_tmem, ad, bd, idesc_nvf4_e2m1_ue4m3(BM, BN),
+                                    sfa_t + 4 * k, sfb_t + 8 * k, acc);
+            }
           }
           umma_commit_pair(empty_bar(stage), 0x3);
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
@@ -296,15 +371,15 @@ bsmxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     const int nblk = args.N / 128;
     GroupedScheduler<BM, BN, TILE_BAND> sched;
     uint32_t stage = 0, phase = 0;
-    // Grouped path: when a row's codes for 4 consecutive stages form one aligned 16-byte
-    // chunk (K % 512 == 0, 16-byte aligned scale arrays), fetch a 4-stage group per row with
-    // one 16-byte copy, two groups ahead, and transpose each stage's words into its packed
-    // blocks in shared memory.
-    const bool grouped = (args.K % (GROUP * BK) == 0) &&
+    // Grouped path: when a row's codes for GROUP consecutive K blocks form one aligned
+    // 16-byte chunk (scale rows of whole chunks, 16-byte aligned scale arrays), fetch a group
+    // per row with one 16-byte copy, STG_AHEAD groups ahead, and transpose each K block's
+    // words into its packed blocks (one per scale group) in shared memory.
+    const bool grouped = (KB % GROUP == 0) && (scale_row % 16 == 0) &&
                          (reinterpret_cast<uintptr_t>(a_sc) % 16 == 0) &&
                          (reinterpret_cast<uintptr_t>(b_sc) % 16 == 0);
     if (grouped) {
-      const int G = KB / GROUP;  // groups per tile
+      const int NG = KB / GROUP;  // groups per tile
       const uint32_t sSTG = smem_u32(smem + SMEM_STG);
       const uint8_t* stg = smem + SMEM_STG;
       GroupedScheduler<BM, BN, TILE_BAND> pre;
@@ -347,7 +422,7 @@ bsmxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
               cp_async_16(dst + STG_A + r * 16, live ? src : b_sc, live ? 16u : 0u);
             }
           }
-          if (++qp == G) {
+          if (++qp == NG) {
             qp = 0;
             tp_t += tile_stride;
             pre_ok = tp_t < total_tiles && pre.locate(args, tp_t, tp);
@@ -355,15 +430,14 @@ bsmxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         }
         cp_async_commit();  // an empty group keeps the group count in step
       };
-      issue_group(0);
-      issue_group(1);
+      for (int a = 0; a < C::STG_AHEAD; ++a) issue_group(a);
       int64_t g = 0;
       bool ok = true;
       TileCoord tc;
       for (int64_t t = tile0; ok && t < total_tiles; t += tile_stride) {
         if (!sched.locate(args, t, tc)) break;
-        for (int q = 0; ok && q < G; ++q, ++g) {
-          cp_async_wait_group<1>();  // group g has landed (g + 1 may be in flight)
+        for (int q = 0; ok && q < NG; ++q, ++g) {
+          cp_async_wait_group<C::STG_AHEAD - 1>();  // group g has landed (later ones in flight)
           __syncwarp();
           const uint8_t* src = stg + (g % STG_SLOTS) * STG_SLOT;
           for (int jg = 0; jg < GROUP; jg += KG) {
@@ -377,26 +451,31 @@ bsmxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
 #pragma unroll
             for (int u = 0; u < KG; ++u) {
             const int j = jg + u;
-            // packed block: row r = 32*rg + lane at byte lane*16 + rg*4
+#pragma unroll
+            for (int b = 0; b < C::G; ++b) {
+            // packed block of scale group b (codes 4b..4b+3 of K block j): row r = 32*rg +
+            // lane at byte lane*16 + rg*4
             auto gather = [&](const uint8_t* rows) {
+              const int off = C::CPK * j + 4 * b;
               uint4 w;
-              w.x = *reinterpret_cast<const uint32_t*>(rows + (0 * 32 + lane) * 16 + 4 * j);
-              w.y = *reinterpret_cast<const uint32_t*>(rows + (1 * 32 + lane) * 16 + 4 * j);
-              w.z = *reinterpret_cast<const uint32_t*>(rows + (2 * 32 + lane) * 16 + 4 * j);
-              w.w = *reinterpret_cast<const uint32_t*>(rows + (3 * 32 + lane) * 16 + 4 * j);
+              w.x = *reinterpret_cast<const uint32_t*>(rows + (0 * 32 + lane) * 16 + off);
+              w.y = *reinterpret_cast<const uint32_t*>(rows + (1 * 32 + lane) * 16 + off);
+              w.z = *reinterpret_cast<const uint32_t*>(rows + (2 * 32 + lane) * 16 + off);
+              w.w = *reinterpret_cast<const uint32_t*>(rows + (3 * 32 + lane) * 16 + off);
               return w;
             };
-            *reinterpret_cast<uint4*>(smem + SMEM_SFA + stage * SFA_STAGE + u * SF_BLOCK +
-                                      lane * 16) = gather(src);
-            uint4* sfb =
-                reinterpret_cast<uint4*>(smem + SMEM_SFB + stage * SFB_STAGE + u * 2 * SF_BLOCK);
-            if constexpr (packed_b) {
+            *reinterpret_cast<uint4*>(smem + SMEM_SFA + stage * SFA_STAGE +
+                                      (u * C::G + b) * SF_BLOCK + lane * 16) = gather(src);
+            uint4* sfb = reinterpret_cast<uint4*>(smem + SMEM_SFB + stage * SFB_STAGE +
+                                                  (u * C::G + b) * 2 * SF_BLOCK);
+            if constexpr (packed_b) {  // (MX-coded forms: one group)
               const uint8_t* pb = src + STG_A + j * SF_BLOCK + lane * 16;
               sfb[lane] = *reinterpret_cast<const uint4*>(pb);
               sfb[32 + lane] = *reinterpret_cast<const uint4*>(pb + 4 * SF_BLOCK);
             } else {
               sfb[lane] = gather(src + STG_A);
               sfb[32 + lane] = gather(src + STG_A + 128 * 16);
+            }
             }
             }
             fence_proxy_async_smem();  // generic-proxy writes -> tcgen05.cp (async proxy)
@@ -406,11 +485,12 @@ bsmxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
           }
           if (!ok) break;
           __syncwarp();
-          issue_group((int)((g + 2) % STG_SLOTS));  // the slot group g - 1 used is free
+          issue_group((int)((g + C::STG_AHEAD) % STG_SLOTS));  // group g - 1's slot is free
         }
       }
       cp_async_wait_group<0>();
-    } else {
+    } else if constexpr (!C::FP4) {
+    // (the fp4 forms never get here: the kernel winds down at its start on such rows)
     uint32_t ring[SCALE_LOOKAHEAD + 1] = {};
     int inflight = 0, head = 0;
     bool ok = true;
@@ -541,16 +621,18 @@ bsmxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
 }  // namespace mxp
 
 namespace mxp {
-template <bool PACKED_B>
+template <int FMT, bool PACKED_B>
 cudaError_t launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& args,
                    int num_sms, cudaStream_t stream) {
+  using C = PCfg<FMT>;
+  static_assert(smem_bytes<C>() <= 232448, "shared memory budget");
   static std::atomic<bool> attr_set[64];  // per device; several host threads may launch
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev >= 64 || !attr_set[dev].load(std::memory_order_acquire)) {
-    cudaError_t e = cudaFuncSetAttribute(bsmxfp8_pair_kernel<PACKED_B>,
+    cudaError_t e = cudaFuncSetAttribute(bsmxfp8_pair_kernel<FMT, PACKED_B>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)SMEM_BYTES);
+                                         (int)smem_bytes<C>());
     if (e != cudaSuccess) return e;
     if (dev < 64) attr_set[dev].store(true, std::memory_order_release);
   }
@@ -561,7 +643,7 @@ cudaError_t launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArg
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(mxp::NUM_THREADS);
-  cfg.dynamicSmemBytes = mxp::SMEM_BYTES;
+  cfg.dynamicSmemBytes = smem_bytes<C>();
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -570,16 +652,29 @@ cudaError_t launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArg
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, bsmxfp8_pair_kernel<PACKED_B>, tmA, tmB, args);
+  return cudaLaunchKernelEx(&cfg, bsmxfp8_pair_kernel<FMT, PACKED_B>, tmA, tmB, args);
 }
 }  // namespace mxp
 
 cudaError_t launch_bsmxfp8_pair(const CUtensorMap& tmA, const CUtensorMap& tmB,
                                 const GemmArgs& args, int num_sms, cudaStream_t stream) {
-  return args.b_scales_packed ? mxp::launch<true>(tmA, tmB, args, num_sms, stream)
-                              : mxp::launch<false>(tmA, tmB, args, num_sms, stream);
+  return args.b_scales_packed ? mxp::launch<mxp::PF_MXFP8, true>(tmA, tmB, args, num_sms, stream)
+                              : mxp::launch<mxp::PF_MXFP8, false>(tmA, tmB, args, num_sms, stream);
 }
 
-TmemPlan mx_pair_tmem_plan() { return mxp::PLAN; }
+cudaError_t launch_bsmx_pair_fp4(int fmt, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                                 const GemmArgs& args, int num_sms, cudaStream_t stream) {
+  using namespace mxp;
+  switch (fmt) {
+    case PF_MIXED:
+      return args.b_scales_packed ? launch<PF_MIXED, true>(tmA, tmB, args, num_sms, stream)
+                                  : launch<PF_MIXED, false>(tmA, tmB, args, num_sms, stream);
+    case PF_MXF4: return launch<PF_MXF4, false>(tmA, tmB, args, num_sms, stream);
+    case PF_NVF4: return launch<PF_NVF4, false>(tmA, tmB, args, num_sms, stream);
+  }
+  return cudaErrorInvalidValue;
+}
+
+TmemPlan mx_pair_tmem_plan() { return mxp::PCfg<mxp::PF_MXFP8>::PLAN; }
 
 }  // namespace bsfp8

@@ -340,6 +340,28 @@ bsfp8_status mx_fmt_gemm(int a_fmt, int b_fmt, const void* A, const void* B,
   if (M_total == 0) return BSFP8_OK;
   GemmArgs args{offsets, a_scales, b_scales, C, M_total, N, K, G, dev->err_word, ids, E,
                 packed_b ? 1 : 0};
+  // Prefill-sized batches (the MX plan's CTA-pair case) run the CTA-pair 256 x 256 kernel on
+  // the fp4 kinds: mxfp8 x mxfp4 with its weights loaded padded (32-byte aligned B), the
+  // fp4 x fp4 pairs in K blocks of 256 where the scale rows are chunkable (K % 512 == 0 for
+  // mxfp4, K % 256 for nvfp4; 16-byte aligned row-major scales).
+  if (fp4_mma_kind() && choose_mx_plan(M_total, G) == MxPlan::Pair) {
+    const int pf = a_fmt == BSMX_MXFP8 ? 1 : nv ? 3 : 2;
+    const bool ok = pf == 1 ? aligned(B, 32)
+                            : !packed_b && K % (nv ? 256 : 512) == 0 && aligned(a_scales, 16) &&
+                                  aligned(b_scales, 16);
+    if (ok) {
+      CUtensorMap pA, pB;
+      const bool maps =
+          encode_u8_2d(&pA, A, a_fp4 ? (uint64_t)K / 2 : (uint64_t)K, (uint64_t)M_total, 128,
+                       128) &&
+          (pf == 1 ? encode_e2m1_padded_2d(&pB, B, (uint64_t)K, (uint64_t)E * N, 128)
+                   : encode_u8_2d(&pB, B, (uint64_t)K / 2, (uint64_t)E * N, 128, 128));
+      if (!maps) return BSFP8_ERR_CUDA;
+      return launch_bsmx_pair_fp4(pf, pA, pB, args, dev->num_sms, stream) == cudaSuccess
+                 ? BSFP8_OK
+                 : BSFP8_ERR_CUDA;
+    }
+  }
   // Both operands fp4: the MMA kinds read the packed tiles as loaded, 256 K per stage
   // (128-byte rows, 128-byte swizzle) when every scale row's codes come in aligned 16-byte
   // chunks of whole stages, else 128 K (64-byte rows, 64-byte swizzle).

@@ -99,6 +99,13 @@ cudaError_t launch_bsnvfp4(int tn, bool mma_kind, int stage_k, const CUtensorMap
 // MXFP8 grouped GEMM with CTA-pair 256 x 256 tiles and overlapping TMEM accumulators.
 cudaError_t launch_bsmxfp8_pair(const CUtensorMap& tmA, const CUtensorMap& tmB,
                                 const GemmArgs& args, int num_sms, cudaStream_t stream);
+// The same CTA-pair kernel with fp4 operands (fmt: 1 = mxfp8 tokens x mxfp4 weights, tmB a
+// padded e2m1 map [128 elements x 128 rows]; 2 = mxfp4 x mxfp4 and 3 = nvfp4 x nvfp4, packed
+// maps [128 bytes x 128 rows], K blocks of 256).  The fp4 x fp4 forms need chunkable scale
+// rows (K % 512 == 0 for mxfp4, K % 256 for nvfp4; 16-byte aligned scales) and row-major
+// weight scales; the host launches them only then.
+cudaError_t launch_bsmx_pair_fp4(int fmt, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                                 const GemmArgs& args, int num_sms, cudaStream_t stream);
 // The TMEM plan that kernel is compiled with.
 TmemPlan mx_pair_tmem_plan();
 

@@ -31,13 +31,18 @@ cases = [("blockwise", "cta1_96", [130, 0, 77, 1], 384, 640),
          ("fp4", "mxfp8:mxfp4", [3, 17, 0, 32, 1, 9], 256, 1024),
          ("fp4", "mxfp4:mxfp4", [40, 0, 7, 64], 384, 1024),
          ("fp4", "nvfp4:nvfp4", [3, 17, 0, 32, 1, 9], 256, 768),
-         ("fp4", "mxfp4:mxfp4", [40, 0, 7], 256, 640)]
+         ("fp4", "mxfp4:mxfp4", [40, 0, 7], 256, 640),
+         ("fp4pair", "mxfp8:mxfp4", [300, 0, 270], 256, 1024),
+         ("fp4pair", "mxfp4:mxfp4", [300, 0, 270], 256, 1024),
+         ("fp4pair", "nvfp4:nvfp4", [300, 0, 270], 256, 768)]
 for mode, form, counts, N, K in cases:
     if mode == "blockwise":
         os.environ["BSFP8_BLOCKWISE_TILE"] = form
         p = gen.blockwise_problem(counts, N, K, seed=77)
-    elif mode == "fp4":
+    elif mode in ("fp4", "fp4pair"):
         a_fmt, b_fmt = form.split(":")
+        if mode == "fp4pair":
+            os.environ["BSFP8_MX_KERNEL"] = "pair"
         p = gen.fmt_problem(counts, N, K, seed=79, a_fmt=a_fmt, b_fmt=b_fmt)
     else:
         os.environ["BSFP8_MX_KERNEL"] = form

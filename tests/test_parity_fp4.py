@@ -347,3 +347,57 @@ def test_scales_not_16_byte_aligned(a_fmt, b_fmt, tn):
     bad, ratio, _ = parity_report(got, ref, T)
     assert bad == 0, f"{bad} elements outside tolerance (max err/tol {ratio:.3g})"
     assert np.all(d.guard_bits() == d.sentinel)
+
+
+PAIR_CASES = [
+    ("one_pair_tile", [256], 256, 1024),
+    ("ragged", [700, 0, 513, 1], 640, 1024),
+    ("many_experts", [300, 7, 0, 45, 260, 129, 511], 384, 2048),
+    ("k_256", [300, 40], 256, 256),       # one K block of 256 (nvfp4), swap for mxfp4
+    ("k_not_chunkable", [300, 40], 256, 640),  # the fp4 x fp4 pairs fall back to swap tiles
+]
+
+
+@pytest.mark.parametrize("a_fmt,b_fmt", PAIRS)
+@pytest.mark.parametrize("name,counts,N,K", PAIR_CASES, ids=[c[0] for c in PAIR_CASES])
+def test_cta_pair_tiles(name, counts, N, K, a_fmt, b_fmt, monkeypatch):
+    # BSFP8_MX_KERNEL=pair: the CTA-pair 256 x 256 kernel on the fp4 kinds (mxfp8 x mxfp4 on
+    # padded e2m1 weights; the fp4 x fp4 pairs in K blocks of 256 where the scale rows are
+    # chunkable, else the swap-AB tiles)
+    monkeypatch.setenv("BSFP8_MX_KERNEL", "pair")
+    _check_full(gen.fmt_problem(counts, N, K, seed=60 + len(name), a_fmt=a_fmt, b_fmt=b_fmt))
+
+
+@pytest.mark.parametrize("a_fmt,b_fmt", PAIRS)
+def test_cta_pair_tiles_exact_and_ids(a_fmt, b_fmt, monkeypatch):
+    monkeypatch.setenv("BSFP8_MX_KERNEL", "pair")
+    p = gen.fmt_problem([300, 0, 260, 41], 256, 1024, seed=61, a_fmt=a_fmt, b_fmt=b_fmt)
+    if a_fmt == "nvfp4":
+        p.a_scales[:] = 0x30 + 8 * (p.a_scales % 3)
+        p.b_scales[:] = 0x30 + 8 * (p.b_scales % 3)
+    else:
+        p.a_scales[:] = 126 + p.a_scales % 3
+        p.b_scales[:] = 126 + p.b_scales % 3
+    got, ref = _check_full(p)
+    assert np.array_equal(got, ref)
+    q = gen.fmt_problem([300, 0, 260, 41], 256, 1024, seed=62, a_fmt=a_fmt, b_fmt=b_fmt,
+                        expert_ids=[2, 0, 2, 1], num_experts=3)
+    _check_full(q)
+
+
+def test_cta_pair_mixed_prepacked_weight_scales(monkeypatch):
+    import block_scaled_fp8_persistent_gb300 as bsfp8
+    from gpu_util import DeviceProblem
+    monkeypatch.setenv("BSFP8_MX_KERNEL", "pair")
+    p = gen.fmt_problem([300, 0, 270], 384, 1024, seed=63, a_fmt="mxfp8", b_fmt="mxfp4")
+    d = DeviceProblem(p)
+    E, N, K = p.num_experts, p.N, p.K
+    packed = torch.empty(E * N * K // 32, dtype=torch.uint8, device="cuda")
+    bsfp8.bsmxfp8_pack_b_scales(d.sb, packed, E, N, K)
+    bsfp8.bsmx_grouped_gemm("mxfp8", "mxfp4", d.A, d.B, d.sa, packed, d.off, d.C, p.M_total, N,
+                            K, p.E, E, b_scales_packed=True)
+    got = d.c_bits()
+    assert bsfp8.bsfp8_get_device_error() == 0
+    ref, T = oracle.problem_reference(p)
+    bad, ratio, _ = parity_report(got, ref, T)
+    assert bad == 0, f"{bad} elements outside tolerance (max err/tol {ratio:.3g})"

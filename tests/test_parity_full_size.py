@@ -110,10 +110,12 @@ def test_fp4_decode_shape_every_element(a_fmt, b_fmt, path, monkeypatch):
     _run_and_compare(p, ref, T)
 
 
+@pytest.mark.parametrize("kernel", ["pair", "swap"])
 @pytest.mark.parametrize("a_fmt,b_fmt", FP4_PAIRS)
-def test_fp4_dense_prefill_every_element(a_fmt, b_fmt):
-    # a dense prefill-sized fp4 problem (one expert, 4096 x 4096 x 7168): 128-token tiles of
-    # the fp4 kinds, 256-K stages for the fp4 x fp4 pairs
+def test_fp4_dense_prefill_every_element(a_fmt, b_fmt, kernel, monkeypatch):
+    # a dense prefill-sized fp4 problem (one expert, 4096 x 4096 x 7168): the CTA-pair kernel
+    # the plan picks, and the 128-token swap-AB tiles of the fp4 kinds
+    monkeypatch.setenv("BSFP8_MX_KERNEL", kernel)
     p, ref, T = _reference(("fp4 dense", a_fmt, b_fmt), lambda: gen.fmt_problem(
         [4096], 4096, 7168, seed=6, a_fmt=a_fmt, b_fmt=b_fmt))
     _run_and_compare(p, ref, T)

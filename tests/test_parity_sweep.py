@@ -79,3 +79,15 @@ def test_fp4_sweep(seed, monkeypatch):
     monkeypatch.setenv("BSFP8_FP4_MMA", path)
     _check(gen.fmt_problem(counts, N, K, seed=3000 + seed, a_fmt=a_fmt, b_fmt=b_fmt,
                            a_recipe="quantized" if seed % 2 else "grid"))
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_fp4_pair_sweep(seed, monkeypatch):
+    # the fp4 pairs with BSFP8_MX_KERNEL=pair: CTA-pair tiles where the form allows, the
+    # swap-AB tiles otherwise
+    rng = np.random.default_rng(4000 + seed)
+    counts, N, K = _case(rng)
+    a_fmt, b_fmt = (("mxfp8", "mxfp4"), ("mxfp4", "mxfp4"), ("nvfp4", "nvfp4"))[seed % 3]
+    monkeypatch.setenv("BSFP8_MX_KERNEL", "pair")
+    _check(gen.fmt_problem(counts, N, K, seed=4000 + seed, a_fmt=a_fmt, b_fmt=b_fmt,
+                           a_recipe="quantized" if seed % 2 else "grid"))
