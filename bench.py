@@ -476,7 +476,7 @@ def time_fp4_formats(args, flush, stream, peaks, ref_ms):
     return out
 
 
-FP4_PER_BF16 = 4.0  # nominal dense fp4 / bf16 tensor throughput ratio (9 / 2.25 PFLOP/s)
+FP4_PER_BF16 = 6.0  # nominal dense fp4 / bf16 tensor throughput ratio (13.5 / 2.25 PFLOP/s)
 
 
 def time_fp4_dense(args, flush, stream, peaks):

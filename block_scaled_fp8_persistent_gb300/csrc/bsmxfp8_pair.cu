@@ -69,6 +69,10 @@ struct PCfg {
   // per KG K blocks
   static constexpr int KG = FP4 ? 1 : 2;
   static constexpr int STAGES = FP4 ? 5 : 3;  // ring stages (64 or 32 KB of operands each)
+  // scale loader warps per CTA: the fp4 x fp4 forms, with 2 or 4 scale groups per K block,
+  // split the work (warp 2: the token rows and weight rows 0-127; warp 3: weight rows
+  // 128-255)
+  static constexpr int LOADERS = FP4 ? 2 : 1;
   static constexpr TmemPlan PLAN = tmem_overlap_plan(KBLK, EPI_N, VEC, true, BN, 512);
   static constexpr uint32_t A_SUB = 128 * 128;  // one K block of this CTA's token rows
   static constexpr uint32_t B_SUB = 128 * 128;  // one K block of this CTA's weight rows
@@ -214,7 +218,8 @@ bsmxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(full_bar(s), 3);   // leader producer (+ both CTAs' bytes) + 2 scale loaders
+      // leader producer (+ both CTAs' bytes) + the scale loaders of both CTAs
+      mbar_init(full_bar(s), 1 + 2 * C::LOADERS);
       mbar_init(empty_bar(s), 1);  // one (multicast) MMA commit
     }
     for (int s = 0; s < 2; ++s) {
@@ -359,7 +364,7 @@ bsmxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
       }
     }
     __syncwarp();
-  } else if (warp == 2) {
+  } else if (warp == 2 || (C::LOADERS == 2 && warp == 3)) {
     // =============================== scale loader ===============================
     // Per stage: this CTA's 128 token rows (one packed block) and all 256 weight rows of
     // the tile (two packed blocks, duplicated in both CTAs: the pair MMA reads the weight
@@ -368,6 +373,7 @@ bsmxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     const uint8_t* b_sc = static_cast<const uint8_t*>(args.b_scales);
     // weight scales either row-major [E, N, K/32] or pre-packed [E][N/128][K/128] blocks
     constexpr bool packed_b = PACKED_B;
+    const bool second = C::LOADERS == 2 && warp == 3;
     const int nblk = args.N / 128;
     GroupedScheduler<BM, BN, TILE_BAND> sched;
     uint32_t stage = 0, phase = 0;
@@ -392,6 +398,7 @@ bsmxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
           const uint32_t dst = sSTG + slot * STG_SLOT;
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
+            if (second) break;  // the second loader fetches weight rows only
             const int r = 32 * i + (int)lane;
             const int64_t m = tp.m0 + 128 * rank + r;
             const bool live = m < args.M_total;
@@ -415,6 +422,8 @@ bsmxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
           } else {
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
+              // weight rows 32i + lane: all of them (one loader), or rows 0-127 / 128-255
+              if (C::LOADERS == 2 && (i >= 4) != second) continue;
               const int r = 32 * i + (int)lane;
               const int n = tp.n0 + r;
               const bool live = n < args.N;
@@ -451,31 +460,46 @@ bsmxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
 #pragma unroll
             for (int u = 0; u < KG; ++u) {
             const int j = jg + u;
+            // 128 rows (row 32*rg + lane at staging byte (32*rg + lane)*16) into the G packed
+            // blocks of K block j, block b (codes 4b..4b+3) at dst + b * step: each lane loads
+            // its 4 rows' CPK codes of the K block (one 4-, 8- or 16-byte load per row) and
+            // writes row 32*rg + lane's word of group b at byte lane*16 + rg*4
+            auto transpose = [&](const uint8_t* rows, uint8_t* dst, uint32_t step) {
+              uint32_t w[4][C::G];
 #pragma unroll
-            for (int b = 0; b < C::G; ++b) {
-            // packed block of scale group b (codes 4b..4b+3 of K block j): row r = 32*rg +
-            // lane at byte lane*16 + rg*4
-            auto gather = [&](const uint8_t* rows) {
-              const int off = C::CPK * j + 4 * b;
-              uint4 w;
-              w.x = *reinterpret_cast<const uint32_t*>(rows + (0 * 32 + lane) * 16 + off);
-              w.y = *reinterpret_cast<const uint32_t*>(rows + (1 * 32 + lane) * 16 + off);
-              w.z = *reinterpret_cast<const uint32_t*>(rows + (2 * 32 + lane) * 16 + off);
-              w.w = *reinterpret_cast<const uint32_t*>(rows + (3 * 32 + lane) * 16 + off);
-              return w;
+              for (int rg = 0; rg < 4; ++rg) {
+                const uint8_t* r = rows + (32 * rg + lane) * 16 + C::CPK * j;
+                if constexpr (C::G == 4) {
+                  const uint4 v = *reinterpret_cast<const uint4*>(r);
+                  w[rg][0] = v.x; w[rg][C::G > 1 ? 1 : 0] = v.y;
+                  w[rg][C::G > 2 ? 2 : 0] = v.z; w[rg][C::G > 3 ? 3 : 0] = v.w;
+                } else if constexpr (C::G == 2) {
+                  const uint2 v = *reinterpret_cast<const uint2*>(r);
+                  w[rg][0] = v.x; w[rg][C::G > 1 ? 1 : 0] = v.y;
+                } else {
+                  w[rg][0] = *reinterpret_cast<const uint32_t*>(r);
+                }
+              }
+#pragma unroll
+              for (int b = 0; b < C::G; ++b)
+                *reinterpret_cast<uint4*>(dst + b * step + lane * 16) =
+                    make_uint4(w[0][b], w[1][b], w[2][b], w[3][b]);
             };
-            *reinterpret_cast<uint4*>(smem + SMEM_SFA + stage * SFA_STAGE +
-                                      (u * C::G + b) * SF_BLOCK + lane * 16) = gather(src);
-            uint4* sfb = reinterpret_cast<uint4*>(smem + SMEM_SFB + stage * SFB_STAGE +
-                                                  (u * C::G + b) * 2 * SF_BLOCK);
-            if constexpr (packed_b) {  // (MX-coded forms: one group)
+            uint8_t* sfa = smem + SMEM_SFA + stage * SFA_STAGE + u * C::G * SF_BLOCK;
+            uint8_t* sfb = smem + SMEM_SFB + stage * SFB_STAGE + u * C::G * 2 * SF_BLOCK;
+            if constexpr (packed_b) {  // (MX-coded forms: one group, one loader)
+              transpose(src, sfa, SF_BLOCK);
               const uint8_t* pb = src + STG_A + j * SF_BLOCK + lane * 16;
-              sfb[lane] = *reinterpret_cast<const uint4*>(pb);
-              sfb[32 + lane] = *reinterpret_cast<const uint4*>(pb + 4 * SF_BLOCK);
+              reinterpret_cast<uint4*>(sfb)[lane] = *reinterpret_cast<const uint4*>(pb);
+              reinterpret_cast<uint4*>(sfb)[32 + lane] =
+                  *reinterpret_cast<const uint4*>(pb + 4 * SF_BLOCK);
             } else {
-              sfb[lane] = gather(src + STG_A);
-              sfb[32 + lane] = gather(src + STG_A + 128 * 16);
-            }
+              if (!second) {
+                transpose(src, sfa, SF_BLOCK);
+                transpose(src + STG_A, sfb, 2 * SF_BLOCK);  // weight rows 0-127
+              }
+              if (C::LOADERS == 1 || second)  // weight rows 128-255
+                transpose(src + STG_A + 128 * 16, sfb + SF_BLOCK, 2 * SF_BLOCK);
             }
             }
             fence_proxy_async_smem();  // generic-proxy writes -> tcgen05.cp (async proxy)
