@@ -70,10 +70,24 @@ struct PCfg {
   static constexpr int KG = FP4 ? 1 : 2;
   static constexpr int STAGES = FP4 ? 5 : 3;  // ring stages (64 or 32 KB of operands each)
   // scale loader warps per CTA: the fp4 x fp4 forms, with 2 or 4 scale groups per K block,
-  // split the work (warp 2: the token rows and weight rows 0-127; warp 3: weight rows
-  // 128-255)
+  // take alternate chunk groups (below; warp 2 the even ones, warp 3 the odd ones), each
+  // fetching and transposing all rows of its own groups, so that one loader per CTA
+  // announces each stage
   static constexpr int LOADERS = FP4 ? 2 : 1;
-  static constexpr TmemPlan PLAN = tmem_overlap_plan(KBLK, EPI_N, VEC, true, BN, 512);
+  // Scale feed.  The MMA thread copies each K block's blocks into the plan's scale columns
+  // (tcgen05.cp), in issue order after the previous K block's MMAs; mxfp4 (SF_ST) instead
+  // has SF_SLOTS scale slots, K block i in slot i % SF_SLOTS, stored (tcgen05.st) by four
+  // writer warps per CTA (one per TMEM lane quarter) from the loaders' packed blocks ahead
+  // of the MMAs.  Its plan is that of a K block SF_SLOTS times as long: the two
+  // accumulators overlap by all the slots (72 columns; nvfp4's 144 would reach past the
+  // column half whose epilogue warps release the overlap).
+  static constexpr bool SF_ST = FMT_ == PF_MXF4;
+  static constexpr int THREADS = SF_ST ? 512 : 384;
+  static constexpr int SF_SLOTS = SF_ST ? 3 : 1;
+  static constexpr TmemPlan PLAN =
+      tmem_overlap_plan(SF_SLOTS * KBLK, EPI_N, VEC, true, BN, 512);
+  static constexpr int SFA_COLS = 4 * G;  // one slot's token-scale columns
+  static constexpr int SFB_COLS = 8 * G;  // one slot's weight-scale columns
   static constexpr uint32_t A_SUB = 128 * 128;  // one K block of this CTA's token rows
   static constexpr uint32_t B_SUB = 128 * 128;  // one K block of this CTA's weight rows
   static constexpr uint32_t A_STAGE = KG * A_SUB;
@@ -92,11 +106,14 @@ struct PCfg {
   static_assert(GROUP == KPC && GROUP % KG == 0, "a chunk covers whole ring stages");
   static constexpr uint32_t STG_A = 128 * 16;
   static constexpr uint32_t STG_SLOT = STG_A + 256 * 16;
-  // groups fetched ahead: 8 K blocks of 128 (4 of 256 for nvfp4's one-block groups)
-  static constexpr int STG_AHEAD = GROUP == 1 ? 4 : 2;
-  static constexpr int STG_SLOTS = STG_AHEAD + 1;
+  // groups fetched ahead by a loader: 8 K blocks of 128 with one loader (4 of 256 for nvfp4's
+  // one-block groups); two of its own groups with two loaders (4 groups of the walk).  Slots
+  // per loader: with two, a group's slot takes the fetch STG_AHEAD groups on, issued by the
+  // same lanes after they consumed it (each lane reads back only the rows it fetched)
+  static constexpr int STG_AHEAD = LOADERS == 2 ? 2 : (GROUP == 1 ? 4 : 2);
+  static constexpr int STG_SLOTS = LOADERS == 2 ? STG_AHEAD : STG_AHEAD + 1;
   static constexpr uint32_t SMEM_STG = SMEM_SFB + STAGES * SFB_STAGE;
-  static constexpr uint32_t SMEM_CTL = SMEM_STG + STG_SLOTS * STG_SLOT;
+  static constexpr uint32_t SMEM_CTL = SMEM_STG + LOADERS * STG_SLOTS * STG_SLOT;
   // both CTAs' bytes of one K block (the padded weight load counts the packed bytes it reads)
   static constexpr uint32_t SUB_TX = 2 * (A_SUB + (FMT_ == PF_MIXED ? B_SUB / 2 : B_SUB));
   // Row-major scale copies in flight before the oldest is announced.  A stage's copies start
@@ -106,9 +123,12 @@ struct PCfg {
   static_assert(SCALE_LOOKAHEAD <= STAGES - 2, "scale announce would wait on the MMA");
   // scale-factor TMEM addresses on 4-column boundaries
   static_assert(PLAN.a_scale_offset % 4 == 0 && PLAN.b_scale_offset % 4 == 0 &&
-                    PLAN.b_scale_offset + 8 * G <= 512 && PLAN.a_scale_cols == 4 * G &&
-                    PLAN.b_scale_cols == 8 * G,
+                    PLAN.b_scale_offset + SF_SLOTS * SFB_COLS <= 512 &&
+                    PLAN.a_scale_cols == SF_SLOTS * SFA_COLS &&
+                    PLAN.b_scale_cols == SF_SLOTS * SFB_COLS,
                 "scale columns of the plan");
+  static_assert(PLAN.early_release_subtile < 128 / EPI_N,
+                "the overlap lies in the first column half of an accumulator");
 };
 // the plan of the MXFP8 form, pinned to the example's values for BLOCK_K 128, VEC 32
 static_assert(PCfg<PF_MXFP8>::PLAN.right_offset == 244 &&
@@ -126,6 +146,8 @@ template <class C>
 struct Ctl {
   uint64_t full[C::STAGES];
   uint64_t empty[C::STAGES];
+  uint64_t sready[C::STAGES];   // SF_ST: this CTA's packed scale blocks of the stage written
+  uint64_t sfull[C::SF_SLOTS];  // SF_ST: a scale slot stored by the writers of both CTAs
   uint64_t acc_full[2];
   uint64_t acc_empty[2];
   uint64_t overlap;
@@ -153,7 +175,7 @@ __device__ __forceinline__ uint64_t sf_block_desc(uint32_t saddr) {
 // PACKED_B: weight scales pre-packed in [E][N/128][K/128] blocks of 512 bytes (else
 // row-major [E, N, K/32]); an instantiation each, so the row-major loader carries no branch.
 template <int FMT, bool PACKED_B>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__global__ void __launch_bounds__(PCfg<FMT>::THREADS, 1)
 bsmxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const GemmArgs args) {
   using C = PCfg<FMT>;
@@ -219,7 +241,7 @@ bsmxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     tma_prefetch_desc(&tmB);
     for (int s = 0; s < STAGES; ++s) {
       // leader producer (+ both CTAs' bytes) + the scale loaders of both CTAs
-      mbar_init(full_bar(s), 1 + 2 * C::LOADERS);
+      mbar_init(full_bar(s), 3);  // the leader's TMA bytes + one scale loader of each CTA
       mbar_init(empty_bar(s), 1);  // one (multicast) MMA commit
     }
     for (int s = 0; s < 2; ++s) {
@@ -227,6 +249,11 @@ bsmxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
       mbar_init(acce_bar(s), NUM_EPI_WARPS * 2);
     }
     mbar_init(ovl_bar, NUM_EPI_WARPS);  // the 4 overlap-owning warps of each CTA
+    if constexpr (C::SF_ST) {
+      for (int s = 0; s < STAGES; ++s) mbar_init(smem_u32(&ctl->sready[s]), 1);  // its loader
+      for (int s = 0; s < C::SF_SLOTS; ++s)  // 4 writers x 2 CTAs
+        mbar_init(smem_u32(&ctl->sfull[s]), 8);
+    }
     mbar_init(smem_u32(&ctl->mma_done), 1);
     fence_mbarrier_init();
   }
@@ -290,6 +317,7 @@ bsmxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
       uint32_t stage = 0, phase = 0;
       bool ok = true;
       int64_t i = 0;  // tiles issued by this pair
+      uint32_t sslot = 0, sphase = 0;  // SF_ST: the next K block's scale slot and its use
       TileCoord tc;
       for (int64_t t = tile0; ok && t < total_tiles; t += tile_stride, ++i) {
         if (!sched.locate(args, t, tc)) break;
@@ -314,18 +342,33 @@ bsmxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
           }
           tc_fence_after();
           for (int u = 0; u < nk; ++u) {
-            // this K block's scales into the TMEM scale columns (after the previous K block's
-            // MMAs, which read them, in this thread's issue order)
-            // scale group g: this CTA's token rows into 4 columns at sfa_t + 4g, the tile's
-            // 256 weight rows into 8 columns at sfb_t + 8g (two 128-row blocks)
-            const uint32_t sfa_s = sSFA + stage * SFA_STAGE + u * C::G * SF_BLOCK;
-            const uint32_t sfb_s = sSFB + stage * SFB_STAGE + u * 2 * C::G * SF_BLOCK;
+            uint32_t sfa_k = sfa_t, sfb_k = sfb_t;
+            if constexpr (C::SF_ST) {
+              // the writers of both CTAs stored this K block's scales into slot sslot
+              if (!mbar_wait(smem_u32(&ctl->sfull[sslot]), sphase, abort)) {
+                record_error(args.err, DEV_TIMEOUT, abort);
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              sfa_k = sfa_t + sslot * C::SFA_COLS;
+              sfb_k = sfb_t + sslot * C::SFB_COLS;
+              if (++sslot == C::SF_SLOTS) { sslot = 0; sphase ^= 1; }
+            } else {
+              // this K block's scales into the TMEM scale columns (after the previous K
+              // block's MMAs, which read them, in this thread's issue order); scale group g:
+              // this CTA's token rows into 4 columns at sfa_t + 4g, the tile's 256 weight
+              // rows into 8 columns at sfb_t + 8g (two 128-row blocks)
+              const uint32_t sfa_s = sSFA + stage * SFA_STAGE + u * C::G * SF_BLOCK;
+              const uint32_t sfb_s = sSFB + stage * SFB_STAGE + u * 2 * C::G * SF_BLOCK;
 #pragma unroll
-            for (int g = 0; g < C::G; ++g) {
-              tmem_cp_32x128b_warpx4<2>(sfa_t + 4 * g, sf_block_desc(sfa_s + g * SF_BLOCK));
-              tmem_cp_32x128b_warpx4<2>(sfb_t + 8 * g, sf_block_desc(sfb_s + 2 * g * SF_BLOCK));
-              tmem_cp_32x128b_warpx4<2>(sfb_t + 8 * g + 4,
-                                        sf_block_desc(sfb_s + (2 * g + 1) * SF_BLOCK));
+              for (int g = 0; g < C::G; ++g) {
+                tmem_cp_32x128b_warpx4<2>(sfa_t + 4 * g, sf_block_desc(sfa_s + g * SF_BLOCK));
+                tmem_cp_32x128b_warpx4<2>(sfb_t + 8 * g,
+                                          sf_block_desc(sfb_s + 2 * g * SF_BLOCK));
+                tmem_cp_32x128b_warpx4<2>(sfb_t + 8 * g + 4,
+                                          sf_block_desc(sfb_s + (2 * g + 1) * SF_BLOCK));
+              }
             }
             const uint64_t adesc = kmajor_sw128_desc(sA + stage * A_STAGE + u * A_SUB);
             const uint64_t bdesc = kmajor_sw128_desc(sB + stage * B_STAGE + u * B_SUB);
@@ -335,20 +378,21 @@ bsmxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
               const uint32_t acc = (kb0 + u > 0 || k > 0) ? 1u : 0u;
               const uint64_t ad = adesc + (uint64_t)(k * 2), bd = bdesc + (uint64_t)(k * 2);
               if constexpr (FMT == PF_MXFP8)
-                umma_mxf8f6f4<2>(d_tmem, ad, bd, idesc_mxf8f6f4_e4m3(BM, BN, k, k), sfa_t, sfb_t,
+                umma_mxf8f6f4<2>(d_tmem, ad, bd, idesc_mxf8f6f4_e4m3(BM, BN, k, k), sfa_k, sfb_k,
                                  acc);
               else if constexpr (FMT == PF_MIXED)
                 umma_mxf8f6f4<2>(d_tmem, ad, bd,
-                                 idesc_mxf8f6f4(BM, BN, MXF_E4M3, MXF_E2M1, k, k), sfa_t, sfb_t,
+                                 idesc_mxf8f6f4(BM, BN, MXF_E4M3, MXF_E2M1, k, k), sfa_k, sfb_k,
                                  acc);
               else if constexpr (FMT == PF_MXF4)  // group k / 2, byte pair 2 (k % 2)
                 umma_mxf4<2>(d_tmem, ad, bd, idesc_mxf4_e2m1(BM, BN, 2 * (k & 1), 2 * (k & 1)),
-                             sfa_t + 4 * (k >> 1), sfb_t + 8 * (k >> 1), acc);
+                             sfa_k + 4 * (k >> 1), sfb_k + 8 * (k >> 1), acc);
               else  // UE4M3 per 16: group k
                 umma_mxf4nvf4_4x<2>(d_tmem, ad, bd, idesc_nvf4_e2m1_ue4m3(BM, BN),
-                                    sfa_t + 4 * k, sfb_t + 8 * k, acc);
+                                    sfa_k + 4 * k, sfb_k + 8 * k, acc);
             }
           }
+          if (!ok) break;
           umma_commit_pair(empty_bar(stage), 0x3);
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
         }
@@ -385,20 +429,30 @@ bsmxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                          (reinterpret_cast<uintptr_t>(a_sc) % 16 == 0) &&
                          (reinterpret_cast<uintptr_t>(b_sc) % 16 == 0);
     if (grouped) {
+      // Two loaders: the walk's groups alternate between them (group g to warp 2 + g % 2),
+      // each loader with its own staging slots.
       const int NG = KB / GROUP;  // groups per tile
-      const uint32_t sSTG = smem_u32(smem + SMEM_STG);
-      const uint8_t* stg = smem + SMEM_STG;
+      const uint32_t stg_off = second ? STG_SLOTS * STG_SLOT : 0;
+      const uint32_t sSTG = smem_u32(smem + SMEM_STG) + stg_off;
+      const uint8_t* stg = smem + SMEM_STG + stg_off;
       GroupedScheduler<BM, BN, TILE_BAND> pre;
       TileCoord tp;
       int64_t tp_t = tile0;
       bool pre_ok = pre.locate(args, tp_t, tp);
       int qp = 0;
+      auto next_pre = [&]() {  // the walk's next group
+        if (pre_ok && ++qp == NG) {
+          qp = 0;
+          tp_t += tile_stride;
+          pre_ok = tp_t < total_tiles && pre.locate(args, tp_t, tp);
+        }
+      };
+      if (second) next_pre();
       auto issue_group = [&](int slot) {
         if (pre_ok) {
           const uint32_t dst = sSTG + slot * STG_SLOT;
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            if (second) break;  // the second loader fetches weight rows only
             const int r = 32 * i + (int)lane;
             const int64_t m = tp.m0 + 128 * rank + r;
             const bool live = m < args.M_total;
@@ -422,33 +476,33 @@ bsmxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
           } else {
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-              // weight rows 32i + lane: all of them (one loader), or rows 0-127 / 128-255
-              if (C::LOADERS == 2 && (i >= 4) != second) continue;
-              const int r = 32 * i + (int)lane;
+              const int r = 32 * i + (int)lane;  // weight rows 32i + lane
               const int n = tp.n0 + r;
               const bool live = n < args.N;
               const uint8_t* src = b_sc + ((int64_t)tp.be * args.N + n) * scale_row + 16 * qp;
               cp_async_16(dst + STG_A + r * 16, live ? src : b_sc, live ? 16u : 0u);
             }
           }
-          if (++qp == NG) {
-            qp = 0;
-            tp_t += tile_stride;
-            pre_ok = tp_t < total_tiles && pre.locate(args, tp_t, tp);
-          }
         }
+        for (int l = 0; l < C::LOADERS; ++l) next_pre();
         cp_async_commit();  // an empty group keeps the group count in step
       };
       for (int a = 0; a < C::STG_AHEAD; ++a) issue_group(a);
-      int64_t g = 0;
+      int64_t g = 0;   // groups of the walk
+      int64_t og = 0;  // this loader's groups
       bool ok = true;
       TileCoord tc;
       for (int64_t t = tile0; ok && t < total_tiles; t += tile_stride) {
         if (!sched.locate(args, t, tc)) break;
         for (int q = 0; ok && q < NG; ++q, ++g) {
-          cp_async_wait_group<C::STG_AHEAD - 1>();  // group g has landed (later ones in flight)
+          if (C::LOADERS == 2 && (int)(g & 1) != (int)second) {  // the other loader's group
+            for (int jg = 0; jg < GROUP; jg += KG)
+              if (++stage == STAGES) { stage = 0; phase ^= 1; }
+            continue;
+          }
+          cp_async_wait_group<C::STG_AHEAD - 1>();  // group og has landed (later in flight)
           __syncwarp();
-          const uint8_t* src = stg + (g % STG_SLOTS) * STG_SLOT;
+          const uint8_t* src = stg + (og % STG_SLOTS) * STG_SLOT;
           for (int jg = 0; jg < GROUP; jg += KG) {
             const bool got =
                 __all_sync(0xffffffffu, mbar_wait(empty_bar(stage), phase ^ 1, abort));
@@ -494,22 +548,24 @@ bsmxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
               reinterpret_cast<uint4*>(sfb)[32 + lane] =
                   *reinterpret_cast<const uint4*>(pb + 4 * SF_BLOCK);
             } else {
-              if (!second) {
-                transpose(src, sfa, SF_BLOCK);
-                transpose(src + STG_A, sfb, 2 * SF_BLOCK);  // weight rows 0-127
-              }
-              if (C::LOADERS == 1 || second)  // weight rows 128-255
-                transpose(src + STG_A + 128 * 16, sfb + SF_BLOCK, 2 * SF_BLOCK);
+              transpose(src, sfa, SF_BLOCK);
+              transpose(src + STG_A, sfb, 2 * SF_BLOCK);                    // weight rows 0-127
+              transpose(src + STG_A + 128 * 16, sfb + SF_BLOCK, 2 * SF_BLOCK);  // 128-255
             }
             }
             fence_proxy_async_smem();  // generic-proxy writes -> tcgen05.cp (async proxy)
             __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(mapa_shared(full_bar(stage), 0));
+            if (lane == 0) {
+              mbar_arrive_cluster(mapa_shared(full_bar(stage), 0));
+              if constexpr (C::SF_ST) mbar_arrive(smem_u32(&ctl->sready[stage]));
+            }
             if (++stage == STAGES) { stage = 0; phase ^= 1; }
           }
           if (!ok) break;
           __syncwarp();
-          issue_group((int)((g + C::STG_AHEAD) % STG_SLOTS));  // group g - 1's slot is free
+          // one loader: group og - 1's slot is free; two: this group's own slot
+          issue_group((int)((og + C::STG_AHEAD) % STG_SLOTS));
+          ++og;
         }
       }
       cp_async_wait_group<0>();
@@ -580,7 +636,61 @@ bsmxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     cp_async_wait_group<0>();
     while (inflight > 0) announce_oldest();
     }
-  } else if (warp >= EPI_WARP0) {
+  } else if (C::SF_ST && warp >= EPI_WARP0 + NUM_EPI_WARPS) {
+    // ============================== scale writers ===============================
+    // Warp 12 + q stores TMEM lane quarter q of K block i's scale slot (i % SF_SLOTS) from
+    // this CTA's packed blocks of the stage: for the token rows (the MMA's M operand) only
+    // column q of each 4-column group is read, row 32q + r's codes at lane r; for the tile's
+    // 256 weight rows (its N operand) every lane quarter reads row 32j + r at lane r of column
+    // j (j < 8).  A slot is stored again only after the MMAs that read it, SF_SLOTS K blocks
+    // earlier, completed (the commit on that K block's stage).
+    static_assert(!C::SF_ST || (KG == 1 && C::SF_SLOTS < STAGES),
+                  "one K block per ring stage; a slot's reuse is within the ring");
+    const uint32_t q = warp & 3;
+    GroupedScheduler<BM, BN, TILE_BAND> sched;
+    uint32_t stage = 0, phase = 0;
+    uint32_t slot = 0;
+    int64_t kbi = 0;  // K blocks stored by this warp
+    bool ok = true;
+    TileCoord tc;
+    for (int64_t t = tile0; ok && t < total_tiles; t += tile_stride) {
+      if (!sched.locate(args, t, tc)) break;
+      for (int kb = 0; kb < KB; ++kb, ++kbi) {
+        bool got = mbar_wait(smem_u32(&ctl->sready[stage]), phase, abort);
+        if (got && kbi >= C::SF_SLOTS) {
+          // K block j = kbi - SF_SLOTS (same slot): the commit of its stage, its use j / STAGES
+          const int64_t j = kbi - C::SF_SLOTS;
+          got = mbar_wait(empty_bar((int)(j % STAGES)), (uint32_t)((j / STAGES) & 1), abort);
+        }
+        if (!__all_sync(0xffffffffu, got)) {
+          if (lane == 0) record_error(args.err, DEV_TIMEOUT, abort);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t lanes = (q * 32) << 16;
+        const uint32_t ta = tmem_base + lanes + PLAN.a_scale_offset + slot * C::SFA_COLS;
+        const uint32_t tb = tmem_base + lanes + PLAN.b_scale_offset + slot * C::SFB_COLS;
+#pragma unroll
+        for (int g = 0; g < C::G; ++g) {
+          // a packed block holds row 32c + r's 4 codes at byte 16r + 4c
+          const uint8_t* pa = smem + SMEM_SFA + stage * SFA_STAGE + g * SF_BLOCK + lane * 16;
+          tmem_st_32x32b_x1(ta + 4 * g + q, *reinterpret_cast<const uint32_t*>(pa + 4 * q));
+          const uint8_t* pb = smem + SMEM_SFB + stage * SFB_STAGE + 2 * g * SF_BLOCK + lane * 16;
+          const uint4 lo = *reinterpret_cast<const uint4*>(pb);
+          const uint4 hi = *reinterpret_cast<const uint4*>(pb + SF_BLOCK);
+          const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+          tmem_st_32x32b_x8(tb + 8 * g, w);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&ctl->sfull[slot]), 0));
+        if (++slot == C::SF_SLOTS) slot = 0;
+        if (++stage == STAGES) { stage = 0; phase ^= 1; }
+      }
+    }
+  } else if (warp >= EPI_WARP0 && warp < EPI_WARP0 + NUM_EPI_WARPS) {
     // ================================= epilogue =================================
     const uint32_t ew = warp - EPI_WARP0;
     const uint32_t quarter = warp & 3;
@@ -588,6 +698,8 @@ bsmxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     __nv_bfloat16* Cmat = static_cast<__nv_bfloat16*>(args.C);
     GroupedScheduler<BM, BN, TILE_BAND> sched;
     const uint64_t pol_c = l2_policy_evict_first();
+    // a 32-byte aligned C takes one full L2 sector per 32-byte store
+    const bool c_vec32 = (reinterpret_cast<uintptr_t>(args.C) & 31) == 0;
     int64_t i = 0;
     TileCoord tc;
     for (int64_t t = tile0; t < total_tiles; t += tile_stride, ++i) {
@@ -605,27 +717,55 @@ bsmxfp8_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
       const bool high_first = (buf == 0);
       const bool owns_overlap = high_first ? (half == 1) : (half == 0);
       const int64_t row = tc.m0 + 128 * rank + quarter * 32 + lane;
-      for (int s = 0; s < 4; ++s) {
-        const int sub = high_first ? 3 - s : s;
-        const int col = (int)half * 128 + sub * EPI_N;  // column inside the tile
+      const uint32_t taddr = tmem_base + ((quarter * 32) << 16) + col_base;
+      // drain step s: subtile high_first ? 3 - s : s of this warp's column half
+      auto col_of = [&](int s) { return (int)half * 128 + (high_first ? 3 - s : s) * EPI_N; };
+      auto load_bf16 = [&](int s, uint32_t (&p)[16]) {
         uint32_t v[32];
-        tmem_ld_32x32b_x32(tmem_base + ((quarter * 32) << 16) + col_base + col, v);
+        tmem_ld_32x32b_x32(taddr + col_of(s), v);
         tmem_ld_wait();
-        if (s == PLAN.early_release_subtile && owns_overlap) {
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive_cluster(mapa_shared(ovl_bar, 0));
-        }
-        const int n = tc.n0 + col;
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          p[j] = pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+      };
+      auto store_bf16 = [&](int s, const uint32_t (&p)[16]) {
+        const int n = tc.n0 + col_of(s);
         if (row < tc.m_end && n < args.N) {
           __nv_bfloat16* dst = Cmat + row * (int64_t)args.N + n;
+          if (c_vec32) {  // N % 128 == 0: dst is 32-byte aligned when C is
+            const uint32_t lo[8] = {p[0], p[1], p[2], p[3], p[4], p[5], p[6], p[7]};
+            const uint32_t hi[8] = {p[8], p[9], p[10], p[11], p[12], p[13], p[14], p[15]};
+            st_global_v8_hint(dst, lo, pol_c);
+            st_global_v8_hint(dst + 16, hi, pol_c);
+          } else {
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            auto f = [&](int j) { return __uint_as_float(v[8 * q + j]); };
-            st_global_v4_hint(dst + 8 * q, pack_bf16x2(f(0), f(1)), pack_bf16x2(f(2), f(3)),
-                              pack_bf16x2(f(4), f(5)), pack_bf16x2(f(6), f(7)), pol_c);
+            for (int q = 0; q < 4; ++q)
+              st_global_v4_hint(dst + 8 * q, p[4 * q], p[4 * q + 1], p[4 * q + 2],
+                                p[4 * q + 3], pol_c);
           }
         }
+      };
+      // The warps owning the shared columns read every subtile up to the plan's release
+      // point out of TMEM before storing any of them: the next tile's MMAs wait on that
+      // release, and a lane's 16-byte stores to its own row of C (32 rows per instruction)
+      // hold the warp for hundreds of cycles per subtile.
+      constexpr int E = PLAN.early_release_subtile;
+      int s0 = 0;
+      if (owns_overlap) {
+        uint32_t head[E + 1][16];
+#pragma unroll
+        for (int s = 0; s <= E; ++s) load_bf16(s, head[s]);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(mapa_shared(ovl_bar, 0));
+#pragma unroll
+        for (int s = 0; s <= E; ++s) store_bf16(s, head[s]);
+        s0 = E + 1;
+      }
+      for (int s = s0; s < 4; ++s) {
+        uint32_t p[16];
+        load_bf16(s, p);
+        store_bf16(s, p);
       }
       tc_fence_before();
       __syncwarp();
@@ -666,7 +806,7 @@ cudaError_t launch(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArg
   const int grid = (int)((max_tiles < pairs ? max_tiles : pairs) * 2);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(mxp::NUM_THREADS);
+  cfg.blockDim = dim3(C::THREADS);
   cfg.dynamicSmemBytes = smem_bytes<C>();
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];

@@ -385,6 +385,14 @@ def test_cta_pair_tiles_exact_and_ids(a_fmt, b_fmt, monkeypatch):
     _check_full(q)
 
 
+@pytest.mark.parametrize("a_fmt,b_fmt", PAIRS)
+def test_cta_pair_c_only_16_byte_aligned(a_fmt, b_fmt, monkeypatch):
+    # C 16-byte aligned but not 32-byte aligned: the epilogue's 16-byte stores
+    monkeypatch.setenv("BSFP8_MX_KERNEL", "pair")
+    p = gen.fmt_problem([300, 0, 261], 384, 1024, seed=64, a_fmt=a_fmt, b_fmt=b_fmt)
+    _check_full(p, c_offset=8)
+
+
 def test_cta_pair_mixed_prepacked_weight_scales(monkeypatch):
     import block_scaled_fp8_persistent_gb300 as bsfp8
     from gpu_util import DeviceProblem

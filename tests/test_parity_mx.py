@@ -24,10 +24,10 @@ def tn(request, monkeypatch):
     return request.param
 
 
-def _check_full(p):
+def _check_full(p, **kw):
     from gpu_util import DeviceProblem
     import block_scaled_fp8_persistent_gb300 as bsfp8
-    d = DeviceProblem(p, c_rows_extra=2)
+    d = DeviceProblem(p, c_rows_extra=2, **kw)
     d.run()
     got = d.c_bits()
     assert bsfp8.bsfp8_get_device_error() == 0
@@ -36,6 +36,12 @@ def _check_full(p):
     assert bad == 0, f"{bad} elements outside tolerance (max err/tol {ratio:.3g})"
     assert np.all(d.guard_bits() == d.sentinel)
     return got, ref
+
+
+def test_c_only_16_byte_aligned(tn):
+    # C 16-byte aligned (the documented minimum) but not 32-byte aligned: 16-byte stores
+    p = gen.mx_problem([300, 0, 261], 384, 512, seed=36)
+    _check_full(p, c_offset=8)
 
 
 CASES = [
