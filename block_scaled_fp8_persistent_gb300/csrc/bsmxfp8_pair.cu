@@ -74,16 +74,17 @@ struct PCfg {
   // fetching and transposing all rows of its own groups, so that one loader per CTA
   // announces each stage
   static constexpr int LOADERS = FP4 ? 2 : 1;
-  // Scale feed.  The MMA thread copies each K block's blocks into the plan's scale columns
-  // (tcgen05.cp), in issue order after the previous K block's MMAs; mxfp4 (SF_ST) instead
-  // has SF_SLOTS scale slots, K block i in slot i % SF_SLOTS, stored (tcgen05.st) by four
-  // writer warps per CTA (one per TMEM lane quarter) from the loaders' packed blocks ahead
-  // of the MMAs.  Its plan is that of a K block SF_SLOTS times as long: the two
-  // accumulators overlap by all the slots (72 columns; nvfp4's 144 would reach past the
-  // column half whose epilogue warps release the overlap).
-  static constexpr bool SF_ST = FMT_ == PF_MXF4;
+  // Scale feed.  MXFP8 forms: the MMA thread copies each K block's blocks into the plan's
+  // scale columns (tcgen05.cp), in issue order after the previous K block's MMAs.  fp4 x fp4
+  // forms (SF_ST): SF_SLOTS scale slots, K block i in slot i % SF_SLOTS, stored
+  // (tcgen05.st) by four writer warps per CTA (one per TMEM lane quarter) from the loaders'
+  // packed blocks ahead of the MMAs.  The plan is that of a K block SF_SLOTS times as long:
+  // the two accumulators overlap by all the slots, which must stay inside the column half
+  // whose epilogue warps release the overlap (mxfp4: three slots, 72 columns; nvfp4: two,
+  // 96 columns, as three would take 144).
+  static constexpr bool SF_ST = FP4;
   static constexpr int THREADS = SF_ST ? 512 : 384;
-  static constexpr int SF_SLOTS = SF_ST ? 3 : 1;
+  static constexpr int SF_SLOTS = FMT_ == PF_MXF4 ? 3 : (FMT_ == PF_NVF4 ? 2 : 1);
   static constexpr TmemPlan PLAN =
       tmem_overlap_plan(SF_SLOTS * KBLK, EPI_N, VEC, true, BN, 512);
   static constexpr int SFA_COLS = 4 * G;  // one slot's token-scale columns
@@ -136,10 +137,12 @@ static_assert(PCfg<PF_MXFP8>::PLAN.right_offset == 244 &&
               PCfg<PF_MXFP8>::PLAN.b_scale_offset == 504 &&
               PCfg<PF_MXFP8>::PLAN.early_release_subtile == 0,
               "plan for BLOCK_K 128, VEC 32");
-// nvfp4: the example's first worked plan (BLOCK_K 256, VEC 16)
-static_assert(PCfg<PF_NVF4>::PLAN.right_offset == 208 && PCfg<PF_NVF4>::PLAN.a_scale_offset == 464 &&
-              PCfg<PF_NVF4>::PLAN.b_scale_offset == 480 &&
-              PCfg<PF_NVF4>::PLAN.early_release_subtile == 1,
+// the example's first worked plan (BLOCK_K 256, VEC 16); the nvfp4 form's slots are two
+// such K blocks
+static_assert(tmem_overlap_plan(256, EPI_N, 16, true, BN, 512).right_offset == 208 &&
+              tmem_overlap_plan(256, EPI_N, 16, true, BN, 512).a_scale_offset == 464 &&
+              tmem_overlap_plan(256, EPI_N, 16, true, BN, 512).b_scale_offset == 480 &&
+              tmem_overlap_plan(256, EPI_N, 16, true, BN, 512).early_release_subtile == 1,
               "plan for BLOCK_K 256, VEC 16");
 
 template <class C>
