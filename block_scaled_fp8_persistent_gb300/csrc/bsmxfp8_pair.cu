@@ -38,6 +38,14 @@
 namespace bsfp8 {
 namespace mxp {
 
+// tcgen05.st of 8 consecutive 32-bit columns per lane (the writer warps' weight-scale words)
+__device__ __forceinline__ void tmem_st_32x32b_x8(uint32_t taddr, const uint32_t (&r)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(
+                   taddr),
+               "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+               : "memory");
+}
+
 constexpr int BK = 128;
 constexpr int BM = 256;        // token rows per pair tile (128 per CTA)
 constexpr int BN = 256;        // weight rows per pair tile (MMA N)
