@@ -233,6 +233,27 @@ def oracle_sample(p, rows: int):
     return dt, flops, th
 
 
+def sample_parity(got_bits, ref_bits, T) -> dict:
+    """The GPU's C against the oracle on the rows the CPU baseline computed, element by
+    element, with the tests' acceptance bound: |C - ref| <= 2 ulp_bf16(ref) + 1e-6 T, where
+    ulp_bf16(x) = 2^(max(floor(log2|x|), -126) - 7) and T is the sum of |products| (both
+    from the oracle)."""
+    import numpy as np
+    to_f64 = lambda b: (np.asarray(b, np.uint16).astype(np.uint32) << 16).view(  # noqa: E731
+        np.float32).astype(np.float64)
+    got, ref = to_f64(got_bits), to_f64(ref_bits)
+    a = np.abs(ref)
+    with np.errstate(divide="ignore"):
+        e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    e = np.where(a > 0, np.maximum(e, -126), -126)
+    bound = 2.0 * np.ldexp(1.0, (e - 7).astype(np.int64)) + 1e-6 * np.asarray(T, np.float64)
+    err = np.abs(got - ref)
+    return {"elements": int(err.size), "outside_bound": int((~(err <= bound)).sum()),
+            "max_err_over_bound": float(np.max(err / bound)) if err.size else 0.0,
+            "bit_identical": int((np.asarray(got_bits, np.uint16)
+                                  == np.asarray(ref_bits, np.uint16)).sum())}
+
+
 # ---------------------------------------------------------------------------
 # arms
 # ---------------------------------------------------------------------------
@@ -775,10 +796,14 @@ def run_ours(args):
 
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
+        import oracle
         rows = oracle_rows_for(p, args.cpu_seconds)
-        dt, fl, th = oracle_sample(p, rows)
+        dt, fl, th, (rsel, ref, T) = oracle.timed_rows(p, rows, keep=True)
+        # the same rows of the GPU's C (the last end-to-end step's read-back of this workload)
+        got = C_host.view(torch.int16).numpy().view(np.uint16)[rsel]
         cpu = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": th, "kind": "oracle",
-               "sample": f"{rows} of {p.M_total} rows x all {p.N} columns (K={p.K}), {dt:.1f} s"}
+               "sample": f"{rows} of {p.M_total} rows x all {p.N} columns (K={p.K}), {dt:.1f} s",
+               "parity_of_sample": sample_parity(got, ref, T)}
 
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,

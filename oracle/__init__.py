@@ -268,17 +268,22 @@ def problem_points(p, rows, cols, nthreads: int = 0):
                                rows, cols, nthreads=nthreads)
 
 
-def timed_rows(p, row_count: int, nthreads: int = 0):
-    """Time the oracle on the first row_count rows of every column (a bounded sample of the
-    workload).  Returns (seconds, flops_done, threads_used)."""
+def timed_rows(p, row_count: int, nthreads: int = 0, keep: bool = False):
+    """Time the oracle on row_count rows spread evenly over the workload, every column (a
+    bounded sample).  Returns (seconds, flops_done, threads_used); with keep, a fourth item
+    (row indices, bf16 bits [rows, N], the bound T [rows, N]) holds the sample's results."""
     M = p.M_total
     rows_sel = np.linspace(0, M - 1, num=min(row_count, M)).astype(np.int64)
     rows = np.repeat(rows_sel, p.N)
     cols = np.tile(np.arange(p.N, dtype=np.int64), rows_sel.size)
     t0 = time.perf_counter()
-    problem_points(p, rows, cols, nthreads=nthreads)
+    ref, T = problem_points(p, rows, cols, nthreads=nthreads)
     dt = time.perf_counter() - t0
-    return dt, 2.0 * rows.size * p.K, threads(nthreads)
+    out = (dt, 2.0 * rows.size * p.K, threads(nthreads))
+    if keep:
+        n = rows_sel.size
+        return out + ((rows_sel, np.asarray(ref).reshape(n, p.N), np.asarray(T).reshape(n, p.N)),)
+    return out
 
 
 def pack_mx_scales(S) -> np.ndarray:

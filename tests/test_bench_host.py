@@ -82,3 +82,26 @@ def test_traffic_read_from_the_workloads_own_section(tmp_path, monkeypatch):
     assert bench.traffic_from_profiles("fp4:mxfp8xmxfp4") == (111.0, "two.txt")
     assert bench.traffic_from_profiles("fp4:nvfp4xnvfp4") == (222.0, "two.txt")
     assert bench.traffic_from_profiles("config5") == (None, None)   # recorded hash differs
+
+
+def test_sample_parity_matches_the_tests_bound():
+    # the bench's check of the CPU baseline's rows uses the parity tests' acceptance bound:
+    # a planted one-element error (in a copy of the oracle's result) is found by both
+    import numpy as np
+    import bench
+    import gen
+    import oracle
+    from helpers import parity_report
+    p = gen.config_problem(0)
+    _, _, _, (rows, ref, T) = oracle.timed_rows(p, 24, keep=True)
+    assert rows.size == 24 and ref.shape == (24, p.N) == T.shape
+    ok = bench.sample_parity(ref, ref, T)
+    assert ok["outside_bound"] == 0 and ok["bit_identical"] == ref.size
+    bad = ref.copy()
+    bad[3, 17] ^= 0x20
+    bad[20, 200] ^= 0x01
+    got = bench.sample_parity(bad, ref, T)
+    n_bad, ratio, exact = parity_report(bad, ref, T)
+    assert got["outside_bound"] == n_bad >= 1
+    assert got["bit_identical"] == exact == ref.size - 2
+    assert abs(got["max_err_over_bound"] - ratio) < 1e-12
