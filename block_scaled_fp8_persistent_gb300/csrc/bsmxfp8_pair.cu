@@ -20,11 +20,14 @@
 // overlap barrier and the next tile's MMA (into the other accumulator) may start, while
 // the MMA two tiles later waits for the whole accumulator (acc_empty).
 //
-// Roles (12 warps per CTA): warp 0 TMA producer (own 128 token rows, own 128 weight rows);
-// warp 1 TMEM owner and, in CTA 0 of the pair, the MMA thread (per 128-K block tcgen05.cp
-// of its scale blocks and 4 x tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale; one
-// commit per ring stage, multicast to both CTAs); warp 2 scale loader; warps 4-11 epilogue
-// (TMEM lane quarter w%4, column half (w-4)/4, 32-column subtiles).
+// Roles (12 warps per CTA; 16 for the fp4 x fp4 forms): warp 0 TMA producer (own 128 token
+// rows, own 128 weight rows); warp 1 TMEM owner and, in CTA 0 of the pair, the MMA thread
+// (per 128-K block tcgen05.cp of its scale blocks and 4 x
+// tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale; one commit per ring stage, multicast
+// to both CTAs); warp 2 scale loader (fp4 x fp4: warps 2 and 3, alternate chunk groups);
+// warps 4-11 epilogue (TMEM lane quarter w%4, column half (w-4)/4, 32-column subtiles);
+// fp4 x fp4: warps 12-15 scale writers (tcgen05.st into the plan's scale slots, so the MMA
+// thread issues only MMAs and commits).
 // A ring stage holds KG = 2 K blocks (the k_group_size grouping of K iterations per
 // pipeline stage): the full/empty barriers, the scale announce and the commit are paid once
 // per 256 of K.
@@ -53,7 +56,7 @@ constexpr int EPI_N = 32;      // epilogue subtile columns
 // Tiles are walked in bands of 16 row tiles (row index fastest inside a band): the 76 pairs
 // in flight share ~5 columns of B, and B is read from DRAM about once per band
 constexpr int TILE_BAND = 16;
-constexpr int NUM_THREADS = 384;
+constexpr int NUM_THREADS = 384;  // the MXFP8 forms' block (PCfg::THREADS per form)
 constexpr int EPI_WARP0 = 4;
 constexpr int NUM_EPI_WARPS = 8;
 constexpr int SF_BLOCK = 512;  // packed scale block: 128 rows x 4 codes
