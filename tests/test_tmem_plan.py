@@ -54,3 +54,18 @@ def test_plan_invariants():
 def test_plan_rejects_bad_shapes():
     with pytest.raises(bsfp8.BsFp8Error):
         bsfp8.bsmxfp8_tmem_plan(100, 32, 32, True)
+
+
+@pytest.mark.parametrize("slots,vec,right,a_off,b_off", [(3, 32, 184, 440, 464), (2, 16, 160, 416, 448)])
+def test_fp4_pair_slot_plans(slots, vec, right, a_off, b_off):
+    # the fp4 x fp4 CTA-pair forms keep `slots` K blocks of 256 worth of scales in TMEM (mxfp4
+    # three, nvfp4 two): the plan of one K block that long, whose shared columns must lie in
+    # the column half an epilogue warp drains first (release before its fifth 32-column
+    # subtile); the same planner for one K block gives the page's worked values
+    p = bsfp8.bsmxfp8_tmem_plan(slots * 256, 32, vec, True)
+    assert (p["right_offset"], p["a_scale_offset"], p["b_scale_offset"]) == (right, a_off, b_off)
+    assert p["a_scale_cols"] == slots * (256 // vec) and p["b_scale_cols"] == 2 * p["a_scale_cols"]
+    assert p["early_release_subtile"] < 4
+    assert p["a_scale_offset"] % 4 == 0 and p["b_scale_offset"] % 4 == 0
+    # a third nvfp4 slot would reach past that half
+    assert bsfp8.bsmxfp8_tmem_plan(3 * 256, 32, 16, True)["early_release_subtile"] >= 4
