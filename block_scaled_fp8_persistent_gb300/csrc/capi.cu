@@ -212,6 +212,18 @@ MxPlan choose_mx_plan(int64_t M_total, int E) {
   return MxPlan::Pair;
 }
 
+// fp4 operands: CTA-pair tiles once the average row group no longer fits one 128-token
+// swap-AB tile (measured with 8 experts, N = 4096, K = 7168: swap-AB ahead for all three
+// pairs up to 128 rows per expert, the CTA pair from 192).  BSFP8_MX_KERNEL = pair | swap
+// overrides (split: swap-AB, the fp4 forms having no split).
+bool choose_fp4_pair(int64_t M_total, int E) {
+  if (const char* v = std::getenv("BSFP8_MX_KERNEL")) {
+    if (!std::strcmp(v, "pair")) return true;
+    if (!std::strcmp(v, "swap") || !std::strcmp(v, "split")) return false;
+  }
+  return M_total > (int64_t)128 * E;
+}
+
 // Token rows per MXFP8 tile: the smallest of 32 / 64 / 128 that holds the average expert
 // (decode batches give a few tokens per expert).  BSFP8_MX_TN overrides it.
 int choose_mx_token_tile(int64_t M_total, int E) {
@@ -340,11 +352,11 @@ bsfp8_status mx_fmt_gemm(int a_fmt, int b_fmt, const void* A, const void* B,
   if (M_total == 0) return BSFP8_OK;
   GemmArgs args{offsets, a_scales, b_scales, C, M_total, N, K, G, dev->err_word, ids, E,
                 packed_b ? 1 : 0};
-  // Prefill-sized batches (the MX plan's CTA-pair case) run the CTA-pair 256 x 256 kernel on
-  // the fp4 kinds: mxfp8 x mxfp4 with its weights loaded padded (32-byte aligned B), the
-  // fp4 x fp4 pairs in K blocks of 256 where the scale rows are chunkable (K % 512 == 0 for
-  // mxfp4, K % 256 for nvfp4; 16-byte aligned row-major scales).
-  if (fp4_mma_kind() && choose_mx_plan(M_total, G) == MxPlan::Pair) {
+  // Prefill-sized batches (more than 128 token rows per row group on average) run the
+  // CTA-pair 256 x 256 kernel on the fp4 kinds: mxfp8 x mxfp4 with its weights loaded padded
+  // (32-byte aligned B), the fp4 x fp4 pairs in K blocks of 256 where the scale rows are
+  // chunkable (K % 512 == 0 for mxfp4, K % 256 for nvfp4; 16-byte aligned row-major scales).
+  if (fp4_mma_kind() && choose_fp4_pair(M_total, G)) {
     const int pf = a_fmt == BSMX_MXFP8 ? 1 : nv ? 3 : 2;
     const bool ok = pf == 1 ? aligned(B, 32)
                             : !packed_b && K % (nv ? 256 : 512) == 0 && aligned(a_scales, 16) &&

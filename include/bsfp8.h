@@ -235,7 +235,8 @@ bsfp8_status bsmxfp8_grouped_gemm_prepacked(const void* A, const void* B, const 
  * Stages of 256 K run where every scale row's codes come in aligned 16-byte chunks (K % 512
  * == 0 for the mx formats, K % 256 for nvfp4, a_scales and b_scales 16-byte aligned), else
  * stages of 128 K; environment variable BSFP8_FP4_STAGE_K=128 keeps 128 K.  Prefill-sized
- * batches (where the MXFP8 plan picks its CTA-pair tiles, BSFP8_MX_KERNEL as there) run the
+ * batches (more than 128 token rows per row group on average; BSFP8_MX_KERNEL = pair | swap
+ * overrides) run the
  * CTA-pair 256 x 256 kernel on the same MMA kinds: mxfp8 x mxfp4 with a 32-byte aligned B,
  * the fp4 x fp4 pairs on chunkable scale rows with row-major weight scales; other batches
  * run the swap-AB tiles.  Results do not depend on these choices.
