@@ -38,7 +38,7 @@ FORMATS = {"mxfp8": 0, "mxfp4": 1, "nvfp4": 2}
 # Every symbol include/bsfp8.h declares (the CPU test checks the library exports them).
 EXPORTED = ("bsfp8_grouped_gemm", "bsmxfp8_grouped_gemm", "bsfp8_grouped_gemm_ids",
             "bsmxfp8_grouped_gemm_ids", "bsmxfp8_pack_b_scales", "bsmxfp8_grouped_gemm_prepacked",
-            "bsmxfp8_tmem_plan", "bsfp8_blockwise_plan", "bsmxfp8_plan",
+            "bsmxfp8_tmem_plan", "bsfp8_blockwise_plan", "bsmxfp8_plan", "bsmx_plan",
             "bsmx_grouped_gemm", "bsfp8_get_device_error", "bsfp8_check_wait_timeout",
             "bsfp8_status_string")
 
@@ -83,6 +83,8 @@ def load_library() -> ctypes.CDLL:
         lib.bsfp8_blockwise_plan.restype = i32
         lib.bsmxfp8_plan.argtypes = [ctypes.c_int64, i32, ctypes.POINTER(ctypes.c_int32)]
         lib.bsmxfp8_plan.restype = i32
+        lib.bsmx_plan.argtypes = [ctypes.c_int64, i32, ctypes.POINTER(ctypes.c_int32)]
+        lib.bsmx_plan.restype = i32
         lib.bsfp8_get_device_error.argtypes = [p, ctypes.POINTER(ctypes.c_int)]
         lib.bsfp8_get_device_error.restype = i32
         lib.bsfp8_check_wait_timeout.argtypes = [ctypes.c_int64, p]
@@ -230,6 +232,16 @@ def bsmxfp8_plan(M_total: int, num_experts: int) -> dict:
         raise BsFp8Error(st, "bsmxfp8_plan")
     return {"kernel": ("swap", "pair", "split")[out[0]], "token_rows": out[1],
             "split_rows": out[2]}
+
+
+def bsmx_plan(M_total: int, num_groups: int) -> dict:
+    """Tile form of the fp4-format GEMM for M_total token rows over num_groups groups (host
+    only): CTA-pair or swap-AB tiles and the swap-AB tile height."""
+    out = (ctypes.c_int32 * 2)()
+    st = load_library().bsmx_plan(int(M_total), int(num_groups), out)
+    if st != BSFP8_OK:
+        raise BsFp8Error(st, "bsmx_plan")
+    return {"kernel": ("swap", "pair")[out[0]], "token_rows": out[1]}
 
 
 def bsfp8_check_wait_timeout(limit_ns: int, stream=None) -> None:

@@ -542,6 +542,15 @@ extern "C" bsfp8_status bsmxfp8_plan(int64_t M_total, int num_experts, int32_t* 
   return BSFP8_OK;
 }
 
+extern "C" bsfp8_status bsmx_plan(int64_t M_total, int num_groups, int32_t* out) {
+  if (!out) return BSFP8_ERR_NULL;
+  if (M_total < 0 || num_groups < 1) return BSFP8_ERR_SHAPE;
+  const bool kinds = fp4_mma_kind();
+  out[0] = kinds && choose_fp4_pair(M_total, num_groups) ? 1 : 0;
+  out[1] = out[0] ? 0 : std::min(choose_mx_token_tile(M_total, num_groups), kinds ? 128 : 64);
+  return BSFP8_OK;
+}
+
 extern "C" bsfp8_status bsfp8_get_device_error(cudaStream_t stream, int* code) {
   if (!code) return BSFP8_ERR_NULL;
   DeviceInfo* dev = nullptr;

@@ -309,6 +309,19 @@ bsfp8_status bsfp8_blockwise_plan(int64_t M_total, int N, int num_experts, int n
 bsfp8_status bsmxfp8_plan(int64_t M_total, int num_experts, int32_t* out);
 
 /*
+ * Tile form bsmx_grouped_gemm (and its _ids form) uses for M_total token rows over
+ * num_groups row groups (host only, no GPU use; BSFP8_MX_KERNEL, BSFP8_MX_TN and
+ * BSFP8_FP4_MMA are honoured as in the GEMM): out[0] = 1 for CTA-pair 256 x 256 tiles (more
+ * than 128 rows per group on average, on the fp4 MMA kinds), 0 for swap-AB tiles; out[1] =
+ * token rows per swap-AB tile (32, 64 or 128; at most 64 on the converting forms; 0 with
+ * CTA-pair tiles).  The GEMM takes the CTA-pair tiles only where the operands also meet their
+ * conditions (mxfp8 x mxfp4: B 32-byte aligned; fp4 x fp4: row-major weight scales, K % 512
+ * == 0 for mxfp4 or K % 256 for nvfp4, 16-byte aligned scales), else swap-AB tiles.  A
+ * performance choice only.  BSFP8_ERR_NULL / BSFP8_ERR_SHAPE on bad input.
+ */
+bsfp8_status bsmx_plan(int64_t M_total, int num_groups, int32_t* out);
+
+/*
  * Read the device error word of the current device (after synchronising `stream`) into
  * *code (0, BSFP8_ERR_DEVICE_OFFSETS, BSFP8_ERR_DEVICE_TIMEOUT, BSFP8_ERR_DEVICE_EXPERT_IDS, or
  * in a debug build BSFP8_ERR_DEVICE_BOUNDS)

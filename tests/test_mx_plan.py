@@ -64,3 +64,43 @@ def test_bad_input():
         bsfp8.bsmxfp8_plan(10, 0)
     with pytest.raises(bsfp8.BsFp8Error):
         bsfp8.bsmxfp8_plan(-1, 4)
+
+
+@pytest.mark.parametrize("M,G,kernel,rows", [
+    (2091, 128, "swap", 32),     # decode: 1..32 tokens per expert
+    (8 * 64, 8, "swap", 64),
+    (8 * 128, 8, "swap", 128),   # 128 per group: one 128-token swap-AB tile still holds it
+    (8 * 128 + 1, 8, "pair", 0),
+    (8192, 1, "pair", 0),        # dense prefill
+    (0, 4, "swap", 32),
+])
+def test_fp4_plan_bands(M, G, kernel, rows, monkeypatch):
+    # the fp4 formats' own threshold: CTA-pair tiles above 128 rows per group on average
+    monkeypatch.delenv("BSFP8_FP4_MMA", raising=False)
+    assert bsfp8.bsmx_plan(M, G) == {"kernel": kernel, "token_rows": rows}
+    # the MXFP8 plan keeps its own bands (CTA pair above 56 rows per expert)
+    if M == 8 * 64:
+        assert bsfp8.bsmxfp8_plan(M, G)["kernel"] == "pair"
+
+
+def test_fp4_plan_overrides(monkeypatch):
+    monkeypatch.delenv("BSFP8_FP4_MMA", raising=False)
+    monkeypatch.setenv("BSFP8_MX_KERNEL", "pair")
+    assert bsfp8.bsmx_plan(100, 8)["kernel"] == "pair"
+    monkeypatch.setenv("BSFP8_MX_KERNEL", "split")  # no split for the fp4 forms: swap-AB
+    assert bsfp8.bsmx_plan(8192, 1) == {"kernel": "swap", "token_rows": 128}
+    monkeypatch.delenv("BSFP8_MX_KERNEL")
+    monkeypatch.setenv("BSFP8_MX_TN", "32")
+    assert bsfp8.bsmx_plan(8 * 100, 8) == {"kernel": "swap", "token_rows": 32}
+    monkeypatch.delenv("BSFP8_MX_TN")
+    # the converting forms: swap-AB tiles only, at most 64 token rows
+    monkeypatch.setenv("BSFP8_FP4_MMA", "convert")
+    assert bsfp8.bsmx_plan(8192, 1) == {"kernel": "swap", "token_rows": 64}
+    assert bsfp8.bsmx_plan(8 * 16, 8) == {"kernel": "swap", "token_rows": 32}
+
+
+def test_fp4_plan_rejects_bad_input():
+    with pytest.raises(bsfp8.BsFp8Error):
+        bsfp8.bsmx_plan(-1, 8)
+    with pytest.raises(bsfp8.BsFp8Error):
+        bsfp8.bsmx_plan(100, 0)
